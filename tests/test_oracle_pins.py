@@ -1,0 +1,455 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a value the pages
+print (tests/golden/*.json, with citations), a closed form, an invariant, a library
+routine for a special case, or brute force on a tiny input.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mtp_synth import configs as C
+from mtp_synth import gen as G
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ number formats
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.005859375, 1.001953125, 65504.0, 3.0e38]])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x), ref)
+
+
+def test_round_bf16_decision_on_fp32_value():
+    # a value just above a bf16 midpoint in fp64 but exactly on it after fp32 rounding
+    mid = 1.0 + 2.0 ** -8            # midpoint between 1 and the next bf16 (1 + 2^-7)
+    x = mid + 2.0 ** -40             # rounds to `mid` in fp32, then ties-to-even -> 1.0
+    assert O.round_bf16(np.array([x]))[0] == 1.0
+
+
+def test_decode_bf16_exact():
+    bits = np.array([0x3F80, 0xBF80, 0x0000, 0x4049, 0x7F7F], dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.decode_bf16(bits), ref)
+
+
+# ------------------------------------------------------------------ elementwise pieces
+
+def test_rms_norm_constant_vector_and_scale_invariance():
+    g = np.linspace(0.5, 1.5, 64)
+    for c in (3.0, -0.25):
+        out = O.rms_norm(np.full(64, c), g, 1e-6)
+        np.testing.assert_allclose(out, np.sign(c) * g * abs(c) / math.sqrt(c * c + 1e-6), rtol=1e-15)
+    v = np.random.default_rng(1).standard_normal(256)
+    np.testing.assert_allclose(O.rms_norm(7.0 * v, 1.0, 0.0), O.rms_norm(v, 1.0, 0.0), rtol=1e-13)
+    assert np.all(O.rms_norm(np.zeros(8), 1.0, 1e-6) == 0.0)
+
+
+def test_rms_norm_matches_torch():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((5, 96))
+    g = 1 + 0.02 * rng.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(v), (96,), torch.from_numpy(g), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(v, g, 1e-6), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_gelu_tanh_closed_forms_and_torch():
+    assert O.gelu_tanh(np.array([0.0]))[0] == 0.0
+    x = np.linspace(-9, 9, 1001)
+    np.testing.assert_allclose(O.gelu_tanh(x) - O.gelu_tanh(-x), x, atol=1e-12)   # odd part is x/2
+    np.testing.assert_allclose(O.gelu_tanh(np.array([30.0, -30.0])), [30.0, 0.0], atol=1e-12)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    np.testing.assert_allclose(O.gelu_tanh(x), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_rope_identity_norm_composition_relative():
+    rng = np.random.default_rng(3)
+    d = 64
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    np.testing.assert_array_equal(O.rope(q, 0, 1e4), q)
+    np.testing.assert_array_equal(O.rope(q, 123, 0.0), q)
+    r = O.rope(q, 4097, 1e6)
+    assert abs(np.linalg.norm(r) - np.linalg.norm(q)) < 1e-12
+    np.testing.assert_allclose(O.rope(O.rope(q, 5, 1e4), 9, 1e4), O.rope(q, 14, 1e4), atol=1e-12)
+    # dot products depend only on the position difference
+    a = O.rope(q, 100, 1e4) @ O.rope(k, 37, 1e4)
+    b = O.rope(q, 63, 1e4) @ k
+    assert abs(a - b) < 1e-10
+    # d = 2: a plain rotation by `pos` radians (inverse frequency 1)
+    v = np.array([1.0, 0.0])
+    np.testing.assert_allclose(O.rope(v, 1, 10.0), [math.cos(1.0), math.sin(1.0)], atol=1e-15)
+
+
+# ------------------------------------------------------------------ attention
+
+def _sdpa(q, k, scale):
+    # torch's scaled_dot_product_attention over an explicit all-true mask (bidirectional)
+    nh, d = q.shape
+    n_kv = k.shape[1]
+    kk = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(nh // n_kv, dim=0)  # [nh][L][d]
+    qq = torch.from_numpy(q)[:, None, :]
+    mask = torch.ones(nh, 1, k.shape[0], dtype=torch.bool)
+    o = torch.nn.functional.scaled_dot_product_attention(qq, kk, kk, attn_mask=mask, scale=scale)
+    return o[:, 0, :].numpy()
+
+
+@pytest.mark.parametrize("nh,n_kv,d,L", [(2, 1, 32, 64), (8, 2, 16, 300), (4, 4, 8, 5)])
+def test_attention_full_equals_bidirectional_sdpa(nh, n_kv, d, L):
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((nh, d)); k = rng.standard_normal((L, n_kv, d))
+    np.testing.assert_allclose(O.attention_q_only(q, k, None, 0.3), _sdpa(q, k, 0.3), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_invariants():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((4, 16)); k = rng.standard_normal((50, 1, 16))
+    o = O.attention_q_only(q, k, None, 0.25)
+    # key order does not matter (q_len = 1: no position in the mask)
+    np.testing.assert_allclose(O.attention_q_only(q, k[::-1], None, 0.25), o, rtol=1e-13)
+    # one key -> that key; identical keys -> that key
+    np.testing.assert_allclose(O.attention_q_only(q, k[:1], None, 0.25), np.repeat(k[0], 4, 0), rtol=0, atol=0)
+    same = np.repeat(k[:1], 7, axis=0)
+    np.testing.assert_allclose(O.attention_q_only(q, same, None, 0.25), np.repeat(k[0], 4, 0), atol=1e-15)
+    # V = None is V = K, bit for bit
+    np.testing.assert_array_equal(O.attention_q_only(q, k, k, 0.25), o)
+
+
+def test_attention_gqa_head_mapping():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((4, 8)); k = rng.standard_normal((20, 2, 8))
+    o = O.attention_q_only(q, k, None, 0.5)
+    # heads 0,1 read kv head 0; heads 2,3 read kv head 1
+    np.testing.assert_allclose(o[:2], O.attention_q_only(q[:2], k[:, :1], None, 0.5), rtol=1e-14)
+    np.testing.assert_allclose(o[2:], O.attention_q_only(q[2:], k[:, 1:], None, 0.5), rtol=1e-14)
+
+
+def test_sliding_window_is_the_flipped_mask():
+    for L, W in [(4096, 512), (300, 512), (512, 512), (513, 512), (1, 4)]:
+        lo, hi = O.key_range("S", L, W)
+        # flip construction: in reversed key order the window is the first W positions;
+        # flipping back gives the mask over the original order
+        rev_mask = np.arange(L) < W
+        mask = rev_mask[::-1]
+        np.testing.assert_array_equal(np.nonzero(mask)[0], np.arange(lo, hi))
+        assert hi - lo == min(L, W)
+        if L > W:
+            assert lo == L - W          # the key at distance exactly W is excluded
+        assert O.key_range("F", L, W) == (0, L)
+
+
+def test_sliding_equals_full_when_context_fits_window():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((2, 8)); k = rng.standard_normal((30, 1, 8))
+    lo, hi = O.key_range("S", 30, 64)
+    np.testing.assert_array_equal(O.attention_q_only(q, k[lo:hi], None, 0.3),
+                                  O.attention_q_only(q, k, None, 0.3))
+
+
+# ------------------------------------------------------------------ heads
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(8)
+    for trial in range(300):
+        n = int(rng.integers(1, 65)); k = int(rng.integers(1, n + 1))
+        v = rng.integers(-4, 5, size=n).astype(np.float32)      # many exact ties
+        brute = [i for _, i in sorted((-float(v[i]), i) for i in range(n))][:k]
+        assert list(O.topk_desc(v, k)) == brute
+
+
+def test_argmax_lowest_id_on_ties():
+    v = np.array([1.0, 3.0, 3.0, 2.0], dtype=np.float32)
+    assert O.argmax_lowest(v) == 1
+    assert O.argmax_lowest(v, ids=np.array([40, 30, 20, 10])) == 20
+
+
+def _tiny_head_shape(V=512, Cn=16, k=3, H=24):
+    return O.Shape(dtype="bf16", backbone=8, hidden=H, layer_types=("F",), n_head=1, head_dim_swa=8,
+                   head_dim_full=8, n_kv_head=1, ffn=8, vocab=V, n_centroids=Cn, top_k=k, window=0,
+                   use_ordered_embeddings=True)
+
+
+def _tiny_head_weights(s, seed):
+    rng = np.random.default_rng(seed)
+    W = O.DecodedWeights(pre_proj=None, post_proj=None, out_norm=None,
+                         token_embd=O.round_bf16(0.02 * rng.standard_normal((s.vocab, s.hidden))),
+                         centroids=O.round_bf16(0.02 * rng.standard_normal((s.n_centroids, s.hidden))),
+                         token_ordering=rng.permutation(s.vocab), target_embed_raw=None, dtype="bf16")
+    return W
+
+
+def test_centroid_head_matches_dense_on_selected_clusters():
+    s = _tiny_head_shape()
+    hits = 0
+    for seed in range(40):
+        W = _tiny_head_weights(s, seed)
+        y = O.round_bf16(np.random.default_rng(100 + seed).standard_normal(s.hidden))
+        head = O.centroid_head(s, W, y)
+        dense = O.dense_head(s, W, y)
+        # sparse logits equal the dense logits at the gathered ids
+        np.testing.assert_array_equal(head.logits, dense.logits[head.ids])
+        # the gathered ids are exactly the members of the selected clusters
+        members = W.token_ordering.reshape(s.n_centroids, s.vsc)[head.selected]
+        assert set(head.ids.tolist()) == set(members.reshape(-1).tolist())
+        assert len(head.ids) == s.top_k * s.vsc
+        # materialised row: -1e30 exactly outside the candidates
+        row = O.materialise_row(s, head)
+        mask = np.ones(s.vocab, bool); mask[head.ids] = False
+        assert np.all(row[mask] == np.float32(-1e30)) and np.sum(~mask) == s.top_k * s.vsc
+        np.testing.assert_array_equal(row[head.ids], head.logits.astype(np.float32))
+        # when the dense argmax lies in a selected cluster the sparse argmax equals it
+        if dense.token in set(head.ids.tolist()):
+            hits += 1
+            assert head.token == dense.token
+    assert hits >= 5
+
+
+def test_centroid_head_recovers_planted_token():
+    # clusters built around centroid directions: y along a member of cluster 5 selects that
+    # cluster first, and the dense winner is found inside it
+    s = _tiny_head_shape(V=256, Cn=8, k=2, H=32)
+    rng = np.random.default_rng(9)
+    cent = rng.standard_normal((s.n_centroids, s.hidden))
+    order = rng.permutation(s.vocab)
+    T = np.empty((s.vocab, s.hidden))
+    for c in range(s.n_centroids):
+        T[order[c * s.vsc:(c + 1) * s.vsc]] = cent[c] + 0.1 * rng.standard_normal((s.vsc, s.hidden))
+    W = O.DecodedWeights(None, None, None, T, cent, order, None, "f32")
+    target = order[5 * s.vsc + 7]
+    y = T[target] * 3.0
+    head = O.centroid_head(s, W, y)
+    assert head.selected[0] == 5 and head.token == O.dense_head(s, W, y).token
+    assert head.token in set(order[5 * s.vsc:6 * s.vsc].tolist()) and target in set(head.ids.tolist())
+
+
+def test_vocab_divisible_and_ordering_permutation():
+    for cfg in C.CONFIGS:
+        s = cfg.shape
+        if s.use_ordered_embeddings:
+            assert s.vocab % s.n_centroids == 0
+    g = _golden("published_shapes.json")["centroid_head"]
+    assert g["vocab"] % g["n_centroids"] == 0
+    assert g["vocab"] // g["n_centroids"] * g["top_k"] == 4096
+
+
+# ------------------------------------------------------------------ shapes pinned by printed sizes
+
+def test_param_count_and_checkpoint_size_match_pages():
+    g = _golden("published_shapes.json")
+    e2b, e4b = O.Shape.of(C.E2B), O.Shape.of(C.E4B)
+    assert e2b.hidden == g["e2b"]["hidden"] and e2b.backbone == g["e2b"]["backbone"]
+    assert e4b.backbone == g["e4b"]["backbone"]
+    # "~78 M" read as within 1 % of 78e6; "~158 MB" as within 0.5 % of 158e6
+    near = lambda v, ref, tol: abs(v / ref - 1.0) < tol
+    assert near(O.param_count(e2b), 1e6 * g["e2b"]["params_approx_millions"], 0.01)
+    assert near(O.param_count(e4b), 1e6 * g["e4b"]["params_approx_millions"], 0.01)
+    assert near(O.checkpoint_bytes(e4b), 1e6 * g["e4b"]["checkpoint_mb_bf16_approx"], 0.005)
+    assert O.param_count(e2b) == 77_731_332
+    # a half-width FFN, or separate K/V projections, would break the printed sizes
+    half_ffn = O.Shape.of(C.E2B); half_ffn.ffn = 1024
+    assert not near(O.param_count(half_ffn), 78e6, 0.01)
+    kv_proj = 2 * sum(O.Shape.of(C.E4B).head_dim(t) * 256 for t in C.E4B.layer_types) * 2
+    assert not near(O.checkpoint_bytes(e4b) + kv_proj, 158e6, 0.005)
+    assert C.A4B_DENSE.backbone == g["a4b_backbone"]["backbone"]
+    assert C.A4B_DENSE.hidden == g["a4b_backbone"]["hidden"]
+    assert float(O.MASK_VALUE) == np.float32(g["mask_value"]["value"])
+
+
+def test_accept_rate_printed_value():
+    g = _golden("accept_rate.json")
+    assert round(100 * O.accept_rate(g["n_accept"], g["n_drafted"]), 1) == g["accept_rate_percent_1dp"]
+
+
+# ------------------------------------------------------------------ verify
+
+def _rows_with_argmax(targets, V, rng):
+    rows = rng.standard_normal((len(targets), V)).astype(np.float32)
+    for i, t in enumerate(targets):
+        rows[i, t] = rows[i].max() + 1.0
+    return rows
+
+
+def test_verify_worked_example():
+    g = _golden("verify_worked_example.json")
+    rng = np.random.default_rng(10)
+    for case in g["cases"]:
+        logits = _rows_with_argmax(case["target_argmax"], g["vocab_size"], rng)[None]
+        acc, out = O.verify_greedy(logits, np.array([case["drafts"]]), logits_dtype="f32")
+        assert acc[0] == case["accept_len"], case["name"]
+        assert out[0].tolist() == case["out_tokens"], case["name"]
+
+
+def test_verify_ties_take_lowest_id():
+    logits = np.zeros((1, 2, 6), dtype=np.float32)
+    logits[0, 0, [2, 4]] = 5.0
+    logits[0, 1, [1, 3]] = 2.0
+    acc, out = O.verify_greedy(logits, np.array([[2]]), logits_dtype="f32")
+    assert acc[0] == 1 and out[0].tolist() == [2, 1]
+    acc, out = O.verify_greedy(logits, np.array([[4]]), logits_dtype="f32")
+    assert acc[0] == 0 and out[0].tolist() == [2, -1]
+
+
+def test_verify_bf16_input_decoded():
+    bits = G.bf16_bits(np.array([[[0.5, 2.0, 1.0], [3.0, 0.0, 0.0]]], dtype=np.float32))
+    acc, out = O.verify_greedy(bits, np.array([[1]]))
+    assert acc[0] == 1 and out[0].tolist() == [1, 0]
+
+
+def test_verify_expected_accept_length_closed_form():
+    # agreement ~ Bernoulli(p) per position, independent: P(accept >= i) = p^i, so
+    # E[accept] = sum_{i=1..n} p^i and E[accept^2] = sum_i (2i-1) p^i
+    p, n, V, B = 0.6, 8, 64, 4000
+    rng = np.random.default_rng(11)
+    drafts = rng.integers(0, V, size=(B, n))
+    agree, alt_raw = G.round_tables(B, n, V, p, seed=77, r=0)
+    tgt = G.planted_targets(drafts, agree, alt_raw, V)
+    logits = rng.standard_normal((B, n + 1, V)).astype(np.float32)
+    logits[np.arange(B)[:, None], np.arange(n + 1)[None, :], tgt] = 16.0
+    acc, out = O.verify_greedy(logits, drafts, logits_dtype="f32")
+    mean = sum(p ** i for i in range(1, n + 1))
+    var = sum((2 * i - 1) * p ** i for i in range(1, n + 1)) - mean ** 2
+    assert abs(acc.mean() - mean) < 3 * math.sqrt(var / B)
+    assert abs(mean - 1.4748) < 1e-4
+    # the token after the accepted prefix is the planted target of that row
+    np.testing.assert_array_equal(out[np.arange(B), acc], tgt[np.arange(B), acc])
+
+
+# ------------------------------------------------------------------ whole step: reduction cases
+
+def _tiny_model(seed=0, dtype="f32", layer_types=("S", "F"), zero_blocks=False):
+    cfg = C.TINY_F32 if dtype == "f32" else C.E2B
+    from dataclasses import replace
+    shape = replace(C.TINY_F32, dtype=dtype, layer_types=layer_types, window=8)
+    w = G.make_weights(shape, seed)
+    if zero_blocks:
+        for L in w.layers:
+            L["o"] = np.zeros_like(L["o"]); L["down"] = np.zeros_like(L["down"])
+    wl = C.Workload(batch=2, ctx=40, ctx_lo=10, n_draft=3)
+    inp = G.make_step_inputs(shape, wl, seed)
+    return shape, w, inp
+
+
+def test_zero_blocks_reduce_to_scaled_preprojection():
+    # with W_o = W_down = 0 every block only multiplies the residual by layer_scalar, and
+    # the final norm removes the scale (up to eps): y = norm(pre_projection([h; e]))
+    shape, w, inp = _tiny_model(zero_blocks=True)
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    b = 0
+    h = O.decode(inp.hidden[b], s.dtype)
+    r = O.drafter_step(s, W, h, int(inp.last_token[b]), {"S": inp.k_swa[b], "F": inp.k_full[b]},
+                       {}, int(inp.ctx_len[b]), int(inp.pos[b]))
+    u = np.concatenate([h, O.decode(w.target_embed[int(inp.last_token[b])], s.dtype)])
+    x0 = W.pre_proj @ u
+    lam = np.prod([L["layer_scalar"] for L in W.layers])
+    np.testing.assert_allclose(r.x_layers[-1], lam * x0, rtol=1e-12)
+    np.testing.assert_allclose(r.y, O.rms_norm(lam * x0, W.out_norm, s.rms_eps), rtol=1e-12)
+    np.testing.assert_allclose(r.y, O.rms_norm(x0, W.out_norm, 0.0), rtol=1e-3)
+
+
+def test_concat_order_reading():
+    # pre_projection = [I | 0] selects the hidden state, [0 | I] the embedding row
+    shape, w, inp = _tiny_model(zero_blocks=True)
+    s = O.Shape.of(shape)
+    H, bb = s.hidden, s.backbone
+    for sel, which in ((0, "h"), (bb, "e")):
+        w.pre_proj = np.zeros((H, 2 * bb), np.float32); w.pre_proj[np.arange(H), sel + np.arange(H)] = 1
+        W = O.decode_weights(w)
+        h = O.decode(inp.hidden[0], s.dtype)
+        tok = int(inp.last_token[0])
+        r = O.drafter_step(s, W, h, tok, {"S": inp.k_swa[0], "F": inp.k_full[0]}, {}, int(inp.ctx_len[0]), 5)
+        lam = np.prod([L["layer_scalar"] for L in W.layers])
+        src = h if which == "h" else O.decode(w.target_embed[tok], s.dtype)
+        np.testing.assert_allclose(r.x_layers[-1], lam * src[:H], rtol=1e-12)
+
+
+def test_last_layer_scalar_cancels_in_final_norm():
+    shape, w, inp = _tiny_model()
+    s = O.Shape.of(shape)
+    def y_of(w_):
+        W = O.decode_weights(w_)
+        return O.drafter_step(s, W, O.decode(inp.hidden[1], s.dtype), int(inp.last_token[1]),
+                              {"S": inp.k_swa[1], "F": inp.k_full[1]}, {}, int(inp.ctx_len[1]), 7).y
+    y0 = y_of(w)
+    w.layers[-1]["layer_scalar"] *= 2.0
+    np.testing.assert_allclose(y_of(w), y0, rtol=1e-5, atol=1e-6)
+    w.layers[-1]["layer_scalar"] /= 2.0
+    w.layers[0]["layer_scalar"] *= 2.0
+    assert np.max(np.abs(y_of(w) - y0)) > 1e-3
+
+
+def test_draft_block_feeds_token_and_rounded_hidden_forward():
+    shape, w, inp = _tiny_model(dtype="bf16")
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    blk = O.draft_block(s, W, inp.hidden, inp.last_token, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, 3,
+                        keep_steps=True)
+    for b in range(2):
+        h = O.decode(inp.hidden[b], "bf16"); tok = int(inp.last_token[b])
+        for i in range(3):
+            r = O.drafter_step(s, W, h, tok, {"S": inp.k_swa[b], "F": inp.k_full[b]}, {},
+                               int(inp.ctx_len[b]), int(inp.pos[b]))
+            assert r.token == blk.tokens[b, i]
+            np.testing.assert_array_equal(r.hidden_out, blk.hidden_out[b, i])
+            h = O.round_bf16(r.hidden_out); tok = r.token
+    # the rounded hidden differs from the unrounded one (rounding really happens)
+    assert np.any(O.round_bf16(blk.hidden_out[0, 0]) != blk.hidden_out[0, 0])
+
+
+def test_ragged_padding_is_never_read():
+    # K padding is NaN: a NaN anywhere in the outputs would mean the padding was attended
+    shape, w, inp = _tiny_model(dtype="bf16")
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    assert np.any(np.isnan(O.decode(inp.k_full, "bf16")))
+    blk = O.draft_block(s, W, inp.hidden, inp.last_token, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, 2)
+    assert np.all(np.isfinite(blk.hidden_out))
+
+
+def _step_y(shape, w, inp, b=0):
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    return O.drafter_step(s, W, O.decode(inp.hidden[b], s.dtype), int(inp.last_token[b]),
+                          {"S": inp.k_swa[b], "F": inp.k_full[b]}, {}, int(inp.ctx_len[b]), 11)
+
+
+def test_norms_make_projection_scale_irrelevant():
+    # post-attention, post-FFN and q norms remove any positive scale (4: exact in fp32) of W_o, W_down, W_q and
+    # W_up (W_up enters the gated product linearly); W_gate enters through the GELU and is
+    # not scale-free. A dropped norm or swapped gate/up would break one of these.
+    from dataclasses import replace
+    shape, w, inp = _tiny_model(dtype="f32")
+    shape = replace(shape, rms_eps=0.0)        # exact scale invariance without eps
+    ref = _step_y(shape, w, inp)
+    for name, changes in (("o", False), ("down", False), ("q", False), ("up", False), ("gate", True)):
+        w2 = G.make_weights(shape, 0)
+        w2.layers[0][name] = (w2.layers[0][name] * 4.0).astype(np.float32)
+        r = _step_y(shape, w2, inp)
+        diff = np.max(np.abs(r.y - ref.y))
+        assert (diff > 1e-3) if changes else (diff < 1e-9), (name, diff)
+
+
+def test_layer_types_read_their_own_k_and_window():
+    shape, w, inp = _tiny_model(dtype="f32")
+    b = int(np.argmax(inp.ctx_len))
+    L = int(inp.ctx_len[b]); W_ = shape.window
+    assert L > W_
+    ref = _step_y(shape, w, inp, b)
+    k_swa = inp.k_swa.copy(); k_swa[b, :L - W_] += 5.0      # outside the sliding window
+    r = _step_y(shape, w, G.StepInputs(inp.hidden, inp.last_token, inp.ctx_len, inp.pos, k_swa, inp.k_full), b)
+    np.testing.assert_array_equal(r.y, ref.y)
+    k_full = inp.k_full.copy(); k_full[b, 0] += 5.0           # the full layer sees key 0
+    r = _step_y(shape, w, G.StepInputs(inp.hidden, inp.last_token, inp.ctx_len, inp.pos, inp.k_swa, k_full), b)
+    assert np.max(np.abs(r.y - ref.y)) > 1e-4
+    k_swa = inp.k_swa.copy(); k_swa[b, L - 1] += 5.0          # the sliding layer sees the newest key
+    r = _step_y(shape, w, G.StepInputs(inp.hidden, inp.last_token, inp.ctx_len, inp.pos, k_swa, inp.k_full), b)
+    assert np.max(np.abs(r.y - ref.y)) > 1e-4

@@ -11,11 +11,13 @@ one sequence at a time, in the order the pages describe the step.
 Precision contract shared with the CUDA path (the pages fix no precision):
   * stored tensors (weights, K, embeddings, hidden input, target logits) are bf16, except
     in fp32 shapes where everything is fp32;
-  * in bf16 shapes every vector that enters a projection (the concatenated input, the
-    normed attention input a, the query used in the attention dot, the attention output,
-    the normed FFN input, the gated product, and the final normed y) is rounded to bf16;
-    the rounding decision is taken on the fp32 value, as the kernels take it;
-  * the post-projected hidden state that feeds the next draft step is rounded to bf16;
+  * every activation stays in floating point wider than storage: fp64 here, fp32 in the
+    kernels; no activation is rounded to bf16 between operations, and the post-projected
+    hidden state carried to the next draft step is not rounded either. (Rounding every
+    projection input to bf16 makes the step discontinuous: a one-ulp change of a single
+    input element was measured to move the post-projected hidden state by 0.6 % and to
+    flip a later drafted token, so fp32-vs-fp64 accumulation differences would cascade
+    into whole-ulp differences.)
   * top-k and argmax decisions are taken on fp32 values (ties: lower centroid index,
     lower vocabulary id);
   * RoPE angles are formed in fp64.
@@ -65,23 +67,6 @@ def decode(arr: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return decode_bf16(arr)
     return np.asarray(arr, dtype=np.float32).astype(np.float64)
-
-
-def round_bf16(x: np.ndarray) -> np.ndarray:
-    """Round to bf16, nearest-even, taking the decision on the fp32 value; returns float64.
-
-    Used for every vector that enters a projection in bf16 shapes (precision contract).
-    """
-    f = np.asarray(x, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
-    return r.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
-def as_operand(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Operand of a projection: bf16-rounded in bf16 shapes, unchanged in fp32 shapes."""
-    return round_bf16(x) if dtype == "bf16" else np.asarray(x, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------------------
@@ -311,7 +296,7 @@ class HeadResult:
 
 
 def centroid_head(s: Shape, W: DecodedWeights, yb: np.ndarray) -> HeadResult:
-    """Centroid-clustered sparse LM head on one bf16-rounded normed hidden state.
+    """Centroid-clustered sparse LM head on one final-normed hidden state.
 
     Steps as in "Gemma 4 Assistant tensor inventory", section "Centroid / ordered embeddings
     LM head", steps 1-4, and "Gemma 4 Assistant 使用指南" section 五 (use_ordered_embeddings
@@ -358,7 +343,7 @@ class StepResult:
     hidden_out: np.ndarray          # post_projection output h' (fp64, [bb])
     head: HeadResult
     x_layers: List[np.ndarray]      # residual stream after each block
-    q: List[np.ndarray]             # attention query per block (after q_norm, RoPE, rounding)
+    q: List[np.ndarray]             # attention query per block (after q_norm and RoPE)
     o: List[np.ndarray]             # attention output per block [n_head][d]
     y: np.ndarray                   # final normed hidden (before rounding)
 
@@ -383,44 +368,43 @@ def drafter_step(s: Shape, W: DecodedWeights, h: np.ndarray, tok: int,
       3. y = output_norm(x); h' = post_projection(y) ("Tensor schema"; "Gemma 4 Assistant
          使用指南" section 六: last_hidden_state is post-projected).
       4. head on y (centroid or dense) -> greedy token.
+    Activations are fp64 throughout (no intermediate rounding).
     """
     dt = s.dtype
     u = np.concatenate([np.asarray(h, dtype=np.float64), W.target_row(tok)])
-    x = W.pre_proj @ as_operand(u, dt)
+    x = W.pre_proj @ u
     x_layers, qs, os_ = [], [], []
     for li, t in enumerate(s.layer_types):
         L = W.layers[li]
         d = s.head_dim(t)
-        a = as_operand(rms_norm(x, L["attn_norm"], s.rms_eps), dt)
+        a = rms_norm(x, L["attn_norm"], s.rms_eps)
         q = (L["q"] @ a).reshape(s.n_head, d)
         q = rms_norm(q, L["q_norm"], s.rms_eps)
         q = np.stack([rope(q[hh], pos, s.theta(t)) for hh in range(s.n_head)])
-        q = as_operand(q, dt)
         lo, hi = key_range(t, ctx_len, s.window)
         k = decode(k_by_type[t][lo:hi], dt)
         v = v_by_type.get(t)
         v = None if v is None else decode(v[lo:hi], dt)
         o = attention_q_only(q, k, v, s.scale(t))
-        attn = L["o"] @ as_operand(o.reshape(-1), dt)
+        attn = L["o"] @ o.reshape(-1)
         x = x + rms_norm(attn, L["post_attn_norm"], s.rms_eps)
-        f = as_operand(rms_norm(x, L["ffn_norm"], s.rms_eps), dt)
-        m = as_operand(gelu_tanh(L["gate"] @ f) * (L["up"] @ f), dt)
+        f = rms_norm(x, L["ffn_norm"], s.rms_eps)
+        m = gelu_tanh(L["gate"] @ f) * (L["up"] @ f)
         x = x + rms_norm(L["down"] @ m, L["post_ffn_norm"], s.rms_eps)
         x = x * L["layer_scalar"]
         x_layers.append(x.copy()); qs.append(q); os_.append(o)
     y = rms_norm(x, W.out_norm, s.rms_eps)
-    yb = as_operand(y, dt)
-    h_out = W.post_proj @ yb
-    head = centroid_head(s, W, yb) if s.use_ordered_embeddings else dense_head(s, W, yb)
+    h_out = W.post_proj @ y
+    head = centroid_head(s, W, y) if s.use_ordered_embeddings else dense_head(s, W, y)
     return StepResult(token=head.token, hidden_out=h_out, head=head, x_layers=x_layers,
                       q=qs, o=os_, y=y)
 
 
-def next_hidden(h_out: np.ndarray, dtype: str) -> np.ndarray:
-    """Hidden state fed to the next draft step: the post-projected output, stored in the
-    model's storage precision ("Gemma 4 drafter explained", "Target Activations": later
-    rounds use the drafter's own up-projected activations)."""
-    return round_bf16(h_out) if dtype == "bf16" else np.asarray(h_out, dtype=np.float32).astype(np.float64)
+def next_hidden(h_out: np.ndarray) -> np.ndarray:
+    """Hidden state fed to the next draft step: the post-projected output itself
+    ("Gemma 4 drafter explained", "Target Activations": later rounds use the drafter's own
+    up-projected activations), carried without rounding."""
+    return np.asarray(h_out, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------------------
@@ -475,7 +459,7 @@ def draft_block(s: Shape, W: DecodedWeights, hidden, last_token, k_swa, k_full, 
             if keep_steps:
                 row.append(r)
             tok = r.token
-            h = next_hidden(r.hidden_out, s.dtype)
+            h = next_hidden(r.hidden_out)
         steps.append(row)
     return BlockResult(tokens=toks, hidden_out=hout, logit_gap=lgap, kth_gap=kgap, selected=sel, steps=steps)
 

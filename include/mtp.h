@@ -1,0 +1,215 @@
+/*
+ * mtp.h -- C ABI of libmtp: the Gemma-4-assistant Multi-Token-Prediction drafter step,
+ * draft block and greedy verification on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers (cudaMalloc / torch CUDA tensors)
+ *     on the current device; the library borrows them and never frees them.
+ *   - Matrices are row-major [out][in]; "model dtype" means bf16 (MTP_DTYPE_BF16) or fp32
+ *     (MTP_DTYPE_F32) as fixed at init. Norm gains are always fp32.
+ *   - Device pointers must be 16-byte aligned; row strides are multiples of 16 bytes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls
+ *     only enqueue work on it and return; nothing synchronises except mtp_init_weights,
+ *     mtp_get_status and mtp_destroy.
+ *   - Return value: MTP_OK or an MTP_ERR_* code; on error nothing was enqueued and
+ *     mtp_last_error() describes the cause (per calling thread).
+ *
+ * Precision contract (both this library and its CPU oracle): stored tensors are bf16 (or
+ * fp32 for fp32 models), activations fp32, every vector entering a projection is rounded
+ * to bf16 (bf16 models), the post-projected hidden state fed to the next draft step is
+ * rounded to the model dtype, top-k / argmax decide on fp32 values with ties going to
+ * the lower centroid index / lower vocabulary id.
+ */
+#ifndef MTP_H_
+#define MTP_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MTP_API __attribute__((visibility("default")))
+#else
+#define MTP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MTP_MAX_LAYERS 8
+
+enum mtp_status {
+  MTP_OK = 0,
+  MTP_ERR_INVALID_ARG = 1,       /* NULL / out-of-range argument (missing hidden or KV included) */
+  MTP_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside what the kernels implement */
+  MTP_ERR_BAD_ORDERING = 3,      /* vocab % n_centroids != 0 or ordering not a permutation */
+  MTP_ERR_CUDA = 4,              /* a CUDA runtime call failed */
+  MTP_ERR_TIMEOUT = 5            /* a device-side wait gave up (reported by mtp_get_status) */
+};
+
+enum mtp_dtype { MTP_DTYPE_BF16 = 0, MTP_DTYPE_F32 = 1 };
+enum mtp_layer_kind { MTP_LAYER_SLIDING = 0, MTP_LAYER_FULL = 1 };
+
+/* Drafter hyper-parameters.
+ * Cited: "Gemma 4 Multi-Token Prediction (MTP) drafter", sections "Conversion" (metadata
+ * keys backbone_hidden_size, num_centroids, centroid_intermediate_top_k,
+ * use_ordered_embeddings) and "Tensor schema"; "Gemma 4 Assistant tensor inventory",
+ * "HF config highlights" (layer_types, attention_k_eq_v, vocab_size, hidden_size). */
+typedef struct mtp_config {
+  int32_t backbone;        /* target hidden size bb (pre_projection input is 2*bb) */
+  int32_t hidden;          /* assistant hidden size H */
+  int32_t n_layers;        /* 1..MTP_MAX_LAYERS */
+  int32_t n_head;          /* query heads */
+  int32_t head_dim_swa;    /* head dim of sliding layers (and of the sliding shared K) */
+  int32_t head_dim_full;   /* head dim of full layers (and of the full shared K) */
+  int32_t n_kv_head;       /* shared KV heads; n_head % n_kv_head == 0 */
+  int32_t ffn;             /* MLP intermediate size */
+  int32_t vocab;           /* V */
+  int32_t n_centroids;     /* C (ordered embeddings only) */
+  int32_t top_k;           /* selected centroids (ordered embeddings only), <= 64 */
+  int32_t window;          /* sliding window W (keys attended by sliding layers) */
+  int32_t use_ordered_embeddings; /* 1: centroid head; 0: dense tied head */
+  int32_t dtype;           /* enum mtp_dtype */
+  int32_t max_batch;       /* largest B any later call will pass (sizes the workspace) */
+  int32_t max_ctx;         /* largest shared-K length any later call will pass */
+  uint8_t layer_type[MTP_MAX_LAYERS]; /* enum mtp_layer_kind per block */
+  float rms_eps;           /* RMSNorm epsilon (1e-6) */
+  float attn_scale;        /* softmax scale; 0 -> 1/sqrt(head_dim) */
+  float rope_theta_swa;    /* RoPE base of sliding layers; 0 disables RoPE */
+  float rope_theta_full;   /* RoPE base of full layers; 0 disables RoPE */
+} mtp_config;
+
+/* Per-block tensors ("Tensor schema": attn_q, attn_q_norm, attn_output, attn_norm,
+ * post_attention_norm, ffn_norm, post_ffw_norm, ffn_gate/up/down, layer_output_scale).
+ * There are no K/V projections: the drafter is Q-only and reads the target's K. */
+typedef struct mtp_layer_weights {
+  const void *q;      /* device [n_head*d][H], model dtype */
+  const void *o;      /* device [H][n_head*d] */
+  const void *gate;   /* device [ffn][H] */
+  const void *up;     /* device [ffn][H] */
+  const void *down;   /* device [H][ffn] */
+  const float *q_norm;          /* device [d] */
+  const float *attn_norm;       /* device [H] */
+  const float *post_attn_norm;  /* device [H] */
+  const float *ffn_norm;        /* device [H] */
+  const float *post_ffn_norm;   /* device [H] */
+  float layer_scalar;           /* host value: multiplies the residual after the block */
+} mtp_layer_weights;
+
+typedef struct mtp_weights {
+  const void *pre_proj;     /* device [H][2*bb]  (input [target_hidden ; embed(token)]) */
+  const void *post_proj;    /* device [bb][H] */
+  const void *token_embd;   /* device [V][H]: tied LM head rows */
+  const void *centroids;    /* device [C][H] (ordered embeddings only, else NULL) */
+  const float *out_norm;    /* device [H] */
+  const int32_t *token_ordering; /* device [V] viewed [C][V/C]: centroid c owns ids
+                                    ordering[c*V/C .. (c+1)*V/C) (ordered only) */
+  mtp_layer_weights layer[MTP_MAX_LAYERS];
+} mtp_weights;
+
+/* Shared K of one attention type: the target's last layer of that type
+ * ("Gemma 4 Assistant 使用指南", section 二.4: shared_kv_states maps
+ * "full_attention" / "sliding_attention" to (key, value)).
+ * Element (b, t, kv_head, i) sits at k[b*stride_b + t*stride_t + kv_head*d + i].
+ * v == NULL means V = K (attention_k_eq_v: "Gemma 4 Assistant tensor inventory",
+ * "Notes for llama.cpp port" item 2); otherwise v has the same layout. ctx_len[b] >= 1 is the
+ * number of valid keys of sequence b (right-padded storage; padding is never read); values
+ * are clamped to [0, max_ctx] on the device, and a sequence with no keys attends nothing
+ * (its attention output is 0). */
+typedef struct mtp_kv {
+  const void *k;           /* device, model dtype */
+  const void *v;           /* device or NULL (V = K) */
+  const int32_t *ctx_len;  /* device [B] */
+  int64_t stride_b;        /* elements between sequences */
+  int64_t stride_t;        /* elements between tokens (>= n_kv_head*d, multiple of 8) */
+  int32_t max_ctx;         /* upper bound of ctx_len[*] (<= mtp_config.max_ctx) */
+} mtp_kv;
+
+typedef struct mtp_handle mtp_handle;
+
+/* Validate the configuration and the weights, check token_ordering, allocate the
+ * workspace for max_batch sequences, and return a handle.
+ * config/weights: host structs (copied). target_embed: device [V][bb] model dtype, the
+ * target's input embedding table that embed(last_token) reads ("Gemma 4 drafter
+ * explained", "Target Activations": the input table is shared with the target).
+ * Errors: INVALID_ARG (NULL pointer, bad field), UNSUPPORTED_SHAPE, BAD_ORDERING
+ * (vocab % n_centroids != 0 -- "Gemma 4 Assistant tensor inventory", "GGUF / converter
+ * layout" verification note -- or ordering not a permutation of 0..V-1), CUDA.
+ * Synchronises the current device. */
+MTP_API int mtp_init_weights(const mtp_config *config, const mtp_weights *weights,
+                     const void *target_embed, mtp_handle **out);
+
+/* Run a draft block: n_draft drafter steps for B independent sequences.
+ * Step 1 consumes hidden[b] (the target's last hidden state) and last_token[b]; step i+1
+ * consumes step i's greedy token and its post-projected hidden state rounded to the
+ * model dtype ("Gemma 4 Assistant 使用指南", section 二.3; "Gemma 4 drafter explained",
+ * "Target Activations"). Each step: pre_projection of [hidden ; embed(token)], every block
+ * (norm, Q projection, q_norm, RoPE at pos[b], attention over the shared K of the block's
+ * type -- sliding blocks attend the last `window` keys, full blocks all ctx_len[b] keys --,
+ * o projection, post-attention norm + residual, gated GELU-tanh MLP, post-FFN norm +
+ * residual, layer_scalar), output_norm, post_projection, and the LM head (centroid head:
+ * top_k centroids, gather of their token_ordering ids, sparse logits, argmax; or the
+ * dense tied head + argmax).
+ *   hidden      device [B][bb] model dtype
+ *   last_token  device [B] int32 in [0, V)
+ *   kv_sliding  host struct, required when any block is sliding (else may be NULL)
+ *   kv_full     host struct, required when any block is full (else may be NULL)
+ *   pos         device [B] int32: the constant position id of the block
+ *   out_tokens  device [B][n_draft] int32
+ *   out_hidden  device [B][n_draft][bb] fp32 post_projection output of every step, or NULL
+ * Errors: INVALID_ARG (NULL hidden / token / needed KV, B outside [1, max_batch],
+ * n_draft < 1, bad stride), UNSUPPORTED_SHAPE, CUDA. */
+MTP_API int mtp_draft_block(mtp_handle *h, const void *hidden, const int32_t *last_token,
+                    const mtp_kv *kv_sliding, const mtp_kv *kv_full, const int32_t *pos,
+                    int32_t B, int32_t n_draft, int32_t *out_tokens, float *out_hidden,
+                    void *stream);
+
+/* LM head on given final-normed hidden states (testing / sampling entry point).
+ * Centroid head ("Gemma 4 Assistant tensor inventory", "Centroid / ordered embeddings LM
+ * head", steps 1-5): centroid logits, top_k centroids, gather of their ids, sparse logits,
+ * and -- when out_logits != NULL -- the full row filled with -1e30f with the sparse logits
+ * scattered at their ids. Dense head (use_ordered_embeddings == 0): all V logits.
+ *   y             device [B][H] fp32 (rounded to bf16 inside for bf16 models)
+ *   out_logits    device [B][V] fp32 or NULL
+ *   out_token     device [B] int32 (argmax, lowest id on ties)
+ *   out_centroids device [B][top_k] int32 selected centroids, best first (ties: lower
+ *                 index first), or NULL; must be NULL for the dense head
+ * Errors: INVALID_ARG, CUDA. */
+MTP_API int mtp_centroid_head(mtp_handle *h, const float *y, int32_t B, float *out_logits,
+                      int32_t *out_token, int32_t *out_centroids, void *stream);
+
+/* Greedy accept-prefix verification ("Gemma 4 drafter explained", "What is Speculative
+ * Decoding?"): t_i = argmax of target row i (lowest id on ties); accept_len[b] = the
+ * largest m with draft[b][i] == t_i for all i < m; out_tokens[b] = draft[b][0..m) followed
+ * by t_m (the target's correction, or its extra token when m == n), then -1 padding.
+ * Rows after the first disagreement are not read.
+ *   target_logits device [B][n+1][V] bf16
+ *   draft         device [B][n] int32
+ *   accept_len    device [B] int32
+ *   out_tokens    device [B][n+1] int32
+ * Errors: INVALID_ARG (NULL, B < 1, n < 0, V < 1, V % 8 != 0), CUDA. */
+MTP_API int mtp_verify_greedy(const void *target_logits, const int32_t *draft, int32_t B, int32_t n,
+                      int32_t V, int32_t *accept_len, int32_t *out_tokens, void *stream);
+
+/* Synchronise the device and return the handle's device-side status word: MTP_OK,
+ * MTP_ERR_TIMEOUT when a bounded device wait of a previous call gave up, or
+ * MTP_ERR_INVALID_ARG when a device-resident input was out of range (a last_token outside
+ * [0, V): embedding row 0 was read instead). The word is cleared by this call. Also reports
+ * a pending CUDA error as MTP_ERR_CUDA. */
+MTP_API int mtp_get_status(mtp_handle *h);
+
+/* Select the implementation of mtp_draft_block: 0 = automatic, 1 = one kernel per phase,
+ * 2 = persistent whole-block kernel (when the shape supports it). For tests and
+ * benchmarks; results agree within the precision contract. Errors: INVALID_ARG. */
+MTP_API int mtp_set_path(mtp_handle *h, int32_t path);
+
+/* Free the workspace and the handle (synchronises). NULL is ignored. */
+MTP_API void mtp_destroy(mtp_handle *h);
+
+/* Text of the last error raised on the calling thread ("" when none). */
+MTP_API const char *mtp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_H_ */

@@ -1,0 +1,514 @@
+// C ABI of libmtp (include/mtp.h): argument validation, workspace ownership and dispatch
+// to the drafter-step kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "mtp.h"
+#include "mtp_launch.h"
+#include "mtp_phases.cuh"
+
+struct mtp_handle {
+  mtp_config cfg;
+  mtp_weights w;
+  const void* target_embed;
+  int device;
+  int num_sms;
+  int path;
+  int dmax;
+  int nsplit_max;
+  void* ws;
+  size_t ws_bytes;
+  mtp::WsP wsp;
+};
+
+namespace mtp {
+
+static thread_local char g_err[1024] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+}  // namespace mtp
+
+using mtp::set_error;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_fail(const char* what, cudaError_t e) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return MTP_ERR_CUDA;
+}
+
+bool has_type(const mtp_config& c, int t) {
+  for (int l = 0; l < c.n_layers; ++l)
+    if (c.layer_type[l] == t) return true;
+  return false;
+}
+
+int validate_config(const mtp_config& c) {
+  if (c.n_layers < 1 || c.n_layers > MTP_MAX_LAYERS) {
+    set_error("n_layers=%d outside [1, %d]", c.n_layers, MTP_MAX_LAYERS);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (c.dtype != MTP_DTYPE_BF16 && c.dtype != MTP_DTYPE_F32) {
+    set_error("dtype=%d is neither BF16 nor F32", c.dtype);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (c.backbone <= 0 || c.hidden <= 0 || c.n_head <= 0 || c.n_kv_head <= 0 || c.ffn <= 0 || c.vocab <= 0 ||
+      c.max_batch <= 0 || c.max_ctx <= 0) {
+    set_error("non-positive size in config");
+    return MTP_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < c.n_layers; ++l)
+    if (c.layer_type[l] > 1) {
+      set_error("layer_type[%d]=%d is neither sliding (0) nor full (1)", l, c.layer_type[l]);
+      return MTP_ERR_INVALID_ARG;
+    }
+  if (!(c.rms_eps >= 0.f) || !(c.attn_scale >= 0.f) || !(c.rope_theta_swa >= 0.f) || !(c.rope_theta_full >= 0.f)) {
+    set_error("rms_eps, attn_scale and rope thetas must be >= 0");
+    return MTP_ERR_INVALID_ARG;
+  }
+  const int vec = c.dtype == MTP_DTYPE_BF16 ? 8 : 4;
+  if (c.hidden % vec || c.backbone % vec || c.ffn % vec) {
+    set_error("hidden, backbone and ffn must be multiples of %d", vec);
+    return MTP_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (c.n_head % c.n_kv_head) {
+    set_error("n_head=%d is not a multiple of n_kv_head=%d", c.n_head, c.n_kv_head);
+    return MTP_ERR_UNSUPPORTED_SHAPE;
+  }
+  const int hpg = c.n_head / c.n_kv_head;
+  for (int t = 0; t < 2; ++t) {
+    if (!has_type(c, t)) continue;
+    const int d = t ? c.head_dim_full : c.head_dim_swa;
+    const bool d_ok = d == 32 || d == 64 || d == 128 || d == 256 || d == 512;
+    const bool h_ok = hpg == 1 || hpg == 2 || hpg == 4 || (hpg == 8 && d <= 256);
+    if (!d_ok || !h_ok) {
+      set_error("attention shape head_dim=%d, heads per KV head=%d not supported", d, hpg);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  if (has_type(c, 0) && c.window < 1) {
+    set_error("sliding layers need window >= 1 (got %d)", c.window);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (c.use_ordered_embeddings) {
+    if (c.n_centroids <= 0 || c.top_k <= 0 || c.top_k > 64 || c.top_k > c.n_centroids || c.n_centroids > 8192) {
+      set_error("centroid head needs 0 < top_k <= min(64, n_centroids), n_centroids <= 8192");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (c.vocab % c.n_centroids) {
+      set_error("vocab=%d is not a multiple of n_centroids=%d", c.vocab, c.n_centroids);
+      return MTP_ERR_BAD_ORDERING;
+    }
+  } else {
+    if (c.hidden % (32 * vec)) {
+      set_error("dense head needs hidden to be a multiple of %d", 32 * vec);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  return MTP_OK;
+}
+
+int validate_weights(const mtp_config& c, const mtp_weights& w, const void* target_embed) {
+  const void* mats[] = {w.pre_proj, w.post_proj, w.token_embd, w.out_norm, target_embed};
+  for (const void* m : mats)
+    if (!m || !aligned16(m)) {
+      set_error("pre_proj, post_proj, token_embd, out_norm and target_embed must be non-NULL, 16-byte aligned");
+      return MTP_ERR_INVALID_ARG;
+    }
+  if (c.use_ordered_embeddings && (!w.centroids || !aligned16(w.centroids) || !w.token_ordering)) {
+    set_error("centroid head needs centroids (16-byte aligned) and token_ordering");
+    return MTP_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = w.layer[l];
+    const void* ptrs[] = {L.q, L.o, L.gate, L.up, L.down, L.q_norm, L.attn_norm, L.post_attn_norm, L.ffn_norm,
+                          L.post_ffn_norm};
+    for (const void* p : ptrs)
+      if (!p || !aligned16(p)) {
+        set_error("layer %d: weight pointer NULL or not 16-byte aligned", l);
+        return MTP_ERR_INVALID_ARG;
+      }
+  }
+  return MTP_OK;
+}
+
+int check_ordering(const mtp_config& c, const int32_t* ord) {
+  std::vector<int32_t> h(c.vocab);
+  cudaError_t e = cudaMemcpy(h.data(), ord, sizeof(int32_t) * c.vocab, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("reading token_ordering", e);
+  std::vector<unsigned char> seen(c.vocab, 0);
+  for (int i = 0; i < c.vocab; ++i) {
+    const int32_t v = h[i];
+    if (v < 0 || v >= c.vocab || seen[v]) {
+      set_error("token_ordering is not a permutation of 0..%d (entry %d = %d)", c.vocab - 1, i, v);
+      return MTP_ERR_BAD_ORDERING;
+    }
+    seen[v] = 1;
+  }
+  return MTP_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Carves the workspace out of one allocation (sizes for max_batch sequences).
+size_t layout_ws(mtp_handle* h, char* base) {
+  const mtp_config& c = h->cfg;
+  const size_t B = c.max_batch, H = c.hidden, bb = c.backbone, F = c.ffn;
+  const size_t nh = c.n_head, dmax = h->dmax, ns = h->nsplit_max;
+  const size_t C = c.use_ordered_embeddings ? c.n_centroids : 1, k = c.use_ordered_embeddings ? c.top_k : 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + off : nullptr;
+    off = align256(off + bytes);
+    return static_cast<void*>(p);
+  };
+  mtp::WsP& w = h->wsp;
+  w.x[0] = static_cast<float*>(take(4 * B * H));
+  w.x[1] = static_cast<float*>(take(4 * B * H));
+  w.qraw = static_cast<float*>(take(4 * B * nh * dmax));
+  w.part_ml = static_cast<float*>(take(4 * B * nh * ns * 2));
+  w.part_acc = static_cast<float*>(take(4 * B * nh * ns * dmax));
+  w.o = static_cast<float*>(take(4 * B * nh * dmax));
+  w.ao = static_cast<float*>(take(4 * B * H));
+  w.gate = static_cast<float*>(take(4 * B * F));
+  w.up = static_cast<float*>(take(4 * B * F));
+  w.dn = static_cast<float*>(take(4 * B * H));
+  w.y = static_cast<float*>(take(4 * B * H));
+  w.h_cur = static_cast<float*>(take(4 * B * bb));
+  w.cl = static_cast<float*>(take(4 * B * C));
+  w.sel = static_cast<int*>(take(4 * B * k));
+  w.best = static_cast<unsigned long long*>(take(8 * B));
+  w.cs = static_cast<float2*>(take(8 * B * 2 * (dmax / 2)));
+  w.bar = static_cast<unsigned int*>(take(16));
+  w.status = static_cast<int*>(take(16));
+  w.nsplit_max = static_cast<int>(ns);
+  w.dmax = static_cast<int>(dmax);
+  return off;
+}
+
+// Splits of the shared-K range per attention item so that the attention phase has about
+// 2 items per SM, with at least 32 keys per split.
+int choose_nsplit(int B, int nkv, int keys, int num_sms, int cap) {
+  const int target = 2 * num_sms;
+  int ns = (target + B * nkv - 1) / (B * nkv);
+  const int by_len = (keys + 31) / 32;
+  if (ns > by_len) ns = by_len;
+  if (ns > cap) ns = cap;
+  return ns < 1 ? 1 : ns;
+}
+
+// Upper bound of the keys one sequence attends in a layer of type t.
+int attended_keys(const mtp_config& c, const mtp_kv* kv, int t) {
+  if (!kv) return 1;
+  return t == 0 && c.window < kv->max_ctx ? c.window : kv->max_ctx;
+}
+
+int check_kv(const mtp_config& c, const mtp_kv* kv, int t, int max_ctx, const char* name) {
+  if (!kv || !kv->k || !kv->ctx_len) {
+    set_error("%s shared K is required (a %s layer exists) and must have k and ctx_len", name, name);
+    return MTP_ERR_INVALID_ARG;
+  }
+  const int d = t ? c.head_dim_full : c.head_dim_swa;
+  const int vec = c.dtype == MTP_DTYPE_BF16 ? 8 : 4;
+  if (!aligned16(kv->k) || (kv->v && !aligned16(kv->v)) || kv->stride_t < static_cast<int64_t>(c.n_kv_head) * d ||
+      kv->stride_t % vec || kv->stride_b % vec || kv->stride_b < 0) {
+    set_error("%s K/V: pointers must be 16-byte aligned, stride_t >= n_kv_head*head_dim and strides multiples of %d",
+              name, vec);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (kv->max_ctx < 1 || kv->max_ctx > max_ctx) {
+    set_error("%s max_ctx=%d outside [1, %d]", name, kv->max_ctx, max_ctx);
+    return MTP_ERR_INVALID_ARG;
+  }
+  return MTP_OK;
+}
+
+mtp::Params base_params(const mtp_handle* h, int B) {
+  const mtp_config& c = h->cfg;
+  mtp::Params p;
+  memset(&p, 0, sizeof(p));
+  mtp::ShapeP& s = p.s;
+  s.B = B;
+  s.bb = c.backbone;
+  s.H = c.hidden;
+  s.nl = c.n_layers;
+  s.nh = c.n_head;
+  s.nkv = c.n_kv_head;
+  s.F = c.ffn;
+  s.V = c.vocab;
+  s.ordered = c.use_ordered_embeddings ? 1 : 0;
+  s.C = s.ordered ? c.n_centroids : 0;
+  s.topk = s.ordered ? c.top_k : 0;
+  s.vsc = s.ordered ? c.vocab / c.n_centroids : 0;
+  s.W = c.window;
+  s.d[0] = c.head_dim_swa;
+  s.d[1] = c.head_dim_full;
+  for (int t = 0; t < 2; ++t) {
+    const int d = s.d[t] > 0 ? s.d[t] : 1;
+    s.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
+  }
+  s.theta[0] = c.rope_theta_swa;
+  s.theta[1] = c.rope_theta_full;
+  s.eps = c.rms_eps;
+  p.w = h->wsp;
+  p.pre = h->w.pre_proj;
+  p.post = h->w.post_proj;
+  p.temb = h->w.token_embd;
+  p.cent = h->w.centroids;
+  p.tgt = h->target_embed;
+  p.out_norm = h->w.out_norm;
+  p.ord = h->w.token_ordering;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    mtp::LayerP& P = p.L[l];
+    P.q = L.q;
+    P.o = L.o;
+    P.gate = L.gate;
+    P.up = L.up;
+    P.down = L.down;
+    P.q_norm = L.q_norm;
+    P.attn_norm = L.attn_norm;
+    P.post_attn_norm = L.post_attn_norm;
+    P.ffn_norm = L.ffn_norm;
+    P.post_ffn_norm = L.post_ffn_norm;
+    P.lambda = L.layer_scalar;
+    P.type = c.layer_type[l];
+  }
+  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  return p;
+}
+
+int set_device(const mtp_handle* h) {
+  cudaError_t e = cudaSetDevice(h->device);
+  return e == cudaSuccess ? MTP_OK : cuda_fail("cudaSetDevice", e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mtp_last_error(void) { return mtp::g_err; }
+
+int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const void* target_embed, mtp_handle** out) {
+  mtp::g_err[0] = 0;
+  if (!config || !weights || !out) {
+    set_error("config, weights and out must be non-NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  int rc = validate_config(*config);
+  if (rc) return rc;
+  rc = validate_weights(*config, *weights, target_embed);
+  if (rc) return rc;
+  mtp_handle* h = static_cast<mtp_handle*>(calloc(1, sizeof(mtp_handle)));
+  if (!h) {
+    set_error("out of host memory");
+    return MTP_ERR_INVALID_ARG;
+  }
+  h->cfg = *config;
+  h->w = *weights;
+  h->target_embed = target_embed;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    free(h);
+    return cuda_fail("querying the device", e);
+  }
+  if (config->use_ordered_embeddings) {
+    rc = check_ordering(*config, weights->token_ordering);
+    if (rc) {
+      free(h);
+      return rc;
+    }
+  }
+  int dmax = 2;
+  for (int l = 0; l < config->n_layers; ++l) {
+    const int d = config->layer_type[l] ? config->head_dim_full : config->head_dim_swa;
+    dmax = d > dmax ? d : dmax;
+  }
+  h->dmax = dmax;
+  int ns = (config->max_ctx + 31) / 32;
+  if (ns > 4 * h->num_sms) ns = 4 * h->num_sms;
+  h->nsplit_max = ns < 1 ? 1 : ns;
+  h->ws_bytes = layout_ws(h, nullptr);
+  e = cudaMalloc(&h->ws, h->ws_bytes);
+  if (e != cudaSuccess) {
+    free(h);
+    return cuda_fail("allocating the workspace", e);
+  }
+  layout_ws(h, static_cast<char*>(h->ws));
+  e = cudaMemset(h->ws, 0, h->ws_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->ws);
+    free(h);
+    return cuda_fail("clearing the workspace", e);
+  }
+  *out = h;
+  return MTP_OK;
+}
+
+int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token, const mtp_kv* kv_sliding,
+                    const mtp_kv* kv_full, const int32_t* pos, int32_t B, int32_t n_draft, int32_t* out_tokens,
+                    float* out_hidden, void* stream) {
+  mtp::g_err[0] = 0;
+  if (!h) {
+    set_error("handle is NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  const mtp_config& c = h->cfg;
+  if (!hidden || !last_token || !pos || !out_tokens) {
+    set_error("hidden, last_token, pos and out_tokens must be non-NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (!aligned16(hidden)) {
+    set_error("hidden must be 16-byte aligned");
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (B < 1 || B > c.max_batch) {
+    set_error("B=%d outside [1, max_batch=%d]", B, c.max_batch);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (n_draft < 1 || n_draft > 1024) {
+    set_error("n_draft=%d outside [1, 1024]", n_draft);
+    return MTP_ERR_INVALID_ARG;
+  }
+  int rc;
+  if (has_type(c, 0) && (rc = check_kv(c, kv_sliding, 0, c.max_ctx, "sliding"))) return rc;
+  if (has_type(c, 1) && (rc = check_kv(c, kv_full, 1, c.max_ctx, "full"))) return rc;
+  if ((rc = set_device(h))) return rc;
+  mtp::Params p = base_params(h, B);
+  p.hidden_in = hidden;
+  p.tok_in = last_token;
+  p.pos = pos;
+  p.out_tokens = out_tokens;
+  p.out_hidden = out_hidden;
+  p.n_draft = n_draft;
+  const mtp_kv* kvs[2] = {kv_sliding, kv_full};
+  for (int t = 0; t < 2; ++t) {
+    if (!has_type(c, t)) continue;
+    p.kv[t].k = kvs[t]->k;
+    p.kv[t].v = kvs[t]->v;
+    p.kv[t].ctx_len = kvs[t]->ctx_len;
+    p.kv[t].sb = kvs[t]->stride_b;
+    p.kv[t].st = kvs[t]->stride_t;
+    p.kv[t].max_ctx = kvs[t]->max_ctx;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = c.dtype == MTP_DTYPE_BF16;
+  int path = h->path;
+  int ncta = h->num_sms;
+  if (path != 1) {
+    p.s.ncta_hint = ncta;
+    for (int t = 0; t < 2; ++t)
+      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), ncta / 2,
+                                                     h->nsplit_max) : 1;
+    const int cap = bf16 ? mtp::persistent_capacity_bf16(p, h->num_sms) : mtp::persistent_capacity_f32(p, h->num_sms);
+    if (cap >= ncta) {
+      return bf16 ? mtp::run_persistent_bf16(p, st) : mtp::run_persistent_f32(p, st);
+    }
+    if (path == 2) {
+      set_error("persistent draft-block kernel cannot be co-resident for this shape");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+  }
+  p.s.ncta_hint = 2 * h->num_sms;
+  for (int t = 0; t < 2; ++t)
+    p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), h->num_sms,
+                                                   h->nsplit_max) : 1;
+  return bf16 ? mtp::run_phases_bf16(p, st) : mtp::run_phases_f32(p, st);
+}
+
+int mtp_centroid_head(mtp_handle* h, const float* y, int32_t B, float* out_logits, int32_t* out_token,
+                      int32_t* out_centroids, void* stream) {
+  mtp::g_err[0] = 0;
+  if (!h || !y || !out_token) {
+    set_error("handle, y and out_token must be non-NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  const mtp_config& c = h->cfg;
+  if (B < 1 || B > c.max_batch) {
+    set_error("B=%d outside [1, max_batch=%d]", B, c.max_batch);
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (!c.use_ordered_embeddings && out_centroids) {
+    set_error("out_centroids must be NULL for the dense head");
+    return MTP_ERR_INVALID_ARG;
+  }
+  int rc;
+  if ((rc = set_device(h))) return rc;
+  mtp::Params p = base_params(h, B);
+  p.s.ncta_hint = 2 * h->num_sms;
+  p.y_in = y;
+  p.out_logits = out_logits;
+  p.out_tokens = out_token;
+  p.out_centroids = out_centroids;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return c.dtype == MTP_DTYPE_BF16 ? mtp::run_head_bf16(p, st) : mtp::run_head_f32(p, st);
+}
+
+int mtp_verify_greedy(const void* target_logits, const int32_t* draft, int32_t B, int32_t n, int32_t V,
+                      int32_t* accept_len, int32_t* out_tokens, void* stream) {
+  mtp::g_err[0] = 0;
+  if (!target_logits || !accept_len || !out_tokens || (n > 0 && !draft)) {
+    set_error("target_logits, draft (n > 0), accept_len and out_tokens must be non-NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (B < 1 || n < 0 || V < 1 || V % 8 || !aligned16(target_logits)) {
+    set_error("need B >= 1, n >= 0, V >= 1 with V %% 8 == 0 and 16-byte aligned logits (B=%d n=%d V=%d)", B, n, V);
+    return MTP_ERR_INVALID_ARG;
+  }
+  return mtp::run_verify(target_logits, draft, B, n, V, accept_len, out_tokens, static_cast<cudaStream_t>(stream));
+}
+
+int mtp_get_status(mtp_handle* h) {
+  mtp::g_err[0] = 0;
+  if (!h) {
+    set_error("handle is NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  int rc;
+  if ((rc = set_device(h))) return rc;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("device synchronisation", e);
+  int status = 0;
+  e = cudaMemcpy(&status, h->wsp.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail("reading the status word", e);
+  if (status != 0) {
+    e = cudaMemset(h->wsp.status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail("clearing the status word", e);
+    set_error("a device-side wait timed out (status %d)", status);
+  }
+  return status;
+}
+
+int mtp_set_path(mtp_handle* h, int32_t path) {
+  mtp::g_err[0] = 0;
+  if (!h || path < 0 || path > 2) {
+    set_error("need a handle and path in {0, 1, 2}");
+    return MTP_ERR_INVALID_ARG;
+  }
+  h->path = path;
+  return MTP_OK;
+}
+
+void mtp_destroy(mtp_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->ws);
+  free(h);
+}
+
+}  // extern "C"

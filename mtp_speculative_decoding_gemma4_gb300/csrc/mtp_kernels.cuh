@@ -1,0 +1,334 @@
+// Kernels of the drafter step (one launch per phase, or one persistent launch for the
+// whole draft block) and their host-side launchers, templated on the model dtype.
+#pragma once
+
+#include <cstdio>
+
+#include "mtp_launch.h"
+#include "mtp_phases.cuh"
+
+namespace mtp {
+
+// ---------------------------------------------------------------- grid barrier
+
+__device__ inline unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the persistent kernel: a monotone arrival counter (bar[0]) that
+// every CTA bumps once per barrier, and an abort word (bar[1]). Waits are bounded: after
+// spin_limit cycles the waiting CTA records MTP_ERR_TIMEOUT and raises the abort word, and
+// every CTA that sees the abort word returns. Returns false when the kernel must stop.
+__device__ inline bool grid_sync(const Params& p, unsigned int& epoch) {
+  __shared__ int ok;
+  __syncthreads();
+  ++epoch;
+  if (threadIdx.x == 0) {
+    const unsigned int target = epoch * gridDim.x;
+    __threadfence();
+    atomicAdd(p.w.bar, 1u);
+    const long long t0 = clock64();
+    int good = 1;
+    while (ld_acquire_u32(p.w.bar) < target) {
+      if (ld_acquire_u32(p.w.bar + 1) != 0u) { good = 0; break; }
+      if (clock64() - t0 > p.spin_limit) {
+        atomicExch(p.w.status, static_cast<int>(MTP_ERR_TIMEOUT));
+        atomicExch(p.w.bar + 1, 1u);
+        good = 0;
+        break;
+      }
+    }
+    __threadfence();
+    ok = good;
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+// ---------------------------------------------------------------- per-phase kernels
+
+#define MTP_KERNEL_PROLOGUE extern __shared__ __align__(16) char smem[];
+
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_rope(Params p) { phase_rope(p, blockIdx.x, gridDim.x); }
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_pre(Params p, int step, int par) {
+  MTP_KERNEL_PROLOGUE phase_pre<WT>(p, step, par, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_q(Params p, int l, int par) {
+  MTP_KERNEL_PROLOGUE phase_q<WT>(p, l, par, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_att(Params p, int l) {
+  MTP_KERNEL_PROLOGUE phase_att<WT>(p, l, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_cmb(Params p, int l) {
+  MTP_KERNEL_PROLOGUE phase_cmb<WT>(p, l, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_o(Params p, int l) {
+  MTP_KERNEL_PROLOGUE phase_o<WT>(p, l, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_gu(Params p, int l, int par) {
+  MTP_KERNEL_PROLOGUE phase_gu<WT>(p, l, par, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_dn(Params p, int l) {
+  MTP_KERNEL_PROLOGUE phase_dn<WT>(p, l, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_head1(Params p, int step, int par) {
+  MTP_KERNEL_PROLOGUE phase_head1<WT>(p, step, par, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_head_entry(Params p) {
+  MTP_KERNEL_PROLOGUE phase_head_entry<WT>(p, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_topk(Params p) {
+  MTP_KERNEL_PROLOGUE phase_topk<WT>(p, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_gather(Params p) {
+  MTP_KERNEL_PROLOGUE phase_gather<WT>(p, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_dense(Params p) {
+  MTP_KERNEL_PROLOGUE phase_dense<WT>(p, blockIdx.x, gridDim.x, smem);
+}
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_fin(Params p, int stride, int col) {
+  phase_fin(p, stride, col, blockIdx.x, gridDim.x);
+}
+
+// Fill of the materialised logits row (-1e30 everywhere before the sparse scatter).
+template <typename WT>
+__global__ void __launch_bounds__(kThreads) k_fill(float* out, long long n, float v) {
+  for (long long i = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * kThreads)
+    out[i] = v;
+}
+
+// ---------------------------------------------------------------- persistent draft block
+
+template <typename WT>
+__global__ void __launch_bounds__(kThreads, 1) k_block(Params p) {
+  MTP_KERNEL_PROLOGUE
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  unsigned int epoch = 0;
+  phase_rope(p, cta, ncta);
+  int par = 0;
+  for (int s = 0; s < p.n_draft; ++s) {
+    phase_pre<WT>(p, s, par, cta, ncta, smem);
+    if (!grid_sync(p, epoch)) return;
+    for (int l = 0; l < p.s.nl; ++l) {
+      phase_q<WT>(p, l, par, cta, ncta, smem);
+      if (l > 0) par ^= 1;
+      if (!grid_sync(p, epoch)) return;
+      phase_att<WT>(p, l, cta, ncta, smem);
+      if (!grid_sync(p, epoch)) return;
+      phase_cmb<WT>(p, l, cta, ncta, smem);
+      if (!grid_sync(p, epoch)) return;
+      phase_o<WT>(p, l, cta, ncta, smem);
+      if (!grid_sync(p, epoch)) return;
+      phase_gu<WT>(p, l, par, cta, ncta, smem);
+      par ^= 1;
+      if (!grid_sync(p, epoch)) return;
+      phase_dn<WT>(p, l, cta, ncta, smem);
+      if (!grid_sync(p, epoch)) return;
+    }
+    phase_head1<WT>(p, s, par, cta, ncta, smem);
+    if (!grid_sync(p, epoch)) return;
+    if (p.s.ordered) {
+      phase_topk<WT>(p, cta, ncta, smem);
+      if (!grid_sync(p, epoch)) return;
+      phase_gather<WT>(p, cta, ncta, smem);
+    } else {
+      phase_dense<WT>(p, cta, ncta, smem);
+    }
+    if (!grid_sync(p, epoch)) return;
+  }
+  phase_fin(p, p.n_draft, p.n_draft - 1, cta, ncta);
+}
+
+// ---------------------------------------------------------------- host: sizes
+
+struct PhaseSizes {
+  int pre, q[kMaxLayers], att[kMaxLayers], cmb[kMaxLayers], o, gu, dn, head1, head_entry, topk, gather, dense;
+  int smem_pre, smem_q, smem_att, smem_o[2], smem_gu, smem_dn, smem_head1, smem_topk, smem_gather, smem_dense;
+  int smem_max;
+};
+
+inline int att_smem_for(const ShapeP& s, int t) { return att_smem_bytes(s.d[t], s.nh / s.nkv); }
+
+template <typename WT>
+PhaseSizes phase_sizes(const Params& p) {
+  const ShapeP& s = p.s;
+  PhaseSizes z{};
+  const int nh = s.ncta_hint;
+  z.pre = gemv_items(s.H, s.B, 2 * s.bb, nh);
+  z.dn = gemv_items(s.H, s.B, s.F, nh);
+  {
+    const int ng = ceil_div(s.B, gemv_group(s.B, s.H));
+    const int ks = choose_ks(2 * s.F, ng, nh);
+    z.gu = ng * 2 * ceil_div(s.F, kWarps / ks);
+    const int rows = s.bb + (s.ordered ? s.C : 0);
+    const int ks2 = choose_ks(rows, ng, nh);
+    z.head1 = ng * (ceil_div(s.bb, kWarps / ks2) + (s.ordered ? ceil_div(s.C, kWarps / ks2) : 0));
+    z.head_entry = s.ordered ? gemv_items(s.C, s.B, s.H, nh) : ng;
+  }
+  for (int l = 0; l < s.nl; ++l) {
+    const int t = p.L[l].type, d = s.d[t];
+    z.q[l] = gemv_items(s.nh * d, s.B, s.H, nh);
+    z.att[l] = s.B * s.nkv * s.nsplit[t];
+    z.cmb[l] = s.B * s.nh * ceil_div(d, kCmbDims);
+  }
+  z.o = 0;
+  z.topk = s.B;
+  z.gather = s.ordered ? s.B * ceil_div(s.topk * s.vsc, kGatherPerItem) : 0;
+  z.dense = s.ordered ? 0 : ceil_div(s.B, kDenseBG) * ceil_div(s.V, kDenseRowsPerItem);
+  auto gs = [&](int K) { return gemv_smem(K, gemv_group(s.B, K), s.H).total; };
+  z.smem_pre = gs(2 * s.bb);
+  z.smem_q = gs(s.H);
+  z.smem_o[0] = gs(s.nh * s.d[0]);
+  z.smem_o[1] = gs(s.nh * s.d[1]);
+  z.smem_gu = gs(s.H);
+  z.smem_dn = gs(s.F);
+  z.smem_head1 = gs(s.H);
+  int att = 0;
+  for (int l = 0; l < s.nl; ++l) {
+    const int a = att_smem_for(s, p.L[l].type);
+    att = a > att ? a : att;
+  }
+  z.smem_att = att;
+  int n2 = 1;
+  while (n2 < s.C) n2 <<= 1;
+  z.smem_topk = s.ordered ? n2 * 8 : 0;
+  z.smem_gather = (s.H + 2) * 4 + kWarps * 8 + 16;
+  z.smem_dense = s.ordered ? 0 : kDenseBG * s.H * 4 + kWarps * 32 * 8;
+  const int cmb = 2 * (kThreads / kCmbDims) * kCmbDims * 4;
+  int m = cmb;
+  const int all[] = {z.smem_pre, z.smem_q, z.smem_o[0], z.smem_o[1], z.smem_gu, z.smem_dn, z.smem_head1,
+                     z.smem_att, z.smem_topk, z.smem_gather, z.smem_dense};
+  for (int v : all) m = v > m ? v : m;
+  z.smem_max = m;
+  return z;
+}
+
+// Items of the O phase of layer l (input width depends on the layer's head dim).
+inline int o_items(const Params& p, int l) {
+  const ShapeP& s = p.s;
+  return gemv_items(s.H, s.B, s.nh * s.d[p.L[l].type], s.ncta_hint);
+}
+
+#define MTP_CHECK_LAUNCH(what)                                                          \
+  do {                                                                                  \
+    cudaError_t e_ = cudaGetLastError();                                                \
+    if (e_ != cudaSuccess) {                                                            \
+      set_error("%s launch failed: %s", what, cudaGetErrorString(e_));                  \
+      return MTP_ERR_CUDA;                                                              \
+    }                                                                                   \
+  } while (0)
+
+template <typename K>
+inline int allow_smem(K kernel, int bytes) {
+  if (bytes > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+      set_error("cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
+      return MTP_ERR_CUDA;
+    }
+  }
+  return MTP_OK;
+}
+
+#define MTP_LAUNCH(kernel, grid, smem_bytes, ...)                                       \
+  do {                                                                                  \
+    if ((grid) > 0) {                                                                   \
+      int rc_ = allow_smem(kernel, smem_bytes);                                         \
+      if (rc_) return rc_;                                                              \
+      kernel<<<(grid), kThreads, (smem_bytes), st>>>(__VA_ARGS__);                      \
+      MTP_CHECK_LAUNCH(#kernel);                                                        \
+    }                                                                                   \
+  } while (0)
+
+// One launch per phase.
+template <typename WT>
+int run_phases(const Params& p, cudaStream_t st) {
+  const PhaseSizes z = phase_sizes<WT>(p);
+  const ShapeP& s = p.s;
+  MTP_LAUNCH(k_rope<WT>, s.B, 0, p);
+  int par = 0;
+  for (int step = 0; step < p.n_draft; ++step) {
+    MTP_LAUNCH(k_pre<WT>, z.pre, z.smem_pre, p, step, par);
+    for (int l = 0; l < s.nl; ++l) {
+      const int t = p.L[l].type;
+      MTP_LAUNCH(k_q<WT>, z.q[l], z.smem_q, p, l, par);
+      if (l > 0) par ^= 1;
+      MTP_LAUNCH(k_att<WT>, z.att[l], att_smem_for(s, t), p, l);
+      MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
+      MTP_LAUNCH(k_o<WT>, o_items(p, l), z.smem_o[t], p, l);
+      MTP_LAUNCH(k_gu<WT>, z.gu, z.smem_gu, p, l, par);
+      par ^= 1;
+      MTP_LAUNCH(k_dn<WT>, z.dn, z.smem_dn, p, l);
+    }
+    MTP_LAUNCH(k_head1<WT>, z.head1, z.smem_head1, p, step, par);
+    if (s.ordered) {
+      MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
+      MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+    } else {
+      MTP_LAUNCH(k_dense<WT>, z.dense, z.smem_dense, p);
+    }
+  }
+  MTP_LAUNCH(k_fin<WT>, 1, 0, p, p.n_draft, p.n_draft - 1);
+  return MTP_OK;
+}
+
+// One cooperative persistent launch for the whole block.
+template <typename WT>
+int run_persistent(const Params& p, cudaStream_t st) {
+  const PhaseSizes z = phase_sizes<WT>(p);
+  int rc = allow_smem(k_block<WT>, z.smem_max);
+  if (rc) return rc;
+  cudaError_t e = cudaMemsetAsync(p.w.bar, 0, 2 * sizeof(unsigned int), st);
+  if (e != cudaSuccess) {
+    set_error("cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  Params pp = p;
+  void* args[] = {&pp};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_block<WT>), dim3(p.s.ncta_hint), dim3(kThreads), args,
+                                  static_cast<size_t>(z.smem_max), st);
+  if (e != cudaSuccess) {
+    set_error("persistent draft-block launch (%d CTAs, %d B smem): %s", p.s.ncta_hint, z.smem_max,
+              cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+// Largest co-resident grid of the persistent kernel (0 when it cannot be resident).
+template <typename WT>
+int persistent_capacity(const Params& p, int num_sms) {
+  const PhaseSizes z = phase_sizes<WT>(p);
+  if (allow_smem(k_block<WT>, z.smem_max)) return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_block<WT>, kThreads, z.smem_max) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per_sm * num_sms;
+}
+
+template <typename WT>
+int run_head(const Params& p, cudaStream_t st) {
+  const PhaseSizes z = phase_sizes<WT>(p);
+  const ShapeP& s = p.s;
+  if (p.out_logits && s.ordered) {
+    const long long n = static_cast<long long>(s.B) * s.V;
+    k_fill<WT><<<1024, kThreads, 0, st>>>(p.out_logits, n, -1e30f);
+    MTP_CHECK_LAUNCH("k_fill");
+  }
+  MTP_LAUNCH(k_head_entry<WT>, z.head_entry, z.smem_head1, p);
+  if (s.ordered) {
+    MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
+    MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+  } else {
+    MTP_LAUNCH(k_dense<WT>, z.dense, z.smem_dense, p);
+  }
+  MTP_LAUNCH(k_fin<WT>, 1, 0, p, 1, 0);
+  return MTP_OK;
+}
+
+}  // namespace mtp

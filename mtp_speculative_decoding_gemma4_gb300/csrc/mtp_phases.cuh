@@ -1,0 +1,837 @@
+// Phases of one drafter step, as device functions that loop over work items
+// (item = cta; item < n_items; item += ncta). The same code runs as one kernel launch per
+// phase (ncta = number of items) or inside the persistent draft-block kernel with a grid
+// barrier between phases.
+//
+// Step structure (Gemma 4 Multi-Token Prediction (MTP) drafter, "What it is" and "Tensor
+// schema"; Gemma 4 Assistant tensor inventory, "Centroid / ordered embeddings LM head"):
+//   PRE    x = W_pre [h ; embed(tok)]                      (staging gathers the embed row)
+//   per block l:
+//     Q    a = norm(x); q = W_q a                          (staging applies the previous
+//                                                           block's post-FFN residual)
+//     ATT  split-KV partial softmax of each head over the shared K (V = K)
+//     CMB  combine the splits -> o (attention output)
+//     O    W_o o
+//     GU   x += norm(W_o o); f = norm(x); gate, up = W_gate f, W_up f
+//     DN   m = gelu_tanh(gate) * up; W_down m
+//   HEAD1  x = lambda (x + norm(W_down m)); y = output_norm(x);
+//          h' = W_post y (output + the hidden of the next step); centroid logits
+// Weights, K and embeddings are read in the model dtype; every activation is fp32 and
+// is never rounded to a narrower type.
+//   TOPK   top_k centroids per sequence
+//   GATHER sparse logits over the selected clusters' token_ordering ids + argmax
+//   DENSE  (dense tied head) logits over all rows of token_embd + argmax
+#pragma once
+
+#include "mtp_common.cuh"
+#include "mtp.h"
+
+namespace mtp {
+
+constexpr int kMaxLayers = 8;
+constexpr int kBG = 8;          // largest GEMV batch group
+constexpr int kGemvInBudget = 96 * 1024;  // shared-memory bytes for a batch group's inputs
+constexpr int kDenseBG = 32;    // sequences per dense-head batch group
+constexpr int kGatherPerItem = 32;
+constexpr int kDenseRowsPerItem = 256;
+constexpr int kCmbDims = 64;    // head dims per combine item
+
+struct LayerP {
+  const void *q, *o, *gate, *up, *down;
+  const float *q_norm, *attn_norm, *post_attn_norm, *ffn_norm, *post_ffn_norm;
+  float lambda;
+  int type;  // 0 sliding, 1 full
+};
+
+struct KvP {
+  const void* k;
+  const void* v;
+  const int* ctx_len;
+  long long sb, st;
+  int max_ctx;
+};
+
+struct ShapeP {
+  int B, bb, H, nl, nh, nkv, F, V, C, topk, vsc, W, ordered;
+  int d[2];
+  int nsplit[2];
+  float scale[2];
+  float theta[2];
+  float eps;
+  int ncta_hint;  // CTA count the work decomposition is sized for
+};
+
+struct WsP {
+  float* x[2];                 // [B][H] residual stream, ping-pong
+  float* qraw;                 // [B][nh*dmax]
+  float* part_ml;              // [B][nh][nsplit_max][2]
+  float* part_acc;             // [B][nh][nsplit_max][dmax]
+  float* o;                    // [B][nh*dmax] attention output
+  float* ao;                   // [B][H]
+  float* gate;                 // [B][F]
+  float* up;                   // [B][F]
+  float* dn;                   // [B][H]
+  float* y;                    // [B][H] final normed hidden state
+  float* h_cur;                // [B][bb] hidden state of the next draft step
+  float* cl;                   // [B][C]
+  int* sel;                    // [B][topk]
+  unsigned long long* best;    // [B]
+  float2* cs;                  // [B][2][dmax/2] RoPE (cos, sin)
+  unsigned int* bar;           // grid barrier counter
+  int* status;                 // device status word (0 = ok)
+  int nsplit_max, dmax;
+};
+
+struct Params {
+  ShapeP s;
+  WsP w;
+  const void *pre, *post, *temb, *cent, *tgt;
+  const float* out_norm;
+  const int* ord;
+  LayerP L[kMaxLayers];
+  KvP kv[2];
+  const void* hidden_in;
+  const int* tok_in;
+  const int* pos;
+  int* out_tokens;     // [B][n_draft] (draft block) or [B] (head entry)
+  float* out_hidden;   // [B][n_draft][bb] or null
+  int n_draft;
+  const float* y_in;   // head entry: [B][H]
+  float* out_logits;   // head entry: [B][V] or null
+  int* out_centroids;  // head entry: [B][topk] or null
+  long long spin_limit;  // bounded grid-barrier wait (clock64 cycles)
+};
+
+// ---------------------------------------------------------------- GEMV machinery
+
+struct GemvJob {
+  const void* W;
+  int R, K, ks;          // rows, columns, warps splitting K
+  float* out;            // result [b*ldo + r] (may be null)
+  long long ldo;
+  float* out2;           // second copy [b*ld2 + r] (may be null)
+  long long ld2;
+};
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Sequences staged together by a GEMV phase whose input vectors have K_in elements.
+__host__ __device__ inline int gemv_group(int B, int K_in) {
+  int g = kGemvInBudget / (K_in * 4);
+  g = g < 1 ? 1 : g;
+  g = g < kBG ? g : kBG;
+  return g < B ? g : B;
+}
+
+// Warps per row so that the phase has about ncta_hint items.
+__host__ __device__ inline int choose_ks(int R, int ngroups, int ncta_hint) {
+  int ks = 1;
+  while (ks < kWarps && ceil_div(R * ks, kWarps) * ngroups < ncta_hint) ks *= 2;
+  return ks;
+}
+
+__host__ __device__ inline int gemv_tiles(const GemvJob& j) { return ceil_div(j.R, kWarps / j.ks); }
+
+// V consecutive fp32 values from shared memory.
+template <int V>
+__device__ inline void load_fvec(const float* p, float* out) {
+#pragma unroll
+  for (int i = 0; i < V; i += 4) {
+    const float4 f = *reinterpret_cast<const float4*>(p + i);
+    out[i] = f.x; out[i + 1] = f.y; out[i + 2] = f.z; out[i + 3] = f.w;
+  }
+}
+
+template <typename WT>
+__device__ inline void gemv_tile(const GemvJob& j, int tile, const float* in_s, int ld_in, int b0, int nb,
+                                 float* red) {
+  constexpr int V = Elem<WT>::kVec;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rpt = kWarps / j.ks;
+  const int roff = warp / j.ks, kp = warp % j.ks;
+  const int r = tile * rpt + roff;
+  const int seg = ceil_div(ceil_div(j.K, j.ks), V) * V;
+  const int k0 = kp * seg, k1 = min(j.K, k0 + seg);
+  float acc[kBG];
+#pragma unroll
+  for (int b = 0; b < kBG; ++b) acc[b] = 0.f;
+  if (r < j.R) {
+    const WT* wr = static_cast<const WT*>(j.W) + static_cast<size_t>(r) * j.K;
+    for (int k = k0 + lane * V; k < k1; k += 32 * V) {
+      float w[V];
+      load_vec_stream(wr + k, w);
+#pragma unroll
+      for (int b = 0; b < kBG; ++b) {
+        if (b < nb) {
+          float xv[V];
+          load_fvec<V>(in_s + b * ld_in + k, xv);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[b] = fmaf(w[v], xv[v], acc[b]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < kBG; ++b) acc[b] = warp_sum(acc[b]);
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < kBG; ++b) red[warp * kBG + b] = acc[b];
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < rpt * nb; t += kThreads) {
+    const int ro = t / nb, b = t % nb;
+    const int row = tile * rpt + ro;
+    if (row < j.R) {
+      float s = 0.f;
+      for (int q = 0; q < j.ks; ++q) s += red[(ro * j.ks + q) * kBG + b];
+      if (j.out) j.out[(b0 + b) * j.ldo + row] = s;
+      if (j.out2) j.out2[(b0 + b) * j.ld2 + row] = s;
+    }
+  }
+  __syncthreads();
+}
+
+// Shared-memory layout of a GEMV phase: fp32 inputs [nbg][K_in], reduction scratch
+// [kWarps][kBG] floats, staging scratch [2][H] floats (residual vectors).
+struct GemvSmem {
+  int in_bytes, red_off, scr_off, total;
+};
+__host__ __device__ inline GemvSmem gemv_smem(int K_in, int nbg, int max_vec) {
+  GemvSmem g;
+  g.in_bytes = ((nbg * K_in * 4 + 15) / 16) * 16;
+  g.red_off = g.in_bytes;
+  g.scr_off = g.red_off + kWarps * kBG * 4;
+  g.total = g.scr_off + 2 * max_vec * 4 + 64;
+  return g;
+}
+
+// Runs the GEMV jobs of one phase. `stage(b0, nb, in_s, scr, red, writer)` fills the
+// inputs of a batch group; `writer` is true in exactly one CTA per group.
+template <typename WT, typename Stage>
+__device__ void gemv_phase(const Params& p, const GemvJob* jobs, int njobs, int K_in, Stage stage,
+                           int cta, int ncta, char* smem) {
+  const int nbg = gemv_group(p.s.B, K_in);
+  const GemvSmem L = gemv_smem(K_in, nbg, p.s.H);
+  float* in_s = reinterpret_cast<float*>(smem);
+  float* red = reinterpret_cast<float*>(smem + L.red_off);
+  float* scr = reinterpret_cast<float*>(smem + L.scr_off);
+  const int ngroups = ceil_div(p.s.B, nbg);
+  int tiles = 0;
+  for (int q = 0; q < njobs; ++q) tiles += gemv_tiles(jobs[q]);
+  const int n_items = ngroups * tiles;
+  int staged = -1;
+  for (int item = cta; item < n_items; item += ncta) {
+    const int g = item / tiles;
+    int t = item % tiles;
+    const int b0 = g * nbg, nb = min(nbg, p.s.B - b0);
+    if (g != staged) {
+      __syncthreads();
+      stage(b0, nb, in_s, K_in, scr, red, t == 0);
+      __syncthreads();
+      staged = g;
+    }
+    int q = 0;
+    while (t >= gemv_tiles(jobs[q])) { t -= gemv_tiles(jobs[q]); ++q; }
+    gemv_tile<WT>(jobs[q], t, in_s, K_in, b0, nb, red);
+  }
+}
+
+// ---------------------------------------------------------------- staging helpers
+
+// Residual update used by the post-attention / post-FFN sandwich norms:
+// xs = lambda * (x + norm(v) * g). `xs` and `v_s` are shared-memory fp32 vectors.
+__device__ inline void residual_update(float* xs, const float* x, float* v_s, const float* v,
+                                       const float* g, float lambda, int n, float eps, float* red) {
+  for (int i = threadIdx.x; i < n; i += kThreads) v_s[i] = v[i];
+  __syncthreads();
+  const float r = rms_factor(v_s, n, eps, red);
+  for (int i = threadIdx.x; i < n; i += kThreads) xs[i] = lambda * (x[i] + v_s[i] * r * g[i]);
+  __syncthreads();
+}
+
+// dst = xs * rms_factor(xs) * g (projection input; stays fp32).
+__device__ inline void norm_to_input(float* dst, const float* xs, const float* g, int n, float eps, float* red) {
+  const float r = rms_factor(xs, n, eps, red);
+  for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = xs[i] * r * g[i];
+}
+
+// n values of type T (multiple of the 16-byte vector) -> fp32 in shared memory.
+template <typename T>
+__device__ inline void load_to_f32(float* dst, const T* src, int n) {
+  constexpr int V = Elem<T>::kVec;
+  for (int i = threadIdx.x * V; i < n; i += kThreads * V) {
+    float v[V];
+    load_vec(src + i, v);
+#pragma unroll
+    for (int e = 0; e < V; ++e) dst[i + e] = v[e];
+  }
+}
+
+// ---------------------------------------------------------------- PRE
+
+template <typename WT>
+__device__ void phase_pre(const Params& p, int step, int par, int cta, int ncta, char* smem) {
+  const int bb = p.s.bb;
+  GemvJob j{p.pre, p.s.H, 2 * bb, choose_ks(p.s.H, ceil_div(p.s.B, gemv_group(p.s.B, 2 * bb)), p.s.ncta_hint),
+            p.w.x[par], p.s.H, nullptr, 0};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float*, float*, bool writer) {
+    for (int b = 0; b < nb; ++b) {
+      const int bi = b0 + b;
+      int tok = step == 0 ? p.tok_in[bi] : key_id(p.w.best[bi]);
+      if (writer && step > 0 && threadIdx.x == 0) p.out_tokens[bi * p.n_draft + step - 1] = tok;
+      if (tok < 0 || tok >= p.s.V) {  // an out-of-range caller token reads row 0 and is reported
+        if (writer && threadIdx.x == 0) atomicExch(p.w.status, static_cast<int>(MTP_ERR_INVALID_ARG));
+        tok = 0;
+      }
+      if (step == 0)
+        load_to_f32<WT>(in_s + b * ld, static_cast<const WT*>(p.hidden_in) + static_cast<size_t>(bi) * bb, bb);
+      else
+        load_to_f32<float>(in_s + b * ld, p.w.h_cur + static_cast<size_t>(bi) * bb, bb);
+      load_to_f32<WT>(in_s + b * ld + bb, static_cast<const WT*>(p.tgt) + static_cast<size_t>(tok) * bb, bb);
+    }
+  };
+  gemv_phase<WT>(p, &j, 1, 2 * bb, stage, cta, ncta, smem);
+}
+
+// ---------------------------------------------------------------- Q
+
+template <typename WT>
+__device__ void phase_q(const Params& p, int l, int par, int cta, int ncta, char* smem) {
+  const LayerP& L = p.L[l];
+  const int d = p.s.d[L.type], H = p.s.H;
+  GemvJob j{L.q, p.s.nh * d, H, choose_ks(p.s.nh * d, ceil_div(p.s.B, gemv_group(p.s.B, H)), p.s.ncta_hint),
+            p.w.qraw, static_cast<long long>(p.s.nh) * p.w.dmax, nullptr, 0};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float* scr, float* red, bool writer) {
+    float* xs = scr;
+    float* vs = scr + p.s.H;
+    for (int b = 0; b < nb; ++b) {
+      const int bi = b0 + b;
+      const float* x = p.w.x[par] + static_cast<size_t>(bi) * H;
+      if (l == 0) {
+        for (int i = threadIdx.x; i < H; i += kThreads) xs[i] = x[i];
+        __syncthreads();
+        if (writer && threadIdx.x == 0) p.w.best[bi] = 0ull;
+      } else {
+        const LayerP& P = p.L[l - 1];
+        residual_update(xs, x, vs, p.w.dn + static_cast<size_t>(bi) * H, P.post_ffn_norm, P.lambda, H,
+                        p.s.eps, red);
+        if (writer)
+          for (int i = threadIdx.x; i < H; i += kThreads) p.w.x[par ^ 1][static_cast<size_t>(bi) * H + i] = xs[i];
+      }
+      norm_to_input(in_s + b * ld, xs, L.attn_norm, H, p.s.eps, red);
+      __syncthreads();
+    }
+  };
+  gemv_phase<WT>(p, &j, 1, H, stage, cta, ncta, smem);
+}
+
+// ---------------------------------------------------------------- ATT
+
+// Loads EPL consecutive elements (a lane's share of a head vector) as fp32.
+template <typename WT, int EPL>
+__device__ inline void load_part(const WT* ptr, float* out) {
+  constexpr int V = Elem<WT>::kVec;
+  if constexpr (EPL % V == 0) {
+#pragma unroll
+    for (int i = 0; i < EPL; i += V) load_vec_stream(ptr + i, out + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) out[i] = Elem<WT>::to_f(ptr[i]);
+  }
+}
+
+// Attention partials for one (sequence, KV head, split) item. The query heads of the KV
+// group read the same K rows; V = K unless a separate V is given.
+template <typename WT, int D, int HPG>
+__device__ void att_item(const Params& p, int l, int b, int g, int c, char* smem) {
+  constexpr int EPL = D / 32;
+  const LayerP& L = p.L[l];
+  const int t = L.type;
+  const KvP& kv = p.kv[t];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* q_s = reinterpret_cast<float*>(smem);            // [HPG][D]
+  float* red = q_s + HPG * D;                              // [kWarps]
+  float* mls = red + kWarps;                               // [kWarps][HPG][2]
+  float* accs = mls + kWarps * HPG * 2;                    // [kWarps][HPG][D]
+
+  // q heads of this group: q_norm, then RoPE at the constant position.
+  const int half = D / 2;
+  for (int hh = 0; hh < HPG; ++hh) {
+    const int h = g * HPG + hh;
+    const float* qr = p.w.qraw + static_cast<size_t>(b) * p.s.nh * p.w.dmax + static_cast<size_t>(h) * D;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < D; i += kThreads) ss += qr[i] * qr[i];
+    ss = block_sum(ss, red);
+    const float rf = rsqrtf(ss / D + p.s.eps);
+    const float2* cs = p.w.cs + (static_cast<size_t>(b) * 2 + t) * (p.w.dmax / 2);
+    for (int i = threadIdx.x; i < half; i += kThreads) {
+      const float a = qr[i] * rf * L.q_norm[i];
+      const float bq = qr[i + half] * rf * L.q_norm[i + half];
+      const float2 e = cs[i];
+      q_s[hh * D + i] = a * e.x - bq * e.y;
+      q_s[hh * D + i + half] = bq * e.x + a * e.y;
+    }
+  }
+  __syncthreads();
+
+  const int Lb = min(max(kv.ctx_len[b], 0), kv.max_ctx);  // never read past the buffer
+  const int lo = t == 0 ? max(0, Lb - p.s.W) : 0, hi = Lb;
+  const int nsp = p.s.nsplit[t];
+  const int chunk = ceil_div(max(hi - lo, 0), nsp);
+  const int j0 = lo + c * chunk, j1 = min(hi, j0 + chunk);
+  const float scale = p.s.scale[t];
+
+  float qv[HPG][EPL], acc[HPG][EPL], m[HPG], lsum[HPG];
+#pragma unroll
+  for (int hh = 0; hh < HPG; ++hh) {
+    m[hh] = -INFINITY;
+    lsum[hh] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      qv[hh][e] = q_s[hh * D + lane * EPL + e];
+      acc[hh][e] = 0.f;
+    }
+  }
+  const WT* kb = static_cast<const WT*>(kv.k) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D + lane * EPL;
+  const WT* vb = kv.v ? static_cast<const WT*>(kv.v) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D + lane * EPL
+                      : nullptr;
+  for (int j = j0 + warp; j < j1; j += kWarps) {
+    float kf[EPL];
+    load_part<WT, EPL>(kb + static_cast<size_t>(j) * kv.st, kf);
+    float vf[EPL];
+    if (vb) load_part<WT, EPL>(vb + static_cast<size_t>(j) * kv.st, vf);
+#pragma unroll
+    for (int hh = 0; hh < HPG; ++hh) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) s = fmaf(qv[hh][e], kf[e], s);
+      s = warp_sum(s) * scale;
+      const float mn = fmaxf(m[hh], s);
+      const float corr = expf(m[hh] - mn);
+      const float pw = expf(s - mn);
+      lsum[hh] = lsum[hh] * corr + pw;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[hh][e] = acc[hh][e] * corr + pw * (vb ? vf[e] : kf[e]);
+      m[hh] = mn;
+    }
+  }
+  // merge the warps of this CTA
+#pragma unroll
+  for (int hh = 0; hh < HPG; ++hh) {
+    if (lane == 0) {
+      mls[(warp * HPG + hh) * 2] = m[hh];
+      mls[(warp * HPG + hh) * 2 + 1] = lsum[hh];
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) accs[(warp * HPG + hh) * D + lane * EPL + e] = acc[hh][e];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < HPG * D; idx += kThreads) {
+    const int hh = idx / D, i = idx % D;
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mls[(w * HPG + hh) * 2]);
+    float a = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = expf(mls[(w * HPG + hh) * 2] - M);
+        a += f * accs[(w * HPG + hh) * D + i];
+        den += f * mls[(w * HPG + hh) * 2 + 1];
+      }
+    }
+    const int h = g * HPG + hh;
+    const size_t slot = (static_cast<size_t>(b) * p.s.nh + h) * p.w.nsplit_max + c;
+    p.w.part_acc[slot * p.w.dmax + i] = a;
+    if (i == 0) {
+      p.w.part_ml[slot * 2] = M;
+      p.w.part_ml[slot * 2 + 1] = den;
+    }
+  }
+  __syncthreads();
+}
+
+__host__ __device__ inline int att_smem_bytes(int D, int HPG) {
+  return (HPG * D + kWarps + kWarps * HPG * 2 + kWarps * HPG * D) * 4;
+}
+
+template <typename WT, int D, int HPG>
+__device__ void att_phase_t(const Params& p, int l, int cta, int ncta, char* smem) {
+  const int t = p.L[l].type;
+  const int nsp = p.s.nsplit[t];
+  const int n_items = p.s.B * p.s.nkv * nsp;
+  for (int item = cta; item < n_items; item += ncta) {
+    const int c = item % nsp;
+    const int g = (item / nsp) % p.s.nkv;
+    const int b = item / (nsp * p.s.nkv);
+    att_item<WT, D, HPG>(p, l, b, g, c, smem);
+  }
+}
+
+template <typename WT>
+__device__ void phase_att(const Params& p, int l, int cta, int ncta, char* smem) {
+  const int D = p.s.d[p.L[l].type];
+  const int hpg = p.s.nh / p.s.nkv;
+#define MTP_ATT_CASE(DD, HH) \
+  if (D == DD && hpg == HH) { att_phase_t<WT, DD, HH>(p, l, cta, ncta, smem); return; }
+  MTP_ATT_CASE(32, 1) MTP_ATT_CASE(32, 2) MTP_ATT_CASE(32, 4) MTP_ATT_CASE(32, 8)
+  MTP_ATT_CASE(64, 1) MTP_ATT_CASE(64, 2) MTP_ATT_CASE(64, 4) MTP_ATT_CASE(64, 8)
+  MTP_ATT_CASE(128, 1) MTP_ATT_CASE(128, 2) MTP_ATT_CASE(128, 4) MTP_ATT_CASE(128, 8)
+  MTP_ATT_CASE(256, 1) MTP_ATT_CASE(256, 2) MTP_ATT_CASE(256, 4) MTP_ATT_CASE(256, 8)
+  MTP_ATT_CASE(512, 1) MTP_ATT_CASE(512, 2) MTP_ATT_CASE(512, 4)
+#undef MTP_ATT_CASE
+}
+
+// ---------------------------------------------------------------- CMB
+
+template <typename WT>
+__device__ void phase_cmb(const Params& p, int l, int cta, int ncta, char* smem) {
+  const int t = p.L[l].type;
+  const int D = p.s.d[t], nsp = p.s.nsplit[t];
+  const int ndc = ceil_div(D, kCmbDims);
+  const int n_items = p.s.B * p.s.nh * ndc;
+  constexpr int kGroups = kThreads / kCmbDims;
+  float* sm = reinterpret_cast<float*>(smem);        // [kGroups][kCmbDims] num, then den
+  for (int item = cta; item < n_items; item += ncta) {
+    const int dc = item % ndc;
+    const int h = (item / ndc) % p.s.nh;
+    const int b = item / (ndc * p.s.nh);
+    const size_t base = (static_cast<size_t>(b) * p.s.nh + h) * p.w.nsplit_max;
+    float M = -INFINITY;
+    for (int c = 0; c < nsp; ++c) M = fmaxf(M, p.w.part_ml[(base + c) * 2]);
+    const int i = dc * kCmbDims + (threadIdx.x % kCmbDims);
+    const int grp = threadIdx.x / kCmbDims;
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY && i < D) {
+      for (int c = grp; c < nsp; c += kGroups) {
+        const float f = expf(p.w.part_ml[(base + c) * 2] - M);
+        num += f * p.w.part_acc[(base + c) * p.w.dmax + i];
+        den += f * p.w.part_ml[(base + c) * 2 + 1];
+      }
+    }
+    sm[grp * kCmbDims + (threadIdx.x % kCmbDims)] = num;
+    sm[(kGroups + grp) * kCmbDims + (threadIdx.x % kCmbDims)] = den;
+    __syncthreads();
+    if (grp == 0 && i < D) {
+      float n = 0.f, dd = 0.f;
+      for (int q = 0; q < kGroups; ++q) {
+        n += sm[q * kCmbDims + threadIdx.x];
+        dd += sm[(kGroups + q) * kCmbDims + threadIdx.x];
+      }
+      const float o = dd > 0.f ? n / dd : 0.f;
+      p.w.o[(static_cast<size_t>(b) * p.s.nh + h) * D + i] = o;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- O
+
+template <typename WT>
+__device__ void phase_o(const Params& p, int l, int cta, int ncta, char* smem) {
+  const LayerP& L = p.L[l];
+  const int K = p.s.nh * p.s.d[L.type];
+  GemvJob j{L.o, p.s.H, K, choose_ks(p.s.H, ceil_div(p.s.B, gemv_group(p.s.B, K)), p.s.ncta_hint), p.w.ao,
+            p.s.H, nullptr, 0};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float*, float*, bool) {
+    for (int b = 0; b < nb; ++b) load_to_f32<float>(in_s + b * ld, p.w.o + static_cast<size_t>(b0 + b) * K, K);
+  };
+  gemv_phase<WT>(p, &j, 1, K, stage, cta, ncta, smem);
+}
+
+// ---------------------------------------------------------------- GU
+
+template <typename WT>
+__device__ void phase_gu(const Params& p, int l, int par, int cta, int ncta, char* smem) {
+  const LayerP& L = p.L[l];
+  const int H = p.s.H, F = p.s.F;
+  const int ks = choose_ks(2 * F, ceil_div(p.s.B, gemv_group(p.s.B, H)), p.s.ncta_hint);
+  GemvJob j[2] = {{L.gate, F, H, ks, p.w.gate, F, nullptr, 0}, {L.up, F, H, ks, p.w.up, F, nullptr, 0}};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float* scr, float* red, bool writer) {
+    float* xs = scr;
+    float* vs = scr + p.s.H;
+    for (int b = 0; b < nb; ++b) {
+      const int bi = b0 + b;
+      residual_update(xs, p.w.x[par] + static_cast<size_t>(bi) * H, vs, p.w.ao + static_cast<size_t>(bi) * H,
+                      L.post_attn_norm, 1.0f, H, p.s.eps, red);
+      if (writer)
+        for (int i = threadIdx.x; i < H; i += kThreads) p.w.x[par ^ 1][static_cast<size_t>(bi) * H + i] = xs[i];
+      norm_to_input(in_s + b * ld, xs, L.ffn_norm, H, p.s.eps, red);
+      __syncthreads();
+    }
+  };
+  gemv_phase<WT>(p, j, 2, H, stage, cta, ncta, smem);
+}
+
+// ---------------------------------------------------------------- DN
+
+template <typename WT>
+__device__ void phase_dn(const Params& p, int l, int cta, int ncta, char* smem) {
+  const LayerP& L = p.L[l];
+  const int H = p.s.H, F = p.s.F;
+  GemvJob j{L.down, H, F, choose_ks(H, ceil_div(p.s.B, gemv_group(p.s.B, F)), p.s.ncta_hint), p.w.dn, H, nullptr,
+            0};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float*, float*, bool) {
+    for (int b = 0; b < nb; ++b) {
+      const float* gt = p.w.gate + static_cast<size_t>(b0 + b) * F;
+      const float* up = p.w.up + static_cast<size_t>(b0 + b) * F;
+      for (int i = threadIdx.x; i < F; i += kThreads) in_s[b * ld + i] = gelu_tanh(gt[i]) * up[i];
+    }
+  };
+  gemv_phase<WT>(p, &j, 1, F, stage, cta, ncta, smem);
+}
+
+// ---------------------------------------------------------------- HEAD1
+
+template <typename WT>
+__device__ void phase_head1(const Params& p, int step, int par, int cta, int ncta, char* smem) {
+  const int H = p.s.H, bb = p.s.bb;
+  const int ngroups = ceil_div(p.s.B, gemv_group(p.s.B, H));
+  const int rows = bb + (p.s.ordered ? p.s.C : 0);
+  const int ks = choose_ks(rows, ngroups, p.s.ncta_hint);
+  float* hout = p.out_hidden ? p.out_hidden + static_cast<size_t>(step) * bb : nullptr;
+  const long long ldo = static_cast<long long>(p.n_draft) * bb;
+  GemvJob j[2] = {{p.post, bb, H, ks, hout, ldo, p.w.h_cur, bb}, {p.cent, p.s.C, H, ks, p.w.cl, p.s.C, nullptr, 0}};
+  const LayerP& P = p.L[p.s.nl - 1];
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float* scr, float* red, bool writer) {
+    float* xs = scr;
+    float* vs = scr + p.s.H;
+    for (int b = 0; b < nb; ++b) {
+      const int bi = b0 + b;
+      residual_update(xs, p.w.x[par] + static_cast<size_t>(bi) * H, vs, p.w.dn + static_cast<size_t>(bi) * H,
+                      P.post_ffn_norm, P.lambda, H, p.s.eps, red);
+      norm_to_input(in_s + b * ld, xs, p.out_norm, H, p.s.eps, red);
+      __syncthreads();
+      if (writer)
+        for (int i = threadIdx.x; i < H; i += kThreads) p.w.y[static_cast<size_t>(bi) * H + i] = in_s[b * ld + i];
+    }
+  };
+  gemv_phase<WT>(p, j, p.s.ordered ? 2 : 1, H, stage, cta, ncta, smem);
+}
+
+// Head entry point: y given by the caller; only the centroid logits are computed here.
+template <typename WT>
+__device__ void phase_head_entry(const Params& p, int cta, int ncta, char* smem) {
+  const int H = p.s.H;
+  const int nbg = gemv_group(p.s.B, H);
+  const int ngroups = ceil_div(p.s.B, nbg);
+  GemvJob j{p.cent, p.s.C, H, choose_ks(p.s.C, ngroups, p.s.ncta_hint), p.w.cl, p.s.C, nullptr, 0};
+  auto stage = [&](int b0, int nb, float* in_s, int ld, float*, float*, bool writer) {
+    for (int b = 0; b < nb; ++b) {
+      const int bi = b0 + b;
+      for (int i = threadIdx.x; i < H; i += kThreads) {
+        const float v = p.y_in[static_cast<size_t>(bi) * H + i];
+        in_s[b * ld + i] = v;
+        if (writer) p.w.y[static_cast<size_t>(bi) * H + i] = v;
+      }
+      if (writer && threadIdx.x == 0) p.w.best[bi] = 0ull;
+    }
+  };
+  if (p.s.ordered) {
+    gemv_phase<WT>(p, &j, 1, H, stage, cta, ncta, smem);
+  } else {
+    // dense head: only stage y (one CTA per group writes it)
+    float* in_s = reinterpret_cast<float*>(smem);
+    for (int g = cta; g < ngroups; g += ncta) {
+      const int b0 = g * nbg, nb = min(nbg, p.s.B - b0);
+      stage(b0, nb, in_s, H, nullptr, nullptr, true);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TOPK
+
+// Top-k centroids of one sequence by a bitonic sort of (value, index) keys, descending.
+template <typename WT>
+__device__ void phase_topk(const Params& p, int cta, int ncta, char* smem) {
+  const int C = p.s.C, k = p.s.topk;
+  int n = 1;
+  while (n < C) n <<= 1;
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
+  for (int b = cta; b < p.s.B; b += ncta) {
+    const float* cl = p.w.cl + static_cast<size_t>(b) * C;
+    for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = i < C ? argmax_key(cl[i], i) : 0ull;
+    __syncthreads();
+    for (int size = 2; size <= n; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < n / 2; i += kThreads) {
+          const int lo = 2 * i - (i & (stride - 1));
+          const int hi = lo + stride;
+          const bool desc = ((lo & size) == 0);
+          const unsigned long long a = keys[lo], c = keys[hi];
+          if ((a < c) == desc) { keys[lo] = c; keys[hi] = a; }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = threadIdx.x; i < k; i += kThreads) {
+      const int id = key_id(keys[i]);
+      p.w.sel[b * k + i] = id;
+      if (p.out_centroids) p.out_centroids[b * k + i] = id;
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- GATHER
+
+template <typename WT>
+__device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
+  constexpr int V = Elem<WT>::kVec;
+  const int H = p.s.H, vsc = p.s.vsc;
+  const int ncand = p.s.topk * vsc;
+  const int per_b = ceil_div(ncand, kGatherPerItem);
+  const int n_items = p.s.B * per_b;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* ys = reinterpret_cast<float*>(smem);                         // [H]
+  unsigned long long* wbest = reinterpret_cast<unsigned long long*>(ys + H + 2);  // [kWarps]
+  int staged = -1;
+  for (int item = cta; item < n_items; item += ncta) {
+    const int b = item / per_b, ci = item % per_b;
+    if (b != staged) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < H; i += kThreads) ys[i] = p.w.y[static_cast<size_t>(b) * H + i];
+      __syncthreads();
+      staged = b;
+    }
+    unsigned long long best = 0ull;
+    for (int q = warp; q < kGatherPerItem; q += kWarps) {
+      const int cand = ci * kGatherPerItem + q;
+      if (cand >= ncand) break;
+      const int cent = p.w.sel[b * p.s.topk + cand / vsc];
+      const int id = p.ord[cent * vsc + cand % vsc];
+      const WT* row = static_cast<const WT*>(p.temb) + static_cast<size_t>(id) * H;
+      float s = 0.f;
+      for (int k = lane * V; k < H; k += 32 * V) {
+        float w[V];
+        load_vec_stream(row + k, w);
+#pragma unroll
+        for (int v = 0; v < V; ++v) s = fmaf(w[v], ys[k + v], s);
+      }
+      s = warp_sum(s);
+      if (p.out_logits && lane == 0) p.out_logits[static_cast<size_t>(b) * p.s.V + id] = s;
+      const unsigned long long key = argmax_key(s, id);
+      best = key > best ? key : best;
+    }
+    if (lane == 0) wbest[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long m = 0ull;
+      for (int w = 0; w < kWarps; ++w) m = wbest[w] > m ? wbest[w] : m;
+      atomicMax(&p.w.best[b], m);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- DENSE
+
+// Dense tied head: all V logits of up to 32 sequences per pass; lane b ends a row with the
+// logit of sequence b (transposing butterfly reduction) and keeps its running argmax.
+template <typename WT>
+__device__ void phase_dense(const Params& p, int cta, int ncta, char* smem) {
+  constexpr int V = Elem<WT>::kVec;
+  const int H = p.s.H;
+  const int ngroups = ceil_div(p.s.B, kDenseBG);
+  const int row_items = ceil_div(p.s.V, kDenseRowsPerItem);
+  const int n_items = ngroups * row_items;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* ys = reinterpret_cast<float*>(smem);  // [kDenseBG][H]
+  unsigned long long* wbest = reinterpret_cast<unsigned long long*>(smem + kDenseBG * H * 4);
+  int staged = -1;
+  for (int item = cta; item < n_items; item += ncta) {
+    const int g = item / row_items, ri = item % row_items;
+    const int b0 = g * kDenseBG, nb = min(kDenseBG, p.s.B - b0);
+    if (g != staged) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < kDenseBG * H; i += kThreads) {
+        const int b = i / H;
+        ys[i] = b < nb ? p.w.y[static_cast<size_t>(b0 + b) * H + (i % H)] : 0.f;
+      }
+      __syncthreads();
+      staged = g;
+    }
+    unsigned long long best = 0ull;
+    const int r0 = ri * kDenseRowsPerItem;
+    for (int rr = warp; rr < kDenseRowsPerItem; rr += kWarps) {
+      const int row = r0 + rr;
+      if (row >= p.s.V) break;
+      const WT* wr = static_cast<const WT*>(p.temb) + static_cast<size_t>(row) * H;
+      float acc[kDenseBG];
+#pragma unroll
+      for (int b = 0; b < kDenseBG; ++b) acc[b] = 0.f;
+      for (int k = lane * V; k < H; k += 32 * V) {
+        float w[V];
+        load_vec_stream(wr + k, w);
+#pragma unroll
+        for (int b = 0; b < kDenseBG; ++b) {
+          float yv[V];
+          load_fvec<V>(ys + b * H + k, yv);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[b] = fmaf(w[v], yv[v], acc[b]);
+        }
+      }
+      // transposing butterfly: after it, acc[0] of lane l is the row's logit for sequence l
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+          const float send = upper ? acc[i] : acc[i + off];
+          const float keep = upper ? acc[i + off] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      if (lane < nb) {
+        if (p.out_logits) p.out_logits[static_cast<size_t>(b0 + lane) * p.s.V + row] = acc[0];
+        const unsigned long long key = argmax_key(acc[0], row);
+        best = key > best ? key : best;
+      }
+    }
+    wbest[warp * 32 + lane] = best;
+    __syncthreads();
+    if (threadIdx.x < nb) {
+      unsigned long long m = 0ull;
+      for (int w = 0; w < kWarps; ++w) m = wbest[w * 32 + threadIdx.x] > m ? wbest[w * 32 + threadIdx.x] : m;
+      atomicMax(&p.w.best[b0 + threadIdx.x], m);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- small phases
+
+// RoPE (cos, sin) of the constant position, per sequence and layer type, angles in fp64.
+__device__ inline void phase_rope(const Params& p, int cta, int ncta) {
+  for (int b = cta; b < p.s.B; b += ncta) {
+    const int pos = p.pos[b];
+    for (int t = 0; t < 2; ++t) {
+      const int d = p.s.d[t];
+      const double theta = p.s.theta[t];
+      for (int i = threadIdx.x; i < d / 2; i += kThreads) {
+        float2 v = make_float2(1.f, 0.f);
+        if (theta != 0.0) {
+          const double ang = static_cast<double>(pos) * pow(theta, -2.0 * i / d);
+          double sv, cv;
+          sincos(ang, &sv, &cv);
+          v = make_float2(static_cast<float>(cv), static_cast<float>(sv));
+        }
+        p.w.cs[(static_cast<size_t>(b) * 2 + t) * (p.w.dmax / 2) + i] = v;
+      }
+    }
+  }
+}
+
+// Tokens of the last drafted step (earlier steps are written by the next PRE phase).
+__device__ inline void phase_fin(const Params& p, int out_stride, int out_col, int cta, int ncta) {
+  if (cta != 0) return;
+  for (int b = threadIdx.x; b < p.s.B; b += kThreads) p.out_tokens[b * out_stride + out_col] = key_id(p.w.best[b]);
+}
+
+// ---------------------------------------------------------------- item counts (host + device)
+
+__host__ __device__ inline int gemv_items(int R, int B, int K_in, int ncta_hint) {
+  const int ng = ceil_div(B, gemv_group(B, K_in));
+  const int ks = choose_ks(R, ng, ncta_hint);
+  return ng * ceil_div(R, kWarps / ks);
+}
+
+}  // namespace mtp

@@ -1,0 +1,292 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the same seeded
+inputs: every benchmark configuration at full size, both implementations of the draft
+block (one launch per phase, and the persistent kernel), the head entry point, greedy
+verification and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mtp_synth import configs as C
+from mtp_synth import gen as G
+
+from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_accept, inputs_to_device,
+                   oracle_block, to_torch, weights_to_device)
+
+pytestmark = pytest.mark.gpu
+
+PHASES, PERSISTENT = 1, 2
+
+
+def _drafter(index, batch=0, ctx=0, max_batch=0):
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape, wl, w, inp = config_data(index, batch, ctx)
+    wd, tgt = weights_to_device(w)
+    return (Drafter(shape, wd, tgt, max_batch=max(wl.batch, max_batch), max_ctx=wl.ctx),
+            inputs_to_device(inp, shape.dtype))
+
+
+def _run_block(dr, d, n_draft, path, **kw):
+    dr.set_path(path)
+    tok, hid = dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"],
+                              n_draft, **kw)
+    torch.cuda.synchronize()
+    assert dr.status() == 0
+    return tok.cpu().numpy(), None if hid is None else hid.cpu().numpy()
+
+
+@pytest.mark.parametrize("index", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("path", [PHASES, PERSISTENT])
+def test_draft_block_matches_oracle(index, path):
+    shape, wl, w, inp = config_data(index)
+    ref = oracle_block(index)
+    dr, d = _drafter(index)
+    tok, hid = _run_block(dr, d, wl.n_draft, path)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    print(f"config {index} path {path}: {cmp.steps_compared} steps, max hidden err {cmp.max_hidden_err:.3g}, "
+          f"near-tie divergences {cmp.tie_divergences}")
+    assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
+def test_paths_agree_bitwise_on_tokens():
+    # the two implementations run the same phase code; only the grid differs
+    dr, d = _drafter(1)
+    a, ha = _run_block(dr, d, 4, PHASES)
+    b, hb = _run_block(dr, d, 4, PERSISTENT)
+    np.testing.assert_array_equal(a, b)
+    assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
+    dr.close()
+
+
+def test_repeated_calls_are_deterministic():
+    dr, d = _drafter(1)
+    a, ha = _run_block(dr, d, 4, PERSISTENT)
+    b, hb = _run_block(dr, d, 4, PERSISTENT)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(ha, hb)
+    dr.close()
+
+
+@pytest.mark.parametrize("index", [0, 1])
+def test_centroid_head_entry_matches_oracle(index):
+    shape, wl, w, inp = config_data(index)
+    s, W = decoded(index)
+    rng = np.random.default_rng(5)
+    B = 3
+    y = (rng.standard_normal((B, s.hidden)) * 0.8).astype(np.float32)
+    dr, _ = _drafter(index, max_batch=B)
+    tok, logits, cents = dr.centroid_head(to_torch(y, "f32"), want_logits=True, want_centroids=True)
+    torch.cuda.synchronize()
+    tok, logits, cents = tok.cpu().numpy(), logits.cpu().numpy(), cents.cpu().numpy()
+    tol, delta = TOL[shape.dtype], NEAR_TIE[shape.dtype]
+    for b in range(B):
+        ref = O.centroid_head(s, W, y[b].astype(np.float64))
+        if not np.array_equal(cents[b], ref.selected):
+            assert ref.kth_gap < delta, (cents[b], ref.selected, ref.kth_gap)
+            continue
+        row = O.materialise_row(s, ref)
+        unsel = row == np.float32(-1e30)
+        # unselected entries are exactly -1e30, selected ones within tolerance
+        assert np.array_equal(logits[b] == np.float32(-1e30), unsel)
+        assert np.max(np.abs(logits[b][ref.ids].astype(np.float64) - ref.logits)) <= tol
+        if tok[b] != ref.token:
+            assert ref.logit_gap < delta
+    dr.close()
+
+
+def test_dense_head_entry_matches_oracle():
+    shape, wl, w, inp = config_data(3)
+    s, W = decoded(3)
+    rng = np.random.default_rng(6)
+    B = 4
+    y = rng.standard_normal((B, s.hidden)).astype(np.float32)
+    dr, _ = _drafter(3, max_batch=B)
+    tok, logits, _c = dr.centroid_head(to_torch(y, "f32"), want_logits=True)
+    torch.cuda.synchronize()
+    tok, logits = tok.cpu().numpy(), logits.cpu().numpy()
+    for b in range(B):
+        ref = O.dense_head(s, W, y[b].astype(np.float64))
+        assert np.max(np.abs(logits[b].astype(np.float64) - ref.logits)) <= TOL["bf16"]
+        assert tok[b] == ref.token or ref.logit_gap < NEAR_TIE["bf16"]
+    dr.close()
+
+
+# ------------------------------------------------------------------ edge cases of the block
+
+@pytest.mark.parametrize("ctx_lens", [[1, 2, 5, 63], [8, 9, 16, 17], [64, 64, 3, 40]])
+def test_short_and_window_edge_contexts(ctx_lens):
+    # tiny shape with a sliding layer of window 8: contexts below, at and just above it
+    from dataclasses import replace
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape = replace(C.TINY_F32, dtype="bf16", layer_types=("S", "F"), window=8)
+    wl = C.Workload(batch=4, ctx=64, n_draft=3)
+    w = G.make_weights(shape, 21)
+    inp = G.make_step_inputs(shape, wl, 21, ctx_len=np.array(ctx_lens, dtype=np.int32))
+    ref = O.draft_block(O.Shape.of(shape), O.decode_weights(w), inp.hidden, inp.last_token, inp.k_swa,
+                        inp.k_full, inp.ctx_len, inp.pos, 3)
+    wd, tgt = weights_to_device(w)
+    dr = Drafter(shape, wd, tgt, max_batch=4, max_ctx=64)
+    d = inputs_to_device(inp, "bf16")
+    for path in (PHASES, PERSISTENT):
+        tok, hid = _run_block(dr, d, 3, path)
+        compare_block(tok, hid, ref, "bf16")
+    dr.close()
+
+
+def test_v_equal_k_pointer_is_bit_identical_to_v_null():
+    dr, d = _drafter(1)
+    dr.set_path(PERSISTENT)
+    a, ha = dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], 2)
+    b, hb = dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], 2,
+                           v_swa=d["k_swa"], v_full=d["k_full"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(ha, hb)
+    dr.close()
+
+
+def test_missing_kv_and_bad_batch_are_rejected():
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
+    dr, d = _drafter(0)
+    with pytest.raises(MtpError) as e:
+        dr.draft_block(d["hidden"], d["last_token"], None, None, d["ctx_len"], d["pos"], 1)
+    assert e.value.code == binding.MTP_ERR_INVALID_ARG
+    big = torch.zeros((5, d["hidden"].shape[1]), dtype=d["hidden"].dtype, device="cuda")
+    with pytest.raises(MtpError) as e:
+        dr.draft_block(big, d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], 1)
+    assert e.value.code == binding.MTP_ERR_INVALID_ARG
+    dr.close()
+
+
+def test_bad_ordering_is_rejected():
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter, MtpError, binding
+    shape, wl, w, inp = config_data(0)
+    wd, tgt = weights_to_device(w)
+    wd["token_ordering"] = wd["token_ordering"].clone()
+    wd["token_ordering"][7] = wd["token_ordering"][8]
+    with pytest.raises(MtpError) as e:
+        Drafter(shape, wd, tgt, max_batch=1, max_ctx=64)
+    assert e.value.code == binding.MTP_ERR_BAD_ORDERING
+
+
+# ------------------------------------------------------------------ greedy verify
+
+def _verify_case(B, n, V, seed, ties=False):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((B, n + 1, V)).astype(np.float32)
+    drafts = rng.integers(0, V, size=(B, n)).astype(np.int32)
+    agree = rng.random((B, n)) < 0.7
+    for b in range(B):
+        for i in range(n):
+            t = drafts[b, i] if agree[b, i] else (drafts[b, i] + 1 + rng.integers(0, V - 1)) % V
+            logits[b, i, t] = 9.0
+        if ties:
+            row = logits[b, 0]
+            m = int(np.argmax(row))
+            row[(m + 3) % V] = row[m]   # an exact tie with another id
+    bits = G.bf16_bits(logits)
+    return bits, drafts
+
+
+@pytest.mark.parametrize("B,n,V,ties", [(64, 8, 262144, False), (3, 0, 64, False), (5, 4, 4096, True),
+                                        (7, 1, 8, False), (2, 8, 131072, True)])
+def test_verify_matches_oracle(B, n, V, ties):
+    from mtp_speculative_decoding_gemma4_gb300 import verify_greedy
+    bits, drafts = _verify_case(B, n, V, seed=B * 1000 + n, ties=ties)
+    acc, out = verify_greedy(to_torch(bits, "bf16"), to_torch(drafts, "i32"))
+    torch.cuda.synchronize()
+    racc, rout = O.verify_greedy(bits, drafts)
+    np.testing.assert_array_equal(acc.cpu().numpy(), racc)
+    np.testing.assert_array_equal(out.cpu().numpy(), rout)
+
+
+def test_verify_rejects_bad_vocab():
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, verify_greedy
+    t = torch.zeros((1, 2, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(MtpError):
+        verify_greedy(t, torch.zeros((1, 1), dtype=torch.int32, device="cuda"))
+
+
+# ------------------------------------------------------------------ draft + verify loop
+
+def _loop(dr, d, shape, wl, rounds, seed, gpu=True):
+    """Draft+verify rounds against the planted synthetic target; returns per-round
+    (drafts, accept_len, out_tokens). The GPU side runs the library; the oracle side the
+    oracle, each from its own drafts."""
+    B, n, V = wl.batch, wl.n_draft, shape.vocab
+    base = G.base_target_logits(B, n + 1, V, seed)
+    hist = []
+    if gpu:
+        logits_dev = to_torch(base, "bf16")
+        hidden, tok = d["hidden"], d["last_token"]
+    else:
+        s, W = decoded(4)
+        hidden = config_data(4)[3].hidden
+        tok = config_data(4)[3].last_token
+        inp = config_data(4)[3]
+    for r in range(rounds):
+        agree, alt_raw = G.round_tables(B, n, V, wl.agree_p, seed, r)
+        if gpu:
+            drafts, _ = dr.draft_block(hidden, tok, d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], n,
+                                       want_hidden=False)
+            dnp = drafts.cpu().numpy()
+            tgt = G.planted_targets(dnp, agree, alt_raw, V)
+            idx = torch.from_numpy(tgt).cuda()
+            bi = torch.arange(B, device="cuda")[:, None]
+            ri = torch.arange(n + 1, device="cuda")[None, :]
+            saved = logits_dev[bi, ri, idx].clone()
+            logits_dev[bi, ri, idx] = G.PLANT_VALUE
+            acc, out = verify_greedy_(logits_dev, drafts)
+            logits_dev[bi, ri, idx] = saved
+            a, o = acc.cpu().numpy(), out.cpu().numpy()
+            hidden = to_torch(G.next_round_hidden(B, shape.backbone, seed, r), "bf16")
+            tok = out[torch.arange(B, device="cuda"), acc.long()].contiguous()
+        else:
+            blk = O.draft_block(s, W, hidden, tok, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, n)
+            dnp = blk.tokens
+            tgt = G.planted_targets(dnp, agree, alt_raw, V)
+            planted = base.copy()
+            planted[np.arange(B)[:, None], np.arange(n + 1)[None, :], tgt] = G.bf16_bits(np.float32([G.PLANT_VALUE]))[0]
+            a, o = O.verify_greedy(planted, dnp)
+            hidden = G.next_round_hidden(B, shape.backbone, seed, r)
+            tok = o[np.arange(B), a].astype(np.int32)
+        hist.append((dnp.copy(), a.copy(), o.copy()))
+    return hist
+
+
+def verify_greedy_(logits, drafts):
+    from mtp_speculative_decoding_gemma4_gb300 import verify_greedy
+    return verify_greedy(logits, drafts)
+
+
+def test_draft_verify_loop_matches_oracle_for_first_rounds():
+    shape, wl, w, inp = config_data(4)
+    dr, d = _drafter(4)
+    dr.set_path(PERSISTENT)
+    g = _loop(dr, d, shape, wl, rounds=2, seed=wl.seed)
+    o = _loop(None, None, shape, wl, rounds=2, seed=wl.seed, gpu=False)
+    for r, ((gd, ga, go), (od, oa, oo)) in enumerate(zip(g, o)):
+        same = np.all(gd == od, axis=1)
+        assert same.mean() >= 0.95, f"round {r}: only {same.mean():.2f} of sequences drafted identically"
+        np.testing.assert_array_equal(ga[same], oa[same])
+        np.testing.assert_array_equal(go[same], oo[same])
+    dr.close()
+
+
+def test_draft_verify_loop_accept_length_statistics():
+    # 1000 rounds of B=64, n=8 against a target agreeing with probability 0.6 per position:
+    # E[accept] = sum_{i=1..8} 0.6^i = 1.4748
+    shape, wl, w, inp = config_data(4)
+    dr, d = _drafter(4)
+    dr.set_path(PERSISTENT)
+    g = _loop(dr, d, shape, wl, rounds=wl.rounds, seed=wl.seed)
+    acc = np.concatenate([a for _, a, _ in g]).astype(np.float64)
+    mean, sd = expected_accept(wl.agree_p, wl.n_draft)
+    print(f"mean accept length {acc.mean():.4f} (expected {mean:.4f}) over {acc.size} sequence-rounds")
+    assert abs(acc.mean() - mean) < 3 * sd / np.sqrt(acc.size)
+    # every output row holds accept_len drafts then the target token, then -1 padding
+    for dn, a, o in g[:50]:
+        for b in range(wl.batch):
+            assert np.array_equal(o[b, :a[b]], dn[b, :a[b]])
+            assert o[b, a[b]] >= 0 and np.all(o[b, a[b] + 1:] == -1)
+    dr.close()

@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the Gemma-4-assistant MTP drafter on GB300.
+
+One step = one pass of the whole hot path on one batch: a draft block (n_draft drafter
+steps: pre_projection, 4 Q-only blocks over the shared K, post_projection, centroid head
++ argmax) followed by greedy verification of the drafted tokens against synthetic target
+logits. Workload: the E2B shape, B=1, ctx 4096, draft block 4 (seeded synthetic inputs).
+
+Metric: draft tokens/s (= B * n_draft / step time) and us per drafter step, plus the
+fraction of the HBM roofline reached by the persistent draft-block kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mtp|reference]
+
+Multi-GPU: independent replicas, one process per GPU (torchrun); per-GPU work is fixed
+("weak" scaling) and nothing is exchanged on the data path.
+--impl reference times the CPU oracle (the reference arm of this build) on the host.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft tokens/s and µs per drafter step (E2B shape, B=1) + % HBM roofline"
+UNIT = "draft tokens/s"
+L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
+HBM_FALLBACK_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------------------
+# workload and algorithmic bytes
+# ---------------------------------------------------------------------------------------
+
+def workload(index: int):
+    from mtp_synth import configs as C
+    cfg = C.config(index)
+    return cfg.shape, cfg.workload
+
+
+def algorithmic_bytes_per_step(shape, B: int, ctx_lens) -> dict:
+    """Unique bytes one drafter step must read, for the whole batch: every weight once
+    (storage dtype; norm gains fp32), per sequence the shared-K range each attention type
+    attends (once per type, not once per layer), the k*vsc gathered token_embd rows with
+    their int32 ids, and the target-embedding row of the input token."""
+    eb = 2 if shape.dtype == "bf16" else 4
+    H, bb, F = shape.hidden, shape.backbone, shape.ffn
+    w = H * 2 * bb + bb * H
+    g = H
+    for t in shape.layer_types:
+        d = shape.head_dim(t)
+        w += 2 * H * shape.n_head * d + 3 * H * F
+        g += 4 * H + d
+    if shape.use_ordered_embeddings:
+        w += shape.n_centroids * H
+    weights = w * eb + g * 4
+    kv = rows = embed = 0
+    for L in ctx_lens:
+        L = int(L)
+        if "F" in shape.layer_types:
+            kv += L * shape.n_kv_head * shape.head_dim_full * eb
+        if "S" in shape.layer_types:
+            kv += min(L, shape.window) * shape.n_kv_head * shape.head_dim_swa * eb
+        if shape.use_ordered_embeddings:
+            n = shape.top_k * shape.vsc
+            rows += n * H * eb + n * 4
+        else:
+            rows += 0
+        embed += bb * eb
+    if not shape.use_ordered_embeddings:
+        weights += shape.vocab * H * eb     # dense tied head reads every row once per step
+    total = weights + kv + rows + embed
+    return dict(weights=weights, kv=kv, rows=rows, embed=embed, total=total)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback 6.8 TB/s"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "mtp_speculative_decoding_gemma4_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(pkg, "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, config_index: int):
+    """DRAM bytes per launch from a committed ncu capture of the same kernel source, else
+    None (also None once the kernel source changed since the capture)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[f"{kernel}@config{config_index}"]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def _to_dev(arr, dtype, torch):
+    import numpy as np
+    if dtype == "bf16" and arr.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def run_mtp(args, rank: int, world: int, dist):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as ge
+    ge.build()
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter, verify_greedy
+    from mtp_synth import gen as G
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    shape, wl = workload(args.config)
+    B, n = wl.batch, wl.n_draft
+    w = G.make_weights(shape, wl.seed)
+    inp = G.make_step_inputs(shape, wl, wl.seed)
+    dt = shape.dtype
+    wd = {k: (None if getattr(w, k) is None else _to_dev(getattr(w, k), "f32" if k == "out_norm" else
+                                                        ("i32" if k == "token_ordering" else dt), torch))
+          for k in ("pre_proj", "post_proj", "out_norm", "token_embd", "centroids", "token_ordering")}
+    wd["layers"] = [{k: (v if k == "layer_scalar" else _to_dev(v, "f32" if k.endswith("norm") else dt, torch))
+                     for k, v in L.items()} for L in w.layers]
+    dr = Drafter(shape, wd, _to_dev(w.target_embed, dt, torch), max_batch=B, max_ctx=wl.ctx)
+    dr.set_path(args.path)
+    d = dict(hidden=_to_dev(inp.hidden, dt, torch), last_token=_to_dev(inp.last_token, "i32", torch),
+             ctx_len=_to_dev(inp.ctx_len, "i32", torch), pos=_to_dev(inp.pos, "i32", torch),
+             k_swa=None if inp.k_swa is None else _to_dev(inp.k_swa, dt, torch),
+             k_full=None if inp.k_full is None else _to_dev(inp.k_full, dt, torch))
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    out_tok = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out_v = torch.empty((B, n + 1), dtype=torch.int32, device="cuda")
+
+    def draft():
+        dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], n,
+                       want_hidden=False, out_tokens=out_tok, stream=sh)
+
+    # synthetic target logits with a planted maximum agreeing with the draft w.p. 0.6
+    draft()
+    torch.cuda.synchronize()
+    agree, alt_raw = G.round_tables(B, n, shape.vocab, 0.6, wl.seed, 0)
+    tgt = G.planted_targets(out_tok.cpu().numpy(), agree, alt_raw, shape.vocab)
+    base = G.base_target_logits(B, n + 1, shape.vocab, wl.seed)
+    base[np.arange(B)[:, None], np.arange(n + 1)[None, :], tgt] = G.bf16_bits(np.float32([G.PLANT_VALUE]))[0]
+    logits = _to_dev(base, "bf16", torch)
+
+    def verify():
+        verify_greedy(logits, out_tok, accept_len=acc, out_tokens=out_v, stream=sh)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(max(3, args.warmup)):
+        draft(); verify()
+    torch.cuda.synchronize()
+    assert dr.status() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()                      # evict the previous step's working set from L2
+            ev[i][0].record(stream)
+            draft()
+            ev[i][1].record(stream)
+            verify()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_per_step = sum(step_ms) / K
+    draft_ms_mean = sum(draft_ms) / K
+    assert dr.status() == 0
+
+    # warm-L2 reference figure: back-to-back steps, no flush
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        draft(); verify()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = e0.elapsed_time(e1) / K
+
+    # end to end through the public API with host buffers: per step, H2D of the step's
+    # inputs from pinned memory, the draft block and verify, D2H of the result, host wait
+    h_hidden = d["hidden"].cpu().pin_memory()
+    h_tok = d["last_token"].cpu().pin_memory()
+    h_pos = d["pos"].cpu().pin_memory()
+    h_ctx = d["ctx_len"].cpu().pin_memory()
+    r_tok = torch.empty((B, n + 1), dtype=torch.int32).pin_memory()
+    r_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_tok, h_pos, h_ctx))
+    d2h = r_tok.numel() * 4 + r_acc.numel() * 4
+    e2e_s = []
+    for i in range(K):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        d["hidden"].copy_(h_hidden, non_blocking=True)
+        d["last_token"].copy_(h_tok, non_blocking=True)
+        d["pos"].copy_(h_pos, non_blocking=True)
+        d["ctx_len"].copy_(h_ctx, non_blocking=True)
+        draft(); verify()
+        r_tok.copy_(out_v, non_blocking=True)
+        r_acc.copy_(acc, non_blocking=True)
+        stream.synchronize()
+        e2e_s.append(time.perf_counter() - t0)
+    e2e_step = sum(e2e_s) / K
+
+    if dist:
+        t = torch.tensor([ms_per_step, e2e_step, draft_ms_mean, warm_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step, e2e_step, draft_ms_mean, warm_ms = t.tolist()
+
+    if rank != 0:
+        return None
+    alg = algorithmic_bytes_per_step(shape, B, inp.ctx_len)
+    per_launch = alg["total"] * n
+    peak, peak_src = measured_peaks()
+    achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
+    tokens = B * n * world
+    launches_per_step = 2 if args.path == 2 else (1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1)
+    res = {
+        "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_drafter_step": ms_per_step * 1e3 / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{shape.name} drafter step: B={B}, ctx {wl.ctx}, draft block {n}, then greedy "
+                               f"verify of [{B},{n + 1},{shape.vocab}] bf16 target logits",
+                   "batch": B, "ctx": wl.ctx, "n_draft": n, "storage": shape.dtype,
+                   "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": ncu_traffic("k_block", args.config),
+                     "kernel": "k_block (persistent draft block)" if args.path == 2 else "phase kernels",
+                     "alg_bytes_per_launch": per_launch, "alg_bytes_per_step": alg, "peak_source": peak_src,
+                     "kernel_ms": draft_ms_mean},
+        "e2e": {"value": tokens / e2e_step, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_step * 1e3},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "warm_l2": {"ms_per_step": warm_ms, "value": tokens / (warm_ms * 1e-3)},
+        "accept_len_mean": float(acc.float().mean().item()),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args, shape, wl, w, inp, base, seconds=args.cpu_seconds)
+    return res
+
+
+# ---------------------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------------------
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step_runner(shape, wl, w, inp, base):
+    import oracle as O
+    s, W = O.Shape.of(shape), O.decode_weights(w)
+
+    def one():
+        blk = O.draft_block(s, W, inp.hidden, inp.last_token, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos,
+                            wl.n_draft)
+        O.verify_greedy(base, blk.tokens)
+        return blk
+    return one
+
+
+def cpu_baseline(args, shape, wl, w, inp, base, seconds: float):
+    one = oracle_step_runner(shape, wl, w, inp, base)
+    one()
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        one()
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or steps >= 10000:
+            break
+    return {"value": steps * wl.batch * wl.n_draft / el, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{steps} full steps (draft block of {wl.n_draft} + verify) of the same workload, "
+                      f"{el:.1f} s, NumPy fp64"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return None
+    import numpy as np
+    from mtp_synth import gen as G
+    shape, wl = workload(args.config)
+    w = G.make_weights(shape, wl.seed)
+    inp = G.make_step_inputs(shape, wl, wl.seed)
+    B, n = wl.batch, wl.n_draft
+    base = G.base_target_logits(B, n + 1, shape.vocab, wl.seed)
+    one = oracle_step_runner(shape, wl, w, inp, base)
+    blk = one()
+    agree, alt_raw = G.round_tables(B, n, shape.vocab, 0.6, wl.seed, 0)
+    tgt = G.planted_targets(blk.tokens, agree, alt_raw, shape.vocab)
+    base[np.arange(B)[:, None], np.arange(n + 1)[None, :], tgt] = G.bf16_bits(np.float32([G.PLANT_VALUE]))[0]
+    for _ in range(args.warmup):
+        one()
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        t.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(t) / len(t)
+    value = B * n / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_drafter_step": ms * 1e3 / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{shape.name} drafter step: B={B}, ctx {wl.ctx}, draft block {n}, then greedy "
+                                   f"verify of [{B},{n + 1},{shape.vocab}] bf16 target logits",
+                       "batch": B, "ctx": wl.ctx, "n_draft": n, "parallelism": "host"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} full steps of the workload, NumPy fp64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mtp", "reference"], default="mtp")
+    ap.add_argument("--config", type=int, default=1, help="benchmark configuration index (default 1: E2B, B=1)")
+    ap.add_argument("--path", type=int, default=2, help="1: one launch per phase, 2: persistent kernel")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1 and args.impl == "mtp":
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend="nccl")
+        dist = tdist
+    res = run_reference(args, rank, world) if args.impl == "reference" else run_mtp(args, rank, world, dist)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,6 +22,8 @@ bit is set and at the alternative otherwise, so every row has a unique maximum.
 """
 from __future__ import annotations
 
+import concurrent.futures as _cf
+import os
 import zlib
 from dataclasses import dataclass
 from typing import Dict, List, Optional
@@ -50,22 +52,32 @@ def _rng(seed: int, name: str, *extra: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence(key)))
 
 
-def _normal(seed: int, name: str, shape, std: float, dtype: str, chunk_rows: int = 16384) -> np.ndarray:
+def _normal(seed: int, name: str, shape, std: float, dtype: str, chunk_rows: int = 4096) -> np.ndarray:
     """N(0, std) in storage form: uint16 bf16 bits ("bf16") or float32 ("f32").
 
-    Large tables are drawn in row chunks so the fp32 temporary stays small.
+    Rows are drawn in chunks, each chunk from its own stream keyed by (seed, name, chunk),
+    on a thread pool: the values do not depend on the number of threads.
     """
-    rng = _rng(seed, name)
     shape = tuple(int(s) for s in shape)
     out = np.empty(shape, dtype=np.uint16 if dtype == "bf16" else np.float32)
     flat = out.reshape(shape[0], -1) if len(shape) > 1 else out.reshape(1, -1)
-    rows = flat.shape[0]
-    for r0 in range(0, rows, chunk_rows):
+    rows, cols = flat.shape
+
+    def fill(ci: int) -> None:
+        r0 = ci * chunk_rows
         r1 = min(rows, r0 + chunk_rows)
-        v = rng.standard_normal((r1 - r0, flat.shape[1]), dtype=np.float32)
+        v = _rng(seed, name, ci).standard_normal((r1 - r0, cols), dtype=np.float32)
         if std != 1.0:
             v *= np.float32(std)
         flat[r0:r1] = bf16_bits(v) if dtype == "bf16" else v
+
+    n_chunks = (rows + chunk_rows - 1) // chunk_rows
+    if n_chunks == 1 or rows * cols < (1 << 20):
+        for ci in range(n_chunks):
+            fill(ci)
+    else:
+        with _cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(n_chunks)))
     return out
 
 

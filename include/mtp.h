@@ -190,6 +190,35 @@ MTP_API int mtp_centroid_head(mtp_handle *h, const float *y, int32_t B, float *o
 MTP_API int mtp_verify_greedy(const void *target_logits, const int32_t *draft, int32_t B, int32_t n,
                       int32_t V, int32_t *accept_len, int32_t *out_tokens, void *stream);
 
+/* Size of the static device scratch of mtp_centroid_head_noalloc (1 MiB). */
+#define MTP_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* The centroid LM head of mtp_centroid_head for callers that cannot allocate device memory:
+ * code running where cudaMalloc is unavailable or forbidden, such as inside a region being
+ * captured into a CUDA graph, an allocator callback, or a runtime that owns every device
+ * allocation and hands out only the caller's tensors. The pages have no counterpart; this is
+ * a library convenience. It needs no handle (creating one allocates a workspace): the head's
+ * tensors are passed directly, and its scratch lives in a fixed device array of
+ * MTP_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the process exits.
+ * Results equal mtp_centroid_head's on the same tensors.
+ *   y              device [B][hidden] fp32 final-normed hidden states
+ *   centroids      device [n_centroids][hidden], dtype (MTP_DTYPE_BF16 or MTP_DTYPE_F32)
+ *   token_ordering device [vocab] int32, a permutation viewed [n_centroids][vocab/n_centroids]
+ *   token_embd     device [vocab][hidden], dtype
+ *   out_logits     device [B][vocab] fp32 (-1e30 outside the selected clusters) or NULL
+ *   out_token      device [B] int32;  out_centroids device [B][top_k] int32 or NULL
+ * Scratch needed: 4*B*(n_centroids + top_k + hidden) + 8*B bytes, each part rounded up to 256;
+ * larger requests fail with MTP_ERR_INVALID_ARG and a message giving both sizes. The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture. Calls share the array and keep its last contents:
+ * calls that overlap on the GPU (concurrent streams, several host threads) race. No
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ * Errors: INVALID_ARG, BAD_ORDERING (vocab % n_centroids != 0), CUDA. */
+MTP_API int mtp_centroid_head_noalloc(const float *y, const void *centroids, const int32_t *token_ordering,
+                                      const void *token_embd, int32_t dtype, int32_t B, int32_t hidden,
+                                      int32_t n_centroids, int32_t top_k, int32_t vocab, float *out_logits,
+                                      int32_t *out_token, int32_t *out_centroids, void *stream);
+
 /* Synchronise the device and return the handle's device-side status word: MTP_OK,
  * MTP_ERR_TIMEOUT when a bounded device wait of a previous call gave up, or
  * MTP_ERR_INVALID_ARG when a device-resident input was out of range (a last_token outside

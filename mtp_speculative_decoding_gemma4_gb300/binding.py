@@ -18,7 +18,7 @@ MTP_LAYER_SLIDING, MTP_LAYER_FULL = 0, 1
 
 # Every symbol include/mtp.h declares.
 EXPORTS = ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy", "mtp_get_status",
-           "mtp_set_path", "mtp_destroy", "mtp_last_error")
+           "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc")
 
 
 class MtpError(RuntimeError):
@@ -72,6 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                     vp]
     lib.mtp_centroid_head.argtypes = [vp, vp, i32, vp, vp, vp, vp]
     lib.mtp_verify_greedy.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.mtp_centroid_head_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.mtp_get_status.argtypes = [vp]
     lib.mtp_set_path.argtypes = [vp, i32]
     lib.mtp_destroy.argtypes = [vp]
@@ -79,7 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mtp_last_error.argtypes = []
     lib.mtp_last_error.restype = ctypes.c_char_p
     for name in ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy",
-                 "mtp_get_status", "mtp_set_path"):
+                 "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -120,6 +121,17 @@ def mtp_verify_greedy(target_logits: int, draft: int, B: int, n: int, V: int, ac
                       stream: int = 0) -> None:
     _check(load_library().mtp_verify_greedy(target_logits, draft or None, B, n, V, accept_len, out_tokens,
                                             stream or None), "mtp_verify_greedy")
+
+
+def mtp_centroid_head_noalloc(y: int, centroids: int, token_ordering: int, token_embd: int, dtype: int, B: int,
+                              hidden: int, n_centroids: int, top_k: int, vocab: int, out_logits: int, out_token: int,
+                              out_centroids: int, stream: int = 0) -> None:
+    """Centroid head without a handle and without any device allocation (static scratch of
+    MTP_NOALLOC_SCRATCH_BYTES); for callers that cannot allocate device memory."""
+    _check(load_library().mtp_centroid_head_noalloc(y, centroids, token_ordering, token_embd, dtype, B, hidden,
+                                                    n_centroids, top_k, vocab, out_logits or None, out_token,
+                                                    out_centroids or None, stream or None),
+           "mtp_centroid_head_noalloc")
 
 
 def mtp_get_status(handle: int) -> int:

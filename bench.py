@@ -308,7 +308,9 @@ def run_mtp(args, rank: int, world: int, dist):
     peak, peak_src = measured_peaks()
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
     tokens = B * n * world
-    launches_per_step = 2 if args.path == 2 else (1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1)
+    launches_per_step = 2 if args.path in (2, 3) else (1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1)
+    kernel_name = {1: "phase kernels", 2: "k_block (persistent draft block, grid barriers)",
+                   3: "k_block_ll (latency draft block, resident weights + mailboxes)"}[args.path]
     res = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -319,8 +321,8 @@ def run_mtp(args, rank: int, world: int, dist):
                    "batch": B, "ctx": wl.ctx, "n_draft": n, "storage": shape.dtype,
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": ncu_traffic("k_block", args.config),
-                     "kernel": "k_block (persistent draft block)" if args.path == 2 else "phase kernels",
+                     "traffic": ncu_traffic(kernel_name.split()[0], args.config),
+                     "kernel": kernel_name,
                      "alg_bytes_per_launch": per_launch, "alg_bytes_per_step": alg, "peak_source": peak_src,
                      "kernel_ms": draft_ms_mean},
         "e2e": {"value": tokens / e2e_step, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -420,11 +422,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mtp", "reference"], default="mtp")
     ap.add_argument("--config", type=int, default=1, help="benchmark configuration index (default 1: E2B, B=1)")
-    ap.add_argument("--path", type=int, default=2, help="1: one launch per phase, 2: persistent kernel")
+    ap.add_argument("--path", type=int, default=-1,
+                    help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
+                         "(one sequence); default: 3 for B=1, else 2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.path < 0:
+        args.path = 3 if workload(args.config)[1].batch == 1 else 2
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -8,6 +8,7 @@
 
 #include "mtp.h"
 #include "mtp_launch.h"
+#include "mtp_ll.cuh"
 #include "mtp_phases.cuh"
 
 struct mtp_handle {
@@ -22,6 +23,11 @@ struct mtp_handle {
   void* ws;
   size_t ws_bytes;
   mtp::WsP wsp;
+  // latency path (one sequence): availability, mailboxes, epoch counter, abort word
+  int ll_ok;
+  unsigned long long* mb[10];
+  unsigned* ll_abort;
+  unsigned epoch;
 };
 
 namespace mtp {
@@ -161,6 +167,82 @@ int check_ordering(const mtp_config& c, const int32_t* ord) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
+// Latency-path parameters that depend only on the handle (shapes, weights, CTA count).
+mtp::ll::Params ll_template(const mtp_handle* h, int kv_max) {
+  const mtp_config& c = h->cfg;
+  mtp::ll::Params p;
+  memset(&p, 0, sizeof(p));
+  p.N = h->num_sms;
+  p.bb = c.backbone;
+  p.H = c.hidden;
+  p.nl = c.n_layers;
+  p.nh = c.n_head;
+  p.nkv = c.n_kv_head;
+  p.F = c.ffn;
+  p.V = c.vocab;
+  p.C = c.n_centroids;
+  p.topk = c.top_k;
+  p.vsc = c.use_ordered_embeddings ? c.vocab / c.n_centroids : 0;
+  p.W = c.window;
+  p.d[0] = c.head_dim_swa;
+  p.d[1] = c.head_dim_full;
+  for (int t = 0; t < 2; ++t) {
+    const int d = p.d[t] > 0 ? p.d[t] : 1;
+    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
+  }
+  p.theta[0] = c.rope_theta_swa;
+  p.theta[1] = c.rope_theta_full;
+  p.eps = c.rms_eps;
+  typedef const __nv_bfloat16* cb;
+  p.pre = static_cast<cb>(h->w.pre_proj);
+  p.post = static_cast<cb>(h->w.post_proj);
+  p.temb = static_cast<cb>(h->w.token_embd);
+  p.cent = static_cast<cb>(h->w.centroids);
+  p.tgt = static_cast<cb>(h->target_embed);
+  p.out_norm = h->w.out_norm;
+  p.ord = h->w.token_ordering;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    p.ltype[l] = c.layer_type[l];
+    p.lambda[l] = L.layer_scalar;
+    p.q[l] = static_cast<cb>(L.q);
+    p.o[l] = static_cast<cb>(L.o);
+    p.gate[l] = static_cast<cb>(L.gate);
+    p.up[l] = static_cast<cb>(L.up);
+    p.down[l] = static_cast<cb>(L.down);
+    p.q_norm[l] = L.q_norm;
+    p.attn_norm[l] = L.attn_norm;
+    p.post_attn_norm[l] = L.post_attn_norm;
+    p.ffn_norm[l] = L.ffn_norm;
+    p.post_ffn_norm[l] = L.post_ffn_norm;
+  }
+  for (int t = 0; t < 2; ++t) {
+    p.has_type[t] = has_type(c, t);
+    p.kv_max[t] = kv_max;
+  }
+  p.spin_limit = 4000000000LL;
+  return p;
+}
+
+// Whether the latency path can run this configuration on this device.
+bool ll_supported(const mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings || c.n_head > 8) return false;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const int d = c.layer_type[l] ? c.head_dim_full : c.head_dim_swa;
+    if (d % 8 || c.hidden % 8 || c.backbone % 8 || c.ffn % 8) return false;
+  }
+  const mtp::ll::Params p = ll_template(h, c.max_ctx);
+  const int smem = mtp::ll_smem_bytes(p);
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (smem <= 0 || smem > optin) return false;
+  return mtp::ll_capacity(smem, h->num_sms) >= h->num_sms;
+}
+
 // Carves the workspace out of one allocation (sizes for max_batch sequences).
 size_t layout_ws(mtp_handle* h, char* base) {
   const mtp_config& c = h->cfg;
@@ -192,6 +274,14 @@ size_t layout_ws(mtp_handle* h, char* base) {
   w.cs = static_cast<float2*>(take(8 * B * 2 * (dmax / 2)));
   w.bar = static_cast<unsigned int*>(take(16));
   w.status = static_cast<int*>(take(16));
+  h->ll_abort = static_cast<unsigned*>(take(16));
+  for (int i = 0; i < 10; ++i) h->mb[i] = nullptr;
+  if (h->ll_ok) {
+    mtp::ll::Params lp = ll_template(h, c.max_ctx);
+    const mtp::ll::MailboxSizes m = mtp::ll::mailbox_sizes(lp);
+    const long long n[10] = {m.x0, m.q, m.part, m.o, m.op, m.m, m.dn, m.h, m.cent, m.key};
+    for (int i = 0; i < 10; ++i) h->mb[i] = static_cast<unsigned long long*>(take(8 * static_cast<size_t>(n[i])));
+  }
   w.nsplit_max = static_cast<int>(ns);
   w.dmax = static_cast<int>(dmax);
   return off;
@@ -341,6 +431,8 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
   int ns = (config->max_ctx + 31) / 32;
   if (ns > 4 * h->num_sms) ns = 4 * h->num_sms;
   h->nsplit_max = ns < 1 ? 1 : ns;
+  h->ll_ok = ll_supported(h) ? 1 : 0;
+  h->epoch = 64u;
   h->ws_bytes = layout_ws(h, nullptr);
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -408,6 +500,64 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == MTP_DTYPE_BF16;
   int path = h->path;
+  if (path == 3 || (path == 0 && B == 1 && h->ll_ok)) {
+    if (!h->ll_ok || B != 1) {
+      set_error("the latency path runs one sequence of a supported shape (B=%d, available=%d)", B, h->ll_ok);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    const int kvm = has_type(c, 1) ? kv_full->max_ctx : kv_sliding->max_ctx;
+    mtp::ll::Params lp = ll_template(h, kvm);
+    for (int t = 0; t < 2; ++t) {
+      if (!lp.has_type[t]) continue;
+      lp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
+      lp.v[t] = static_cast<const __nv_bfloat16*>(kvs[t]->v);
+      lp.ctx_len[t] = kvs[t]->ctx_len;
+      lp.sb[t] = kvs[t]->stride_b;
+      lp.st[t] = kvs[t]->stride_t;
+      lp.kv_max[t] = kvs[t]->max_ctx;
+    }
+    if (lp.v[0] || lp.v[1]) {
+      set_error("the latency path reads V = K (attention_k_eq_v); pass v = NULL");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    lp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
+    lp.tok_in = last_token;
+    lp.pos = pos;
+    lp.out_tokens = out_tokens;
+    lp.out_hidden = out_hidden;
+    lp.n_draft = n_draft;
+    lp.mb_x0 = h->mb[0];
+    lp.mb_q = h->mb[1];
+    lp.mb_part = h->mb[2];
+    lp.mb_o = h->mb[3];
+    lp.mb_op = h->mb[4];
+    lp.mb_m = h->mb[5];
+    lp.mb_dn = h->mb[6];
+    lp.mb_h = h->mb[7];
+    lp.mb_cent = h->mb[8];
+    lp.mb_key = h->mb[9];
+    lp.status = h->wsp.status;
+    lp.abort_flag = h->ll_abort;
+    const unsigned span = static_cast<unsigned>(n_draft + 1) * mtp::ll::kExPerStep;
+    if (h->epoch > 0xffffffffu - span) {
+      // epochs wrap: clear every mailbox so that no stale word can carry a reused epoch
+      char* lo = reinterpret_cast<char*>(h->mb[0]);
+      char* hi = static_cast<char*>(h->ws) + h->ws_bytes;
+      cudaError_t e = cudaMemsetAsync(lo, 0, static_cast<size_t>(hi - lo), st);
+      if (e != cudaSuccess) return cuda_fail("clearing the mailboxes", e);
+      h->epoch = 64u;
+    }
+    lp.epoch_base = h->epoch;
+    h->epoch += span;
+    const int smem = mtp::ll_smem_bytes(lp);
+    if (smem <= 0) {
+      set_error("latency path: shape not supported for this call");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
+    return mtp::run_ll(lp, smem, st);
+  }
   int ncta = h->num_sms;
   if (path != 1) {
     p.s.ncta_hint = ncta;
@@ -495,8 +645,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 2) {
-    set_error("need a handle and path in {0, 1, 2}");
+  if (!h || path < 0 || path > 3) {
+    set_error("need a handle and path in {0, 1, 2, 3}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;

@@ -9,6 +9,9 @@
 namespace mtp {
 
 struct Params;
+namespace ll {
+struct Params;
+}
 
 // Records the calling thread's last error text (printf-style).
 void set_error(const char* fmt, ...);
@@ -22,6 +25,12 @@ int run_phases_f32(const Params& p, cudaStream_t st);
 int run_persistent_f32(const Params& p, cudaStream_t st);
 int persistent_capacity_f32(const Params& p, int num_sms);
 int run_head_f32(const Params& p, cudaStream_t st);
+
+// Latency-path draft block (one sequence): shared-memory bytes it needs for these
+// parameters (0: shape not supported), co-resident capacity for that size, launch.
+int ll_smem_bytes(const ll::Params& p);
+int ll_capacity(int smem, int num_sms);
+int run_ll(const ll::Params& p, int smem, cudaStream_t st);
 
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st);

@@ -15,7 +15,7 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT = 1, 2
+PHASES, PERSISTENT, LATENCY = 1, 2, 3
 
 
 def _drafter(index, batch=0, ctx=0, max_batch=0):
@@ -46,6 +46,49 @@ def test_draft_block_matches_oracle(index, path):
     print(f"config {index} path {path}: {cmp.steps_compared} steps, max hidden err {cmp.max_hidden_err:.3g}, "
           f"near-tie divergences {cmp.tie_divergences}")
     assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
+def test_latency_path_matches_oracle_e2b_b1():
+    shape, wl, w, inp = config_data(1)
+    ref = oracle_block(1)
+    dr, d = _drafter(1)
+    tok, hid = _run_block(dr, d, wl.n_draft, LATENCY)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    print(f"latency path config 1: max hidden err {cmp.max_hidden_err:.3g}, near-ties {cmp.tie_divergences}")
+    # more steps than the bench block, and repeated calls (mailbox epochs advance)
+    ref8 = oracle_block(1, n_draft=8)
+    for _ in range(3):
+        tok, hid = _run_block(dr, d, 8, LATENCY)
+        compare_block(tok, hid, ref8, shape.dtype)
+    dr.close()
+
+
+@pytest.mark.parametrize("ctx,n_kv", [(1, 1), (5, 1), (8, 1), (9, 2), (63, 2), (64, 1)])
+def test_latency_path_short_and_window_edge_contexts(ctx, n_kv):
+    from dataclasses import replace
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape = replace(C.TINY_F32, dtype="bf16", layer_types=("S", "F", "S"), window=8, n_head=4, n_kv_head=n_kv)
+    wl = C.Workload(batch=1, ctx=64, n_draft=4)
+    w = G.make_weights(shape, 31 + ctx)
+    inp = G.make_step_inputs(shape, wl, 31 + ctx, ctx_len=np.array([ctx], dtype=np.int32))
+    ref = O.draft_block(O.Shape.of(shape), O.decode_weights(w), inp.hidden, inp.last_token, inp.k_swa,
+                        inp.k_full, inp.ctx_len, inp.pos, 4)
+    wd, tgt = weights_to_device(w)
+    dr = Drafter(shape, wd, tgt, max_batch=1, max_ctx=64)
+    d = inputs_to_device(inp, "bf16")
+    tok, hid = _run_block(dr, d, 4, LATENCY)
+    compare_block(tok, hid, ref, "bf16")
+    dr.close()
+
+
+def test_latency_path_rejects_batches():
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
+    dr, d = _drafter(2)
+    dr.set_path(LATENCY)
+    with pytest.raises(MtpError) as e:
+        dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], 1)
+    assert e.value.code == binding.MTP_ERR_UNSUPPORTED_SHAPE
     dr.close()
 
 

@@ -308,9 +308,10 @@ def run_mtp(args, rank: int, world: int, dist):
     peak, peak_src = measured_peaks()
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
     tokens = B * n * world
-    launches_per_step = 2 if args.path in (2, 3) else (1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1)
+    launches_per_step = 2 if args.path in (2, 3, 4) else (1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1)
     kernel_name = {1: "phase kernels", 2: "k_block (persistent draft block, grid barriers)",
-                   3: "k_block_ll (latency draft block, resident weights + mailboxes)"}[args.path]
+                   3: "k_block_ll (latency draft block, resident weights + mailboxes)",
+                   4: "k_block_cl (cluster draft block, streamed weights + DSMEM exchanges)"}[args.path]
     res = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -424,7 +425,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, help="benchmark configuration index (default 1: E2B, B=1)")
     ap.add_argument("--path", type=int, default=-1,
                     help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
-                         "(one sequence); default: 3 for B=1, else 2")
+                         "(one sequence), 4: cluster kernel (one sequence); default: 3 for B=1, else 2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

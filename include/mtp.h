@@ -229,10 +229,14 @@ MTP_API int mtp_get_status(mtp_handle *h);
 /* Select the implementation of mtp_draft_block: 0 = automatic, 1 = one kernel per phase,
  * 2 = persistent whole-block kernel with grid barriers, 3 = latency kernel for one sequence
  * (weights and attended K resident in shared memory, CTAs exchanging vectors through
- * mailboxes; bf16 centroid-head shapes whose per-SM share fits shared memory, V = K).
- * Automatic picks 3 for B = 1 when available, else 2 when co-resident, else 1. Results agree
- * within the precision contract. Errors: INVALID_ARG; a forced path the call cannot use
- * makes mtp_draft_block return UNSUPPORTED_SHAPE. */
+ * mailboxes; bf16 centroid-head shapes whose per-SM share fits shared memory, V = K),
+ * 4 = cluster kernel for one sequence (one 16-CTA thread-block cluster streams the weights
+ * and the attended K through shared memory and exchanges vectors in distributed shared
+ * memory; bf16 centroid-head shapes within its buffer limits, V = K; mtp_init_weights keeps
+ * a copy of token_embd in token_ordering order for it, vocab * hidden * 2 bytes).
+ * Automatic picks 3 for B = 1 when available, else 4 when available, else 2 when
+ * co-resident, else 1. Results agree within the precision contract. Errors: INVALID_ARG; a
+ * forced path the call cannot use makes mtp_draft_block return UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);
 
 /* Free the workspace and the handle (synchronises). NULL is ignored. */

@@ -8,6 +8,7 @@
 
 #include "mtp.h"
 #include "mtp_launch.h"
+#include "mtp_cl.cuh"
 #include "mtp_ll.cuh"
 #include "mtp_phases.cuh"
 
@@ -28,6 +29,9 @@ struct mtp_handle {
   unsigned long long* mb[10];
   unsigned* ll_abort;
   unsigned epoch;
+  // cluster path (one sequence): availability, token_embd in token_ordering order
+  int cl_ok;
+  void* temb_ord;
 };
 
 namespace mtp {
@@ -243,6 +247,77 @@ bool ll_supported(const mtp_handle* h) {
   return mtp::ll_capacity(smem, h->num_sms) >= h->num_sms;
 }
 
+// Cluster-path parameters that depend only on the handle.
+mtp::clk::Params cl_template(const mtp_handle* h, int kv_max) {
+  const mtp_config& c = h->cfg;
+  mtp::clk::Params p;
+  memset(&p, 0, sizeof(p));
+  p.bb = c.backbone;
+  p.H = c.hidden;
+  p.nl = c.n_layers;
+  p.nh = c.n_head;
+  p.nkv = c.n_kv_head;
+  p.F = c.ffn;
+  p.V = c.vocab;
+  p.C = c.n_centroids;
+  p.topk = c.top_k;
+  p.vsc = c.use_ordered_embeddings && c.n_centroids > 0 ? c.vocab / c.n_centroids : 0;
+  p.W = c.window;
+  p.d[0] = c.head_dim_swa;
+  p.d[1] = c.head_dim_full;
+  for (int t = 0; t < 2; ++t) {
+    const int d = p.d[t] > 0 ? p.d[t] : 1;
+    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
+  }
+  p.theta[0] = c.rope_theta_swa;
+  p.theta[1] = c.rope_theta_full;
+  p.eps = c.rms_eps;
+  typedef const __nv_bfloat16* cb;
+  p.pre = static_cast<cb>(h->w.pre_proj);
+  p.post = static_cast<cb>(h->w.post_proj);
+  p.cent = static_cast<cb>(h->w.centroids);
+  p.tgt = static_cast<cb>(h->target_embed);
+  p.temb_ord = static_cast<cb>(h->temb_ord);
+  p.out_norm = h->w.out_norm;
+  p.ord = h->w.token_ordering;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    p.ltype[l] = c.layer_type[l];
+    p.lambda[l] = L.layer_scalar;
+    p.q[l] = static_cast<cb>(L.q);
+    p.o[l] = static_cast<cb>(L.o);
+    p.gate[l] = static_cast<cb>(L.gate);
+    p.up[l] = static_cast<cb>(L.up);
+    p.down[l] = static_cast<cb>(L.down);
+    p.q_norm[l] = L.q_norm;
+    p.attn_norm[l] = L.attn_norm;
+    p.post_attn_norm[l] = L.post_attn_norm;
+    p.ffn_norm[l] = L.ffn_norm;
+    p.post_ffn_norm[l] = L.post_ffn_norm;
+  }
+  for (int t = 0; t < 2; ++t) {
+    p.has_type[t] = has_type(c, t);
+    p.kv_max[t] = kv_max;
+  }
+  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  return p;
+}
+
+// Whether the cluster path can run this configuration on this device.
+bool cl_supported(const mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings) return false;
+  const mtp::clk::Params p = cl_template(h, c.max_ctx);
+  const int smem = mtp::cl_smem_bytes(p);
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (smem <= 0 || smem > optin) return false;
+  return mtp::cl_capacity(smem) >= 1;
+}
+
 // Carves the workspace out of one allocation (sizes for max_batch sequences).
 size_t layout_ws(mtp_handle* h, char* base) {
   const mtp_config& c = h->cfg;
@@ -433,6 +508,8 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
   h->nsplit_max = ns < 1 ? 1 : ns;
   h->ll_ok = ll_supported(h) ? 1 : 0;
   h->epoch = 64u;
+  h->cl_ok = cl_supported(h) ? 1 : 0;
+  h->temb_ord = nullptr;
   h->ws_bytes = layout_ws(h, nullptr);
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -446,6 +523,23 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     cudaFree(h->ws);
     free(h);
     return cuda_fail("clearing the workspace", e);
+  }
+  if (h->cl_ok) {
+    // the cluster path reads token_embd rows in token_ordering order (one contiguous block of
+    // vocab / n_centroids rows per centroid): a copy made once here
+    const size_t bytes = static_cast<size_t>(config->vocab) * config->hidden * 2;
+    e = cudaMalloc(&h->temb_ord, bytes);
+    if (e == cudaSuccess) {
+      rc = mtp::reorder_rows(weights->token_embd, weights->token_ordering, h->temb_ord, config->vocab,
+                             config->hidden, 0);
+      e = rc ? cudaErrorUnknown : cudaDeviceSynchronize();
+    }
+    if (e != cudaSuccess) {
+      if (h->temb_ord) cudaFree(h->temb_ord);
+      cudaFree(h->ws);
+      free(h);
+      return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
+    }
   }
   *out = h;
   return MTP_OK;
@@ -500,6 +594,41 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == MTP_DTYPE_BF16;
   int path = h->path;
+  if (path == 4 || (path == 0 && B == 1 && h->cl_ok && !h->ll_ok)) {
+    if (!h->cl_ok || B != 1) {
+      set_error("the cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->cl_ok);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    const int kvm = has_type(c, 1) ? kv_full->max_ctx : kv_sliding->max_ctx;
+    mtp::clk::Params cp = cl_template(h, kvm);
+    for (int t = 0; t < 2; ++t) {
+      if (!cp.has_type[t]) continue;
+      if (kvs[t]->v) {
+        set_error("the cluster path reads V = K (attention_k_eq_v); pass v = NULL");
+        return MTP_ERR_UNSUPPORTED_SHAPE;
+      }
+      cp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
+      cp.ctx_len[t] = kvs[t]->ctx_len;
+      cp.st[t] = kvs[t]->stride_t;
+      cp.kv_max[t] = kvs[t]->max_ctx;
+    }
+    cp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
+    cp.tok_in = last_token;
+    cp.pos = pos;
+    cp.out_tokens = out_tokens;
+    cp.out_hidden = out_hidden;
+    cp.n_draft = n_draft;
+    cp.status = h->wsp.status;
+    cp.abort_flag = h->ll_abort;
+    const int smem = mtp::cl_smem_bytes(cp);
+    if (smem <= 0) {
+      set_error("cluster path: shape not supported for this call");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
+    return mtp::run_cl(cp, smem, st);
+  }
   if (path == 3 || (path == 0 && B == 1 && h->ll_ok)) {
     if (!h->ll_ok || B != 1) {
       set_error("the latency path runs one sequence of a supported shape (B=%d, available=%d)", B, h->ll_ok);
@@ -645,8 +774,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 3) {
-    set_error("need a handle and path in {0, 1, 2, 3}");
+  if (!h || path < 0 || path > 4) {
+    set_error("need a handle and path in {0, 1, 2, 3, 4}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;
@@ -658,6 +787,7 @@ void mtp_destroy(mtp_handle* h) {
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
   cudaFree(h->ws);
+  if (h->temb_ord) cudaFree(h->temb_ord);
   free(h);
 }
 

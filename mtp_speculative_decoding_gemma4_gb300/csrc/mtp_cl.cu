@@ -1,0 +1,1004 @@
+// Cluster-path draft block (B = 1): see mtp_cl.cuh for the data flow.
+//
+// Failure handling: every wait is bounded. A wait that gives up records MTP_ERR_TIMEOUT and
+// raises the abort word; a raised abort word makes every later wait give up after a few
+// polls. Control flow never depends on a wait's outcome, so every thread keeps executing the
+// same sequence of named barriers, exchanges and ring releases and no barrier is left short
+// of arrivals. Values derived from exchanged data (centroid ids, token ids) are clamped
+// before they address memory. Before the CTA ends, its producer waits (time-bounded,
+// independent of the abort word) for its own copies still in flight, and a final cluster
+// barrier keeps every CTA alive while peers may still write to it.
+//
+// Work split inside a CTA (16 compute warps):
+//   GEMV slot: (row quad, k slice) tasks, one warp each; a warp reads four rows at once,
+//     keeps its x slice in registers and reduces the four dot products with one transposed
+//     butterfly; k-split partial sums are added in a fixed order (deterministic).
+//   scores: (key quad, head group, k slice) tasks; the heads sharing a KV head reuse each
+//     K load.
+//   weighted sum (V = K): a thread owns four dims of one KV head for a group of heads and one
+//     key group; key groups are lane groups of a warp, reduced by shuffles at the end.
+#include <cmath>
+#include <cstring>
+
+#include "mtp_cl.cuh"
+#include "mtp_launch.h"
+
+namespace mtp {
+namespace clk {
+
+// ------------------------------------------------------------------ primitives
+
+__device__ __forceinline__ unsigned sa(const void* p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ unsigned mapa(unsigned addr, int rank) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Asynchronous 4-byte store into a peer CTA's shared memory that counts its bytes on the
+// peer's mbarrier (both addresses in the shared::cluster window).
+__device__ __forceinline__ void st_async_f32(unsigned caddr, float v, unsigned cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+               "r"(__float_as_uint(v)), "r"(cbar)
+               : "memory");
+}
+__device__ __forceinline__ void arrive_local(unsigned bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// A waiting thread is suspended until the phase completes or this many ns pass, so waits
+// do not take issue slots from the warps that still compute.
+constexpr unsigned kSuspendNs = 100000;
+// Phase test of a ring barrier (filled by this CTA's copies / released by its own warps).
+__device__ __forceinline__ bool try_wait_cta(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+// Phase test of a receive barrier (bytes from peer CTAs, observed at cluster scope).
+__device__ __forceinline__ bool try_wait_cluster(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned ld_rlx32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Loads from shared memory by 32-bit shared address (hot loops keep addresses in one register).
+__device__ __forceinline__ uint4 lds128(unsigned a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 ldsf4(unsigned a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(unsigned a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ldsf(unsigned a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+// named barrier of the compute warps (the producer warp never takes part)
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+struct Fail {
+  int* status;
+  unsigned* abort_flag;
+  long long spin_limit;
+};
+// Bounded wait on an mbarrier phase. A raised abort word ends it early (false); running
+// past the time limit records MTP_ERR_TIMEOUT and raises the abort word (false).
+__device__ __noinline__ bool wait_bar(Fail f, unsigned bar, unsigned parity, bool cluster_scope) {
+  if (cluster_scope ? try_wait_cluster(bar, parity) : try_wait_cta(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (cluster_scope ? try_wait_cluster(bar, parity) : try_wait_cta(bar, parity)) return true;
+    if (ld_rlx32(f.abort_flag)) return false;
+    if (clock64() - t0 > f.spin_limit) {
+      set_status(f.status, MTP_ERR_TIMEOUT);
+      atomicExch(f.abort_flag, 1u);
+      return false;
+    }
+  }
+}
+// Time-bounded wait that ignores the abort word: the drain of this CTA's own copies.
+__device__ __noinline__ void drain_bar(Fail f, unsigned bar, unsigned parity) {
+  const long long t0 = clock64();
+  while (!try_wait_cta(bar, parity)) {
+    if (clock64() - t0 > f.spin_limit) {
+      set_status(f.status, MTP_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// RMSNorm factor 1/sqrt(mean(v^2) + eps) of a shared-memory vector. Every warp computes it
+// on its own, in the same order, so all threads get the same value without a barrier.
+__device__ __noinline__ float rms_inv(const float* v, int n, float eps) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int i = lane; i < n; i += 32) s = fmaf(v[i], v[i], s);
+  s = warp_sum(s);
+  return rsqrtf(s / n + eps);
+}
+
+// acc + the dot product of 8 bf16 weights (one 16-byte word) with 8 fp32 values
+__device__ __forceinline__ float dot8(uint4 w, float4 a, float4 b, float acc) {
+  acc = fmaf(__uint_as_float(w.x << 16), a.x, acc);
+  acc = fmaf(__uint_as_float(w.x & 0xffff0000u), a.y, acc);
+  acc = fmaf(__uint_as_float(w.y << 16), a.z, acc);
+  acc = fmaf(__uint_as_float(w.y & 0xffff0000u), a.w, acc);
+  acc = fmaf(__uint_as_float(w.z << 16), b.x, acc);
+  acc = fmaf(__uint_as_float(w.z & 0xffff0000u), b.y, acc);
+  acc = fmaf(__uint_as_float(w.w << 16), b.z, acc);
+  acc = fmaf(__uint_as_float(w.w & 0xffff0000u), b.w, acc);
+  return acc;
+}
+
+// Sums M per-lane values over the 32 lanes of a warp with one transposed butterfly: at each
+// of the first log2(M) levels a lane keeps half of its values and receives its partner's
+// share of them. Afterwards every lane holds the full sum of value index lane >> (5 - log2 M).
+template <int M>
+__device__ __forceinline__ float xreduce(float (&a)[M], int lane) {
+  int o = 16;
+#pragma unroll
+  for (int c = M; c > 1; c >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < c / 2; ++i) {
+      const float send = up ? a[i] : a[i + c / 2];
+      const float keep = up ? a[i + c / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+    o >>= 1;
+  }
+  float v = a[0];
+  for (; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+template <int M> struct Log2;
+template <> struct Log2<4> { static constexpr int v = 2; };
+template <> struct Log2<8> { static constexpr int v = 3; };
+template <> struct Log2<16> { static constexpr int v = 4; };
+
+// ------------------------------------------------------------------ stream schedule
+
+// One section of the stream: rows [0, nrows) of `row_bytes` each, row i at src + i*stride.
+struct Sec {
+  const char* src;
+  long long stride;
+  int row_bytes, nrows, rpc;  // rpc: rows per chunk (one ring slot)
+};
+__device__ __forceinline__ int n_chunks(const Sec& s) { return s.nrows > 0 ? (s.nrows + s.rpc - 1) / s.rpc : 0; }
+
+// Sections of one step, in the order the step consumes them:
+//   0 PRE | per block l: 1+6l Q, 2+6l K, 3+6l O, 4+6l gate, 5+6l up, 6+6l down | CENT | POST
+__device__ __forceinline__ int sec_count(const Params& p) { return 1 + 6 * p.nl + 2; }
+
+struct Keys {
+  int f_lo, f_n, s_lo, s_n;  // this CTA's keys of the full layers and of the sliding window
+};
+
+__device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
+  Sec s{nullptr, 0, 0, 0, 1};
+  auto rows = [&](const bf16* W, int R, int K) {
+    const Range rg = split(R, kNC, r);
+    s.src = reinterpret_cast<const char*>(W + static_cast<size_t>(rg.lo) * K);
+    s.row_bytes = K * 2;
+    s.stride = s.row_bytes;
+    s.nrows = rg.hi - rg.lo;
+  };
+  if (idx == 0) {
+    rows(p.pre, p.H, 2 * p.bb);
+  } else if (idx >= 1 + 6 * p.nl) {
+    if (idx == 1 + 6 * p.nl) rows(p.cent, p.C, p.H);
+    else rows(p.post, p.bb, p.H);
+  } else {
+    const int l = (idx - 1) / 6, what = (idx - 1) % 6;
+    const int lt = p.ltype[l], d = p.d[lt];
+    switch (what) {
+      case 0: rows(p.q[l], p.nh * d, p.H); break;
+      case 1: {
+        const int lo = lt ? kr.f_lo : kr.s_lo, n = lt ? kr.f_n : kr.s_n;
+        s.src = reinterpret_cast<const char*>(p.k[lt] + static_cast<size_t>(lo) * p.st[lt]);
+        s.row_bytes = p.nkv * d * 2;
+        s.stride = p.st[lt] * 2;
+        s.nrows = n;
+        break;
+      }
+      case 2: rows(p.o[l], p.H, p.nh * d); break;
+      case 3: rows(p.gate[l], p.F, p.H); break;
+      case 4: rows(p.up[l], p.F, p.H); break;
+      default: rows(p.down[l], p.H, p.F); break;
+    }
+  }
+  s.rpc = (idx >= 1 && idx < 1 + 6 * p.nl && (idx - 1) % 6 == 1) ? keys_per_slot(s.row_bytes) : rows_per_slot(s.row_bytes);
+  return s;
+}
+
+// Consumer side of the ring: shared addresses of the barriers and the generic slot base.
+struct Ring {
+  unsigned base, full0, empty0;  // shared addresses: slot 0, full barriers, empty barriers
+  Fail f;
+};
+__device__ __forceinline__ unsigned ring_wait(const Ring& rg, int g) {
+  const int slot = g % kSlots;
+  wait_bar(rg.f, rg.full0 + 8 * slot, static_cast<unsigned>((g / kSlots) & 1), false);
+  return rg.base + slot * kSlotBytes;
+}
+__device__ __forceinline__ void ring_release(const Ring& rg, int g) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) arrive_local(rg.empty0 + 8 * (g % kSlots));
+}
+
+// ------------------------------------------------------------------ phase functions
+
+// out[i] = W_i . x for the rows of a streamed section (chunk counter g at its first chunk);
+// x is fp32 in shared memory. Returns the chunk counter after the section.
+__device__ __noinline__ int gemv_sec(Ring rg, int g, Sec s, const float* x, float* out, float* part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nc = n_chunks(s), K = s.row_bytes / 2, V8 = K / 8;
+  const int ns = gemv_ns(s.rpc), nq = (s.rpc + 3) / 4, ntask = nq * ns;
+  const unsigned xs = sa(x);
+  for (int ch = 0; ch < nc; ++ch, ++g) {
+    const unsigned W = ring_wait(rg, g);
+    const int r0 = ch * s.rpc, n = min(s.rpc, s.nrows - r0);
+    for (int t = warp; t < ntask; t += kCW) {
+      const int rq = 4 * (t % nq), sl = t / nq;
+      if (rq >= n) continue;  // warp-uniform
+      const int vlo = V8 * sl / ns, vhi = V8 * (sl + 1) / ns;
+      const unsigned w0 = W + static_cast<unsigned>(min(rq, n - 1) * s.row_bytes);
+      const unsigned w1 = W + static_cast<unsigned>(min(rq + 1, n - 1) * s.row_bytes);
+      const unsigned w2 = W + static_cast<unsigned>(min(rq + 2, n - 1) * s.row_bytes);
+      const unsigned w3 = W + static_cast<unsigned>(min(rq + 3, n - 1) * s.row_bytes);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int v = vlo + lane; v < vhi; v += 32) {
+        const float4 xa = ldsf4(xs + 32 * v), xb = ldsf4(xs + 32 * v + 16);
+        const uint4 q0 = lds128(w0 + 16 * v), q1 = lds128(w1 + 16 * v);
+        const uint4 q2 = lds128(w2 + 16 * v), q3 = lds128(w3 + 16 * v);
+        acc[0] = dot8(q0, xa, xb, acc[0]);
+        acc[1] = dot8(q1, xa, xb, acc[1]);
+        acc[2] = dot8(q2, xa, xb, acc[2]);
+        acc[3] = dot8(q3, xa, xb, acc[3]);
+      }
+      const float val = xreduce<4>(acc, lane);
+      const int row = rq + (lane >> 3);
+      if ((lane & 7) == 0 && row < n) {
+        if (ns == 1) out[r0 + row] = val;
+        else part[sl * s.nrows + r0 + row] = val;
+      }
+    }
+    ring_release(rg, g);
+  }
+  if (ns > 1) {
+    cbar();
+    for (int i = threadIdx.x; i < s.nrows; i += kCT) {
+      float v = 0.f;
+      for (int sl = 0; sl < ns; ++sl) v += part[sl * s.nrows + i];
+      out[i] = v;
+    }
+  }
+  cbar();
+  return g;
+}
+
+// Scores of the nh heads against the n keys of one K slot (shared address K), scaled; with
+// ns > 1 k slices the partial scores go to ns slices of sstride floats each.
+template <int NHT>
+__device__ __noinline__ void qk_chunk(const Params& p, unsigned K, int n, const float* q, float* sc, int d, float scale,
+                                      int ns, int sstride) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nh = p.nh, nkv = p.nkv, hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
+  const int row = nkv * d, V8 = d / 8;
+  const int nq = (n + 3) / 4, base = nq * nhg;
+  const unsigned qs = sa(q);
+  for (int t = warp; t < base * ns; t += kCW) {
+    const int kq = 4 * (t % nq), hg = (t / nq) % nhg, sl = t / base;
+    if (kq >= n) continue;  // warp-uniform
+    const int gk = hg / HG, h0 = gk * hpg + (hg % HG) * NHT;
+    const int vlo = V8 * sl / ns, vhi = V8 * (sl + 1) / ns;
+    const unsigned k0 = K + 2u * static_cast<unsigned>(min(kq, n - 1) * row + gk * d);
+    const unsigned k1 = K + 2u * static_cast<unsigned>(min(kq + 1, n - 1) * row + gk * d);
+    const unsigned k2 = K + 2u * static_cast<unsigned>(min(kq + 2, n - 1) * row + gk * d);
+    const unsigned k3 = K + 2u * static_cast<unsigned>(min(kq + 3, n - 1) * row + gk * d);
+    const unsigned qh0 = qs + 4u * static_cast<unsigned>(h0 * d);
+    float a[4 * NHT];
+#pragma unroll
+    for (int i = 0; i < 4 * NHT; ++i) a[i] = 0.f;
+    for (int v = vlo + lane; v < vhi; v += 32) {
+      const uint4 kw0 = lds128(k0 + 16 * v), kw1 = lds128(k1 + 16 * v);
+      const uint4 kw2 = lds128(k2 + 16 * v), kw3 = lds128(k3 + 16 * v);
+#pragma unroll
+      for (int th = 0; th < NHT; ++th) {
+        const unsigned qa_ = qh0 + 4u * static_cast<unsigned>(th * d) + 32 * v;
+        const float4 qa = ldsf4(qa_), qb = ldsf4(qa_ + 16);
+        a[0 * NHT + th] = dot8(kw0, qa, qb, a[0 * NHT + th]);
+        a[1 * NHT + th] = dot8(kw1, qa, qb, a[1 * NHT + th]);
+        a[2 * NHT + th] = dot8(kw2, qa, qb, a[2 * NHT + th]);
+        a[3 * NHT + th] = dot8(kw3, qa, qb, a[3 * NHT + th]);
+      }
+    }
+    const float val = xreduce<4 * NHT>(a, lane);
+    const int idx = lane >> (5 - Log2<4 * NHT>::v);
+    const int key = kq + idx / NHT, h = h0 + idx % NHT;
+    if ((lane & ((32 >> Log2<4 * NHT>::v) - 1)) == 0 && key < n) sc[sl * sstride + key * nh + h] = val * scale;
+  }
+}
+
+// Attention of the nh query heads over this CTA's keys of one block (online softmax over the
+// streamed K chunks, V = K). q: [nh][d] after q_norm and RoPE. Leaves in stage the
+// unnormalised sums [nh][d] followed by (m_h, l_h) of every head. Returns the chunk counter.
+template <int NHT>
+__device__ __noinline__ int att_sec(const Params& p, Ring rg, int g, Sec s, int d, float scale, const float* q,
+                                    float* sc, float* red, float* stage) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nh = p.nh, nkv = p.nkv, hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
+  const int row = nkv * d, V8 = d / 8, DQ = d / 4;
+  const int nc = n_chunks(s);
+  // score tasks: (key quad, head group, k slice)
+  const int nq = (s.rpc + 3) / 4, base = nq * nhg;
+  int ns = 1;
+  while (ns * 2 <= kQkSlices && ns * 2 * base <= kCW && V8 / (ns * 2) >= 32) ns *= 2;
+  const int sstride = s.rpc * nh;  // floats per score slice; two alternating buffers of ns slices
+  // weighted-sum slots: (head group, dim quad) per thread, key groups in lane bits
+  const int D = nhg * DQ;
+  int kgw = 1;
+  while (kgw * 2 <= 32 && D * kgw * 2 <= kCT) kgw *= 2;
+  const int lpk = 32 / kgw, slot = warp * lpk + lane % lpk, kg = lane / lpk;
+  const bool own = slot < D;
+  const int dq = own ? slot % DQ : 0, hgi = own ? slot / DQ : 0;
+  const int gk_pv = hgi / HG, h0_pv = gk_pv * hpg + (hgi % HG) * NHT;
+  float acc[NHT][4];
+#pragma unroll
+  for (int t = 0; t < NHT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+
+  for (int ch = 0; ch < nc; ++ch, ++g) {
+    const unsigned K = ring_wait(rg, g);
+    const int n = min(s.rpc, s.nrows - ch * s.rpc);
+    float* scb = sc + (ch & 1) * (kQkSlices * sstride);
+    qk_chunk<NHT>(p, K, n, q, scb, d, scale, ns, sstride);
+    cbar();
+    // ---- running max / exp-sum: one warp per head; probabilities overwrite slice 0
+    if (warp < nh) {
+      float cm = -INFINITY;
+      for (int j = lane; j < n; j += 32) {
+        float v = scb[j * nh + warp];
+        for (int sl = 1; sl < ns; ++sl) v += scb[sl * sstride + j * nh + warp];
+        scb[j * nh + warp] = v;
+        cm = fmaxf(cm, v);
+      }
+      cm = warp_max(cm);
+      const float mold = red[48 + warp];
+      const float mnew = fmaxf(mold, cm);
+      float ls = 0.f;
+      for (int j = lane; j < n; j += 32) {
+        const float e = expf(scb[j * nh + warp] - mnew);
+        scb[j * nh + warp] = e;
+        ls += e;
+      }
+      ls = warp_sum(ls);
+      if (lane == 0) {
+        const float corr = expf(mold - mnew);
+        red[80 + warp] = corr;
+        red[64 + warp] = red[64 + warp] * corr + ls;
+        red[48 + warp] = mnew;
+      }
+    }
+    cbar();
+    // ---- weighted sum of the keys
+    if (own) {
+#pragma unroll
+      for (int t = 0; t < NHT; ++t) {
+        const float c = red[80 + h0_pv + t];
+        acc[t][0] *= c;
+        acc[t][1] *= c;
+        acc[t][2] *= c;
+        acc[t][3] *= c;
+      }
+      const unsigned kb = K + 2u * static_cast<unsigned>(gk_pv * d + 4 * dq);
+      for (int j = kg; j < n; j += kgw) {
+        const uint2 raw = lds64(kb + 2u * static_cast<unsigned>(j * row));
+        const float k0 = __uint_as_float(raw.x << 16), k1 = __uint_as_float(raw.x & 0xffff0000u);
+        const float k2 = __uint_as_float(raw.y << 16), k3 = __uint_as_float(raw.y & 0xffff0000u);
+        const unsigned pj = sa(scb) + 4u * static_cast<unsigned>(j * nh + h0_pv);
+#pragma unroll
+        for (int t = 0; t < NHT; ++t) {
+          const float w = ldsf(pj + 4 * t);
+          acc[t][0] = fmaf(w, k0, acc[t][0]);
+          acc[t][1] = fmaf(w, k1, acc[t][1]);
+          acc[t][2] = fmaf(w, k2, acc[t][2]);
+          acc[t][3] = fmaf(w, k3, acc[t][3]);
+        }
+      }
+    }
+    // no barrier here: the next chunk's scores go to the other buffer, and the barrier after
+    // them orders this chunk's reads of its buffer before that buffer is written again
+    ring_release(rg, g);
+  }
+  // key groups -> one sum per (head, dim)
+#pragma unroll
+  for (int t = 0; t < NHT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      for (int o = lpk; o < 32; o <<= 1) acc[t][i] += __shfl_xor_sync(0xffffffffu, acc[t][i], o);
+  if (own && kg == 0) {
+#pragma unroll
+    for (int t = 0; t < NHT; ++t)
+      *reinterpret_cast<float4*>(stage + (h0_pv + t) * d + 4 * dq) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+  }
+  if (tid < nh) {
+    stage[nh * d + 2 * tid] = red[48 + tid];
+    stage[nh * d + 2 * tid + 1] = red[64 + tid];
+  }
+  cbar();
+  return g;
+}
+
+// Logits of the rows of this CTA's selected centroids [slo, shi) (contiguous blocks of the
+// cluster-ordered embedding copy) against y; each warp's best (value, id) key goes to lk.
+__device__ __noinline__ void gather_best(const Params& p, const int* selc, int slo, int shi, const float* y,
+                                         unsigned long long* lk) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.H, vsc = p.vsc;
+  unsigned long long best = 0ull;
+  for (int c = slo; c < shi; ++c) {
+    const size_t base = static_cast<size_t>(selc[c]) * vsc;
+    for (int jb = warp * 8; jb < vsc; jb += kCW * 8) {
+      const int myrow = jb + (lane >> 2);  // the row this lane holds after the reduction
+      const int id = myrow < vsc ? __ldg(p.ord + base + myrow) : 0;
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = 0.f;
+      for (int k = lane * 8; k < H; k += 256) {
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          raw[i] = __ldcs(reinterpret_cast<const uint4*>(p.temb_ord + (base + min(jb + i, vsc - 1)) * H + k));
+        const float4 ya = *reinterpret_cast<const float4*>(y + k);
+        const float4 yb = *reinterpret_cast<const float4*>(y + k + 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = dot8(raw[i], ya, yb, a[i]);
+      }
+      const float v = xreduce<8>(a, lane);
+      if ((lane & 3) == 0 && myrow < vsc) {
+        const unsigned long long key = argmax_key(v, id);
+        best = key > best ? key : best;
+      }
+    }
+  }
+  best = warp_max_u64(best);
+  if (lane == 0) lk[warp] = best;
+}
+
+// Global top-k by rank over kNC sorted (descending) lists of k keys ([kNC][k][hi word, lo
+// word]): a key's rank is the sum over the lists of the number of keys greater than it,
+// found by binary searches run side by side; keys of rank < k go to selc[rank].
+__device__ __noinline__ void merge_rank(const unsigned* lists, int k, int C, int* selc) {
+  auto key_at = [&](int s1, int i) -> unsigned long long {
+    return (static_cast<unsigned long long>(lists[(s1 * k + i) * 2]) << 32) | lists[(s1 * k + i) * 2 + 1];
+  };
+  int top = 1;
+  while (top * 2 <= k) top *= 2;
+  for (int t = threadIdx.x; t < kNC * k; t += kCT) {
+    const unsigned long long e = key_at(t / k, t % k);
+    int pos[kNC];
+#pragma unroll
+    for (int s1 = 0; s1 < kNC; ++s1) pos[s1] = 0;
+    for (int step = top; step > 0; step >>= 1) {
+#pragma unroll
+      for (int s1 = 0; s1 < kNC; ++s1)
+        if (pos[s1] + step <= k && key_at(s1, pos[s1] + step - 1) > e) pos[s1] += step;
+    }
+    int rank = 0;
+#pragma unroll
+    for (int s1 = 0; s1 < kNC; ++s1) rank += pos[s1];
+    if (rank < k) selc[rank] = min(max(key_id(e), 0), C - 1);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) char sm[];
+  const Layout L = make_layout(p);
+  unsigned rank_u;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank_u));
+  const int r = static_cast<int>(rank_u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(sm + L.bars);
+  const unsigned full0 = sa(bars), empty0 = sa(bars + kSlots), xbar0 = sa(bars + 2 * kSlots);
+  const unsigned ring0 = sa(sm + L.ring);
+  // receive buffers: set 1 directly follows set 0
+  float* const xb0 = reinterpret_cast<float*>(sm + L.xch0);
+  const unsigned xba0 = sa(sm + L.xch0);
+  float* u = reinterpret_cast<float*>(sm + L.u);
+  float* x = reinterpret_cast<float*>(sm + L.x);
+  float* a = reinterpret_cast<float*>(sm + L.a);
+  float* rowsb = reinterpret_cast<float*>(sm + L.rows);
+  float* gtb = reinterpret_cast<float*>(sm + L.gt);
+  float* utb = reinterpret_cast<float*>(sm + L.ut);
+  float* part = reinterpret_cast<float*>(sm + L.part);
+  float* sc = reinterpret_cast<float*>(sm + L.sc);
+  float* red = reinterpret_cast<float*>(sm + L.red);
+  float2* cs = reinterpret_cast<float2*>(sm + L.cs);
+  unsigned long long* lk = reinterpret_cast<unsigned long long*>(sm + L.lk);
+  int* selc = reinterpret_cast<int*>(sm + L.ids);
+  const Fail fl{p.status, p.abort_flag, p.spin_limit};
+
+  // this CTA's keys: a contiguous share of the full layers' [0, L) and of the window
+  Keys kr{0, 0, 0, 0};
+  {
+    const int Lf = p.has_type[1] ? min(max(p.ctx_len[1][0], 0), p.kv_max[1]) : 0;
+    const int Ls = p.has_type[0] ? min(max(p.ctx_len[0][0], 0), p.kv_max[0]) : 0;
+    const int ws_lo = max(0, Ls - p.W);
+    const Range f = split(Lf, kNC, r), s = split(Ls - ws_lo, kNC, r);
+    kr = Keys{f.lo, f.hi - f.lo, ws_lo + s.lo, s.hi - s.lo};
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kCW);
+    }
+    mbar_init(xbar0, 1);  // receive barriers: the local expect_tx arrival + the bytes of the peers
+    mbar_init(xbar0 + 8, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // RoPE (cos, sin) at the block's position: the angle pos * theta^(-2i/d) in fp64, reduced
+  // mod 2 pi, then fp32 sin / cos
+  for (int t = 0; t < 2; ++t) {
+    const int d = p.has_type[t] ? p.d[t] : 0;
+    const double theta = p.theta[t];
+    for (int i = tid; i < d / 2; i += kT) {
+      float2 v = make_float2(1.f, 0.f);
+      if (theta != 0.0) {
+        const double two_pi = 6.283185307179586476925286766559;
+        double ang = static_cast<double>(p.pos[0]) * exp2(-2.0 * i / d * log2(theta));
+        ang -= two_pi * floor(ang / two_pi);
+        float sv, cv;
+        sincosf(static_cast<float>(ang), &sv, &cv);
+        v = make_float2(cv, sv);
+      }
+      cs[(t ? L.cs_off1 : 0) + i] = v;
+    }
+  }
+  // every barrier of the cluster is initialised before any CTA arrives on a peer's
+  cluster_sync_all();
+
+  const int nsec = sec_count(p);
+  if (warp == kCW) {
+    // ====================== producer warp: stream every section of every step in order
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int step = 0; step < p.n_draft && ok; ++step) {
+        for (int si = 0; si < nsec && ok; ++si) {
+          const Sec s = make_sec(p, si, r, kr);
+          const int nc = n_chunks(s);
+          for (int ch = 0; ch < nc; ++ch) {
+            const int slot = g % kSlots;
+            if (g >= kSlots && !wait_bar(fl, empty0 + 8 * slot, static_cast<unsigned>((g / kSlots - 1) & 1), false)) {
+              ok = false;
+              break;
+            }
+            const int r0 = ch * s.rpc, n = min(s.rpc, s.nrows - r0);
+            const unsigned bytes = static_cast<unsigned>(n * s.row_bytes);
+            const unsigned fb = full0 + 8 * slot, dst = ring0 + slot * kSlotBytes;
+            mbar_expect_tx(fb, bytes);
+            if (s.stride == s.row_bytes) {
+              bulk_g2s(dst, s.src + static_cast<size_t>(r0) * s.row_bytes, bytes, fb);
+            } else {
+              for (int j = 0; j < n; ++j)
+                bulk_g2s(dst + j * s.row_bytes, s.src + static_cast<size_t>(r0 + j) * s.stride,
+                         static_cast<unsigned>(s.row_bytes), fb);
+            }
+            ++g;
+          }
+        }
+      }
+      // no copy of this CTA may still be in flight when it ends
+      for (int h = (g > kSlots ? g - kSlots : 0); h < g; ++h)
+        drain_bar(fl, full0 + 8 * (h % kSlots), static_cast<unsigned>((h / kSlots) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ====================== compute warps
+    const Ring rg{ring0, full0, empty0, fl};
+    int gc = 0;  // chunks consumed
+    int xe = 0;  // exchanges done: buffer xe & 1, phase parity (xe >> 1) & 1
+    const int H = p.H;
+
+    // Exchange protocol. Each exchange uses receive buffer xe & 1 and its mbarrier (phase
+    // parity (xe >> 1) & 1). The receiver arms the barrier with the number of bytes it will get
+    // (one local arrival); warp w of every CTA writes that CTA's payload for CTA w with
+    // st.async, whose bytes complete on CTA w's barrier. A buffer is rewritten only two
+    // exchanges later, which no CTA can start before every CTA has sent the exchange in
+    // between, i.e. has finished reading this one (a named barrier separates every last read
+    // from the next send).
+    // After a failed exchange wait a thread neither arms nor sends any more: a barrier must not
+    // get a second arrival in an unfinished phase, nor unbounded bytes without an arm.
+    bool live = true;
+    auto xch_arm = [&](int nfloats) {
+      if (tid == 0 && live) mbar_expect_tx(xbar0 + 8 * (xe & 1), 4u * static_cast<unsigned>(nfloats));
+    };
+    auto xch_dst = [&](int w) { return mapa(xba0 + (xe & 1) * (kXchFloats * 4), w); };
+    auto xch_bar = [&](int w) { return mapa(xbar0 + 8 * (xe & 1), w); };
+    // The named barrier first: a warp past its receive wait must not overwrite the staged
+    // slice a sibling warp is still sending (the wait only covers this CTA's incoming data).
+    auto xch_wait = [&]() -> float* {
+      const int cur = xe & 1;
+      cbar();
+      if (live && !wait_bar(fl, xbar0 + 8 * cur, static_cast<unsigned>((xe >> 1) & 1), true)) live = false;
+      ++xe;
+      return xb0 + cur * kXchFloats;
+    };
+    // all-gather of a vector of `total` floats: every CTA receives this CTA's slice [lo, hi)
+    // (held in src from index 0)
+    auto all_gather = [&](int lo, int hi, const float* src, int total) -> float* {
+      xch_arm(total);
+      if (warp < kNC && live) {
+        const unsigned base = xch_dst(warp) + 4u * static_cast<unsigned>(lo), rb = xch_bar(warp);
+        for (int i = lane; i < hi - lo; i += 32) st_async_f32(base + 4u * i, src[i], rb);
+      }
+      return xch_wait();
+    };
+    auto sec = [&](int idx) { return make_sec(p, idx, r, kr); };
+
+    int tok = 0;
+    for (int step = 0; step < p.n_draft; ++step) {
+      // ================= PRE: x0 = W_pre [h ; embed(token)]
+      {
+        if (step == 0) {
+          tok = p.tok_in[0];
+          for (int i = tid * 8; i < p.bb; i += kCT * 8) load_vec(p.hidden_in + i, u + i);
+        }
+        if (tok < 0 || tok >= p.V) {
+          if (r == 0 && tid == 0) set_status(p.status, MTP_ERR_INVALID_ARG);
+          tok = 0;
+        }
+        const bf16* er = p.tgt + static_cast<size_t>(tok) * p.bb;
+        for (int i = tid * 8; i < p.bb; i += kCT * 8) load_vec(er + i, u + p.bb + i);
+        cbar();
+        gc = gemv_sec(rg, gc, sec(0), u, rowsb, part);
+        const Range rg0 = split(H, kNC, r);
+        const float* xg = all_gather(rg0.lo, rg0.hi, rowsb, H);
+        for (int i = tid; i < H; i += kCT) x[i] = xg[i];
+        cbar();
+      }
+      // ================= decoder blocks
+      for (int l = 0; l < p.nl; ++l) {
+        const int lt = p.ltype[l], d = p.d[lt], QD = p.nh * d;
+        const Range hr = split(H, kNC, r);
+        // ---- Q rows of attn_norm(x)
+        {
+          const float rf = rms_inv(x, H, p.eps);
+          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * __ldg(p.attn_norm[l] + i);
+          cbar();
+          gc = gemv_sec(rg, gc, sec(1 + 6 * l), a, rowsb, part);
+        }
+        const Range qr = split(QD, kNC, r);
+        float* q = all_gather(qr.lo, qr.hi, rowsb, QD);
+        // ---- q_norm + RoPE in place (the receive buffer stays ours until the next-but-one exchange)
+        {
+          if (warp < p.nh) {
+            float s = 0.f;
+            for (int i = lane * 4; i < d; i += 128) {
+              const float4 v = *reinterpret_cast<const float4*>(q + warp * d + i);
+              s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+            s = warp_sum(s);
+            if (lane == 0) red[32 + warp] = rsqrtf(s / d + p.eps);
+          }
+          cbar();
+          const float2* c2 = cs + (lt ? L.cs_off1 : 0);
+          const float* gq = p.q_norm[l];
+          const int half = d / 2;
+          for (int idx = tid; idx < p.nh * half; idx += kCT) {
+            const int h = idx / half, i = idx % half;
+            const float rfq = red[32 + h];
+            const float av = q[h * d + i] * rfq * __ldg(gq + i);
+            const float bv = q[h * d + i + half] * rfq * __ldg(gq + i + half);
+            q[h * d + i] = av * c2[i].x - bv * c2[i].y;
+            q[h * d + i + half] = bv * c2[i].x + av * c2[i].y;
+          }
+          if (tid < p.nh) {  // running max and exp-sum of every head
+            red[48 + tid] = -INFINITY;
+            red[64 + tid] = 0.f;
+          }
+          cbar();
+        }
+        // ---- attention over this CTA's keys
+        {
+          const Sec s = sec(2 + 6 * l);
+          const int hpg = p.nh / p.nkv;
+          if (hpg % 4 == 0) gc = att_sec<4>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          else if (hpg == 2) gc = att_sec<2>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          else gc = att_sec<1>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+        }
+        // ---- partials to the owner of each output dim: CTA w receives, from every CTA r,
+        // [m_0 l_0 .. m_nh-1 l_nh-1 | r's sums of w's dims] at offset r * per
+        const int per = 2 * p.nh + split_max(QD, kNC);
+        const Range dr = split(QD, kNC, r);
+        xch_arm(kNC * (2 * p.nh + (dr.hi - dr.lo)));
+        if (warp < kNC && live) {
+          const Range dw = split(QD, kNC, warp);
+          const unsigned base = xch_dst(warp) + 4u * static_cast<unsigned>(r * per), rb = xch_bar(warp);
+          for (int i = lane; i < 2 * p.nh + (dw.hi - dw.lo); i += 32)
+            st_async_f32(base + 4u * i, i < 2 * p.nh ? rowsb[QD + i] : rowsb[dw.lo + i - 2 * p.nh], rb);
+        }
+        const float* pb = xch_wait();
+        // ---- combine this CTA's dims: per head, the weight of every source's partial sums
+        // exp(m_s - M) / sum_s' exp(m_s' - M) l_s'; then one thread per dim
+        float* wgt = sc;  // [nh][kNC]
+        if (tid < p.nh) {
+          const int h = tid;
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < kNC; ++s2) M = fmaxf(M, pb[s2 * per + 2 * h]);
+          float den = 0.f;
+          for (int s2 = 0; s2 < kNC; ++s2) {
+            const float e = M == -INFINITY ? 0.f : expf(pb[s2 * per + 2 * h] - M);
+            wgt[h * kNC + s2] = e;
+            den = fmaf(e, pb[s2 * per + 2 * h + 1], den);
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;
+          for (int s2 = 0; s2 < kNC; ++s2) wgt[h * kNC + s2] *= inv;
+        }
+        cbar();
+        for (int fi = tid; fi < dr.hi - dr.lo; fi += kCT) {
+          const float* wh = wgt + ((dr.lo + fi) / d) * kNC;
+          float v = 0.f;
+          for (int s2 = 0; s2 < kNC; ++s2) v = fmaf(wh[s2], pb[s2 * per + 2 * p.nh + fi], v);
+          rowsb[fi] = v;
+        }
+        cbar();
+        const float* o = all_gather(dr.lo, dr.hi, rowsb, QD);
+        // ---- O rows, residual with post_attn_norm, ffn_norm
+        gc = gemv_sec(rg, gc, sec(3 + 6 * l), o, rowsb, part);
+        const float* op = all_gather(hr.lo, hr.hi, rowsb, H);
+        {
+          const float rf = rms_inv(op, H, p.eps);
+          for (int i = tid; i < H; i += kCT) x[i] = x[i] + op[i] * rf * __ldg(p.post_attn_norm[l] + i);
+          cbar();
+          const float rf2 = rms_inv(x, H, p.eps);
+          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf2 * __ldg(p.ffn_norm[l] + i);
+          cbar();
+        }
+        // ---- MLP: gate / up rows, m = gelu_tanh(gate) * up, down rows
+        gc = gemv_sec(rg, gc, sec(4 + 6 * l), a, gtb, part);
+        gc = gemv_sec(rg, gc, sec(5 + 6 * l), a, utb, part);
+        const Range fr = split(p.F, kNC, r);
+        for (int i = tid; i < fr.hi - fr.lo; i += kCT) rowsb[i] = gelu_tanh(gtb[i]) * utb[i];
+        cbar();
+        const float* mv = all_gather(fr.lo, fr.hi, rowsb, p.F);
+        gc = gemv_sec(rg, gc, sec(6 + 6 * l), mv, rowsb, part);
+        const float* dn = all_gather(hr.lo, hr.hi, rowsb, H);
+        {
+          const float rf = rms_inv(dn, H, p.eps);
+          for (int i = tid; i < H; i += kCT) x[i] = p.lambda[l] * (x[i] + dn[i] * rf * __ldg(p.post_ffn_norm[l] + i));
+          cbar();
+        }
+      }
+      // ================= HEAD
+      const int k = p.topk;
+      {
+        const float rf = rms_inv(x, H, p.eps);
+        for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * __ldg(p.out_norm + i);  // a = y
+        cbar();
+      }
+      // centroid logits of this CTA's centroids -> local top-k (warp 0)
+      gc = gemv_sec(rg, gc, sec(1 + 6 * p.nl), a, gtb, part);
+      {
+        // local top-k by rank: key i goes to position #{j : key_j > key_i} when that is < k
+        const Range cr = split(p.C, kNC, r);
+        const int nce = cr.hi - cr.lo;
+        unsigned long long* ck = reinterpret_cast<unsigned long long*>(sc);
+        for (int i = tid; i < nce; i += kCT) ck[i] = argmax_key(gtb[i], cr.lo + i);
+        cbar();
+        for (int i = tid; i < nce; i += kCT) {
+          const unsigned long long key = ck[i];
+          int rank = 0;
+          for (int j = 0; j < nce; ++j) rank += ck[j] > key ? 1 : 0;
+          if (rank < k) lk[rank] = key;
+        }
+      }
+      // post rows -> this CTA's slice of h' (output, and the next step's input)
+      gc = gemv_sec(rg, gc, sec(2 + 6 * p.nl), a, rowsb, part);
+      const Range br = split(p.bb, kNC, r);
+      if (p.out_hidden)
+        for (int i = tid; i < br.hi - br.lo; i += kCT) p.out_hidden[static_cast<size_t>(step) * p.bb + br.lo + i] = rowsb[i];
+      for (int i = tid; i < k; i += kCT) {
+        gtb[2 * i] = __uint_as_float(static_cast<unsigned>(lk[i] >> 32));
+        gtb[2 * i + 1] = __uint_as_float(static_cast<unsigned>(lk[i]));
+      }
+      cbar();
+      // exchange: every CTA receives [h' (bb floats) | kNC local top-k lists of 2k words]
+      xch_arm(p.bb + kNC * 2 * k);
+      if (warp < kNC && live) {
+        const unsigned base = xch_dst(warp), rb = xch_bar(warp);
+        for (int i = lane; i < br.hi - br.lo; i += 32) st_async_f32(base + 4u * (br.lo + i), rowsb[i], rb);
+        for (int i = lane; i < 2 * k; i += 32) st_async_f32(base + 4u * (p.bb + r * 2 * k + i), gtb[i], rb);
+      }
+      const float* hx = xch_wait();
+      for (int i = tid; i < p.bb; i += kCT) u[i] = hx[i];
+      // global top-k by rank over the kNC sorted lists: key i of list s has rank
+      // sum over lists of #{keys > it}, found by binary searches run side by side
+      merge_rank(reinterpret_cast<const unsigned*>(hx + p.bb), k, p.C, selc);
+      cbar();
+      // ---- logits of this CTA's share of the candidate rows -> best key per warp
+      {
+        const Range sr = split(k, kNC, r);
+        gather_best(p, selc, sr.lo, sr.hi, a, lk);
+      }
+      cbar();
+      if (warp == 0) {
+        unsigned long long m = lane < kCW ? lk[lane] : 0ull;
+        m = warp_max_u64(m);
+        if (lane == 0) {
+          gtb[0] = __uint_as_float(static_cast<unsigned>(m >> 32));
+          gtb[1] = __uint_as_float(static_cast<unsigned>(m));
+        }
+        if (m != 0ull) {  // warm L2 with the embedding row of this CTA's best token
+          const int id = min(max(key_id(m), 0), p.V - 1);
+          const char* er = reinterpret_cast<const char*>(p.tgt + static_cast<size_t>(id) * p.bb);
+          for (int off = lane * 128; off < p.bb * 2; off += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(er + off));
+        }
+      }
+      cbar();
+      const float* kx = all_gather(2 * r, 2 * r + 2, gtb, 2 * kNC);
+      unsigned long long m = 0ull;
+      for (int i = 0; i < kNC; ++i) {
+        const unsigned long long kv = (static_cast<unsigned long long>(__float_as_uint(kx[2 * i])) << 32) |
+                                      __float_as_uint(kx[2 * i + 1]);
+        m = kv > m ? kv : m;
+      }
+      tok = min(max(key_id(m), 0), p.V - 1);
+      if (r == 0 && tid == 0) p.out_tokens[step] = tok;
+      cbar();
+    }
+  }
+  // no CTA leaves while a peer may still write into its shared memory
+  cluster_sync_all();
+}
+
+}  // namespace clk
+
+// Host: shared-memory bytes of the cluster kernel for these parameters, or 0 when the shape
+// is outside the kernel's limits.
+int cl_smem_bytes(const clk::Params& p) {
+  using namespace clk;
+  if (p.nl < 1 || p.nl > kMaxL) return 0;
+  int dmax = 0;
+  for (int l = 0; l < p.nl; ++l) {
+    const int d = p.d[p.ltype[l]];
+    if (d < 8 || d % 8) return 0;
+    dmax = d > dmax ? d : dmax;
+  }
+  const int per = 2 * p.nh + split_max(p.nh * dmax, kNC);
+  // weighted-sum slots (head groups x dim quads) must fit the compute threads
+  const int hpg = p.nkv > 0 ? p.nh / p.nkv : 0;
+  const int nht = hpg % 4 == 0 ? 4 : (hpg == 2 ? 2 : 1);
+  if (hpg < 1 || p.nkv * (hpg / nht) * (dmax / 4) > kCT) return 0;
+  const bool fits =
+      p.H % 8 == 0 && p.bb % 8 == 0 && p.F % 8 == 0 && p.H >= 8 &&  // 16-byte rows and vector loads
+      p.nh >= 1 && p.nh <= 16 && p.nkv >= 1 && p.nh % p.nkv == 0 &&
+      p.nh * dmax <= 4 * kCT &&                                      // 4 output dims per compute thread
+      p.nh * dmax <= kXchFloats && kNC * per <= kXchFloats && p.F <= kXchFloats && p.H <= kXchFloats &&
+      p.bb + kNC * 2 * p.topk <= kXchFloats && 2 * kNC <= kXchFloats &&
+      2 * p.bb * 2 <= kSlotBytes && p.H * 2 <= kSlotBytes && p.F * 2 <= kSlotBytes &&
+      p.nh * dmax * 2 <= kSlotBytes && p.nkv * dmax * 2 <= kSlotBytes &&
+      p.topk >= 1 && p.topk <= 64 && p.C >= kNC && split_max(p.C, kNC) <= 128 && p.topk <= p.C / kNC &&
+      p.vsc > 0 && static_cast<long long>(p.C) * p.vsc == p.V;
+  if (!fits) return 0;
+  return make_layout(p).total;
+}
+
+int run_cl(const clk::Params& p, int smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(clk::k_block_cl, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(clk::k_block_cl, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) {
+    set_error("cluster kernel attributes: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clk::kNC);
+  cfg.blockDim = dim3(clk::kT);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = clk::kNC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, clk::k_block_cl, p);
+  if (e != cudaSuccess) {
+    set_error("cluster draft-block launch (%d CTAs, %d B shared memory): %s", clk::kNC, smem, cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+// Number of kNC-CTA clusters of this kernel that can be resident at once (0: none).
+int cl_capacity(int smem) {
+  if (cudaFuncSetAttribute(clk::k_block_cl, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(clk::k_block_cl, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clk::kNC);
+  cfg.blockDim = dim3(clk::kT);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = clk::kNC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<void*>(clk::k_block_cl), &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// dst[j] = src[ord[j]] for the V rows of H elements: token_embd in token_ordering order, so
+// that the rows of one centroid are one contiguous block.
+__global__ void k_reorder_rows(const __nv_bfloat16* __restrict__ src, const int* __restrict__ ord,
+                               __nv_bfloat16* __restrict__ dst, int V, int H) {
+  const int vec = H / 8;
+  const long long total = static_cast<long long>(V) * vec;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / vec, c = i % vec;
+    const int s = ord[row];
+    reinterpret_cast<uint4*>(dst + row * H)[c] = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * H)[c];
+  }
+}
+
+int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaStream_t st) {
+  k_reorder_rows<<<1024, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), ord, static_cast<__nv_bfloat16*>(dst), V,
+                                       H);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("reordering token_embd: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+}  // namespace mtp

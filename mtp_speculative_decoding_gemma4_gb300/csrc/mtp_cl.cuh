@@ -1,0 +1,159 @@
+// Cluster-path draft block for one sequence (B = 1): the whole drafter step runs inside one
+// thread-block cluster of NC CTAs (one per SM). In every CTA a producer warp streams the
+// CTA's row-slices of each weight matrix and its share of the shared K, in the order the
+// step consumes them, through a ring of shared-memory slots filled by TMA bulk copies
+// (full / empty mbarriers); sixteen compute warps consume the slots. Vectors are exchanged
+// inside the cluster only: each CTA writes its slice into every CTA's receive buffer with
+// st.async, whose bytes complete on the receiver's mbarrier (armed by the receiver with the
+// byte count it expects); receive buffers and their mbarriers alternate between two sets.
+//
+// Step (rows of every GEMV split over the NC CTAs; every CTA keeps its own residual x):
+//   PRE   token from the last exchange; u = [h ; embed(token)]; x0[rows] = W_pre u  -> all x0
+//   per block: Q rows -> all q; q_norm + RoPE; attention over this CTA's keys (online
+//     softmax over the streamed K chunks) -> partials to the owner of each output dim;
+//     owners combine -> all o; O rows -> all o'; x += norm(o'); f = norm(x);
+//     gate/up rows -> m rows -> all m; W_down rows -> all dn; x = lambda (x + norm(dn))
+//   HEAD  y = output_norm(x); centroid rows -> local top-k; post rows -> h';
+//         exchange (h', local top-k lists); rank merge -> selected centroids; this CTA's
+//         selected clusters' rows of the cluster-ordered token_embd copy -> logits ->
+//         local argmax -> exchange keys -> next token
+#pragma once
+
+#include "mtp_common.cuh"
+#include "mtp.h"
+
+namespace mtp {
+namespace clk {
+
+constexpr int kNC = 16;            // CTAs per cluster
+constexpr int kCW = 16;            // compute warps
+constexpr int kCT = kCW * 32;      // compute threads
+constexpr int kT = kCT + 32;       // + one producer warp
+constexpr int kSlots = 5;
+constexpr int kSlotBytes = 32768;
+constexpr int kMaxL = 8;
+constexpr int kXchFloats = 4096;   // floats per receive buffer
+
+typedef __nv_bfloat16 bf16;
+
+struct Range {
+  int lo, hi;
+};
+__host__ __device__ inline Range split(int R, int N, int c) {
+  const long long lo = static_cast<long long>(R) * c / N, hi = static_cast<long long>(R) * (c + 1) / N;
+  return Range{static_cast<int>(lo), static_cast<int>(hi)};
+}
+__host__ __device__ inline int split_max(int R, int N) { return (R + N - 1) / N; }
+
+struct Params {
+  int bb, H, nl, nh, nkv, F, V, C, topk, vsc, W;
+  int d[2];
+  float scale[2], theta[2], eps;
+  int ltype[kMaxL];
+  float lambda[kMaxL];
+  const bf16 *pre, *post, *cent, *tgt;
+  const bf16* temb_ord;     // token_embd rows in token_ordering order [V][H]
+  const float* out_norm;
+  const int* ord;
+  const bf16 *q[kMaxL], *o[kMaxL], *gate[kMaxL], *up[kMaxL], *down[kMaxL];
+  const float *q_norm[kMaxL], *attn_norm[kMaxL], *post_attn_norm[kMaxL], *ffn_norm[kMaxL], *post_ffn_norm[kMaxL];
+  const bf16* k[2];
+  const int* ctx_len[2];
+  long long st[2];
+  int kv_max[2];
+  bool has_type[2];
+  const bf16* hidden_in;
+  const int* tok_in;
+  const int* pos;
+  int* out_tokens;
+  float* out_hidden;
+  int n_draft;
+  int* status;
+  unsigned* abort_flag;
+  long long spin_limit;
+};
+
+// GEMV work split inside one ring slot of `rpc` rows: tasks are (row quad, k slice) pairs for
+// the compute warps; rows wider than one slot's share get split along k so that every warp
+// has a task. Number of k slices:
+__host__ __device__ inline int gemv_ns(int rpc) {
+  const int nq = (rpc + 3) / 4;
+  if (nq >= kCW) return 1;
+  int ns = 1;
+  while (ns * 2 * nq <= kCW) ns *= 2;
+  return ns;
+}
+__host__ __device__ inline int rows_per_slot(int row_bytes) {
+  const int r = row_bytes > 0 ? kSlotBytes / row_bytes : 1;
+  return r < 1 ? 1 : r;
+}
+// Floats of k-split partial sums a GEMV section of R rows (split over the cluster) of
+// row_bytes-wide rows needs.
+__host__ __device__ inline int gemv_part_floats(int R, int row_bytes) {
+  const int ns = gemv_ns(rows_per_slot(row_bytes));
+  return ns > 1 ? ns * split_max(R, kNC) : 0;
+}
+constexpr int kQkSlices = 2;  // most k slices of the attention score pass
+constexpr int kMaxKeysPerSlot = 128;
+// Keys per ring slot for K rows of row_bytes (bounded so that the score buffer stays small).
+__host__ __device__ inline int keys_per_slot(int row_bytes) {
+  const int r = rows_per_slot(row_bytes);
+  return r < kMaxKeysPerSlot ? r : kMaxKeysPerSlot;
+}
+
+// Shared-memory layout (bytes), identical in every CTA.
+struct Layout {
+  int ring, xch0, xch1, u, x, a, rows, gt, ut, part, sc, red, cs, lk, ids, bars, total;
+  int cs_off1;  // float2 index of the full-attention RoPE table inside cs
+};
+__host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ inline Layout make_layout(const Params& p) {
+  Layout L{};
+  int off = 0;
+  int dmax = 0, dmin = 1 << 30;
+  for (int l = 0; l < p.nl; ++l) {
+    dmax = imax(dmax, p.d[p.ltype[l]]);
+    dmin = p.d[p.ltype[l]] < dmin ? p.d[p.ltype[l]] : dmin;
+  }
+  if (dmin <= 0) dmin = 1;
+  L.ring = off;  off += kSlots * kSlotBytes;
+  L.xch0 = off;  off += kXchFloats * 4;
+  L.xch1 = off;  off += kXchFloats * 4;  // must directly follow xch0
+  L.u = off;     off += al16(2 * p.bb * 4);
+  L.x = off;     off += al16(p.H * 4);
+  L.a = off;     off += al16(p.H * 4);
+  int rmax = imax(imax(split_max(p.bb, kNC), split_max(p.C, kNC)), split_max(p.F, kNC));
+  rmax = imax(rmax, split_max(p.H, kNC));
+  // also stages the attention sums of every output dim and the (max, sum) of every head
+  rmax = imax(rmax, p.nh * dmax + 2 * p.nh);
+  L.rows = off;  off += al16(rmax * 4);
+  const int gmax = imax(imax(split_max(p.F, kNC), split_max(p.C, kNC)), 2 * p.topk);
+  L.gt = off;    off += al16(gmax * 4);        // gate rows / centroid logits / staged keys
+  L.ut = off;    off += al16(split_max(p.F, kNC) * 4);
+  int part = imax(gemv_part_floats(p.H, 2 * p.bb * 2), gemv_part_floats(p.bb, p.H * 2));
+  part = imax(part, imax(gemv_part_floats(p.F, p.H * 2), gemv_part_floats(p.H, p.F * 2)));
+  part = imax(part, gemv_part_floats(p.C, p.H * 2));
+  for (int l = 0; l < p.nl; ++l) {
+    const int QD = p.nh * p.d[p.ltype[l]];
+    part = imax(part, imax(gemv_part_floats(QD, p.H * 2), gemv_part_floats(p.H, QD * 2)));
+  }
+  L.part = off;  off += al16(part * 4);
+  // two alternating buffers of score partials (up to kQkSlices k slices) for one slot of keys;
+  // also holds the combine weights and the centroid keys of the head
+  int scf = 2 * kQkSlices * keys_per_slot(p.nkv * dmin * 2) * p.nh;
+  scf = imax(scf, imax(kNC * p.nh, 2 * split_max(p.C, kNC)));
+  L.sc = off;    off += al16(scf * 4);
+  L.red = off;   off += 128 * 4;
+  const int h0 = p.has_type[0] ? p.d[0] / 2 : 0, h1 = p.has_type[1] ? p.d[1] / 2 : 0;
+  L.cs_off1 = h0;
+  L.cs = off;    off += al16((h0 + h1) * 8);   // RoPE (cos, sin) of the sliding, then full, head_dim
+  L.lk = off;    off += al16(64 * 8);          // local top-k keys / per-warp best keys
+  L.ids = off;   off += al16(64 * 4);          // selected centroids
+  L.bars = off;  off += (2 * kSlots + 2) * 8;
+  L.total = al16(off);
+  return L;
+}
+
+}  // namespace clk
+}  // namespace mtp

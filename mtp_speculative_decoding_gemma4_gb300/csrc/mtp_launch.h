@@ -1,5 +1,5 @@
 // Internal interface between the C ABI (mtp_api.cu) and the dtype-specific kernel
-// translation units (mtp_bf16.cu, mtp_f32.cu, mtp_verify.cu).
+// translation units (mtp_bf16.cu, mtp_f32.cu, mtp_ll.cu, mtp_cl.cu, mtp_verify.cu).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -10,6 +10,9 @@ namespace mtp {
 
 struct Params;
 namespace ll {
+struct Params;
+}
+namespace clk {
 struct Params;
 }
 
@@ -31,6 +34,14 @@ int run_head_f32(const Params& p, cudaStream_t st);
 int ll_smem_bytes(const ll::Params& p);
 int ll_capacity(int smem, int num_sms);
 int run_ll(const ll::Params& p, int smem, cudaStream_t st);
+
+// Cluster-path draft block (one sequence, one 16-CTA cluster): shared-memory bytes (0: shape
+// not supported), resident clusters for that size, launch; and the init-time copy of
+// token_embd in token_ordering order that the path reads.
+int cl_smem_bytes(const clk::Params& p);
+int cl_capacity(int smem);
+int run_cl(const clk::Params& p, int smem, cudaStream_t st);
+int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaStream_t st);
 
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st);

@@ -15,7 +15,8 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT, LATENCY = 1, 2, 3
+PHASES, PERSISTENT, LATENCY, CLUSTER = 1, 2, 3, 4
+ONE_SEQ = [LATENCY, CLUSTER]  # the two single-sequence paths
 
 
 def _drafter(index, batch=0, ctx=0, max_batch=0):
@@ -49,23 +50,28 @@ def test_draft_block_matches_oracle(index, path):
     dr.close()
 
 
-def test_latency_path_matches_oracle_e2b_b1():
+@pytest.mark.parametrize("path", ONE_SEQ)
+def test_one_sequence_path_matches_oracle_e2b_b1(path):
     shape, wl, w, inp = config_data(1)
     ref = oracle_block(1)
     dr, d = _drafter(1)
-    tok, hid = _run_block(dr, d, wl.n_draft, LATENCY)
+    tok, hid = _run_block(dr, d, wl.n_draft, path)
     cmp = compare_block(tok, hid, ref, shape.dtype)
-    print(f"latency path config 1: max hidden err {cmp.max_hidden_err:.3g}, near-ties {cmp.tie_divergences}")
-    # more steps than the bench block, and repeated calls (mailbox epochs advance)
+    print(f"path {path} config 1: max hidden err {cmp.max_hidden_err:.3g}, near-ties {cmp.tie_divergences}")
+    # more steps than the bench block, and repeated calls (mailbox epochs / barrier phases)
     ref8 = oracle_block(1, n_draft=8)
     for _ in range(3):
-        tok, hid = _run_block(dr, d, 8, LATENCY)
+        tok, hid = _run_block(dr, d, 8, path)
         compare_block(tok, hid, ref8, shape.dtype)
+    # without the hidden output
+    tok2, _ = _run_block(dr, d, 8, path, want_hidden=False)
+    np.testing.assert_array_equal(tok2, tok)
     dr.close()
 
 
+@pytest.mark.parametrize("path", ONE_SEQ)
 @pytest.mark.parametrize("ctx,n_kv", [(1, 1), (5, 1), (8, 1), (9, 2), (63, 2), (64, 1)])
-def test_latency_path_short_and_window_edge_contexts(ctx, n_kv):
+def test_one_sequence_path_short_and_window_edge_contexts(ctx, n_kv, path):
     from dataclasses import replace
     from mtp_speculative_decoding_gemma4_gb300 import Drafter
     shape = replace(C.TINY_F32, dtype="bf16", layer_types=("S", "F", "S"), window=8, n_head=4, n_kv_head=n_kv)
@@ -77,15 +83,16 @@ def test_latency_path_short_and_window_edge_contexts(ctx, n_kv):
     wd, tgt = weights_to_device(w)
     dr = Drafter(shape, wd, tgt, max_batch=1, max_ctx=64)
     d = inputs_to_device(inp, "bf16")
-    tok, hid = _run_block(dr, d, 4, LATENCY)
+    tok, hid = _run_block(dr, d, 4, path)
     compare_block(tok, hid, ref, "bf16")
     dr.close()
 
 
-def test_latency_path_rejects_batches():
+@pytest.mark.parametrize("path", ONE_SEQ)
+def test_one_sequence_paths_reject_batches(path):
     from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
     dr, d = _drafter(2)
-    dr.set_path(LATENCY)
+    dr.set_path(path)
     with pytest.raises(MtpError) as e:
         dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], 1)
     assert e.value.code == binding.MTP_ERR_UNSUPPORTED_SHAPE
@@ -97,6 +104,15 @@ def test_paths_agree_bitwise_on_tokens():
     dr, d = _drafter(1)
     a, ha = _run_block(dr, d, 4, PHASES)
     b, hb = _run_block(dr, d, 4, PERSISTENT)
+    np.testing.assert_array_equal(a, b)
+    assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
+    dr.close()
+
+
+def test_one_sequence_paths_agree_on_tokens():
+    dr, d = _drafter(1)
+    a, ha = _run_block(dr, d, 8, LATENCY)
+    b, hb = _run_block(dr, d, 8, CLUSTER)
     np.testing.assert_array_equal(a, b)
     assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
     dr.close()

@@ -29,9 +29,12 @@ struct mtp_handle {
   unsigned long long* mb[10];
   unsigned* ll_abort;
   unsigned epoch;
-  // cluster path (one sequence): availability, token_embd in token_ordering order
+  // cluster path (one sequence): availability, token_embd in token_ordering order, and the
+  // hidden-wide matrices re-laid out as tensor-core tiles (one allocation)
   int cl_ok;
   void* temb_ord;
+  void* wpack;
+  const __nv_bfloat16 *pk_q[MTP_MAX_LAYERS], *pk_gate[MTP_MAX_LAYERS], *pk_up[MTP_MAX_LAYERS], *pk_cent, *pk_post;
 };
 
 namespace mtp {
@@ -278,6 +281,9 @@ mtp::clk::Params cl_template(const mtp_handle* h, int kv_max) {
   p.cent = static_cast<cb>(h->w.centroids);
   p.tgt = static_cast<cb>(h->target_embed);
   p.temb_ord = static_cast<cb>(h->temb_ord);
+  p.mma = h->wpack != nullptr;
+  p.pk_cent = h->pk_cent;
+  p.pk_post = h->pk_post;
   p.out_norm = h->w.out_norm;
   p.ord = h->w.token_ordering;
   for (int l = 0; l < c.n_layers; ++l) {
@@ -294,6 +300,9 @@ mtp::clk::Params cl_template(const mtp_handle* h, int kv_max) {
     p.post_attn_norm[l] = L.post_attn_norm;
     p.ffn_norm[l] = L.ffn_norm;
     p.post_ffn_norm[l] = L.post_ffn_norm;
+    p.pk_q[l] = h->pk_q[l];
+    p.pk_gate[l] = h->pk_gate[l];
+    p.pk_up[l] = h->pk_up[l];
   }
   for (int t = 0; t < 2; ++t) {
     p.has_type[t] = has_type(c, t);
@@ -301,6 +310,53 @@ mtp::clk::Params cl_template(const mtp_handle* h, int kv_max) {
   }
   p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
   return p;
+}
+
+// Re-lays out the hidden-wide matrices (Q, gate, up per block; centroids; post_projection)
+// as tensor-core tiles for the cluster path. Returns MTP_OK with h->wpack NULL when the shape
+// does not allow it (the path then uses its CUDA-core GEMVs).
+int build_packed(mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  h->wpack = nullptr;
+  const int H = c.hidden;
+  if (H % 64 != 0 || H > 1024) return MTP_OK;
+  struct Item {
+    const void* W;
+    int R;
+    const __nv_bfloat16** out;
+  };
+  std::vector<Item> items;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const int d = c.layer_type[l] ? c.head_dim_full : c.head_dim_swa;
+    items.push_back({h->w.layer[l].q, c.n_head * d, &h->pk_q[l]});
+    items.push_back({h->w.layer[l].gate, c.ffn, &h->pk_gate[l]});
+    items.push_back({h->w.layer[l].up, c.ffn, &h->pk_up[l]});
+  }
+  items.push_back({h->w.centroids, c.n_centroids, &h->pk_cent});
+  items.push_back({h->w.post_proj, c.backbone, &h->pk_post});
+  size_t total = 0;
+  for (const Item& it : items) total += static_cast<size_t>(mtp::packed_tile_bytes(it.R, H));
+  void* buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, total);
+  if (e != cudaSuccess) return cuda_fail("allocating the tensor-core weight tiles", e);
+  size_t off = 0;
+  for (const Item& it : items) {
+    char* dst = static_cast<char*>(buf) + off;
+    const int rc = mtp::pack_tiles(it.W, it.R, H, dst, 0);
+    if (rc) {
+      cudaFree(buf);
+      return rc;
+    }
+    *it.out = reinterpret_cast<const __nv_bfloat16*>(dst);
+    off += static_cast<size_t>(mtp::packed_tile_bytes(it.R, H));
+  }
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(buf);
+    return cuda_fail("packing the tensor-core weight tiles", e);
+  }
+  h->wpack = buf;
+  return MTP_OK;
 }
 
 // Whether the cluster path can run this configuration on this device.
@@ -539,6 +595,13 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       cudaFree(h->ws);
       free(h);
       return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
+    }
+    rc = build_packed(h);
+    if (rc) {
+      cudaFree(h->temb_ord);
+      cudaFree(h->ws);
+      free(h);
+      return rc;
     }
   }
   *out = h;
@@ -788,6 +851,7 @@ void mtp_destroy(mtp_handle* h) {
   cudaDeviceSynchronize();
   cudaFree(h->ws);
   if (h->temb_ord) cudaFree(h->temb_ord);
+  if (h->wpack) cudaFree(h->wpack);
   free(h);
 }
 

@@ -9,9 +9,12 @@
 // independent of the abort word) for its own copies still in flight, and a final cluster
 // barrier keeps every CTA alive while peers may still write to it.
 //
-// Work split inside a CTA (16 compute warps):
-//   GEMV slot: (row quad, k slice) tasks, one warp each; a warp reads four rows at once,
-//     keeps its x slice in registers and reduces the four dot products with one transposed
+// Work split inside a CTA (kCW compute warps):
+//   hidden-wide GEMVs (Q, gate, up, centroids, post_projection): tensor cores on tiles packed
+//     at init (mma.m16n8k16, the fp32 input split into three exact bf16 terms); warps take
+//     (row tile, k quarter) pairs, the quarters added in a fixed order.
+//   other GEMV slots (pre_projection, O, down): (row quad, k slice) tasks, one warp each; a
+//     warp reads four rows at once and reduces the four dot products with one transposed
 //     butterfly; k-split partial sums are added in a fixed order (deterministic).
 //   scores: (key quad, head group, k slice) tasks; the heads sharing a KV head reuse each
 //     K load.
@@ -119,8 +122,7 @@ struct Fail {
 };
 // Bounded wait on an mbarrier phase. A raised abort word ends it early (false); running
 // past the time limit records MTP_ERR_TIMEOUT and raises the abort word (false).
-__device__ __noinline__ bool wait_bar(Fail f, unsigned bar, unsigned parity, bool cluster_scope) {
-  if (cluster_scope ? try_wait_cluster(bar, parity) : try_wait_cta(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(Fail f, unsigned bar, unsigned parity, bool cluster_scope) {
   const long long t0 = clock64();
   for (;;) {
     if (cluster_scope ? try_wait_cluster(bar, parity) : try_wait_cta(bar, parity)) return true;
@@ -131,6 +133,11 @@ __device__ __noinline__ bool wait_bar(Fail f, unsigned bar, unsigned parity, boo
       return false;
     }
   }
+}
+// The common case (phase already complete) without a call.
+__device__ __forceinline__ bool wait_bar(const Fail& f, unsigned bar, unsigned parity, bool cluster_scope) {
+  if (cluster_scope ? try_wait_cluster(bar, parity) : try_wait_cta(bar, parity)) return true;
+  return wait_bar_slow(f, bar, parity, cluster_scope);
 }
 // Time-bounded wait that ignores the abort word: the drain of this CTA's own copies.
 __device__ __noinline__ void drain_bar(Fail f, unsigned bar, unsigned parity) {
@@ -145,7 +152,7 @@ __device__ __noinline__ void drain_bar(Fail f, unsigned bar, unsigned parity) {
 
 // RMSNorm factor 1/sqrt(mean(v^2) + eps) of a shared-memory vector. Every warp computes it
 // on its own, in the same order, so all threads get the same value without a barrier.
-__device__ __noinline__ float rms_inv(const float* v, int n, float eps) {
+__device__ __forceinline__ float rms_inv(const float* v, int n, float eps) {
   const int lane = threadIdx.x & 31;
   float s = 0.f;
   for (int i = lane; i < n; i += 32) s = fmaf(v[i], v[i], s);
@@ -194,12 +201,6 @@ template <> struct Log2<16> { static constexpr int v = 4; };
 
 // ------------------------------------------------------------------ stream schedule
 
-// One section of the stream: rows [0, nrows) of `row_bytes` each, row i at src + i*stride.
-struct Sec {
-  const char* src;
-  long long stride;
-  int row_bytes, nrows, rpc;  // rpc: rows per chunk (one ring slot)
-};
 __device__ __forceinline__ int n_chunks(const Sec& s) { return s.nrows > 0 ? (s.nrows + s.rpc - 1) / s.rpc : 0; }
 
 // Sections of one step, in the order the step consumes them:
@@ -211,7 +212,17 @@ struct Keys {
 };
 
 __device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
-  Sec s{nullptr, 0, 0, 0, 1};
+  Sec s{nullptr, 0, 0, 0, 1, 0, 0};
+  // a packed matrix: this CTA's block of 512-byte tiles, streamed as `rows` of one tile
+  auto packed = [&](const bf16* P, int R, int K) {
+    s.src = reinterpret_cast<const char*>(P) + tiles_before(R, K, r) * kTileBytes;
+    s.row_bytes = kTileBytes;
+    s.stride = kTileBytes;
+    s.kt = K / 16;
+    s.nrows = padded_rows(R, r) / 16 * s.kt;
+    const Range g = split(R, kNC, r);
+    s.rrows = g.hi - g.lo;
+  };
   auto rows = [&](const bf16* W, int R, int K) {
     const Range rg = split(R, kNC, r);
     s.src = reinterpret_cast<const char*>(W + static_cast<size_t>(rg.lo) * K);
@@ -222,13 +233,21 @@ __device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
   if (idx == 0) {
     rows(p.pre, p.H, 2 * p.bb);
   } else if (idx >= 1 + 6 * p.nl) {
-    if (idx == 1 + 6 * p.nl) rows(p.cent, p.C, p.H);
-    else rows(p.post, p.bb, p.H);
+    if (idx == 1 + 6 * p.nl) {
+      if (p.mma) packed(p.pk_cent, p.C, p.H);
+      else rows(p.cent, p.C, p.H);
+    } else {
+      if (p.mma) packed(p.pk_post, p.bb, p.H);
+      else rows(p.post, p.bb, p.H);
+    }
   } else {
     const int l = (idx - 1) / 6, what = (idx - 1) % 6;
     const int lt = p.ltype[l], d = p.d[lt];
     switch (what) {
-      case 0: rows(p.q[l], p.nh * d, p.H); break;
+      case 0:
+        if (p.mma) packed(p.pk_q[l], p.nh * d, p.H);
+        else rows(p.q[l], p.nh * d, p.H);
+        break;
       case 1: {
         const int lo = lt ? kr.f_lo : kr.s_lo, n = lt ? kr.f_n : kr.s_n;
         s.src = reinterpret_cast<const char*>(p.k[lt] + static_cast<size_t>(lo) * p.st[lt]);
@@ -238,8 +257,14 @@ __device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
         break;
       }
       case 2: rows(p.o[l], p.H, p.nh * d); break;
-      case 3: rows(p.gate[l], p.F, p.H); break;
-      case 4: rows(p.up[l], p.F, p.H); break;
+      case 3:
+        if (p.mma) packed(p.pk_gate[l], p.F, p.H);
+        else rows(p.gate[l], p.F, p.H);
+        break;
+      case 4:
+        if (p.mma) packed(p.pk_up[l], p.F, p.H);
+        else rows(p.up[l], p.F, p.H);
+        break;
       default: rows(p.down[l], p.H, p.F); break;
     }
   }
@@ -313,13 +338,86 @@ __device__ __noinline__ int gemv_sec(Ring rg, int g, Sec s, const float* x, floa
   return g;
 }
 
+// D += A (16x16 bf16, row) x B (16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lds32(unsigned a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Splits the n fp32 values of x into three bf16 terms hi + mid + lo (x == hi + mid + lo up to
+// the rounding of lo, i.e. fp32 precision), written as rows 0..2 of xt [4][n]; row 3 is zero.
+// The tensor-core GEMVs multiply these terms by the bf16 weights: every product is exact and
+// the sums are fp32, so the result equals an fp32 dot product up to summation order.
+__device__ __forceinline__ void split_terms(const float* x, int n, bf16* xt) {
+  for (int i = threadIdx.x; i < n; i += kCT) {
+    const float v = x[i];
+    const bf16 h = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(h);
+    const bf16 m = __float2bfloat16_rn(r1);
+    const bf16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+    xt[i] = h;
+    xt[n + i] = m;
+    xt[2 * n + i] = l;
+    xt[3 * n + i] = __float2bfloat16_rn(0.f);
+  }
+}
+
+// out[i] = W_i . x for a packed section (tiles of this CTA's rows, see Params::pk_q) with the
+// input already split into xt [4][K]. Per slot, warp w multiplies row tile (w / 4) (+4, ...)
+// over the k quarter (w % 4); B column n < 3 carries term n of x, so a row's value is the sum
+// of D's first three columns. The four k-quarter partials are added in a fixed order.
+__device__ __noinline__ int gemv_mma_sec(Ring rg, int g, Sec s, const bf16* xt, float* out, float* part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, ti = lane & 3;
+  const int KT = s.kt, K = KT * 16, kq = warp & 3, ktn = KT / 4, kt0 = kq * ktn;
+  const int nc = n_chunks(s), rts = s.rpc / KT, PR = (s.rrows + 15) / 16 * 16;
+  // this lane's B column: term gi of x for gi < 3, the zero row otherwise
+  const unsigned xb = sa(xt) + 2u * static_cast<unsigned>((gi < 3 ? gi : 3) * K + 2 * ti);
+  for (int ch = 0; ch < nc; ++ch, ++g) {
+    const unsigned W = ring_wait(rg, g);
+    const int nt = min(s.rpc, s.nrows - ch * s.rpc), nrt = nt / KT;
+    for (int rt = warp >> 2; rt < nrt; rt += kCW / 4) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const unsigned a0 = W + static_cast<unsigned>((rt * KT + kt0) * kTileBytes + lane * 16);
+      for (int j = 0; j < ktn; ++j) {
+        const uint4 a = lds128(a0 + j * kTileBytes);
+        const unsigned bk = xb + 32u * static_cast<unsigned>(kt0 + j);
+        mma_bf16(d, a, lds32(bk), lds32(bk + 16));
+      }
+      // row sums of columns 0..2 (column 3 is zero): lanes ti = 0, 1 hold them
+      float v0 = d[0] + d[1], v1 = d[2] + d[3];
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+      if (ti == 0) {
+        const int row = (ch * rts + rt) * 16 + gi;
+        part[kq * PR + row] = v0;
+        part[kq * PR + row + 8] = v1;
+      }
+    }
+    ring_release(rg, g);
+  }
+  cbar();
+  for (int i = threadIdx.x; i < s.rrows; i += kCT)
+    out[i] = ((part[i] + part[PR + i]) + part[2 * PR + i]) + part[3 * PR + i];
+  cbar();
+  return g;
+}
+
 // Scores of the nh heads against the n keys of one K slot (shared address K), scaled; with
 // ns > 1 k slices the partial scores go to ns slices of sstride floats each.
 template <int NHT>
-__device__ __noinline__ void qk_chunk(const Params& p, unsigned K, int n, const float* q, float* sc, int d, float scale,
+__device__ __noinline__ void qk_chunk(int nh, int nkv, unsigned K, int n, const float* q, float* sc, int d, float scale,
                                       int ns, int sstride) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nh = p.nh, nkv = p.nkv, hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
+  const int hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
   const int row = nkv * d, V8 = d / 8;
   const int nq = (n + 3) / 4, base = nq * nhg;
   const unsigned qs = sa(q);
@@ -360,10 +458,10 @@ __device__ __noinline__ void qk_chunk(const Params& p, unsigned K, int n, const 
 // streamed K chunks, V = K). q: [nh][d] after q_norm and RoPE. Leaves in stage the
 // unnormalised sums [nh][d] followed by (m_h, l_h) of every head. Returns the chunk counter.
 template <int NHT>
-__device__ __noinline__ int att_sec(const Params& p, Ring rg, int g, Sec s, int d, float scale, const float* q,
+__device__ __noinline__ int att_sec(int nh, int nkv, Ring rg, int g, Sec s, int d, float scale, const float* q,
                                     float* sc, float* red, float* stage) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nh = p.nh, nkv = p.nkv, hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
+  const int hpg = nh / nkv, HG = hpg / NHT, nhg = nkv * HG;
   const int row = nkv * d, V8 = d / 8, DQ = d / 4;
   const int nc = n_chunks(s);
   // score tasks: (key quad, head group, k slice)
@@ -387,7 +485,7 @@ __device__ __noinline__ int att_sec(const Params& p, Ring rg, int g, Sec s, int 
     const unsigned K = ring_wait(rg, g);
     const int n = min(s.rpc, s.nrows - ch * s.rpc);
     float* scb = sc + (ch & 1) * (kQkSlices * sstride);
-    qk_chunk<NHT>(p, K, n, q, scb, d, scale, ns, sstride);
+    qk_chunk<NHT>(nh, nkv, K, n, q, scb, d, scale, ns, sstride);
     cbar();
     // ---- running max / exp-sum: one warp per head; probabilities overwrite slice 0
     if (warp < nh) {
@@ -467,16 +565,17 @@ __device__ __noinline__ int att_sec(const Params& p, Ring rg, int g, Sec s, int 
 
 // Logits of the rows of this CTA's selected centroids [slo, shi) (contiguous blocks of the
 // cluster-ordered embedding copy) against y; each warp's best (value, id) key goes to lk.
-__device__ __noinline__ void gather_best(const Params& p, const int* selc, int slo, int shi, const float* y,
-                                         unsigned long long* lk) {
+__device__ __noinline__ void gather_best(const bf16* temb_ord, const int* ord, int H, int vsc, int nclust, const int* selc,
+                                         int slo, int shi, const float* y, unsigned long long* lk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = p.H, vsc = p.vsc;
   unsigned long long best = 0ull;
   for (int c = slo; c < shi; ++c) {
-    const size_t base = static_cast<size_t>(selc[c]) * vsc;
+    // selc entries are clamped where written, but a rank slot left unwritten (only possible
+    // after an aborted exchange) must not address memory either
+    const size_t base = static_cast<size_t>(min(max(selc[c], 0), nclust - 1)) * vsc;
     for (int jb = warp * 8; jb < vsc; jb += kCW * 8) {
       const int myrow = jb + (lane >> 2);  // the row this lane holds after the reduction
-      const int id = myrow < vsc ? __ldg(p.ord + base + myrow) : 0;
+      const int id = myrow < vsc ? __ldg(ord + base + myrow) : 0;
       float a[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) a[i] = 0.f;
@@ -484,7 +583,7 @@ __device__ __noinline__ void gather_best(const Params& p, const int* selc, int s
         uint4 raw[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          raw[i] = __ldcs(reinterpret_cast<const uint4*>(p.temb_ord + (base + min(jb + i, vsc - 1)) * H + k));
+          raw[i] = __ldcs(reinterpret_cast<const uint4*>(temb_ord + (base + min(jb + i, vsc - 1)) * H + k));
         const float4 ya = *reinterpret_cast<const float4*>(y + k);
         const float4 yb = *reinterpret_cast<const float4*>(y + k + 4);
 #pragma unroll
@@ -549,11 +648,14 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
   float* gtb = reinterpret_cast<float*>(sm + L.gt);
   float* utb = reinterpret_cast<float*>(sm + L.ut);
   float* part = reinterpret_cast<float*>(sm + L.part);
+  bf16* xt = reinterpret_cast<bf16*>(sm + L.xt);
   float* sc = reinterpret_cast<float*>(sm + L.sc);
   float* red = reinterpret_cast<float*>(sm + L.red);
   float2* cs = reinterpret_cast<float2*>(sm + L.cs);
   unsigned long long* lk = reinterpret_cast<unsigned long long*>(sm + L.lk);
   int* selc = reinterpret_cast<int*>(sm + L.ids);
+  Sec* tab = reinterpret_cast<Sec*>(sm + L.tab);
+  float* nrm = reinterpret_cast<float*>(sm + L.nrm);
   const Fail fl{p.status, p.abort_flag, p.spin_limit};
 
   // this CTA's keys: a contiguous share of the full layers' [0, L) and of the window
@@ -593,10 +695,26 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       cs[(t ? L.cs_off1 : 0) + i] = v;
     }
   }
-  // every barrier of the cluster is initialised before any CTA arrives on a peer's
+  for (int i = tid; i < 64; i += kT) selc[i] = 0;
+  // this CTA's stream sections, and every norm gain, once per launch
+  const int nsec = sec_count(p);
+  for (int i = tid; i < nsec; i += kT) tab[i] = make_sec(p, i, r, kr);
+  for (int l = 0; l < p.nl; ++l) {
+    float* nl_ = nrm + l * L.nrm_stride;
+    const int d = p.d[p.ltype[l]];
+    for (int i = tid; i < p.H; i += kT) {
+      nl_[i] = __ldg(p.attn_norm[l] + i);
+      nl_[p.H + i] = __ldg(p.post_attn_norm[l] + i);
+      nl_[2 * p.H + i] = __ldg(p.ffn_norm[l] + i);
+      nl_[3 * p.H + i] = __ldg(p.post_ffn_norm[l] + i);
+    }
+    for (int i = tid; i < d; i += kT) nl_[4 * p.H + i] = __ldg(p.q_norm[l] + i);
+  }
+  for (int i = tid; i < p.H; i += kT) nrm[p.nl * L.nrm_stride + i] = __ldg(p.out_norm + i);
+  // every barrier of the cluster is initialised before any CTA arrives on a peer's (this
+  // also orders the tables above before their first use)
   cluster_sync_all();
 
-  const int nsec = sec_count(p);
   if (warp == kCW) {
     // ====================== producer warp: stream every section of every step in order
     if (lane == 0) {
@@ -604,7 +722,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       bool ok = true;
       for (int step = 0; step < p.n_draft && ok; ++step) {
         for (int si = 0; si < nsec && ok; ++si) {
-          const Sec s = make_sec(p, si, r, kr);
+          const Sec s = tab[si];
           const int nc = n_chunks(s);
           for (int ch = 0; ch < nc; ++ch) {
             const int slot = g % kSlots;
@@ -641,7 +759,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
 
     // Exchange protocol. Each exchange uses receive buffer xe & 1 and its mbarrier (phase
     // parity (xe >> 1) & 1). The receiver arms the barrier with the number of bytes it will get
-    // (one local arrival); warp w of every CTA writes that CTA's payload for CTA w with
+    // (one local arrival); warp w % kCW of every CTA writes that CTA's payload for CTA w with
     // st.async, whose bytes complete on CTA w's barrier. A buffer is rewritten only two
     // exchanges later, which no CTA can start before every CTA has sent the exchange in
     // between, i.e. has finished reading this one (a named barrier separates every last read
@@ -667,13 +785,13 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
     // (held in src from index 0)
     auto all_gather = [&](int lo, int hi, const float* src, int total) -> float* {
       xch_arm(total);
-      if (warp < kNC && live) {
-        const unsigned base = xch_dst(warp) + 4u * static_cast<unsigned>(lo), rb = xch_bar(warp);
+      for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
+        const unsigned base = xch_dst(w2) + 4u * static_cast<unsigned>(lo), rb = xch_bar(w2);
         for (int i = lane; i < hi - lo; i += 32) st_async_f32(base + 4u * i, src[i], rb);
       }
       return xch_wait();
     };
-    auto sec = [&](int idx) { return make_sec(p, idx, r, kr); };
+    auto sec = [&](int idx) { return tab[idx]; };
 
     int tok = 0;
     for (int step = 0; step < p.n_draft; ++step) {
@@ -703,9 +821,15 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         // ---- Q rows of attn_norm(x)
         {
           const float rf = rms_inv(x, H, p.eps);
-          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * __ldg(p.attn_norm[l] + i);
+          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * nrm[l * L.nrm_stride + i];
           cbar();
-          gc = gemv_sec(rg, gc, sec(1 + 6 * l), a, rowsb, part);
+          if (p.mma) {
+            split_terms(a, H, xt);
+            cbar();
+            gc = gemv_mma_sec(rg, gc, sec(1 + 6 * l), xt, rowsb, part);
+          } else {
+            gc = gemv_sec(rg, gc, sec(1 + 6 * l), a, rowsb, part);
+          }
         }
         const Range qr = split(QD, kNC, r);
         float* q = all_gather(qr.lo, qr.hi, rowsb, QD);
@@ -722,13 +846,13 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
           }
           cbar();
           const float2* c2 = cs + (lt ? L.cs_off1 : 0);
-          const float* gq = p.q_norm[l];
+          const float* gq = nrm + l * L.nrm_stride + 4 * H;
           const int half = d / 2;
           for (int idx = tid; idx < p.nh * half; idx += kCT) {
             const int h = idx / half, i = idx % half;
             const float rfq = red[32 + h];
-            const float av = q[h * d + i] * rfq * __ldg(gq + i);
-            const float bv = q[h * d + i + half] * rfq * __ldg(gq + i + half);
+            const float av = q[h * d + i] * rfq * gq[i];
+            const float bv = q[h * d + i + half] * rfq * gq[i + half];
             q[h * d + i] = av * c2[i].x - bv * c2[i].y;
             q[h * d + i + half] = bv * c2[i].x + av * c2[i].y;
           }
@@ -742,18 +866,18 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         {
           const Sec s = sec(2 + 6 * l);
           const int hpg = p.nh / p.nkv;
-          if (hpg % 4 == 0) gc = att_sec<4>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
-          else if (hpg == 2) gc = att_sec<2>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
-          else gc = att_sec<1>(p, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          if (hpg % 4 == 0) gc = att_sec<4>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          else if (hpg == 2) gc = att_sec<2>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          else gc = att_sec<1>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
         }
         // ---- partials to the owner of each output dim: CTA w receives, from every CTA r,
         // [m_0 l_0 .. m_nh-1 l_nh-1 | r's sums of w's dims] at offset r * per
         const int per = 2 * p.nh + split_max(QD, kNC);
         const Range dr = split(QD, kNC, r);
         xch_arm(kNC * (2 * p.nh + (dr.hi - dr.lo)));
-        if (warp < kNC && live) {
-          const Range dw = split(QD, kNC, warp);
-          const unsigned base = xch_dst(warp) + 4u * static_cast<unsigned>(r * per), rb = xch_bar(warp);
+        for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
+          const Range dw = split(QD, kNC, w2);
+          const unsigned base = xch_dst(w2) + 4u * static_cast<unsigned>(r * per), rb = xch_bar(w2);
           for (int i = lane; i < 2 * p.nh + (dw.hi - dw.lo); i += 32)
             st_async_f32(base + 4u * i, i < 2 * p.nh ? rowsb[QD + i] : rowsb[dw.lo + i - 2 * p.nh], rb);
         }
@@ -788,15 +912,22 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         const float* op = all_gather(hr.lo, hr.hi, rowsb, H);
         {
           const float rf = rms_inv(op, H, p.eps);
-          for (int i = tid; i < H; i += kCT) x[i] = x[i] + op[i] * rf * __ldg(p.post_attn_norm[l] + i);
+          for (int i = tid; i < H; i += kCT) x[i] = x[i] + op[i] * rf * nrm[l * L.nrm_stride + H + i];
           cbar();
           const float rf2 = rms_inv(x, H, p.eps);
-          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf2 * __ldg(p.ffn_norm[l] + i);
+          for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf2 * nrm[l * L.nrm_stride + 2 * H + i];
           cbar();
         }
         // ---- MLP: gate / up rows, m = gelu_tanh(gate) * up, down rows
-        gc = gemv_sec(rg, gc, sec(4 + 6 * l), a, gtb, part);
-        gc = gemv_sec(rg, gc, sec(5 + 6 * l), a, utb, part);
+        if (p.mma) {
+          split_terms(a, H, xt);
+          cbar();
+          gc = gemv_mma_sec(rg, gc, sec(4 + 6 * l), xt, gtb, part);
+          gc = gemv_mma_sec(rg, gc, sec(5 + 6 * l), xt, utb, part);
+        } else {
+          gc = gemv_sec(rg, gc, sec(4 + 6 * l), a, gtb, part);
+          gc = gemv_sec(rg, gc, sec(5 + 6 * l), a, utb, part);
+        }
         const Range fr = split(p.F, kNC, r);
         for (int i = tid; i < fr.hi - fr.lo; i += kCT) rowsb[i] = gelu_tanh(gtb[i]) * utb[i];
         cbar();
@@ -805,7 +936,8 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         const float* dn = all_gather(hr.lo, hr.hi, rowsb, H);
         {
           const float rf = rms_inv(dn, H, p.eps);
-          for (int i = tid; i < H; i += kCT) x[i] = p.lambda[l] * (x[i] + dn[i] * rf * __ldg(p.post_ffn_norm[l] + i));
+          for (int i = tid; i < H; i += kCT)
+            x[i] = p.lambda[l] * (x[i] + dn[i] * rf * nrm[l * L.nrm_stride + 3 * H + i]);
           cbar();
         }
       }
@@ -813,11 +945,17 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       const int k = p.topk;
       {
         const float rf = rms_inv(x, H, p.eps);
-        for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * __ldg(p.out_norm + i);  // a = y
+        for (int i = tid; i < H; i += kCT) a[i] = x[i] * rf * nrm[p.nl * L.nrm_stride + i];  // a = y
         cbar();
       }
       // centroid logits of this CTA's centroids -> local top-k (warp 0)
-      gc = gemv_sec(rg, gc, sec(1 + 6 * p.nl), a, gtb, part);
+      if (p.mma) {
+        split_terms(a, H, xt);
+        cbar();
+        gc = gemv_mma_sec(rg, gc, sec(1 + 6 * p.nl), xt, gtb, part);
+      } else {
+        gc = gemv_sec(rg, gc, sec(1 + 6 * p.nl), a, gtb, part);
+      }
       {
         // local top-k by rank: key i goes to position #{j : key_j > key_i} when that is < k
         const Range cr = split(p.C, kNC, r);
@@ -833,7 +971,8 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         }
       }
       // post rows -> this CTA's slice of h' (output, and the next step's input)
-      gc = gemv_sec(rg, gc, sec(2 + 6 * p.nl), a, rowsb, part);
+      if (p.mma) gc = gemv_mma_sec(rg, gc, sec(2 + 6 * p.nl), xt, rowsb, part);
+      else gc = gemv_sec(rg, gc, sec(2 + 6 * p.nl), a, rowsb, part);
       const Range br = split(p.bb, kNC, r);
       if (p.out_hidden)
         for (int i = tid; i < br.hi - br.lo; i += kCT) p.out_hidden[static_cast<size_t>(step) * p.bb + br.lo + i] = rowsb[i];
@@ -844,8 +983,8 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       cbar();
       // exchange: every CTA receives [h' (bb floats) | kNC local top-k lists of 2k words]
       xch_arm(p.bb + kNC * 2 * k);
-      if (warp < kNC && live) {
-        const unsigned base = xch_dst(warp), rb = xch_bar(warp);
+      for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
+        const unsigned base = xch_dst(w2), rb = xch_bar(w2);
         for (int i = lane; i < br.hi - br.lo; i += 32) st_async_f32(base + 4u * (br.lo + i), rowsb[i], rb);
         for (int i = lane; i < 2 * k; i += 32) st_async_f32(base + 4u * (p.bb + r * 2 * k + i), gtb[i], rb);
       }
@@ -858,7 +997,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       // ---- logits of this CTA's share of the candidate rows -> best key per warp
       {
         const Range sr = split(k, kNC, r);
-        gather_best(p, selc, sr.lo, sr.hi, a, lk);
+        gather_best(p.temb_ord, p.ord, p.H, p.vsc, p.C, selc, sr.lo, sr.hi, a, lk);
       }
       cbar();
       if (warp == 0) {
@@ -912,7 +1051,6 @@ int cl_smem_bytes(const clk::Params& p) {
   const bool fits =
       p.H % 8 == 0 && p.bb % 8 == 0 && p.F % 8 == 0 && p.H >= 8 &&  // 16-byte rows and vector loads
       p.nh >= 1 && p.nh <= 16 && p.nkv >= 1 && p.nh % p.nkv == 0 &&
-      p.nh * dmax <= 4 * kCT &&                                      // 4 output dims per compute thread
       p.nh * dmax <= kXchFloats && kNC * per <= kXchFloats && p.F <= kXchFloats && p.H <= kXchFloats &&
       p.bb + kNC * 2 * p.topk <= kXchFloats && 2 * kNC <= kXchFloats &&
       2 * p.bb * 2 <= kSlotBytes && p.H * 2 <= kSlotBytes && p.F * 2 <= kSlotBytes &&
@@ -996,6 +1134,49 @@ int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaS
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("reordering token_embd: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+// Packs W [R][K] (bf16, row-major) for the cluster kernel's tensor-core GEMVs: per CTA r of
+// the cluster its rows split(R, kNC, r), padded with zero rows to a multiple of 16, as 16x16
+// tiles (row tile major) of 32 lanes x 16 bytes in mma.m16n8k16 A-fragment order: lane
+// (g = lane / 4, t = lane % 4) holds rows g and g + 8 at columns 2t, 2t + 1 and 2t + 8, 2t + 9.
+__global__ void k_pack_tiles(const __nv_bfloat16* __restrict__ W, int R, int K, uint4* __restrict__ dst) {
+  const int KT = K / 16;
+  long long total = 0;
+  for (int r = 0; r < clk::kNC; ++r) total += static_cast<long long>(clk::padded_rows(R, r) / 16) * KT * 32;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    // locate the CTA block, tile and lane of entry i
+    long long rem = i;
+    int r = 0;
+    for (; r < clk::kNC; ++r) {
+      const long long n = static_cast<long long>(clk::padded_rows(R, r) / 16) * KT * 32;
+      if (rem < n) break;
+      rem -= n;
+    }
+    const int lane = static_cast<int>(rem % 32), tile = static_cast<int>(rem / 32);
+    const int rt = tile / KT, kt = tile % KT, g = lane >> 2, t = lane & 3;
+    const clk::Range rg = clk::split(R, clk::kNC, r);
+    auto word = [&](int row, int col) -> uint32_t {
+      const int gr = rg.lo + rt * 16 + row;
+      if (gr >= rg.hi) return 0u;
+      const uint16_t* p = reinterpret_cast<const uint16_t*>(W + static_cast<size_t>(gr) * K + kt * 16 + col);
+      return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 16);
+    };
+    dst[i] = make_uint4(word(g, 2 * t), word(g + 8, 2 * t), word(g, 2 * t + 8), word(g + 8, 2 * t + 8));
+  }
+}
+
+long long packed_tile_bytes(int R, int K) { return clk::tiles_before(R, K, clk::kNC) * clk::kTileBytes; }
+
+int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st) {
+  k_pack_tiles<<<512, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(W), R, K, static_cast<uint4*>(dst));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("packing weight tiles: %s", cudaGetErrorString(e));
     return MTP_ERR_CUDA;
   }
   return MTP_OK;

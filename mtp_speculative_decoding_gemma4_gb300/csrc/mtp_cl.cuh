@@ -2,7 +2,7 @@
 // thread-block cluster of NC CTAs (one per SM). In every CTA a producer warp streams the
 // CTA's row-slices of each weight matrix and its share of the shared K, in the order the
 // step consumes them, through a ring of shared-memory slots filled by TMA bulk copies
-// (full / empty mbarriers); sixteen compute warps consume the slots. Vectors are exchanged
+// (full / empty mbarriers); kCW compute warps consume the slots. Vectors are exchanged
 // inside the cluster only: each CTA writes its slice into every CTA's receive buffer with
 // st.async, whose bytes complete on the receiver's mbarrier (armed by the receiver with the
 // byte count it expects); receive buffers and their mbarriers alternate between two sets.
@@ -26,10 +26,14 @@ namespace mtp {
 namespace clk {
 
 constexpr int kNC = 16;            // CTAs per cluster
-constexpr int kCW = 16;            // compute warps
+// compute warps (a multiple of 4). Nine warps per CTA leave each scheduler at most three, so
+// a thread may hold 168 registers; measured on the E2B shape, 8 compute warps beat 4, 12 and
+// 16 (fewer spills and cheaper barriers outweigh the lost parallelism).
+constexpr int kCW = 8;
 constexpr int kCT = kCW * 32;      // compute threads
 constexpr int kT = kCT + 32;       // + one producer warp
-constexpr int kSlots = 5;
+static_assert(kCW % 4 == 0, "the tensor-core GEMV splits k over groups of four warps");
+constexpr int kSlots = 4;
 constexpr int kSlotBytes = 32768;
 constexpr int kMaxL = 8;
 constexpr int kXchFloats = 4096;   // floats per receive buffer
@@ -53,6 +57,12 @@ struct Params {
   float lambda[kMaxL];
   const bf16 *pre, *post, *cent, *tgt;
   const bf16* temb_ord;     // token_embd rows in token_ordering order [V][H]
+  // Matrices with hidden-wide rows (Q, gate, up, centroids, post_projection), re-laid out
+  // once at init for the tensor cores: per CTA of the cluster, its rows padded to a multiple
+  // of 16, as 16x16 tiles (row tile major, k tile minor) of 512 bytes each in mma.m16n8k16
+  // A-fragment order. Used when `mma` is set.
+  bool mma;
+  const bf16 *pk_q[kMaxL], *pk_gate[kMaxL], *pk_up[kMaxL], *pk_cent, *pk_post;
   const float* out_norm;
   const int* ord;
   const bf16 *q[kMaxL], *o[kMaxL], *gate[kMaxL], *up[kMaxL], *down[kMaxL];
@@ -101,9 +111,34 @@ __host__ __device__ inline int keys_per_slot(int row_bytes) {
   return r < kMaxKeysPerSlot ? r : kMaxKeysPerSlot;
 }
 
+// Packed tile layout of a matrix with R rows split over the cluster (see Params::pk_q):
+// CTA r's rows padded to 16 and the number of 512-byte tiles before its block.
+__host__ __device__ inline int padded_rows(int R, int r) {
+  const Range g = split(R, kNC, r);
+  return (g.hi - g.lo + 15) / 16 * 16;
+}
+__host__ __device__ inline long long tiles_before(int R, int K, int r) {
+  long long t = 0;
+  for (int i = 0; i < r; ++i) t += static_cast<long long>(padded_rows(R, i) / 16) * (K / 16);
+  return t;
+}
+constexpr int kTileBytes = 512;
+
+// One section of a CTA's weight / K stream: rows [0, nrows) of `row_bytes` each, row i at
+// src + i*stride; rpc rows per ring slot. Packed sections (tensor-core tiles) stream tiles as
+// rows and carry their k tiles per row tile and real row count (else both 0).
+struct Sec {
+  const char* src;
+  long long stride;
+  int row_bytes, nrows, rpc;
+  int kt, rrows;
+};
+constexpr int kMaxSec = 1 + 6 * kMaxL + 2;  // PRE | 6 per block | CENT | POST
+
 // Shared-memory layout (bytes), identical in every CTA.
 struct Layout {
-  int ring, xch0, xch1, u, x, a, rows, gt, ut, part, sc, red, cs, lk, ids, bars, total;
+  int ring, xch0, xch1, u, x, a, rows, gt, ut, part, xt, sc, red, cs, lk, ids, tab, nrm, bars, total;
+  int nrm_stride;  // floats of norm gains per block: attn, post_attn, ffn, post_ffn (H each), q_norm (dmax)
   int cs_off1;  // float2 index of the full-attention RoPE table inside cs
 };
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
@@ -138,7 +173,11 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
     const int QD = p.nh * p.d[p.ltype[l]];
     part = imax(part, imax(gemv_part_floats(QD, p.H * 2), gemv_part_floats(p.H, QD * 2)));
   }
+  // k-quarter partials of the tensor-core GEMVs: 4 x padded rows of the largest section
+  int pr = imax(imax(split_max(p.nh * dmax, kNC), split_max(p.F, kNC)), imax(split_max(p.C, kNC), split_max(p.bb, kNC)));
+  part = imax(part, 4 * ((pr + 15) / 16 * 16));
   L.part = off;  off += al16(part * 4);
+  L.xt = off;    off += al16(4 * p.H * 2);     // bf16 hi / mid / lo terms of a GEMV input + a zero row
   // two alternating buffers of score partials (up to kQkSlices k slices) for one slot of keys;
   // also holds the combine weights and the centroid keys of the head
   int scf = 2 * kQkSlices * keys_per_slot(p.nkv * dmin * 2) * p.nh;
@@ -150,6 +189,9 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
   L.cs = off;    off += al16((h0 + h1) * 8);   // RoPE (cos, sin) of the sliding, then full, head_dim
   L.lk = off;    off += al16(64 * 8);          // local top-k keys / per-warp best keys
   L.ids = off;   off += al16(64 * 4);          // selected centroids
+  L.tab = off;   off += al16(kMaxSec * static_cast<int>(sizeof(Sec)));  // this CTA's stream sections
+  L.nrm_stride = 4 * p.H + dmax;
+  L.nrm = off;   off += al16((p.nl * L.nrm_stride + p.H) * 4);  // all norm gains, then output_norm
   L.bars = off;  off += (2 * kSlots + 2) * 8;
   L.total = al16(off);
   return L;

@@ -42,6 +42,9 @@ int cl_smem_bytes(const clk::Params& p);
 int cl_capacity(int smem);
 int run_cl(const clk::Params& p, int smem, cudaStream_t st);
 int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaStream_t st);
+// Tensor-core tile packing of a [R][K] bf16 matrix for the cluster kernel (bytes, pack).
+long long packed_tile_bytes(int R, int K);
+int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);
 
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st);

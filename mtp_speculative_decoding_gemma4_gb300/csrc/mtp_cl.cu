@@ -568,6 +568,15 @@ __device__ __noinline__ int att_sec(int nh, int nkv, Ring rg, int g, Sec s, int 
 __device__ __noinline__ void gather_best(const bf16* temb_ord, const int* ord, int H, int vsc, int nclust, const int* selc,
                                          int slo, int shi, const float* y, unsigned long long* lk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // request every candidate block (vsc rows of H bf16, and its vsc ids) from memory at once
+  if (threadIdx.x < shi - slo) {
+    const size_t base = static_cast<size_t>(min(max(selc[slo + threadIdx.x], 0), nclust - 1)) * vsc;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(temb_ord + base * H),
+                 "r"(static_cast<unsigned>(vsc * H * 2))
+                 : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ord + base), "r"(static_cast<unsigned>(vsc * 4))
+                 : "memory");
+  }
   unsigned long long best = 0ull;
   for (int c = slo; c < shi; ++c) {
     // selc entries are clamped where written, but a rank slot left unwritten (only possible
@@ -600,29 +609,46 @@ __device__ __noinline__ void gather_best(const bf16* temb_ord, const int* ord, i
   if (lane == 0) lk[warp] = best;
 }
 
-// Global top-k by rank over kNC sorted (descending) lists of k keys ([kNC][k][hi word, lo
-// word]): a key's rank is the sum over the lists of the number of keys greater than it,
-// found by binary searches run side by side; keys of rank < k go to selc[rank].
-__device__ __noinline__ void merge_rank(const unsigned* lists, int k, int C, int* selc) {
-  auto key_at = [&](int s1, int i) -> unsigned long long {
-    return (static_cast<unsigned long long>(lists[(s1 * k + i) * 2]) << 32) | lists[(s1 * k + i) * 2 + 1];
-  };
-  int top = 1;
-  while (top * 2 <= k) top *= 2;
-  for (int t = threadIdx.x; t < kNC * k; t += kCT) {
-    const unsigned long long e = key_at(t / k, t % k);
-    int pos[kNC];
-#pragma unroll
-    for (int s1 = 0; s1 < kNC; ++s1) pos[s1] = 0;
-    for (int step = top; step > 0; step >>= 1) {
-#pragma unroll
-      for (int s1 = 0; s1 < kNC; ++s1)
-        if (pos[s1] + step <= k && key_at(s1, pos[s1] + step - 1) > e) pos[s1] += step;
+// Global top-k of kNC sorted (descending) lists of k <= 64 distinct keys, by a tree of pairwise
+// merges (16 -> 8 -> 4 -> 2 -> 1 lists, one warp per merge, a named barrier between levels).
+// In a merge of lists A and B, A[i] lands at i + #{B > A[i]} and B[j] at j + #{A > B[j]}
+// (binary searches); only positions < k are kept. Level inputs and outputs alternate between
+// two scratch areas; the last level writes the selected centroid ids to selc.
+__device__ __forceinline__ int count_greater(const unsigned long long* L, int k, unsigned long long e) {
+  int pos = 0;
+  for (int step = 64; step > 0; step >>= 1)  // k <= 64
+    if (pos + step <= k && L[pos + step - 1] > e) pos += step;
+  return pos;
+}
+__device__ __noinline__ void merge_tree(const unsigned* lists, int k, int C, unsigned long long* buf_a,
+                                        unsigned long long* buf_b, int* selc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // level 0: word-pair lists -> buf_a as 64-bit keys
+  for (int i = threadIdx.x; i < kNC * k; i += kCT)
+    buf_a[i] = (static_cast<unsigned long long>(lists[2 * i]) << 32) | lists[2 * i + 1];
+  cbar();
+  unsigned long long* in = buf_a;
+  unsigned long long* out = buf_b;
+  for (int n = kNC; n > 1; n >>= 1) {
+    for (int m = warp; m < n / 2; m += kCW) {
+      const unsigned long long* A = in + (2 * m) * k;
+      const unsigned long long* B = in + (2 * m + 1) * k;
+      for (int i = lane; i < k; i += 32) {
+        const unsigned long long ea = A[i], eb = B[i];
+        const int pa = i + count_greater(B, k, ea), pb = i + count_greater(A, k, eb);
+        if (n > 2) {
+          if (pa < k) out[m * k + pa] = ea;
+          if (pb < k) out[m * k + pb] = eb;
+        } else {
+          if (pa < k) selc[pa] = min(max(key_id(ea), 0), C - 1);
+          if (pb < k) selc[pb] = min(max(key_id(eb), 0), C - 1);
+        }
+      }
     }
-    int rank = 0;
-#pragma unroll
-    for (int s1 = 0; s1 < kNC; ++s1) rank += pos[s1];
-    if (rank < k) selc[rank] = min(max(key_id(e), 0), C - 1);
+    cbar();
+    unsigned long long* t = in;
+    in = out;
+    out = t;
   }
 }
 
@@ -963,11 +989,15 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         unsigned long long* ck = reinterpret_cast<unsigned long long*>(sc);
         for (int i = tid; i < nce; i += kCT) ck[i] = argmax_key(gtb[i], cr.lo + i);
         cbar();
-        for (int i = tid; i < nce; i += kCT) {
-          const unsigned long long key = ck[i];
+        // two threads per key, each counting over half of the keys
+        for (int base = 0; base < nce; base += kCT / 2) {  // warp-uniform trip count
+          const int i = base + (tid >> 1), ic = min(i, nce - 1);
+          const unsigned long long key = ck[ic];
+          const int half = tid & 1, jlo = half * (nce / 2), jhi = half ? nce : nce / 2;
           int rank = 0;
-          for (int j = 0; j < nce; ++j) rank += ck[j] > key ? 1 : 0;
-          if (rank < k) lk[rank] = key;
+          for (int j = jlo; j < jhi; ++j) rank += ck[j] > key ? 1 : 0;
+          rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+          if (half == 0 && i < nce && rank < k) lk[rank] = key;
         }
       }
       // post rows -> this CTA's slice of h' (output, and the next step's input)
@@ -990,10 +1020,10 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       }
       const float* hx = xch_wait();
       for (int i = tid; i < p.bb; i += kCT) u[i] = hx[i];
-      // global top-k by rank over the kNC sorted lists: key i of list s has rank
-      // sum over lists of #{keys > it}, found by binary searches run side by side
-      merge_rank(reinterpret_cast<const unsigned*>(hx + p.bb), k, p.C, selc);
-      cbar();
+      // global top-k: tree merge of the kNC sorted lists (scratch: the score buffer, and the
+      // received lists' own area once level 1 has read them)
+      merge_tree(reinterpret_cast<const unsigned*>(hx + p.bb), k, p.C, reinterpret_cast<unsigned long long*>(sc),
+                 reinterpret_cast<unsigned long long*>(const_cast<float*>(hx) + p.bb), selc);
       // ---- logits of this CTA's share of the candidate rows -> best key per warp
       {
         const Range sr = split(k, kNC, r);

@@ -179,9 +179,10 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
   L.part = off;  off += al16(part * 4);
   L.xt = off;    off += al16(4 * p.H * 2);     // bf16 hi / mid / lo terms of a GEMV input + a zero row
   // two alternating buffers of score partials (up to kQkSlices k slices) for one slot of keys;
-  // also holds the combine weights and the centroid keys of the head
+  // also holds the combine weights, the centroid keys and the candidate lists of the head
   int scf = 2 * kQkSlices * keys_per_slot(p.nkv * dmin * 2) * p.nh;
   scf = imax(scf, imax(kNC * p.nh, 2 * split_max(p.C, kNC)));
+  scf = imax(scf, 2 * kNC * p.topk);  // 64-bit candidate lists of the top-k merge
   L.sc = off;    off += al16(scf * 4);
   L.red = off;   off += 128 * 4;
   const int h0 = p.has_type[0] ? p.d[0] / 2 : 0, h1 = p.has_type[1] ? p.d[1] / 2 : 0;

@@ -425,13 +425,13 @@ def main():
     ap.add_argument("--config", type=int, default=1, help="benchmark configuration index (default 1: E2B, B=1)")
     ap.add_argument("--path", type=int, default=-1,
                     help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
-                         "(one sequence), 4: cluster kernel (one sequence); default: 3 for B=1, else 2")
+                         "(one sequence), 4: cluster kernel (one sequence); default: 4 for B=1, else 2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.path < 0:
-        args.path = 3 if workload(args.config)[1].batch == 1 else 2
+        args.path = 4 if workload(args.config)[1].batch == 1 else 2
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -234,7 +234,7 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * and the attended K through shared memory and exchanges vectors in distributed shared
  * memory; bf16 centroid-head shapes within its buffer limits, V = K; mtp_init_weights keeps
  * a copy of token_embd in token_ordering order for it, vocab * hidden * 2 bytes).
- * Automatic picks 3 for B = 1 when available, else 4 when available, else 2 when
+ * Automatic picks 4 for B = 1 when available, else 3 when available, else 2 when
  * co-resident, else 1. Results agree within the precision contract. Errors: INVALID_ARG; a
  * forced path the call cannot use makes mtp_draft_block return UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);

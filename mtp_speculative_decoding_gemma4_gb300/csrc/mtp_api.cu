@@ -657,7 +657,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == MTP_DTYPE_BF16;
   int path = h->path;
-  if (path == 4 || (path == 0 && B == 1 && h->cl_ok && !h->ll_ok)) {
+  if (path == 4 || (path == 0 && B == 1 && h->cl_ok)) {
     if (!h->cl_ok || B != 1) {
       set_error("the cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->cl_ok);
       return MTP_ERR_UNSUPPORTED_SHAPE;

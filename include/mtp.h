@@ -233,10 +233,14 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * 4 = cluster kernel for one sequence (one 16-CTA thread-block cluster streams the weights
  * and the attended K through shared memory and exchanges vectors in distributed shared
  * memory; bf16 centroid-head shapes within its buffer limits, V = K; mtp_init_weights keeps
- * a copy of token_embd in token_ordering order for it, vocab * hidden * 2 bytes).
- * Automatic picks 4 for B = 1 when available, else 3 when available, else 2 when
- * co-resident, else 1. Results agree within the precision contract. Errors: INVALID_ARG; a
- * forced path the call cannot use makes mtp_draft_block return UNSUPPORTED_SHAPE. */
+ * a copy of token_embd in token_ordering order and tensor-core tiles of the hidden-wide
+ * matrices for it), 5 = one kernel per phase with every projection (and the dense tied
+ * head) as a tcgen05 tensor-core GEMM (bf16, max_batch <= 64; mtp_init_weights keeps the
+ * tensor maps and a staging buffer of 3 * roundup(max_batch, 32) * max input width bf16).
+ * Automatic picks 4 for B = 1 when available, else 3 when available; 5 for B >= 32 when
+ * available; else 2 when co-resident, else 1. Results agree within the precision contract.
+ * Errors: INVALID_ARG; a forced path the call cannot use makes mtp_draft_block return
+ * UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);
 
 /* Free the workspace and the handle (synchronises). NULL is ignored. */

@@ -9,6 +9,7 @@
 #include "mtp.h"
 #include "mtp_launch.h"
 #include "mtp_cl.cuh"
+#include "mtp_tc.cuh"
 #include "mtp_ll.cuh"
 #include "mtp_phases.cuh"
 
@@ -35,6 +36,10 @@ struct mtp_handle {
   void* temb_ord;
   void* wpack;
   const __nv_bfloat16 *pk_q[MTP_MAX_LAYERS], *pk_gate[MTP_MAX_LAYERS], *pk_up[MTP_MAX_LAYERS], *pk_cent, *pk_post;
+  // tensor-core phase path (batches of 32..64): tensor maps (64-byte aligned host memory) and
+  // the staging buffer of the input terms
+  mtp::TcPlan* tc;
+  void* tc_mem;
 };
 
 namespace mtp {
@@ -359,6 +364,71 @@ int build_packed(mtp_handle* h) {
   return MTP_OK;
 }
 
+// Tensor maps and staging buffer of the tensor-core phase path; leaves h->tc NULL when the
+// configuration or the device does not allow it.
+int build_tc(mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  h->tc = nullptr;
+  h->tc_mem = nullptr;
+  if (c.dtype != MTP_DTYPE_BF16 || c.max_batch < 2 || c.max_batch > mtp::tc::kMaxB || !mtp::tc_available()) return MTP_OK;
+  const int bb = c.backbone, H = c.hidden, F = c.ffn;
+  int qd[2] = {0, 0};
+  for (int t = 0; t < 2; ++t) qd[t] = has_type(c, t) ? c.n_head * (t ? c.head_dim_full : c.head_dim_swa) : 0;
+  const int ks[] = {2 * bb, H, F, qd[0], qd[1]};
+  int kmax = 0;
+  for (int k : ks) {
+    if (k % mtp::tc::kKStage) return MTP_OK;
+    kmax = k > kmax ? k : kmax;
+  }
+  void* mem = nullptr;
+  if (posix_memalign(&mem, 64, sizeof(mtp::TcPlan)) != 0 || !mem) return MTP_OK;
+  memset(mem, 0, sizeof(mtp::TcPlan));
+  mtp::TcPlan* plan = static_cast<mtp::TcPlan*>(mem);
+  plan->bp = (c.max_batch + 31) / 32 * 32;
+  const size_t xs_bytes = static_cast<size_t>(3) * plan->bp * kmax * 2;
+  cudaError_t e = cudaMalloc(&h->tc_mem, xs_bytes);
+  if (e == cudaSuccess) e = cudaMemset(h->tc_mem, 0, xs_bytes);
+  if (e != cudaSuccess) {
+    free(mem);
+    h->tc_mem = nullptr;
+    return cuda_fail("allocating the tensor-core staging buffer", e);
+  }
+  plan->xs = static_cast<__nv_bfloat16*>(h->tc_mem);
+  int rc = MTP_OK;
+  auto wmap = [&](CUtensorMap* m, const void* W, int R, int K) {
+    if (!rc) rc = mtp::tc_make_map(m, W, R, K, K, mtp::tc::kM);
+  };
+  auto xmap = [&](CUtensorMap* m, int K) {
+    if (!rc && K > 0) rc = mtp::tc_make_map(m, plan->xs, 3 * plan->bp, K, K, 3 * plan->bp);
+  };
+  wmap(&plan->pre, h->w.pre_proj, H, 2 * bb);
+  wmap(&plan->post, h->w.post_proj, bb, H);
+  if (c.use_ordered_embeddings) wmap(&plan->cent, h->w.centroids, c.n_centroids, H);
+  else wmap(&plan->temb, h->w.token_embd, c.vocab, H);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    const int q = qd[c.layer_type[l]];
+    wmap(&plan->q[l], L.q, q, H);
+    wmap(&plan->o[l], L.o, H, q);
+    wmap(&plan->gate[l], L.gate, F, H);
+    wmap(&plan->up[l], L.up, F, H);
+    wmap(&plan->down[l], L.down, H, F);
+  }
+  xmap(&plan->xs_pre, 2 * bb);
+  xmap(&plan->xs_h, H);
+  xmap(&plan->xs_f, F);
+  xmap(&plan->xs_o[0], qd[0]);
+  xmap(&plan->xs_o[1], qd[1]);
+  if (rc) {
+    cudaFree(h->tc_mem);
+    h->tc_mem = nullptr;
+    free(mem);
+    return rc;
+  }
+  h->tc = plan;
+  return MTP_OK;
+}
+
 // Whether the cluster path can run this configuration on this device.
 bool cl_supported(const mtp_handle* h) {
   const mtp_config& c = h->cfg;
@@ -573,6 +643,12 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     return cuda_fail("allocating the workspace", e);
   }
   layout_ws(h, static_cast<char*>(h->ws));
+  rc = build_tc(h);
+  if (rc) {
+    cudaFree(h->ws);
+    free(h);
+    return rc;
+  }
   e = cudaMemset(h->ws, 0, h->ws_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -751,6 +827,17 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     return mtp::run_ll(lp, smem, st);
   }
   int ncta = h->num_sms;
+  if (path == 5 || (path == 0 && B >= 32 && h->tc)) {
+    if (!h->tc) {
+      set_error("the tensor-core path needs a bf16 drafter with max_batch in [2, %d] on this device", mtp::tc::kMaxB);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    p.s.ncta_hint = 2 * h->num_sms;
+    for (int t = 0; t < 2; ++t)
+      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), h->num_sms,
+                                                     h->nsplit_max) : 1;
+    return mtp::run_phases_tc_bf16(p, *h->tc, st);
+  }
   if (path != 1) {
     p.s.ncta_hint = ncta;
     for (int t = 0; t < 2; ++t)
@@ -837,8 +924,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 4) {
-    set_error("need a handle and path in {0, 1, 2, 3, 4}");
+  if (!h || path < 0 || path > 5) {
+    set_error("need a handle and path in {0, 1, 2, 3, 4, 5}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;
@@ -852,6 +939,8 @@ void mtp_destroy(mtp_handle* h) {
   cudaFree(h->ws);
   if (h->temb_ord) cudaFree(h->temb_ord);
   if (h->wpack) cudaFree(h->wpack);
+  if (h->tc_mem) cudaFree(h->tc_mem);
+  if (h->tc) free(h->tc);
   free(h);
 }
 

@@ -6,6 +6,7 @@
 
 #include "mtp_launch.h"
 #include "mtp_phases.cuh"
+#include "mtp_tc.cuh"
 
 namespace mtp {
 
@@ -269,6 +270,62 @@ int run_phases(const Params& p, cudaStream_t st) {
       MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
     } else {
       MTP_LAUNCH(k_dense<WT>, z.dense, z.smem_dense, p);
+    }
+  }
+  MTP_LAUNCH(k_fin<WT>, 1, 0, p, p.n_draft, p.n_draft - 1);
+  return MTP_OK;
+}
+
+// One launch per phase, every GEMV split into staging (the phase kernel with p.tc_xs set, one
+// CTA per batch group) and tcgen05 GEMMs over the staged terms.
+template <typename WT>
+int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
+  const PhaseSizes z = phase_sizes<WT>(p);
+  const ShapeP& s = p.s;
+  Params ps = p;
+  ps.tc_xs = plan.xs;
+  ps.tc_bp = plan.bp;
+  auto groups = [&](int K) { return ceil_div(s.B, gemv_group(s.B, K)); };
+  auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
+                  long long ld2, unsigned long long* best) -> int {
+    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, p.w.status, p.spin_limit};
+    return tc_gemm(&w, &x, a, best != nullptr, st);
+  };
+  int rc;
+  MTP_LAUNCH(k_rope<WT>, s.B, 0, p);
+  int par = 0;
+  for (int step = 0; step < p.n_draft; ++step) {
+    MTP_LAUNCH(k_pre<WT>, groups(2 * s.bb), z.smem_pre, ps, step, par);
+    if ((rc = gemm(plan.pre, plan.xs_pre, s.H, 2 * s.bb, p.w.x[par], s.H, nullptr, 0, nullptr))) return rc;
+    for (int l = 0; l < s.nl; ++l) {
+      const int t = p.L[l].type, QD = s.nh * s.d[t];
+      MTP_LAUNCH(k_q<WT>, groups(s.H), z.smem_q, ps, l, par);
+      if ((rc = gemm(plan.q[l], plan.xs_h, QD, s.H, p.w.qraw, static_cast<long long>(s.nh) * p.w.dmax, nullptr, 0,
+                     nullptr)))
+        return rc;
+      if (l > 0) par ^= 1;
+      MTP_LAUNCH(k_att<WT>, z.att[l], att_smem_for(s, t), p, l);
+      MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
+      MTP_LAUNCH(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
+      if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;
+      MTP_LAUNCH(k_gu<WT>, groups(s.H), z.smem_gu, ps, l, par);
+      if ((rc = gemm(plan.gate[l], plan.xs_h, s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr))) return rc;
+      if ((rc = gemm(plan.up[l], plan.xs_h, s.F, s.H, p.w.up, s.F, nullptr, 0, nullptr))) return rc;
+      par ^= 1;
+      MTP_LAUNCH(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
+      if ((rc = gemm(plan.down[l], plan.xs_f, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
+    }
+    MTP_LAUNCH(k_head1<WT>, groups(s.H), z.smem_head1, ps, step, par);
+    float* hout = p.out_hidden ? p.out_hidden + static_cast<size_t>(step) * s.bb : nullptr;
+    if ((rc = gemm(plan.post, plan.xs_h, s.bb, s.H, hout, static_cast<long long>(p.n_draft) * s.bb, p.w.h_cur, s.bb,
+                   nullptr)))
+      return rc;
+    if (s.ordered) {
+      if ((rc = gemm(plan.cent, plan.xs_h, s.C, s.H, p.w.cl, s.C, nullptr, 0, nullptr))) return rc;
+      MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
+      MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+    } else {
+      if ((rc = gemm(plan.temb, plan.xs_h, s.V, s.H, nullptr, 0, nullptr, 0, p.w.best))) return rc;
     }
   }
   MTP_LAUNCH(k_fin<WT>, 1, 0, p, p.n_draft, p.n_draft - 1);

@@ -2,6 +2,8 @@
 // translation units (mtp_bf16.cu, mtp_f32.cu, mtp_ll.cu, mtp_cl.cu, mtp_verify.cu).
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "mtp.h"
@@ -45,6 +47,18 @@ int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaS
 // Tensor-core tile packing of a [R][K] bf16 matrix for the cluster kernel (bytes, pack).
 long long packed_tile_bytes(int R, int K);
 int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);
+
+// Tensor maps of the tensor-core phase path (host memory; see mtp_tc.cuh): every weight
+// matrix, and the staged input terms [3][bp][K] for each input width K.
+struct TcPlan {
+  CUtensorMap pre, post, cent, temb;
+  CUtensorMap q[MTP_MAX_LAYERS], o[MTP_MAX_LAYERS], gate[MTP_MAX_LAYERS], up[MTP_MAX_LAYERS], down[MTP_MAX_LAYERS];
+  CUtensorMap xs_pre, xs_h, xs_o[2], xs_f;  // K = 2 backbone, hidden, n_head * head_dim (sliding, full), ffn
+  __nv_bfloat16* xs;                         // the staging buffer
+  int bp;                                    // sequences of the staged terms (multiple of 32)
+};
+// One launch per phase with every GEMV as staging + tcgen05 GEMMs (bf16, B <= bp).
+int run_phases_tc_bf16(const Params& p, const TcPlan& plan, cudaStream_t st);
 
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st);

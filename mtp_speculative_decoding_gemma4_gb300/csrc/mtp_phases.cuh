@@ -100,6 +100,10 @@ struct Params {
   float* out_logits;   // head entry: [B][V] or null
   int* out_centroids;  // head entry: [B][topk] or null
   long long spin_limit;  // bounded grid-barrier wait (clock64 cycles)
+  // Tensor-core path: when set, a GEMV phase only stages its inputs and writes them as three
+  // bf16 terms [3][tc_bp][K_in] (hi, mid, lo of every fp32 input) for the tcgen05 GEMMs.
+  __nv_bfloat16* tc_xs;
+  int tc_bp;
 };
 
 // ---------------------------------------------------------------- GEMV machinery
@@ -216,6 +220,28 @@ __device__ void gemv_phase(const Params& p, const GemvJob* jobs, int njobs, int 
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   float* scr = reinterpret_cast<float*>(smem + L.scr_off);
   const int ngroups = ceil_div(p.s.B, nbg);
+  if (p.tc_xs) {
+    // staging only: one CTA per batch group, inputs split into exact bf16 terms
+    for (int g = cta; g < ngroups; g += ncta) {
+      const int b0 = g * nbg, nb = min(nbg, p.s.B - b0);
+      __syncthreads();
+      stage(b0, nb, in_s, K_in, scr, red, true);
+      __syncthreads();
+      for (int i = threadIdx.x; i < nb * K_in; i += kThreads) {
+        const int b = i / K_in, k = i % K_in;
+        const float v = in_s[b * K_in + k];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = v - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        const size_t row = static_cast<size_t>(b0 + b) * K_in + k, term = static_cast<size_t>(p.tc_bp) * K_in;
+        p.tc_xs[row] = hi;
+        p.tc_xs[term + row] = mid;
+        p.tc_xs[2 * term + row] = lo;
+      }
+    }
+    return;
+  }
   int tiles = 0;
   for (int q = 0; q < njobs; ++q) tiles += gemv_tiles(jobs[q]);
   const int n_items = ngroups * tiles;

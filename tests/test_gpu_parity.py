@@ -15,7 +15,7 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT, LATENCY, CLUSTER = 1, 2, 3, 4
+PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR = 1, 2, 3, 4, 5
 ONE_SEQ = [LATENCY, CLUSTER]  # the two single-sequence paths
 
 
@@ -47,6 +47,24 @@ def test_draft_block_matches_oracle(index, path):
     print(f"config {index} path {path}: {cmp.steps_compared} steps, max hidden err {cmp.max_hidden_err:.3g}, "
           f"near-tie divergences {cmp.tie_divergences}")
     assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
+@pytest.mark.parametrize("index", [2, 3, 4])
+def test_tensor_core_path_matches_oracle(index):
+    # every projection (and the dense head of config 3) as a tcgen05 GEMM; config 2 (B=8)
+    # exercises the padding of the staged terms to 32 sequences
+    shape, wl, w, inp = config_data(index)
+    ref = oracle_block(index)
+    dr, d = _drafter(index)
+    tok, hid = _run_block(dr, d, wl.n_draft, TENSOR)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    print(f"config {index} tensor-core path: {cmp.steps_compared} steps, max hidden err {cmp.max_hidden_err:.3g}, "
+          f"near-tie divergences {cmp.tie_divergences}")
+    assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    # same tokens as the CUDA-core phases
+    a, _ = _run_block(dr, d, wl.n_draft, PHASES)
+    assert np.mean(a == tok) >= 0.98
     dr.close()
 
 

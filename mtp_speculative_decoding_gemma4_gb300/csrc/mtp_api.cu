@@ -488,12 +488,11 @@ size_t layout_ws(mtp_handle* h, char* base) {
   return off;
 }
 
-// Splits of the shared-K range per attention item so that the attention phase has about
-// 2 items per SM, with at least 32 keys per split.
-int choose_nsplit(int B, int nkv, int keys, int num_sms, int cap) {
-  const int target = 2 * num_sms;
-  int ns = (target + B * nkv - 1) / (B * nkv);
-  const int by_len = (keys + 31) / 32;
+// Splits of the shared-K range per attention item. An item is one warp; the splits fill
+// `slots` warps (one wave) with at least 16 keys per split.
+int choose_nsplit(int B, int nkv, int keys, int slots, int cap) {
+  int ns = slots / (B * nkv);
+  const int by_len = (keys + 15) / 16;
   if (ns > by_len) ns = by_len;
   if (ns > cap) ns = cap;
   return ns < 1 ? 1 : ns;
@@ -834,14 +833,14 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     }
     p.s.ncta_hint = 2 * h->num_sms;
     for (int t = 0; t < 2; ++t)
-      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), h->num_sms,
+      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * h->num_sms,
                                                      h->nsplit_max) : 1;
     return mtp::run_phases_tc_bf16(p, *h->tc, st);
   }
   if (path != 1) {
     p.s.ncta_hint = ncta;
     for (int t = 0; t < 2; ++t)
-      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), ncta / 2,
+      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * ncta,
                                                      h->nsplit_max) : 1;
     const int cap = bf16 ? mtp::persistent_capacity_bf16(p, h->num_sms) : mtp::persistent_capacity_f32(p, h->num_sms);
     if (cap >= ncta) {
@@ -854,7 +853,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   }
   p.s.ncta_hint = 2 * h->num_sms;
   for (int t = 0; t < 2; ++t)
-    p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), h->num_sms,
+    p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * h->num_sms,
                                                    h->nsplit_max) : 1;
   return bf16 ? mtp::run_phases_bf16(p, st) : mtp::run_phases_f32(p, st);
 }

@@ -59,8 +59,9 @@ template <typename WT> __global__ void __launch_bounds__(kThreads) k_pre(Params 
 template <typename WT> __global__ void __launch_bounds__(kThreads) k_q(Params p, int l, int par) {
   MTP_KERNEL_PROLOGUE phase_q<WT>(p, l, par, blockIdx.x, gridDim.x, smem);
 }
-template <typename WT> __global__ void __launch_bounds__(kThreads) k_att(Params p, int l) {
-  MTP_KERNEL_PROLOGUE phase_att<WT>(p, l, blockIdx.x, gridDim.x, smem);
+// One attention kernel per (head dim, heads per KV head): each gets its own register budget.
+template <typename WT, int D, int HPG> __global__ void __launch_bounds__(kThreads) k_att(Params p, int l) {
+  MTP_KERNEL_PROLOGUE att_phase_t<WT, D, HPG>(p, l, blockIdx.x, gridDim.x, smem);
 }
 template <typename WT> __global__ void __launch_bounds__(kThreads) k_cmb(Params p, int l) {
   MTP_KERNEL_PROLOGUE phase_cmb<WT>(p, l, blockIdx.x, gridDim.x, smem);
@@ -151,7 +152,8 @@ struct PhaseSizes {
   int smem_max;
 };
 
-inline int att_smem_for(const ShapeP& s, int t) { return att_smem_bytes(s.d[t], s.nh / s.nkv); }
+template <typename WT>
+inline int att_smem_for(const ShapeP& s, int t) { return att_smem_bytes<WT>(s.d[t], s.nh / s.nkv); }
 
 template <typename WT>
 PhaseSizes phase_sizes(const Params& p) {
@@ -172,7 +174,7 @@ PhaseSizes phase_sizes(const Params& p) {
   for (int l = 0; l < s.nl; ++l) {
     const int t = p.L[l].type, d = s.d[t];
     z.q[l] = gemv_items(s.nh * d, s.B, s.H, nh);
-    z.att[l] = s.B * s.nkv * s.nsplit[t];
+    z.att[l] = ceil_div(s.B * s.nkv * s.nsplit[t], kWarps);  // one warp per item
     z.cmb[l] = s.B * s.nh * ceil_div(d, kCmbDims);
   }
   z.o = 0;
@@ -189,13 +191,11 @@ PhaseSizes phase_sizes(const Params& p) {
   z.smem_head1 = gs(s.H);
   int att = 0;
   for (int l = 0; l < s.nl; ++l) {
-    const int a = att_smem_for(s, p.L[l].type);
+    const int a = att_smem_for<WT>(s, p.L[l].type);
     att = a > att ? a : att;
   }
   z.smem_att = att;
-  int n2 = 1;
-  while (n2 < s.C) n2 <<= 1;
-  z.smem_topk = s.ordered ? n2 * 8 : 0;
+  z.smem_topk = s.ordered ? topk_smem_bytes(s.C, s.topk) : 0;
   z.smem_gather = (s.H + 2) * 4 + kWarps * 8 + 16;
   z.smem_dense = s.ordered ? 0 : kDenseBG * s.H * 4 + kWarps * 32 * 8;
   const int cmb = 2 * (kThreads / kCmbDims) * kCmbDims * 4;
@@ -224,7 +224,7 @@ inline int o_items(const Params& p, int l) {
 
 template <typename K>
 inline int allow_smem(K kernel, int bytes) {
-  if (bytes > 48 * 1024) {
+  if (bytes + 1024 > 48 * 1024) {  // the default limit also covers the kernel's static shared memory
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) {
       set_error("cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
@@ -244,6 +244,28 @@ inline int allow_smem(K kernel, int bytes) {
     }                                                                                   \
   } while (0)
 
+// Launches the attention kernel of layer l's head dim and group size on `grid` CTAs.
+template <typename WT>
+int launch_att(const Params& p, int l, int grid, cudaStream_t st) {
+  const int D = p.s.d[p.L[l].type], hpg = p.s.nh / p.s.nkv;
+  const int smem = att_smem_bytes<WT>(D, hpg);
+#define MTP_ATT_CASE(DD, HH) \
+  if (D == DD && hpg == HH) {                    \
+    MTP_LAUNCH((k_att<WT, DD, HH>), grid, smem, p, l); \
+    return MTP_OK;                               \
+  }
+  MTP_ATT_CASES
+#undef MTP_ATT_CASE
+  set_error("no attention kernel for head_dim %d with %d query heads per KV head", D, hpg);
+  return MTP_ERR_UNSUPPORTED_SHAPE;
+}
+
+#define MTP_LAUNCH_ATT(l)                                 \
+  do {                                                    \
+    int rc_a_ = launch_att<WT>(p, (l), z.att[(l)], st);   \
+    if (rc_a_) return rc_a_;                              \
+  } while (0)
+
 // One launch per phase.
 template <typename WT>
 int run_phases(const Params& p, cudaStream_t st) {
@@ -257,7 +279,7 @@ int run_phases(const Params& p, cudaStream_t st) {
       const int t = p.L[l].type;
       MTP_LAUNCH(k_q<WT>, z.q[l], z.smem_q, p, l, par);
       if (l > 0) par ^= 1;
-      MTP_LAUNCH(k_att<WT>, z.att[l], att_smem_for(s, t), p, l);
+      MTP_LAUNCH_ATT(l);
       MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
       MTP_LAUNCH(k_o<WT>, o_items(p, l), z.smem_o[t], p, l);
       MTP_LAUNCH(k_gu<WT>, z.gu, z.smem_gu, p, l, par);
@@ -285,7 +307,7 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   Params ps = p;
   ps.tc_xs = plan.xs;
   ps.tc_bp = plan.bp;
-  auto groups = [&](int K) { return ceil_div(s.B, gemv_group(s.B, K)); };
+  auto groups = [&](int) { return s.B; };  // staging runs one sequence per CTA
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
                   long long ld2, unsigned long long* best) -> int {
     tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, p.w.status, p.spin_limit};
@@ -304,7 +326,7 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
                      nullptr)))
         return rc;
       if (l > 0) par ^= 1;
-      MTP_LAUNCH(k_att<WT>, z.att[l], att_smem_for(s, t), p, l);
+      MTP_LAUNCH_ATT(l);
       MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
       MTP_LAUNCH(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
       if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;

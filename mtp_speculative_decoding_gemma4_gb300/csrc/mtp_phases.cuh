@@ -32,7 +32,7 @@ constexpr int kMaxLayers = 8;
 constexpr int kBG = 8;          // largest GEMV batch group
 constexpr int kGemvInBudget = 96 * 1024;  // shared-memory bytes for a batch group's inputs
 constexpr int kDenseBG = 32;    // sequences per dense-head batch group
-constexpr int kGatherPerItem = 32;
+constexpr int kGatherPerItem = 32 * kWarps;  // candidates per gather item (32 per warp)
 constexpr int kDenseRowsPerItem = 256;
 constexpr int kCmbDims = 64;    // head dims per combine item
 
@@ -214,7 +214,8 @@ __host__ __device__ inline GemvSmem gemv_smem(int K_in, int nbg, int max_vec) {
 template <typename WT, typename Stage>
 __device__ void gemv_phase(const Params& p, const GemvJob* jobs, int njobs, int K_in, Stage stage,
                            int cta, int ncta, char* smem) {
-  const int nbg = gemv_group(p.s.B, K_in);
+  // staging for the tensor-core GEMMs: one sequence per CTA (the most parallel split)
+  const int nbg = p.tc_xs ? 1 : gemv_group(p.s.B, K_in);
   const GemvSmem L = gemv_smem(K_in, nbg, p.s.H);
   float* in_s = reinterpret_cast<float*>(smem);
   float* red = reinterpret_cast<float*>(smem + L.red_off);
@@ -353,52 +354,145 @@ __device__ void phase_q(const Params& p, int l, int par, int cta, int ncta, char
 
 // ---------------------------------------------------------------- ATT
 
-// Loads EPL consecutive elements (a lane's share of a head vector) as fp32.
-template <typename WT, int EPL>
-__device__ inline void load_part(const WT* ptr, float* out) {
-  constexpr int V = Elem<WT>::kVec;
-  if constexpr (EPL % V == 0) {
+// Warp geometry of the attention phase for head dim D, HPG query heads per KV head and
+// model dtype WT. One warp owns one (sequence, KV head, split) item and walks its keys in
+// blocks of KB. Every lane owns NVEC 16-byte vectors of a key row (LPK lanes cover one row,
+// KPL rows sit side by side in the warp); each lane streams R rows per block into a private
+// shared-memory ring with cp.async, so nothing of the block waits on another lane.
+template <typename WT, int D, int HPG>
+struct AttGeom {
+  static constexpr int VE = 16 / static_cast<int>(sizeof(WT));  // elements per 16-byte vector
+  static constexpr int VPK = D / VE;                             // vectors per key row
+  static constexpr int LPK0 = VPK < 32 ? VPK : 32;
+  static constexpr int LPK = LPK0 < HPG ? HPG : LPK0;            // lanes per row (>= HPG)
+  static constexpr int NVEC = VPK > LPK ? VPK / LPK : 1;         // vectors per lane per row
+  static constexpr int KPL = 32 / LPK;                           // rows per warp load
+  static constexpr int RA = LPK / HPG, RB = 8 / NVEC;
+  static constexpr int R = RA < RB ? RA : RB;                    // rows per lane per block
+  static constexpr int KB = R * KPL;                             // keys per block
+  static constexpr int NVAL = R * HPG;                           // (row, head) scores per lane group
+  static constexpr int DUP = LPK / NVAL;                         // lanes holding the same score
+  static constexpr int S = 3;                                    // ring stages (2 blocks ahead)
+  static constexpr int kStageBytes = R * NVEC * 32 * 16;
+  static constexpr int kWarpBytes = S * kStageBytes;
+  static_assert(VPK >= 1 && (VPK & (VPK - 1)) == 0, "head dim must be a power-of-two multiple of a vector");
+  static_assert(R >= 1 && NVAL <= LPK, "one score per lane group");
+};
+
+// Reduce-scatter over the lanes `O, O/2, .., 1` apart: N values per lane in, and lane i ends
+// with the full sum of value (i mod 2*O) / (2*O / N) in v[0] (the halving steps come first).
+template <int N, int O>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+  if constexpr (O > 0) {
+    if constexpr (N > 1) {
+      constexpr int h = N / 2;
+      const bool up = (lane & O) != 0;
 #pragma unroll
-    for (int i = 0; i < EPL; i += V) load_vec_stream(ptr + i, out + i);
-  } else {
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) out[i] = Elem<WT>::to_f(ptr[i]);
+      for (int i = 0; i < h; ++i) {
+        const float send = up ? v[i] : v[i + h];
+        const float keep = up ? v[i + h] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+      }
+      reduce_scatter<h, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      reduce_scatter<1, O / 2>(v, lane);
+    }
   }
 }
 
-// Attention partials for one (sequence, KV head, split) item. The query heads of the KV
-// group read the same K rows; V = K unless a separate V is given.
+__device__ __forceinline__ void cp_async16(unsigned dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void vec_to_f32(const uint4& u, float* out) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+// One staged 16-byte vector of a K row from the ring as fp32 (zeros on lanes without dims).
+template <typename WT, int VE>
+__device__ __forceinline__ void ld_row_vec(bool has, unsigned addr, float* out) {
+  if (!has) {
+#pragma unroll
+    for (int e = 0; e < VE; ++e) out[e] = 0.f;
+    return;
+  }
+  uint4 u;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "r"(addr));
+  if constexpr (sizeof(WT) == 2) {
+    vec_to_f32(u, out);
+  } else {
+    out[0] = __uint_as_float(u.x);
+    out[1] = __uint_as_float(u.y);
+    out[2] = __uint_as_float(u.z);
+    out[3] = __uint_as_float(u.w);
+  }
+}
+
+// Split-KV attention partials of one (sequence b, KV head g, split c) item, run by one warp.
+// The HPG query heads of the group read the same K rows; V = K unless a separate V is given.
+// Writes, per head, the unnormalised sum of p_j v_j over the split's keys with the running
+// max m and the sum of p_j (Gemma 4 MTP drafter, "What it is": the drafter's queries attend
+// the target's shared K, values equal to the keys).
 template <typename WT, int D, int HPG>
-__device__ void att_item(const Params& p, int l, int b, int g, int c, char* smem) {
-  constexpr int EPL = D / 32;
+__device__ void att_warp_item(const Params& p, int l, int b, int g, int c, char* wsm) {
+  using G = AttGeom<WT, D, HPG>;
+  constexpr int VE = G::VE, LPK = G::LPK, NVEC = G::NVEC, R = G::R, KB = G::KB, NVAL = G::NVAL,
+                DUP = G::DUP, S = G::S;
+  constexpr int QE = NVEC * VE;  // head dims a lane owns
   const LayerP& L = p.L[l];
   const int t = L.type;
   const KvP& kv = p.kv[t];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* q_s = reinterpret_cast<float*>(smem);            // [HPG][D]
-  float* red = q_s + HPG * D;                              // [kWarps]
-  float* mls = red + kWarps;                               // [kWarps][HPG][2]
-  float* accs = mls + kWarps * HPG * 2;                    // [kWarps][HPG][D]
-
-  // q heads of this group: q_norm, then RoPE at the constant position.
+  const int lane = threadIdx.x & 31;
+  const int dg = lane % LPK, ks = lane / LPK;
+  // lanes past the row hold no dims (only when HPG exceeds the vectors of a row)
+  const bool has = G::VPK >= LPK || dg < G::VPK;
   const int half = D / 2;
-  for (int hh = 0; hh < HPG; ++hh) {
-    const int h = g * HPG + hh;
-    const float* qr = p.w.qraw + static_cast<size_t>(b) * p.s.nh * p.w.dmax + static_cast<size_t>(h) * D;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < D; i += kThreads) ss += qr[i] * qr[i];
-    ss = block_sum(ss, red);
-    const float rf = rsqrtf(ss / D + p.s.eps);
+
+  // q heads of the group: q_norm, then RoPE at the constant position, for the dims this lane
+  // owns: dims (dg + v*LPK)*VE + e.
+  float q[HPG][QE];
+  {
     const float2* cs = p.w.cs + (static_cast<size_t>(b) * 2 + t) * (p.w.dmax / 2);
-    for (int i = threadIdx.x; i < half; i += kThreads) {
-      const float a = qr[i] * rf * L.q_norm[i];
-      const float bq = qr[i + half] * rf * L.q_norm[i + half];
-      const float2 e = cs[i];
-      q_s[hh * D + i] = a * e.x - bq * e.y;
-      q_s[hh * D + i + half] = bq * e.x + a * e.y;
+#pragma unroll
+    for (int hh = 0; hh < HPG; ++hh) {
+      const float* qr = p.w.qraw + static_cast<size_t>(b) * p.s.nh * p.w.dmax + static_cast<size_t>(g * HPG + hh) * D;
+      float ss = 0.f;
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const float x = has ? qr[(dg + v * LPK) * VE + e] : 0.f;
+          ss = fmaf(x, x, ss);
+        }
+#pragma unroll
+      for (int o = LPK / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rf = rsqrtf(ss / D + p.s.eps);
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v)
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          const int i = (dg + v * LPK) * VE + e;
+          float out = 0.f;
+          if (has) {
+            const int ip = i < half ? i + half : i - half;  // RoPE partner
+            const float a = qr[i] * rf * L.q_norm[i];
+            const float bq = qr[ip] * rf * L.q_norm[ip];
+            const float2 r = cs[i < half ? i : ip];
+            out = i < half ? a * r.x - bq * r.y : a * r.x + bq * r.y;
+          }
+          q[hh][v * VE + e] = out;
+        }
     }
   }
-  __syncthreads();
 
   const int Lb = min(max(kv.ctx_len[b], 0), kv.max_ctx);  // never read past the buffer
   const int lo = t == 0 ? max(0, Lb - p.s.W) : 0, hi = Lb;
@@ -406,77 +500,159 @@ __device__ void att_item(const Params& p, int l, int b, int g, int c, char* smem
   const int chunk = ceil_div(max(hi - lo, 0), nsp);
   const int j0 = lo + c * chunk, j1 = min(hi, j0 + chunk);
   const float scale = p.s.scale[t];
+  const int nblk = j1 > j0 ? ceil_div(j1 - j0, KB) : 0;
 
-  float qv[HPG][EPL], acc[HPG][EPL], m[HPG], lsum[HPG];
+  const WT* kb = static_cast<const WT*>(kv.k) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D;
+  const WT* vb = kv.v ? static_cast<const WT*>(kv.v) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D
+                      : nullptr;
+  const unsigned ring = static_cast<unsigned>(__cvta_generic_to_shared(wsm));
+  // block i -> stage i % S: rows ks*R + r of the block, this lane's vectors
+  auto issue = [&](int i) {
+    if (i < nblk && has) {
+      const int st = i % S;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int key = j0 + i * KB + ks * R + r;
+        const bool ok = key < j1;
+        const WT* row = kb + static_cast<size_t>(ok ? key : j0) * kv.st;
+#pragma unroll
+        for (int v = 0; v < NVEC; ++v)
+          cp_async16(ring + (((st * R + r) * NVEC + v) * 32 + lane) * 16, row + (dg + v * LPK) * VE, ok ? 16 : 0);
+      }
+    }
+    cp_async_commit();  // one group per block index, empty or not
+  };
+
+  // score index of this lane after the reduce-scatter: head my_h, row my_r of its sub-slot
+  const int my_idx = (lane % LPK) / DUP;
+  const int my_h = my_idx / R, my_r = my_idx % R;
+  float m[HPG], acc[HPG][QE];
 #pragma unroll
   for (int hh = 0; hh < HPG; ++hh) {
     m[hh] = -INFINITY;
-    lsum[hh] = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      qv[hh][e] = q_s[hh * D + lane * EPL + e];
-      acc[hh][e] = 0.f;
-    }
+    for (int e = 0; e < QE; ++e) acc[hh][e] = 0.f;
   }
-  const WT* kb = static_cast<const WT*>(kv.k) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D + lane * EPL;
-  const WT* vb = kv.v ? static_cast<const WT*>(kv.v) + static_cast<size_t>(b) * kv.sb + static_cast<size_t>(g) * D + lane * EPL
-                      : nullptr;
-  for (int j = j0 + warp; j < j1; j += kWarps) {
-    float kf[EPL];
-    load_part<WT, EPL>(kb + static_cast<size_t>(j) * kv.st, kf);
-    float vf[EPL];
-    if (vb) load_part<WT, EPL>(vb + static_cast<size_t>(j) * kv.st, vf);
+  float lsum = 0.f;  // sum of p over this lane's (head, row) scores
+
+#pragma unroll
+  for (int i = 0; i < S - 1; ++i) issue(i);
+  for (int i = 0; i < nblk; ++i) {
+    issue(i + S - 1);
+    cp_async_wait<S - 1>();
+    const unsigned stage = ring + (i % S) * (R * NVEC * 32 * 16);
+    const int base = j0 + i * KB;
+    // scores of (head, row) pairs, partial over this lane's dims
+    float sc[NVAL];
+#pragma unroll
+    for (int n = 0; n < NVAL; ++n) sc[n] = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v) {
+        float kf[VE];
+        ld_row_vec<WT, VE>(has, stage + ((r * NVEC + v) * 32 + lane) * 16, kf);
+#pragma unroll
+        for (int hh = 0; hh < HPG; ++hh)
+#pragma unroll
+          for (int e = 0; e < VE; ++e) sc[hh * R + r] = fmaf(q[hh][v * VE + e], kf[e], sc[hh * R + r]);
+      }
+    reduce_scatter<NVAL, LPK / 2>(sc, lane);
+    float s = sc[0] * scale;
+    if (base + ks * R + my_r >= j1) s = -INFINITY;
+    // block max of each head: over its rows, its duplicate lanes and the sub-slots
+    float bm = s;
+#pragma unroll
+    for (int o = 1; o < R * DUP; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+#pragma unroll
+    for (int o = LPK; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+    float corr[HPG], m_me = 0.f, corr_me = 0.f;
 #pragma unroll
     for (int hh = 0; hh < HPG; ++hh) {
-      float s = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) s = fmaf(qv[hh][e], kf[e], s);
-      s = warp_sum(s) * scale;
-      const float mn = fmaxf(m[hh], s);
-      const float corr = expf(m[hh] - mn);
-      const float pw = expf(s - mn);
-      lsum[hh] = lsum[hh] * corr + pw;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[hh][e] = acc[hh][e] * corr + pw * (vb ? vf[e] : kf[e]);
+      const float mn = fmaxf(m[hh], __shfl_sync(0xffffffffu, bm, hh * R * DUP));
+      corr[hh] = expf(m[hh] - mn);  // 0 on the first block (m = -inf, mn finite)
       m[hh] = mn;
-    }
-  }
-  // merge the warps of this CTA
-#pragma unroll
-  for (int hh = 0; hh < HPG; ++hh) {
-    if (lane == 0) {
-      mls[(warp * HPG + hh) * 2] = m[hh];
-      mls[(warp * HPG + hh) * 2 + 1] = lsum[hh];
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) accs[(warp * HPG + hh) * D + lane * EPL + e] = acc[hh][e];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < HPG * D; idx += kThreads) {
-    const int hh = idx / D, i = idx % D;
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mls[(w * HPG + hh) * 2]);
-    float a = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = expf(mls[(w * HPG + hh) * 2] - M);
-        a += f * accs[(w * HPG + hh) * D + i];
-        den += f * mls[(w * HPG + hh) * 2 + 1];
+      if (hh == my_h) {
+        m_me = mn;
+        corr_me = corr[hh];
       }
     }
-    const int h = g * HPG + hh;
-    const size_t slot = (static_cast<size_t>(b) * p.s.nh + h) * p.w.nsplit_max + c;
-    p.w.part_acc[slot * p.w.dmax + i] = a;
-    if (i == 0) {
-      p.w.part_ml[slot * 2] = M;
+    const float pw = expf(s - m_me);  // 0 for keys past the split
+    lsum = lsum * corr_me + pw;
+#pragma unroll
+    for (int hh = 0; hh < HPG; ++hh)
+#pragma unroll
+      for (int e = 0; e < QE; ++e) acc[hh][e] *= corr[hh];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float pr[HPG];
+#pragma unroll
+      for (int hh = 0; hh < HPG; ++hh) pr[hh] = __shfl_sync(0xffffffffu, pw, ks * LPK + (hh * R + r) * DUP);
+      const int key = base + ks * R + r;
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v) {
+        float kf[VE];
+        if (vb) {
+          if (has && key < j1)
+            load_vec(vb + static_cast<size_t>(key) * kv.st + (dg + v * LPK) * VE, kf);
+          else
+#pragma unroll
+            for (int e = 0; e < VE; ++e) kf[e] = 0.f;
+        } else {
+          ld_row_vec<WT, VE>(has, stage + ((r * NVEC + v) * 32 + lane) * 16, kf);
+        }
+#pragma unroll
+        for (int hh = 0; hh < HPG; ++hh)
+#pragma unroll
+          for (int e = 0; e < VE; ++e) acc[hh][v * VE + e] = fmaf(pr[hh], kf[e], acc[hh][v * VE + e]);
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // sub-slots hold disjoint rows of the same dims: add them up
+#pragma unroll
+  for (int o = LPK; o < 32; o <<= 1)
+#pragma unroll
+    for (int hh = 0; hh < HPG; ++hh)
+#pragma unroll
+      for (int e = 0; e < QE; ++e) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], o);
+  const bool first_dup = (lane % LPK) % DUP == 0;
+#pragma unroll
+  for (int hh = 0; hh < HPG; ++hh) {
+    const float den = warp_sum(first_dup && my_h == hh ? lsum : 0.f);
+    const size_t slot = (static_cast<size_t>(b) * p.s.nh + g * HPG + hh) * p.w.nsplit_max + c;
+    if (ks == 0 && has) {
+      float* dst = p.w.part_acc + slot * p.w.dmax;
+#pragma unroll
+      for (int v = 0; v < NVEC; ++v)
+#pragma unroll
+        for (int e = 0; e < VE; e += 4)
+          *reinterpret_cast<float4*>(dst + (dg + v * LPK) * VE + e) =
+              make_float4(acc[hh][v * VE + e], acc[hh][v * VE + e + 1], acc[hh][v * VE + e + 2], acc[hh][v * VE + e + 3]);
+    }
+    if (lane == 0) {
+      p.w.part_ml[slot * 2] = m[hh];
       p.w.part_ml[slot * 2 + 1] = den;
     }
   }
-  __syncthreads();
 }
 
+#define MTP_ATT_CASES                                                                       \
+  MTP_ATT_CASE(32, 1) MTP_ATT_CASE(32, 2) MTP_ATT_CASE(32, 4) MTP_ATT_CASE(32, 8)           \
+  MTP_ATT_CASE(64, 1) MTP_ATT_CASE(64, 2) MTP_ATT_CASE(64, 4) MTP_ATT_CASE(64, 8)           \
+  MTP_ATT_CASE(128, 1) MTP_ATT_CASE(128, 2) MTP_ATT_CASE(128, 4) MTP_ATT_CASE(128, 8)       \
+  MTP_ATT_CASE(256, 1) MTP_ATT_CASE(256, 2) MTP_ATT_CASE(256, 4) MTP_ATT_CASE(256, 8)       \
+  MTP_ATT_CASE(512, 1) MTP_ATT_CASE(512, 2) MTP_ATT_CASE(512, 4)
+
+// Shared memory of the attention phase: one cp.async ring per warp (0: unsupported shape).
+template <typename WT>
 __host__ __device__ inline int att_smem_bytes(int D, int HPG) {
-  return (HPG * D + kWarps + kWarps * HPG * 2 + kWarps * HPG * D) * 4;
+#define MTP_ATT_CASE(DD, HH) \
+  if (D == DD && HPG == HH) return kWarps * AttGeom<WT, DD, HH>::kWarpBytes;
+  MTP_ATT_CASES
+#undef MTP_ATT_CASE
+  return 0;
 }
 
 template <typename WT, int D, int HPG>
@@ -484,25 +660,24 @@ __device__ void att_phase_t(const Params& p, int l, int cta, int ncta, char* sme
   const int t = p.L[l].type;
   const int nsp = p.s.nsplit[t];
   const int n_items = p.s.B * p.s.nkv * nsp;
-  for (int item = cta; item < n_items; item += ncta) {
+  const int warp = threadIdx.x >> 5;
+  char* wsm = smem + warp * AttGeom<WT, D, HPG>::kWarpBytes;
+  for (int item = cta * kWarps + warp; item < n_items; item += ncta * kWarps) {
     const int c = item % nsp;
     const int g = (item / nsp) % p.s.nkv;
     const int b = item / (nsp * p.s.nkv);
-    att_item<WT, D, HPG>(p, l, b, g, c, smem);
+    att_warp_item<WT, D, HPG>(p, l, b, g, c, wsm);
   }
 }
 
+// Items of the attention phase are warps: B * n_kv_head * nsplit of them.
 template <typename WT>
 __device__ void phase_att(const Params& p, int l, int cta, int ncta, char* smem) {
   const int D = p.s.d[p.L[l].type];
   const int hpg = p.s.nh / p.s.nkv;
 #define MTP_ATT_CASE(DD, HH) \
   if (D == DD && hpg == HH) { att_phase_t<WT, DD, HH>(p, l, cta, ncta, smem); return; }
-  MTP_ATT_CASE(32, 1) MTP_ATT_CASE(32, 2) MTP_ATT_CASE(32, 4) MTP_ATT_CASE(32, 8)
-  MTP_ATT_CASE(64, 1) MTP_ATT_CASE(64, 2) MTP_ATT_CASE(64, 4) MTP_ATT_CASE(64, 8)
-  MTP_ATT_CASE(128, 1) MTP_ATT_CASE(128, 2) MTP_ATT_CASE(128, 4) MTP_ATT_CASE(128, 8)
-  MTP_ATT_CASE(256, 1) MTP_ATT_CASE(256, 2) MTP_ATT_CASE(256, 4) MTP_ATT_CASE(256, 8)
-  MTP_ATT_CASE(512, 1) MTP_ATT_CASE(512, 2) MTP_ATT_CASE(512, 4)
+  MTP_ATT_CASES
 #undef MTP_ATT_CASE
 }
 
@@ -665,33 +840,124 @@ __device__ void phase_head_entry(const Params& p, int cta, int ncta, char* smem)
 
 // ---------------------------------------------------------------- TOPK
 
-// Top-k centroids of one sequence by a bitonic sort of (value, index) keys, descending.
-template <typename WT>
-__device__ void phase_topk(const Params& p, int cta, int ncta, char* smem) {
-  const int C = p.s.C, k = p.s.topk;
-  int n = 1;
-  while (n < C) n <<= 1;
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);
-  for (int b = cta; b < p.s.B; b += ncta) {
-    const float* cl = p.w.cl + static_cast<size_t>(b) * C;
-    for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = i < C ? argmax_key(cl[i], i) : 0ull;
-    __syncthreads();
-    for (int size = 2; size <= n; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = threadIdx.x; i < n / 2; i += kThreads) {
-          const int lo = 2 * i - (i & (stride - 1));
-          const int hi = lo + stride;
-          const bool desc = ((lo & size) == 0);
-          const unsigned long long a = keys[lo], c = keys[hi];
-          if ((a < c) == desc) { keys[lo] = c; keys[hi] = a; }
-        }
-        __syncthreads();
+// One in-lane compare-exchange stage (partner slot j + S) of the warp sort below.
+template <int P, int S>
+__device__ __forceinline__ void sort_stage_lane(unsigned long long (&v)[P], int lane, int size) {
+#pragma unroll
+  for (int j = 0; j < P; ++j) {
+    if ((j & S) == 0) {
+      const bool desc = ((lane * P + j) & size) == 0;
+      const unsigned long long a = v[j], c = v[j + S];
+      if ((a < c) == desc) {
+        v[j] = c;
+        v[j + S] = a;
       }
     }
-    for (int i = threadIdx.x; i < k; i += kThreads) {
-      const int id = key_id(keys[i]);
-      p.w.sel[b * k + i] = id;
-      if (p.out_centroids) p.out_centroids[b * k + i] = id;
+  }
+}
+
+// Bitonic sort of the 32*P keys of a warp, descending; key lane*P + j sits in v[j] of `lane`.
+// The stage loops stay rolled (a compact kernel); only the per-slot work is unrolled.
+template <int P>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&v)[P], int lane) {
+  static_assert(P == 1 || P == 2 || P == 4 || P == 8, "slots per lane");
+#pragma unroll 1
+  for (int size = 2; size <= 32 * P; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size / 2; stride > 0; stride >>= 1) {
+      if (stride >= P) {  // partner in lane ^ (stride / P), same slot
+        const bool upper = (lane & (stride / P)) != 0;
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const bool desc = ((lane * P + j) & size) == 0;
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], stride / P);
+          const bool keep_max = desc != upper;
+          v[j] = keep_max ? (o > v[j] ? o : v[j]) : (o < v[j] ? o : v[j]);
+        }
+      } else if constexpr (P > 1) {  // partner in the same lane
+        if (P > 4 && stride == 4) sort_stage_lane<P, (P > 4 ? 4 : 1)>(v, lane, size);
+        else if (P > 2 && stride == 2) sort_stage_lane<P, (P > 2 ? 2 : 1)>(v, lane, size);
+        else sort_stage_lane<P, 1>(v, lane, size);
+      }
+    }
+  }
+}
+
+constexpr int kTopkP = 8, kTopkChunk = 32 * kTopkP;  // keys per warp sort
+__host__ __device__ inline int topk_keep(int k) {
+  int t = 1;
+  while (t < k) t <<= 1;
+  return t;
+}
+__host__ __device__ inline int topk_smem_bytes(int C, int k) {
+  return 2 * ((C + kTopkChunk - 1) / kTopkChunk) * topk_keep(k) * 8;
+}
+
+// Top-k centroids of one sequence, best first: every warp sorts chunks of 256 (value, index)
+// keys in registers and keeps each chunk's best T (the power of two >= k); the kept lists
+// are reduced the same way until one chunk is left, whose first k keys are the answer.
+template <typename WT>
+__device__ void phase_topk(const Params& p, int cta, int ncta, char* smem) {
+  constexpr int P = kTopkP, CH = kTopkChunk;
+  const int C = p.s.C, k = p.s.topk, T = topk_keep(k);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch1 = ceil_div(C, CH);
+  unsigned long long* la = reinterpret_cast<unsigned long long*>(smem);  // [nch1 * T]
+  unsigned long long* lb = la + nch1 * T;                                 // [nch1 * T]
+  for (int b = cta; b < p.s.B; b += ncta) {
+    const float* cl = p.w.cl + static_cast<size_t>(b) * C;
+    for (int ch = warp; ch < nch1; ch += kWarps) {
+      unsigned long long v[P];
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        const int i = ch * CH + lane * P + j;
+        v[j] = i < C ? argmax_key(cl[i], i) : 0ull;
+      }
+      warp_sort_desc<P>(v, lane);
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        if (lane * P + j < T) la[ch * T + lane * P + j] = v[j];
+    }
+    __syncthreads();
+    unsigned long long *src = la, *dst = lb;
+    int m = nch1 * T;
+    while (m > CH) {
+      const int nch = ceil_div(m, CH);
+      for (int ch = warp; ch < nch; ch += kWarps) {
+        unsigned long long v[P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const int i = ch * CH + lane * P + j;
+          v[j] = i < m ? src[i] : 0ull;
+        }
+        warp_sort_desc<P>(v, lane);
+#pragma unroll
+        for (int j = 0; j < P; ++j)
+          if (lane * P + j < T) dst[ch * T + lane * P + j] = v[j];
+      }
+      __syncthreads();
+      m = nch * T;
+      unsigned long long* t = src;
+      src = dst;
+      dst = t;
+    }
+    if (warp == 0) {
+      unsigned long long v[P];
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        const int i = lane * P + j;
+        v[j] = i < m ? src[i] : 0ull;
+      }
+      warp_sort_desc<P>(v, lane);
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        const int i = lane * P + j;
+        if (i < k) {
+          const int id = key_id(v[j]);
+          p.w.sel[b * k + i] = id;
+          if (p.out_centroids) p.out_centroids[b * k + i] = id;
+        }
+      }
     }
     __syncthreads();
   }
@@ -699,9 +965,14 @@ __device__ void phase_topk(const Params& p, int cta, int ncta, char* smem) {
 
 // ---------------------------------------------------------------- GATHER
 
+// Sparse logits over the selected clusters' candidates (ids from token_ordering) and their
+// argmax. A warp scores 32 candidates: lane i fetches candidate i's id, every lane reads its
+// slice of all 32 rows (loads of several rows in flight), and a reduce-scatter leaves row
+// i's logit in lane i.
 template <typename WT>
 __device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
   constexpr int V = Elem<WT>::kVec;
+  constexpr int kRowsInFlight = 8;
   const int H = p.s.H, vsc = p.s.vsc;
   const int ncand = p.s.topk * vsc;
   const int per_b = ceil_div(ncand, kGatherPerItem);
@@ -719,23 +990,38 @@ __device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
       staged = b;
     }
     unsigned long long best = 0ull;
-    for (int q = warp; q < kGatherPerItem; q += kWarps) {
-      const int cand = ci * kGatherPerItem + q;
-      if (cand >= ncand) break;
-      const int cent = p.w.sel[b * p.s.topk + cand / vsc];
-      const int id = p.ord[cent * vsc + cand % vsc];
-      const WT* row = static_cast<const WT*>(p.temb) + static_cast<size_t>(id) * H;
-      float s = 0.f;
-      for (int k = lane * V; k < H; k += 32 * V) {
-        float w[V];
-        load_vec_stream(row + k, w);
+    const int c0 = ci * kGatherPerItem + warp * 32;
+    if (c0 < ncand) {
+      const int cand = c0 + lane;
+      const bool valid = cand < ncand;
+      const int cc = valid ? cand : c0;  // rows past the end re-read the first one
+      const int cent = p.w.sel[b * p.s.topk + cc / vsc];
+      const int id = p.ord[cent * vsc + cc % vsc];
+      float sc[32];
 #pragma unroll
-        for (int v = 0; v < V; ++v) s = fmaf(w[v], ys[k + v], s);
+      for (int r = 0; r < 32; ++r) sc[r] = 0.f;
+#pragma unroll
+      for (int r0 = 0; r0 < 32; r0 += kRowsInFlight) {
+        const WT* rows[kRowsInFlight];
+#pragma unroll
+        for (int rr = 0; rr < kRowsInFlight; ++rr)
+          rows[rr] = static_cast<const WT*>(p.temb) + static_cast<size_t>(__shfl_sync(0xffffffffu, id, r0 + rr)) * H;
+        for (int k = lane * V; k < H; k += 32 * V) {
+          float w[kRowsInFlight][V];
+#pragma unroll
+          for (int rr = 0; rr < kRowsInFlight; ++rr) load_vec_stream(rows[rr] + k, w[rr]);
+#pragma unroll
+          for (int rr = 0; rr < kRowsInFlight; ++rr)
+#pragma unroll
+            for (int v = 0; v < V; ++v) sc[r0 + rr] = fmaf(w[rr][v], ys[k + v], sc[r0 + rr]);
+        }
       }
-      s = warp_sum(s);
-      if (p.out_logits && lane == 0) p.out_logits[static_cast<size_t>(b) * p.s.V + id] = s;
-      const unsigned long long key = argmax_key(s, id);
-      best = key > best ? key : best;
+      reduce_scatter<32, 16>(sc, lane);  // lane i: the logit of candidate c0 + i
+      if (valid) {
+        if (p.out_logits) p.out_logits[static_cast<size_t>(b) * p.s.V + id] = sc[0];
+        best = argmax_key(sc[0], id);
+      }
+      best = warp_max_u64(best);
     }
     if (lane == 0) wbest[warp] = best;
     __syncthreads();

@@ -44,6 +44,19 @@ __device__ __forceinline__ void st_async_f32(unsigned caddr, float v, unsigned c
                "r"(__float_as_uint(v)), "r"(cbar)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this CTA's
+// shared memory into a peer CTA's, counted on the peer's mbarrier like st.async.
+__device__ __forceinline__ void bulk_s2c(unsigned dst_caddr, unsigned src, unsigned bytes, unsigned cbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_caddr),
+               "r"(src), "r"(bytes), "r"(cbar)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until this thread's bulk copies have read their sources (bounded by the copies).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Orders this thread's shared-memory writes before later bulk copies that read them.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void arrive_local(unsigned bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -212,7 +225,7 @@ struct Keys {
 };
 
 __device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
-  Sec s{nullptr, 0, 0, 0, 1, 0, 0};
+  Sec s{nullptr, 0, 0, 0, 1, 0, 0, 0};
   // a packed matrix: this CTA's block of 512-byte tiles, streamed as `rows` of one tile
   auto packed = [&](const bf16* P, int R, int K) {
     s.src = reinterpret_cast<const char*>(P) + tiles_before(R, K, r) * kTileBytes;
@@ -268,7 +281,14 @@ __device__ __noinline__ Sec make_sec(const Params& p, int idx, int r, Keys kr) {
       default: rows(p.down[l], p.H, p.F); break;
     }
   }
-  s.rpc = (idx >= 1 && idx < 1 + 6 * p.nl && (idx - 1) % 6 == 1) ? keys_per_slot(s.row_bytes) : rows_per_slot(s.row_bytes);
+  const bool kv = idx >= 1 && idx < 1 + 6 * p.nl && (idx - 1) % 6 == 1;
+  s.pitch = s.row_bytes;
+  if (kv && att_mma_ok(p)) {  // padded rows for the tensor-core attention
+    s.pitch = s.row_bytes + 16;
+    s.rpc = keys_per_slot_mma(s.row_bytes);
+  } else {
+    s.rpc = kv ? keys_per_slot(s.row_bytes) : rows_per_slot(s.row_bytes);
+  }
   return s;
 }
 
@@ -280,7 +300,7 @@ struct Ring {
 __device__ __forceinline__ unsigned ring_wait(const Ring& rg, int g) {
   const int slot = g % kSlots;
   wait_bar(rg.f, rg.full0 + 8 * slot, static_cast<unsigned>((g / kSlots) & 1), false);
-  return rg.base + slot * kSlotBytes;
+  return rg.base + slot * kSlotStride;
 }
 __device__ __forceinline__ void ring_release(const Ring& rg, int g) {
   __syncwarp();
@@ -338,9 +358,10 @@ __device__ __noinline__ int gemv_sec(Ring rg, int g, Sec s, const float* x, floa
   return g;
 }
 
-// D += A (16x16 bf16, row) x B (16x8 bf16, col), fp32 accumulate.
+// D += A (16x16 bf16, row) x B (16x8 bf16, col), fp32 accumulate. A pure register operation
+// (not volatile), so the compiler may overlap it with the shared-memory loads of later steps.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -387,6 +408,7 @@ __device__ __noinline__ int gemv_mma_sec(Ring rg, int g, Sec s, const bf16* xt, 
     for (int rt = warp >> 2; rt < nrt; rt += kCW / 4) {
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       const unsigned a0 = W + static_cast<unsigned>((rt * KT + kt0) * kTileBytes + lane * 16);
+#pragma unroll 4
       for (int j = 0; j < ktn; ++j) {
         const uint4 a = lds128(a0 + j * kTileBytes);
         const unsigned bk = xb + 32u * static_cast<unsigned>(kt0 + j);
@@ -554,6 +576,245 @@ __device__ __noinline__ int att_sec(int nh, int nkv, Ring rg, int g, Sec s, int 
 #pragma unroll
     for (int t = 0; t < NHT; ++t)
       *reinterpret_cast<float4*>(stage + (h0_pv + t) * d + 4 * dq) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+  }
+  if (tid < nh) {
+    stage[nh * d + 2 * tid] = red[48 + tid];
+    stage[nh * d + 2 * tid + 1] = red[64 + tid];
+  }
+  cbar();
+  return g;
+}
+
+// Four 8x8 bf16 matrices from shared memory (lane i gives a row address of matrix i / 8).
+__device__ __forceinline__ uint4 ldsm_x4(unsigned addr) {
+  uint4 r;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+// The same, each matrix transposed.
+__device__ __forceinline__ uint4 ldsm_x4_t(unsigned addr) {
+  uint4 r;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+// The bf16 pair of keys (key, key + 1) in v with the keys at or past n set to zero.
+__device__ __forceinline__ uint32_t keep_keys(uint32_t v, int key, int n) {
+  return key + 1 < n ? v : (key < n ? (v & 0xffffu) : 0u);
+}
+// Three bf16 terms of v (hi + mid + lo == v to fp32 precision) at rows 0, rs, 2 rs of dst.
+__device__ __forceinline__ void put_terms(bf16* dst, int rs, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h);
+  const bf16 m = __float2bfloat16_rn(r1);
+  dst[0] = h;
+  dst[rs] = m;
+  dst[2 * rs] = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
+
+constexpr int kAttMaxNT = 2;  // n tiles of the attention MMAs: 4 columns per head, nh <= 4
+constexpr int kAttMaxMT = 4;  // dim tiles of the weighted sum per warp: d <= 16 * 4 * kCW
+constexpr int kAttMaxKU = 4;  // keys per lane in the softmax: a slot holds at most 128 keys
+
+// Attention of the nh query heads (one KV head, V = K) over this CTA's keys of one block on
+// tensor cores (mma.m16n8k16, bf16 operands, fp32 accumulation). K rows sit in the slots at
+// pitch s.pitch (= 2d + 16 bytes). q is given as three bf16 terms per head, row 3h + t of qt
+// (pitch d + 8 elements); column 4h + t of the MMAs carries term t of head h (t < 3, the
+// fourth column is zero), so every product is exact and a head's value is the sum of its
+// three columns. Per slot of n keys:
+//   scores  S[key][col] = K q: tasks (16-key tile, quarter of the dims) over the warps, the
+//           dims chained in the MMA in groups of 4 steps (64 dims), then added in fp32;
+//   softmax one warp per head sums the four quarter partials in a fixed order, updates the
+//           running max / exp-sum and writes p as three bf16 terms (row 3h + t of pt);
+//   sums    O^T[dim][col] += K^T P^T: every warp owns dim tiles, keys chained per slot.
+// Leaves the unnormalised sums [nh][d] and (m_h, l_h) in stage, like att_sec.
+__device__ __noinline__ int att_sec_mma(int nh, Ring rg, int g, Sec s, int d, float scale, const bf16* qt,
+                                        float* sc, bf16* pt, float* red, float* stage) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, ti = lane & 3;
+  const int nc = n_chunks(s), kps = s.rpc, P = s.pitch, qp = d + 8, pp = kps + 8;
+  const int KS = d / 16, KQ = (KS + 3) / 4, NT = (nh + 1) / 2, MT = d / 16;
+  const unsigned qts = sa(qt), pts = sa(pt);
+  // this lane's B column of n tile nt: head and term (term 3: the zero column)
+  auto bcol_row = [&](int nt) -> int {
+    const int c = nt * 8 + gi, h = c >> 2, t = c & 3;
+    return (t == 3 || h >= nh) ? -1 : 3 * h + t;
+  };
+  float acc[kAttMaxMT][kAttMaxNT][4];
+#pragma unroll
+  for (int m = 0; m < kAttMaxMT; ++m)
+#pragma unroll
+    for (int nt = 0; nt < kAttMaxNT; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
+
+  for (int ch = 0; ch < nc; ++ch, ++g) {
+    const unsigned K = ring_wait(rg, g);
+    const int n = min(kps, s.nrows - ch * kps), nmt = (n + 15) / 16;
+    // ---- scores: task (key tile, dim quarter)
+    for (int task = warp; task < nmt * 4; task += kCW) {
+      const int j0 = (task >> 2) * 16, kq = task & 3;
+      const int ks0 = kq * KQ, ks1 = min(KS, ks0 + KQ);
+      float sv[kAttMaxNT][4];
+#pragma unroll
+      for (int nt = 0; nt < kAttMaxNT; ++nt) sv[nt][0] = sv[nt][1] = sv[nt][2] = sv[nt][3] = 0.f;
+      // lane's ldmatrix row: key j0 + (lane & 7) + 8 * ((lane >> 3) & 1), dims + 8 * (lane >> 4)
+      const unsigned arow = K + static_cast<unsigned>((j0 + (lane & 7) + ((lane >> 3) & 1) * 8) * P + (lane >> 4) * 16);
+      for (int kb = ks0; kb < ks1; kb += 4) {
+        float dg[kAttMaxNT][4];
+#pragma unroll
+        for (int nt = 0; nt < kAttMaxNT; ++nt) dg[nt][0] = dg[nt][1] = dg[nt][2] = dg[nt][3] = 0.f;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int ks = kb + k4;
+          if (ks >= ks1) break;
+          const uint4 a = ldsm_x4(arow + ks * 32);
+#pragma unroll
+          for (int nt = 0; nt < kAttMaxNT; ++nt) {
+            if (nt < NT) {
+              const int row = bcol_row(nt);
+              uint32_t b0 = 0u, b1 = 0u;
+              if (row >= 0) {
+                const unsigned bq = qts + 2u * static_cast<unsigned>(row * qp + ks * 16 + 2 * ti);
+                b0 = lds32(bq);
+                b1 = lds32(bq + 16);
+              }
+              mma_bf16(dg[nt], a, b0, b1);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < kAttMaxNT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sv[nt][i] += dg[nt][i];
+      }
+      // head values: columns 2ti, 2ti + 1 of lanes ti and ti ^ 1 hold the three terms
+#pragma unroll
+      for (int nt = 0; nt < kAttMaxNT; ++nt) {
+        if (nt < NT) {
+          float v0 = sv[nt][0] + sv[nt][1], v1 = sv[nt][2] + sv[nt][3];
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          const int h = (nt * 8 + 2 * ti) >> 2;
+          if ((ti & 1) == 0 && h < nh) {
+            sc[(kq * kps + j0 + gi) * nh + h] = v0;
+            sc[(kq * kps + j0 + gi + 8) * nh + h] = v1;
+          }
+        }
+      }
+    }
+    cbar();
+    // ---- running max / exp-sum per head; p of the slot's keys as three bf16 terms
+    if (warp < nh) {
+      const int h = warp;
+      float sv[kAttMaxKU];
+      float cm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kAttMaxKU; ++u) {
+        const int j = lane + 32 * u;
+        float v = -INFINITY;
+        if (j < n) {
+          v = ((sc[(0 * kps + j) * nh + h] + sc[(1 * kps + j) * nh + h]) + sc[(2 * kps + j) * nh + h]) +
+              sc[(3 * kps + j) * nh + h];
+          v *= scale;
+        }
+        sv[u] = v;
+        cm = fmaxf(cm, v);
+      }
+      cm = warp_max(cm);
+      const float mold = red[48 + h];
+      const float mnew = fmaxf(mold, cm);
+      float ls = 0.f;
+#pragma unroll
+      for (int u = 0; u < kAttMaxKU; ++u) {
+        const int j = lane + 32 * u;
+        if (j < nmt * 16) {
+          const float e = j < n ? expf(sv[u] - mnew) : 0.f;
+          ls += e;
+          put_terms(pt + 3 * h * pp + j, pp, e);
+        }
+      }
+      ls = warp_sum(ls);
+      if (lane == 0) {
+        const float corr = expf(mold - mnew);
+        red[80 + h] = corr;
+        red[64 + h] = red[64 + h] * corr + ls;
+        red[48 + h] = mnew;
+      }
+    }
+    cbar();
+    // ---- weighted sums: this warp's dim tiles
+    {
+      float cr[kAttMaxNT];
+#pragma unroll
+      for (int nt = 0; nt < kAttMaxNT; ++nt) {
+        const int h = (nt * 8 + 2 * ti) >> 2;
+        cr[nt] = (nt < NT && h < nh) ? red[80 + h] : 0.f;
+      }
+      float dg[kAttMaxMT][kAttMaxNT][4];
+#pragma unroll
+      for (int m = 0; m < kAttMaxMT; ++m)
+#pragma unroll
+        for (int nt = 0; nt < kAttMaxNT; ++nt) dg[m][nt][0] = dg[m][nt][1] = dg[m][nt][2] = dg[m][nt][3] = 0.f;
+      for (int ks = 0; ks < nmt; ++ks) {
+        const int j0 = ks * 16;
+        uint32_t b0[kAttMaxNT], b1[kAttMaxNT];
+#pragma unroll
+        for (int nt = 0; nt < kAttMaxNT; ++nt) {
+          const int row = nt < NT ? bcol_row(nt) : -1;
+          b0[nt] = b1[nt] = 0u;
+          if (row >= 0) {
+            const unsigned bp = pts + 2u * static_cast<unsigned>(row * pp + j0 + 2 * ti);
+            b0[nt] = lds32(bp);
+            b1[nt] = lds32(bp + 16);
+          }
+        }
+        // lane's transposed-ldmatrix row: key j0 + (lane & 7) + 8 * (lane >> 4), dims + 8 * ((lane >> 3) & 1)
+        const unsigned arow = K + static_cast<unsigned>((j0 + (lane & 7) + (lane >> 4) * 8) * P + ((lane >> 3) & 1) * 16);
+        const bool tail = j0 + 16 > n;
+#pragma unroll
+        for (int m = 0; m < kAttMaxMT; ++m) {
+          const int mt = warp + m * kCW;
+          if (mt < MT) {
+            uint4 a = ldsm_x4_t(arow + mt * 32);
+            if (tail) {  // keys past the slot's rows: zero (their rows hold no K)
+              a.x = keep_keys(a.x, j0 + 2 * ti, n);
+              a.y = keep_keys(a.y, j0 + 2 * ti, n);
+              a.z = keep_keys(a.z, j0 + 8 + 2 * ti, n);
+              a.w = keep_keys(a.w, j0 + 8 + 2 * ti, n);
+            }
+#pragma unroll
+            for (int nt = 0; nt < kAttMaxNT; ++nt)
+              if (nt < NT) mma_bf16(dg[m][nt], a, b0[nt], b1[nt]);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < kAttMaxMT; ++m)
+#pragma unroll
+        for (int nt = 0; nt < kAttMaxNT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[m][nt][i] = fmaf(acc[m][nt][i], cr[nt], dg[m][nt][i]);
+    }
+    // the next slot's scores and probabilities are written only after the barrier that
+    // follows its score pass, which every warp reaches after these reads
+    ring_release(rg, g);
+  }
+  // head sums of the term columns -> stage [h][dim]
+#pragma unroll
+  for (int m = 0; m < kAttMaxMT; ++m) {
+    const int mt = warp + m * kCW;
+#pragma unroll
+    for (int nt = 0; nt < kAttMaxNT; ++nt) {
+      float v0 = acc[m][nt][0] + acc[m][nt][1], v1 = acc[m][nt][2] + acc[m][nt][3];
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+      const int h = (nt * 8 + 2 * ti) >> 2;
+      if (mt < MT && nt < NT && (ti & 1) == 0 && h < nh) {
+        stage[h * d + mt * 16 + gi] = v0;
+        stage[h * d + mt * 16 + gi + 8] = v1;
+      }
+    }
   }
   if (tid < nh) {
     stage[nh * d + 2 * tid] = red[48 + tid];
@@ -758,13 +1019,13 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
             }
             const int r0 = ch * s.rpc, n = min(s.rpc, s.nrows - r0);
             const unsigned bytes = static_cast<unsigned>(n * s.row_bytes);
-            const unsigned fb = full0 + 8 * slot, dst = ring0 + slot * kSlotBytes;
+            const unsigned fb = full0 + 8 * slot, dst = ring0 + slot * kSlotStride;
             mbar_expect_tx(fb, bytes);
-            if (s.stride == s.row_bytes) {
+            if (s.stride == s.row_bytes && s.pitch == s.row_bytes) {
               bulk_g2s(dst, s.src + static_cast<size_t>(r0) * s.row_bytes, bytes, fb);
             } else {
               for (int j = 0; j < n; ++j)
-                bulk_g2s(dst + j * s.row_bytes, s.src + static_cast<size_t>(r0 + j) * s.stride,
+                bulk_g2s(dst + j * s.pitch, s.src + static_cast<size_t>(r0 + j) * s.stride,
                          static_cast<unsigned>(s.row_bytes), fb);
             }
             ++g;
@@ -779,6 +1040,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
   } else {
     // ====================== compute warps
     const Ring rg{ring0, full0, empty0, fl};
+    const bool amma = att_mma_ok(p);  // tensor-core attention (K rows at a padded pitch)
     int gc = 0;  // chunks consumed
     int xe = 0;  // exchanges done: buffer xe & 1, phase parity (xe >> 1) & 1
     const int H = p.H;
@@ -800,21 +1062,46 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
     auto xch_bar = [&](int w) { return mapa(xbar0 + 8 * (xe & 1), w); };
     // The named barrier first: a warp past its receive wait must not overwrite the staged
     // slice a sibling warp is still sending (the wait only covers this CTA's incoming data).
+    bool bulk_sent = false;  // this thread issued bulk copies not yet known to have read their source
     auto xch_wait = [&]() -> float* {
       const int cur = xe & 1;
+      if (bulk_sent) {  // the sources may be rewritten after the barrier
+        bulk_wait_read();
+        bulk_sent = false;
+      }
       cbar();
       if (live && !wait_bar(fl, xbar0 + 8 * cur, static_cast<unsigned>((xe >> 1) & 1), true)) live = false;
       ++xe;
       return xb0 + cur * kXchFloats;
     };
+    // Start of a send: every thread's writes of the payloads become visible to the bulk
+    // copies (proxy fence, then the barrier), and every earlier read of the receive buffer
+    // that the coming exchanges may rewrite is ordered before them.
+    auto send_begin = [&]() {
+      fence_async_smem();
+      cbar();
+    };
+    // This warp's part of sending n floats of src (this CTA's shared memory) to float offset
+    // off of peer w2's receive buffer: one bulk copy when both ends are 16-byte aligned and the
+    // size is a multiple of 16 bytes, else 4-byte st.async stores by the lanes.
+    auto send = [&](int w2, int off, const float* src, int n) {
+      if (n <= 0) return;
+      const unsigned dst = xch_dst(w2) + 4u * static_cast<unsigned>(off), rb = xch_bar(w2), sp = sa(src);
+      if (((dst | sp) & 15u) == 0 && (n & 3) == 0) {
+        if (lane == 0) {
+          bulk_s2c(dst, sp, 4u * static_cast<unsigned>(n), rb);
+          bulk_sent = true;
+        }
+      } else {
+        for (int i = lane; i < n; i += 32) st_async_f32(dst + 4u * i, src[i], rb);
+      }
+    };
     // all-gather of a vector of `total` floats: every CTA receives this CTA's slice [lo, hi)
     // (held in src from index 0)
     auto all_gather = [&](int lo, int hi, const float* src, int total) -> float* {
       xch_arm(total);
-      for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
-        const unsigned base = xch_dst(w2) + 4u * static_cast<unsigned>(lo), rb = xch_bar(w2);
-        for (int i = lane; i < hi - lo; i += 32) st_async_f32(base + 4u * i, src[i], rb);
-      }
+      send_begin();
+      for (int w2 = warp; w2 < kNC && live; w2 += kCW) send(w2, lo, src, hi - lo);
       return xch_wait();
     };
     auto sec = [&](int idx) { return tab[idx]; };
@@ -870,21 +1157,51 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
             s = warp_sum(s);
             if (lane == 0) red[32 + warp] = rsqrtf(s / d + p.eps);
           }
+          if (tid < p.nh) {  // running max and exp-sum of every head
+            red[48 + tid] = -INFINITY;
+            red[64 + tid] = 0.f;
+          }
           cbar();
           const float2* c2 = cs + (lt ? L.cs_off1 : 0);
           const float* gq = nrm + l * L.nrm_stride + 4 * H;
           const int half = d / 2;
-          for (int idx = tid; idx < p.nh * half; idx += kCT) {
-            const int h = idx / half, i = idx % half;
-            const float rfq = red[32 + h];
-            const float av = q[h * d + i] * rfq * gq[i];
-            const float bv = q[h * d + i + half] * rfq * gq[i + half];
-            q[h * d + i] = av * c2[i].x - bv * c2[i].y;
-            q[h * d + i + half] = bv * c2[i].x + av * c2[i].y;
-          }
-          if (tid < p.nh) {  // running max and exp-sum of every head
-            red[48 + tid] = -INFINITY;
-            red[64 + tid] = 0.f;
+          if (amma) {
+            // rotated pairs (h, i), at most 4 per thread, then three bf16 terms per value into
+            // rows 3h + t of the same buffer (pitch d + 8) once every thread has read its pairs
+            float va[4], vb[4];
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int idx = tid + k2 * kCT;
+              va[k2] = vb[k2] = 0.f;
+              if (idx < p.nh * half) {
+                const int h = idx / half, i = idx % half;
+                const float rfq = red[32 + h];
+                const float av = q[h * d + i] * rfq * gq[i];
+                const float bv = q[h * d + i + half] * rfq * gq[i + half];
+                va[k2] = av * c2[i].x - bv * c2[i].y;
+                vb[k2] = bv * c2[i].x + av * c2[i].y;
+              }
+            }
+            cbar();
+            bf16* qt = reinterpret_cast<bf16*>(q);
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              const int idx = tid + k2 * kCT;
+              if (idx < p.nh * half) {
+                const int h = idx / half, i = idx % half;
+                put_terms(qt + 3 * h * (d + 8) + i, d + 8, va[k2]);
+                put_terms(qt + 3 * h * (d + 8) + i + half, d + 8, vb[k2]);
+              }
+            }
+          } else {
+            for (int idx = tid; idx < p.nh * half; idx += kCT) {
+              const int h = idx / half, i = idx % half;
+              const float rfq = red[32 + h];
+              const float av = q[h * d + i] * rfq * gq[i];
+              const float bv = q[h * d + i + half] * rfq * gq[i + half];
+              q[h * d + i] = av * c2[i].x - bv * c2[i].y;
+              q[h * d + i + half] = bv * c2[i].x + av * c2[i].y;
+            }
           }
           cbar();
         }
@@ -892,7 +1209,10 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         {
           const Sec s = sec(2 + 6 * l);
           const int hpg = p.nh / p.nkv;
-          if (hpg % 4 == 0) gc = att_sec<4>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
+          if (amma)
+            gc = att_sec_mma(p.nh, rg, gc, s, d, p.scale[lt], reinterpret_cast<const bf16*>(q), sc,
+                             reinterpret_cast<bf16*>(part), red, rowsb);
+          else if (hpg % 4 == 0) gc = att_sec<4>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
           else if (hpg == 2) gc = att_sec<2>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
           else gc = att_sec<1>(p.nh, p.nkv, rg, gc, s, d, p.scale[lt], q, sc, red, rowsb);
         }
@@ -901,28 +1221,30 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
         const int per = 2 * p.nh + split_max(QD, kNC);
         const Range dr = split(QD, kNC, r);
         xch_arm(kNC * (2 * p.nh + (dr.hi - dr.lo)));
+        send_begin();
         for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
           const Range dw = split(QD, kNC, w2);
-          const unsigned base = xch_dst(w2) + 4u * static_cast<unsigned>(r * per), rb = xch_bar(w2);
-          for (int i = lane; i < 2 * p.nh + (dw.hi - dw.lo); i += 32)
-            st_async_f32(base + 4u * i, i < 2 * p.nh ? rowsb[QD + i] : rowsb[dw.lo + i - 2 * p.nh], rb);
+          send(w2, r * per, rowsb + QD, 2 * p.nh);
+          send(w2, r * per + 2 * p.nh, rowsb + dw.lo, dw.hi - dw.lo);
         }
         const float* pb = xch_wait();
         // ---- combine this CTA's dims: per head, the weight of every source's partial sums
         // exp(m_s - M) / sum_s' exp(m_s' - M) l_s'; then one thread per dim
+        // (one thread per (head, source): kNC consecutive lanes share a head)
         float* wgt = sc;  // [nh][kNC]
-        if (tid < p.nh) {
-          const int h = tid;
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < kNC; ++s2) M = fmaxf(M, pb[s2 * per + 2 * h]);
-          float den = 0.f;
-          for (int s2 = 0; s2 < kNC; ++s2) {
-            const float e = M == -INFINITY ? 0.f : expf(pb[s2 * per + 2 * h] - M);
-            wgt[h * kNC + s2] = e;
-            den = fmaf(e, pb[s2 * per + 2 * h + 1], den);
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          for (int s2 = 0; s2 < kNC; ++s2) wgt[h * kNC + s2] *= inv;
+        static_assert(32 % kNC == 0, "a head's sources lie inside one warp");
+        if (tid < (p.nh * kNC + 31) / 32 * 32) {  // whole warps (the shuffles need every lane)
+          const int h = tid / kNC, s2 = tid % kNC;
+          const bool on = h < p.nh;
+          const float m_s = on ? pb[s2 * per + 2 * h] : -INFINITY;
+          float M = m_s;
+#pragma unroll
+          for (int o = 1; o < kNC; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          const float e = M == -INFINITY ? 0.f : expf(m_s - M);
+          float den = on ? e * pb[s2 * per + 2 * h + 1] : 0.f;
+#pragma unroll
+          for (int o = 1; o < kNC; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+          if (on) wgt[h * kNC + s2] = den > 0.f ? e * (1.f / den) : 0.f;
         }
         cbar();
         for (int fi = tid; fi < dr.hi - dr.lo; fi += kCT) {
@@ -1013,10 +1335,10 @@ __global__ void __launch_bounds__(kT, 1) k_block_cl(const __grid_constant__ Para
       cbar();
       // exchange: every CTA receives [h' (bb floats) | kNC local top-k lists of 2k words]
       xch_arm(p.bb + kNC * 2 * k);
+      send_begin();
       for (int w2 = warp; w2 < kNC && live; w2 += kCW) {
-        const unsigned base = xch_dst(w2), rb = xch_bar(w2);
-        for (int i = lane; i < br.hi - br.lo; i += 32) st_async_f32(base + 4u * (br.lo + i), rowsb[i], rb);
-        for (int i = lane; i < 2 * k; i += 32) st_async_f32(base + 4u * (p.bb + r * 2 * k + i), gtb[i], rb);
+        send(w2, br.lo, rowsb, br.hi - br.lo);
+        send(w2, p.bb + r * 2 * k, gtb, 2 * k);
       }
       const float* hx = xch_wait();
       for (int i = tid; i < p.bb; i += kCT) u[i] = hx[i];

@@ -34,7 +34,11 @@ constexpr int kCT = kCW * 32;      // compute threads
 constexpr int kT = kCT + 32;       // + one producer warp
 static_assert(kCW % 4 == 0, "the tensor-core GEMV splits k over groups of four warps");
 constexpr int kSlots = 4;
-constexpr int kSlotBytes = 32768;
+constexpr int kSlotBytes = 32768;  // payload of a weight slot
+// Slots are kSlotPad bytes longer than their weight payload so that 32 K rows of d = 512 fit
+// at a padded pitch (row + 16 bytes: 8 rows at the same column fall in distinct banks).
+constexpr int kSlotPad = 512;
+constexpr int kSlotStride = kSlotBytes + kSlotPad;
 constexpr int kMaxL = 8;
 constexpr int kXchFloats = 4096;   // floats per receive buffer
 
@@ -111,6 +115,27 @@ __host__ __device__ inline int keys_per_slot(int row_bytes) {
   return r < kMaxKeysPerSlot ? r : kMaxKeysPerSlot;
 }
 
+// Keys per slot of a K section at the padded pitch of the tensor-core attention (a multiple of
+// the 16-key MMA tile).
+__host__ __device__ inline int keys_per_slot_mma(int row_bytes) {
+  const int r = kSlotStride / (row_bytes + 16) / 16 * 16;
+  return r < kMaxKeysPerSlot ? r : kMaxKeysPerSlot;
+}
+// The tensor-core attention (one KV head and at most 4 query heads, q as three bf16 terms of
+// every head in a receive buffer, at most four (head, dim-pair) items per thread in its q
+// set-up, 16-key tiles, at most 4 dim tiles of 16 per compute warp).
+__host__ __device__ inline bool att_mma_ok(const Params& p) {
+  if (!p.mma || p.nkv != 1 || p.nh < 1 || p.nh > 4) return false;
+  for (int t = 0; t < 2; ++t) {
+    if (!p.has_type[t]) continue;
+    const int d = p.d[t];
+    if (d % 16 || d < 16 || d > 16 * 4 * kCW || p.nh * d > 2048 || 3 * p.nh * (d + 8) * 2 > kXchFloats * 4 ||
+        keys_per_slot_mma(d * 2) < 16)
+      return false;
+  }
+  return true;
+}
+
 // Packed tile layout of a matrix with R rows split over the cluster (see Params::pk_q):
 // CTA r's rows padded to 16 and the number of 512-byte tiles before its block.
 __host__ __device__ inline int padded_rows(int R, int r) {
@@ -132,6 +157,7 @@ struct Sec {
   long long stride;
   int row_bytes, nrows, rpc;
   int kt, rrows;
+  int pitch;  // bytes between rows in the slot (row_bytes, or padded K rows)
 };
 constexpr int kMaxSec = 1 + 6 * kMaxL + 2;  // PRE | 6 per block | CENT | POST
 
@@ -152,7 +178,7 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
     dmin = p.d[p.ltype[l]] < dmin ? p.d[p.ltype[l]] : dmin;
   }
   if (dmin <= 0) dmin = 1;
-  L.ring = off;  off += kSlots * kSlotBytes;
+  L.ring = off;  off += kSlots * kSlotStride;
   L.xch0 = off;  off += kXchFloats * 4;
   L.xch1 = off;  off += kXchFloats * 4;  // must directly follow xch0
   L.u = off;     off += al16(2 * p.bb * 4);
@@ -176,11 +202,15 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
   // k-quarter partials of the tensor-core GEMVs: 4 x padded rows of the largest section
   int pr = imax(imax(split_max(p.nh * dmax, kNC), split_max(p.F, kNC)), imax(split_max(p.C, kNC), split_max(p.bb, kNC)));
   part = imax(part, 4 * ((pr + 15) / 16 * 16));
+  const bool amma = att_mma_ok(p);
+  // tensor-core attention: probabilities of a slot of keys as three bf16 terms per head
+  if (amma) part = imax(part, (3 * p.nh * (keys_per_slot_mma(dmin * 2) + 8) * 2 + 3) / 4);
   L.part = off;  off += al16(part * 4);
   L.xt = off;    off += al16(4 * p.H * 2);     // bf16 hi / mid / lo terms of a GEMV input + a zero row
   // two alternating buffers of score partials (up to kQkSlices k slices) for one slot of keys;
   // also holds the combine weights, the centroid keys and the candidate lists of the head
   int scf = 2 * kQkSlices * keys_per_slot(p.nkv * dmin * 2) * p.nh;
+  if (amma) scf = imax(scf, 4 * keys_per_slot_mma(dmin * 2) * p.nh);  // 4 k-quarter score partials
   scf = imax(scf, imax(kNC * p.nh, 2 * split_max(p.C, kNC)));
   scf = imax(scf, 2 * kNC * p.topk);  // 64-bit candidate lists of the top-k merge
   L.sc = off;    off += al16(scf * 4);

@@ -47,6 +47,14 @@ enum mtp_status {
 };
 
 enum mtp_dtype { MTP_DTYPE_BF16 = 0, MTP_DTYPE_F32 = 1 };
+
+/* Value of the vocabulary entries outside the selected clusters in a materialised logits row
+ * of the centroid head: -1e30f ("Gemma 4 Assistant tensor inventory", "Centroid / ordered
+ * embeddings LM head", step 5: dense fill, then the sparse logits set at their ids), or the
+ * smallest selected logit minus one ("Gemma 4 Assistant 使用指南", section 五, step 3 of
+ * use_ordered_embeddings; named there as the MLX-style alternative). The argmax is the same
+ * either way. */
+enum mtp_logit_mask { MTP_MASK_NEG_1E30 = 0, MTP_MASK_MIN_MINUS_ONE = 1 };
 enum mtp_layer_kind { MTP_LAYER_SLIDING = 0, MTP_LAYER_FULL = 1 };
 
 /* Drafter hyper-parameters.
@@ -167,7 +175,8 @@ MTP_API int mtp_draft_block(mtp_handle *h, const void *hidden, const int32_t *la
  * Centroid head ("Gemma 4 Assistant tensor inventory", "Centroid / ordered embeddings LM
  * head", steps 1-5): centroid logits, top_k centroids, gather of their ids, sparse logits,
  * and -- when out_logits != NULL -- the full row filled with -1e30f with the sparse logits
- * scattered at their ids. Dense head (use_ordered_embeddings == 0): all V logits.
+ * scattered at their ids (or the other mask of mtp_set_logit_mask). Dense head
+ * (use_ordered_embeddings == 0): all V logits.
  *   y             device [B][H] fp32 (rounded to bf16 inside for bf16 models)
  *   out_logits    device [B][V] fp32 or NULL
  *   out_token     device [B] int32 (argmax, lowest id on ties)
@@ -176,6 +185,14 @@ MTP_API int mtp_draft_block(mtp_handle *h, const void *hidden, const int32_t *la
  * Errors: INVALID_ARG, CUDA. */
 MTP_API int mtp_centroid_head(mtp_handle *h, const float *y, int32_t B, float *out_logits,
                       int32_t *out_token, int32_t *out_centroids, void *stream);
+
+/* Select the mask of the materialised rows of mtp_centroid_head on this handle (default
+ * MTP_MASK_NEG_1E30). With MTP_MASK_MIN_MINUS_ONE, after the sparse logits are scattered,
+ * every entry still holding the -1e30f fill becomes min over the sequence's candidate
+ * logits minus 1 (fp32). A candidate logit equal to -1e30f exactly would be treated as
+ * fill. Has no effect on the dense head or on mtp_draft_block (which materialises no row).
+ * Errors: INVALID_ARG (NULL handle, unknown mode). */
+MTP_API int mtp_set_logit_mask(mtp_handle *h, int32_t mode);
 
 /* Greedy accept-prefix verification ("Gemma 4 drafter explained", "What is Speculative
  * Decoding?"): t_i = argmax of target row i (lowest id on ties); accept_len[b] = the

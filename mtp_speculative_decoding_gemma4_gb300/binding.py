@@ -18,7 +18,8 @@ MTP_LAYER_SLIDING, MTP_LAYER_FULL = 0, 1
 
 # Every symbol include/mtp.h declares.
 EXPORTS = ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy", "mtp_get_status",
-           "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc")
+           "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc", "mtp_set_logit_mask")
+MASK_NEG_1E30, MASK_MIN_MINUS_ONE = 0, 1  # enum mtp_logit_mask
 
 
 class MtpError(RuntimeError):
@@ -75,12 +76,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mtp_centroid_head_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.mtp_get_status.argtypes = [vp]
     lib.mtp_set_path.argtypes = [vp, i32]
+    lib.mtp_set_logit_mask.argtypes = [vp, i32]
     lib.mtp_destroy.argtypes = [vp]
     lib.mtp_destroy.restype = None
     lib.mtp_last_error.argtypes = []
     lib.mtp_last_error.restype = ctypes.c_char_p
     for name in ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy",
-                 "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc"):
+                 "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc", "mtp_set_logit_mask"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -140,6 +142,10 @@ def mtp_get_status(handle: int) -> int:
 
 def mtp_set_path(handle: int, path: int) -> None:
     _check(load_library().mtp_set_path(handle, path), "mtp_set_path")
+
+
+def mtp_set_logit_mask(handle: int, mode: int) -> None:
+    _check(load_library().mtp_set_logit_mask(handle, mode), "mtp_set_logit_mask")
 
 
 def mtp_destroy(handle: int) -> None:

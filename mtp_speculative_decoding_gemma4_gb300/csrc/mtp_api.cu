@@ -20,6 +20,7 @@ struct mtp_handle {
   int device;
   int num_sms;
   int path;
+  int mask_mode;  // materialised rows of the centroid head: MTP_MASK_NEG_1E30 / MIN_MINUS_ONE
   int dmax;
   int nsplit_max;
   void* ws;
@@ -472,6 +473,7 @@ size_t layout_ws(mtp_handle* h, char* base) {
   w.cl = static_cast<float*>(take(4 * B * C));
   w.sel = static_cast<int*>(take(4 * B * k));
   w.best = static_cast<unsigned long long*>(take(8 * B));
+  w.lmin = static_cast<float*>(take(4 * B));
   w.cs = static_cast<float2*>(take(8 * B * 2 * (dmax / 2)));
   w.bar = static_cast<unsigned int*>(take(16));
   w.status = static_cast<int*>(take(16));
@@ -882,8 +884,19 @@ int mtp_centroid_head(mtp_handle* h, const float* y, int32_t B, float* out_logit
   p.out_logits = out_logits;
   p.out_tokens = out_token;
   p.out_centroids = out_centroids;
+  p.mask_mode = h->mask_mode;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return c.dtype == MTP_DTYPE_BF16 ? mtp::run_head_bf16(p, st) : mtp::run_head_f32(p, st);
+}
+
+int mtp_set_logit_mask(mtp_handle* h, int32_t mode) {
+  mtp::g_err[0] = 0;
+  if (!h || (mode != MTP_MASK_NEG_1E30 && mode != MTP_MASK_MIN_MINUS_ONE)) {
+    set_error("need a handle and mode MTP_MASK_NEG_1E30 (0) or MTP_MASK_MIN_MINUS_ONE (1), got %d", mode);
+    return MTP_ERR_INVALID_ARG;
+  }
+  h->mask_mode = mode;
+  return MTP_OK;
 }
 
 int mtp_verify_greedy(const void* target_logits, const int32_t* draft, int32_t B, int32_t n, int32_t V,

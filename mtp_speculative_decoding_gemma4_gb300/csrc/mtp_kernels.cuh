@@ -94,6 +94,19 @@ template <typename WT> __global__ void __launch_bounds__(kThreads) k_fin(Params 
   phase_fin(p, stride, col, blockIdx.x, gridDim.x);
 }
 
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_cand_min(Params p) {
+  MTP_KERNEL_PROLOGUE phase_cand_min<WT>(p, blockIdx.x, gridDim.x, smem);
+}
+// Entries of the materialised rows still holding the -1e30 fill (those outside the selected
+// clusters) -> the sequence's smallest candidate logit minus one.
+template <typename WT>
+__global__ void __launch_bounds__(kThreads) k_remask(float* out, long long V, long long n, const float* lmin) {
+  const unsigned fill = __float_as_uint(-1e30f);
+  for (long long i = blockIdx.x * static_cast<long long>(kThreads) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * kThreads)
+    if (__float_as_uint(out[i]) == fill) out[i] = lmin[i / V] - 1.f;
+}
+
 // Fill of the materialised logits row (-1e30 everywhere before the sparse scatter).
 template <typename WT>
 __global__ void __launch_bounds__(kThreads) k_fill(float* out, long long n, float v) {
@@ -403,6 +416,12 @@ int run_head(const Params& p, cudaStream_t st) {
   if (s.ordered) {
     MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
     MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+    if (p.out_logits && p.mask_mode == MTP_MASK_MIN_MINUS_ONE) {
+      MTP_LAUNCH(k_cand_min<WT>, s.B, kWarps * 4, p);
+      const long long n = static_cast<long long>(s.B) * s.V;
+      k_remask<WT><<<1024, kThreads, 0, st>>>(p.out_logits, s.V, n, p.w.lmin);
+      MTP_CHECK_LAUNCH("k_remask");
+    }
   } else {
     MTP_LAUNCH(k_dense<WT>, z.dense, z.smem_dense, p);
   }

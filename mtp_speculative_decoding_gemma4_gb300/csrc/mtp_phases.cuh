@@ -76,6 +76,7 @@ struct WsP {
   float* cl;                   // [B][C]
   int* sel;                    // [B][topk]
   unsigned long long* best;    // [B]
+  float* lmin;                 // [B] smallest candidate logit (the min(selected) - 1 mask)
   float2* cs;                  // [B][2][dmax/2] RoPE (cos, sin)
   unsigned int* bar;           // grid barrier counter
   int* status;                 // device status word (0 = ok)
@@ -99,6 +100,7 @@ struct Params {
   const float* y_in;   // head entry: [B][H]
   float* out_logits;   // head entry: [B][V] or null
   int* out_centroids;  // head entry: [B][topk] or null
+  int mask_mode;       // head entry: unselected logits -1e30 (MTP_MASK_NEG_1E30) or min - 1
   long long spin_limit;  // bounded grid-barrier wait (clock64 cycles)
   // Tensor-core path: when set, a GEMV phase only stages its inputs and writes them as three
   // bf16 terms [3][tc_bp][K_in] (hi, mid, lo of every fp32 input) for the tcgen05 GEMMs.
@@ -1029,6 +1031,38 @@ __device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kWarps; ++w) m = wbest[w] > m ? wbest[w] : m;
       atomicMax(&p.w.best[b], m);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- MASK (min(selected) - 1)
+
+// Smallest logit among each sequence's candidates (the entries the gather scattered into its
+// materialised row), for the mask variant that fills the other entries with that minus one
+// ("Gemma 4 Assistant 使用指南" section 五, use_ordered_embeddings step 3; the -1e30 fill
+// of "Gemma 4 Assistant tensor inventory", "Centroid / ordered embeddings LM head" step 5,
+// names it as the MLX alternative).
+template <typename WT>
+__device__ void phase_cand_min(const Params& p, int cta, int ncta, char* smem) {
+  const int vsc = p.s.vsc, k = p.s.topk, ncand = k * vsc;
+  float* red = reinterpret_cast<float*>(smem);  // [kWarps]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int b = cta; b < p.s.B; b += ncta) {
+    float m = INFINITY;
+    for (int c = threadIdx.x; c < ncand; c += kThreads) {
+      const int cent = p.w.sel[b * k + c / vsc];
+      const int id = p.ord[cent * vsc + c % vsc];
+      m = fminf(m, p.out_logits[static_cast<size_t>(b) * p.s.V + id]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mm = red[0];
+      for (int w = 1; w < kWarps; ++w) mm = fminf(mm, red[w]);
+      p.w.lmin[b] = mm;
     }
     __syncthreads();
   }

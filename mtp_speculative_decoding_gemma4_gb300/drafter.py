@@ -106,6 +106,11 @@ class Drafter:
     def set_path(self, path: int) -> None:
         B.mtp_set_path(self.handle, path)
 
+    def set_logit_mask(self, mode: int) -> None:
+        """Mask of the rows centroid_head materialises: binding.MASK_NEG_1E30 (default) or
+        binding.MASK_MIN_MINUS_ONE (smallest selected logit minus one)."""
+        B.mtp_set_logit_mask(self.handle, mode)
+
     def status(self) -> int:
         return B.mtp_get_status(self.handle)
 

@@ -33,7 +33,8 @@ Readings where the pages are silent or disagree (each is stated again where it i
     attends [0, L); q_len is 1 so both masks are bidirectional;
   * head i reads KV head i // (n_head / n_kv_head);
   * token_ordering viewed row-major [C][vsc]: centroid c owns ids ordering[c*vsc:(c+1)*vsc];
-  * unselected vocabulary entries of the materialised row are -1e30 (fp32).
+  * unselected vocabulary entries of the materialised row are -1e30 (fp32), or, in the
+    other variant the pages give, the smallest candidate logit minus one.
 
 Pins: every helper and the centroid head, top-k, attention, verify and the shape counts are
 pinned by the not-gpu tests against closed forms, invariants, brute force and the values
@@ -316,11 +317,24 @@ def centroid_head(s: Shape, W: DecodedWeights, yb: np.ndarray) -> HeadResult:
                       logit_gap=top2_gap(logits), kth_gap=kth_gap)
 
 
-def materialise_row(s: Shape, head: HeadResult) -> np.ndarray:
-    """Full-vocabulary fp32 row: -1e30 everywhere, the sparse logits scattered at their ids
-    ("Gemma 4 Assistant tensor inventory", "Centroid / ordered embeddings LM head", step 5)."""
-    row = np.full(s.vocab, MASK_VALUE, dtype=np.float32)
-    row[head.ids] = head.logits.astype(np.float32)
+def materialise_row(s: Shape, head: HeadResult, mask: str = "neg_1e30") -> np.ndarray:
+    """Full-vocabulary fp32 row with the sparse logits scattered at their ids.
+
+    mask "neg_1e30": every other entry is -1e30 ("Gemma 4 Assistant tensor inventory",
+    "Centroid / ordered embeddings LM head", step 5: a dense -1e30 fill, then the rows set).
+    mask "min_minus_one": every other entry is the smallest candidate logit minus one, both
+    in fp32 ("Gemma 4 Assistant 使用指南", section 五, use_ordered_embeddings step 3, where the
+    unscored positions take a mask value one below the smallest logit; the tensor-inventory
+    page names it as the MLX variant)."""
+    vals = head.logits.astype(np.float32)
+    if mask == "neg_1e30":
+        fill = MASK_VALUE
+    elif mask == "min_minus_one":
+        fill = np.float32(np.float32(vals.min()) - np.float32(1.0))
+    else:
+        raise ValueError(f"unknown mask {mask!r}")
+    row = np.full(s.vocab, fill, dtype=np.float32)
+    row[head.ids] = vals
     return row
 
 

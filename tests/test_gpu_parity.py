@@ -172,6 +172,50 @@ def test_centroid_head_entry_matches_oracle(index):
     dr.close()
 
 
+@pytest.mark.parametrize("index", [0, 1])
+def test_centroid_head_min_minus_one_mask_matches_oracle(index):
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
+    shape, wl, w, inp = config_data(index)
+    s, W = decoded(index)
+    rng = np.random.default_rng(15)
+    B = 3
+    y = (rng.standard_normal((B, s.hidden)) * 0.8).astype(np.float32)
+    dr, _ = _drafter(index, max_batch=B)
+    with pytest.raises(MtpError):
+        dr.set_logit_mask(2)
+    dr.set_logit_mask(binding.MASK_MIN_MINUS_ONE)
+    tok, logits, cents = dr.centroid_head(to_torch(y, "f32"), want_logits=True, want_centroids=True)
+    torch.cuda.synchronize()
+    tok, logits, cents = tok.cpu().numpy(), logits.cpu().numpy(), cents.cpu().numpy()
+    tol, delta = TOL[shape.dtype], NEAR_TIE[shape.dtype]
+    for b in range(B):
+        ref = O.centroid_head(s, W, y[b].astype(np.float64))
+        if not np.array_equal(cents[b], ref.selected):
+            assert ref.kth_gap < delta, (cents[b], ref.selected, ref.kth_gap)
+            continue
+        row = O.materialise_row(s, ref, mask="min_minus_one")
+        unsel = np.ones(s.vocab, bool)
+        unsel[ref.ids] = False
+        cand = logits[b][ref.ids]
+        assert np.max(np.abs(cand.astype(np.float64) - ref.logits)) <= tol
+        # every other entry: the GPU's own smallest candidate minus one (fp32), within
+        # tolerance of the oracle's fill
+        fill = np.float32(cand.min()) - np.float32(1.0)
+        assert np.all(logits[b][unsel] == fill)
+        assert abs(float(fill) - float(row[unsel][0])) <= tol
+        if tok[b] != ref.token:
+            assert ref.logit_gap < delta
+        else:
+            assert int(np.argmax(logits[b])) == ref.token
+    # back to the -1e30 fill
+    dr.set_logit_mask(binding.MASK_NEG_1E30)
+    _t, logits0, _c = dr.centroid_head(to_torch(y, "f32"), want_logits=True)
+    torch.cuda.synchronize()
+    l0 = logits0.cpu().numpy()
+    assert np.sum(l0 == np.float32(-1e30)) == B * (s.vocab - s.top_k * s.vsc)
+    dr.close()
+
+
 def test_dense_head_entry_matches_oracle():
     shape, wl, w, inp = config_data(3)
     s, W = decoded(3)

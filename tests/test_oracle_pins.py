@@ -202,6 +202,31 @@ def test_centroid_head_matches_dense_on_selected_clusters():
     assert hits >= 5
 
 
+def test_min_minus_one_mask_orders_every_unselected_entry_below_the_candidates():
+    # "Gemma 4 Assistant 使用指南" section 五, use_ordered_embeddings step 3: the entries no
+    # cluster scored take a mask value one below the smallest logit. Invariants: the argmax is
+    # the head's token under both masks; every masked entry lies strictly below every
+    # candidate (a dropped "- 1", a "+ 1" or a max in place of the min breaks this) and one
+    # unit below the smallest; the candidates are the same under both masks.
+    s = _tiny_head_shape()
+    for seed in range(40):
+        W = _tiny_head_weights(s, seed)
+        y = np.random.default_rng(300 + seed).standard_normal(s.hidden)
+        head = O.centroid_head(s, W, y)
+        r0 = O.materialise_row(s, head)
+        r1 = O.materialise_row(s, head, mask="min_minus_one")
+        unsel = np.ones(s.vocab, bool)
+        unsel[head.ids] = False
+        cand = r1[~unsel]
+        np.testing.assert_array_equal(cand, r0[~unsel])
+        assert np.all(r1[unsel] < cand.min())
+        assert len(np.unique(r1[unsel])) == 1
+        assert abs(float(cand.min()) - float(r1[unsel][0]) - 1.0) < 1e-6 * max(1.0, abs(float(cand.min())))
+        assert int(np.argmax(r1)) == int(np.argmax(r0)) == head.token
+    with pytest.raises(ValueError):
+        O.materialise_row(s, head, mask="zero")
+
+
 def test_centroid_head_recovers_planted_token():
     # clusters built around centroid directions: y along a member of cluster 5 selects that
     # cluster first, and the dense winner is found inside it

@@ -311,7 +311,7 @@ __device__ __forceinline__ void ring_release(const Ring& rg, int g) {
 
 // out[i] = W_i . x for the rows of a streamed section (chunk counter g at its first chunk);
 // x is fp32 in shared memory. Returns the chunk counter after the section.
-__device__ __noinline__ int gemv_sec(Ring rg, int g, Sec s, const float* x, float* out, float* part) {
+__device__ __forceinline__ int gemv_sec(Ring rg, int g, Sec s, const float* x, float* out, float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nc = n_chunks(s), K = s.row_bytes / 2, V8 = K / 8;
   const int ns = gemv_ns(s.rpc), nq = (s.rpc + 3) / 4, ntask = nq * ns;
@@ -395,7 +395,7 @@ __device__ __forceinline__ void split_terms(const float* x, int n, bf16* xt) {
 // input already split into xt [4][K]. Per slot, warp w multiplies row tile (w / 4) (+4, ...)
 // over the k quarter (w % 4); B column n < 3 carries term n of x, so a row's value is the sum
 // of D's first three columns. The four k-quarter partials are added in a fixed order.
-__device__ __noinline__ int gemv_mma_sec(Ring rg, int g, Sec s, const bf16* xt, float* out, float* part) {
+__device__ __forceinline__ int gemv_mma_sec(Ring rg, int g, Sec s, const bf16* xt, float* out, float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;
   const int KT = s.kt, K = KT * 16, kq = warp & 3, ktn = KT / 4, kt0 = kq * ktn;
@@ -631,7 +631,7 @@ constexpr int kAttMaxKU = 4;  // keys per lane in the softmax: a slot holds at m
 //           running max / exp-sum and writes p as three bf16 terms (row 3h + t of pt);
 //   sums    O^T[dim][col] += K^T P^T: every warp owns dim tiles, keys chained per slot.
 // Leaves the unnormalised sums [nh][d] and (m_h, l_h) in stage, like att_sec.
-__device__ __noinline__ int att_sec_mma(int nh, Ring rg, int g, Sec s, int d, float scale, const bf16* qt,
+__device__ __forceinline__ int att_sec_mma(int nh, Ring rg, int g, Sec s, int d, float scale, const bf16* qt,
                                         float* sc, bf16* pt, float* red, float* stage) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, ti = lane & 3;
   const int nc = n_chunks(s), kps = s.rpc, P = s.pitch, qp = d + 8, pp = kps + 8;
@@ -826,7 +826,7 @@ __device__ __noinline__ int att_sec_mma(int nh, Ring rg, int g, Sec s, int d, fl
 
 // Logits of the rows of this CTA's selected centroids [slo, shi) (contiguous blocks of the
 // cluster-ordered embedding copy) against y; each warp's best (value, id) key goes to lk.
-__device__ __noinline__ void gather_best(const bf16* temb_ord, const int* ord, int H, int vsc, int nclust, const int* selc,
+__device__ __forceinline__ void gather_best(const bf16* temb_ord, const int* ord, int H, int vsc, int nclust, const int* selc,
                                          int slo, int shi, const float* y, unsigned long long* lk) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // request every candidate block (vsc rows of H bf16, and its vsc ids) from memory at once
@@ -881,7 +881,7 @@ __device__ __forceinline__ int count_greater(const unsigned long long* L, int k,
     if (pos + step <= k && L[pos + step - 1] > e) pos += step;
   return pos;
 }
-__device__ __noinline__ void merge_tree(const unsigned* lists, int k, int C, unsigned long long* buf_a,
+__device__ __forceinline__ void merge_tree(const unsigned* lists, int k, int C, unsigned long long* buf_a,
                                         unsigned long long* buf_b, int* selc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // level 0: word-pair lists -> buf_a as 64-bit keys

@@ -325,7 +325,7 @@ int build_packed(mtp_handle* h) {
   const mtp_config& c = h->cfg;
   h->wpack = nullptr;
   const int H = c.hidden;
-  if (H % 64 != 0 || H > 1024) return MTP_OK;
+  if (H % 64 != 0 || H > 512) return MTP_OK;  // the GEMV keeps a k quarter of B fragments (H / 64 <= 8 steps)
   struct Item {
     const void* W;
     int R;

@@ -374,10 +374,12 @@ __device__ __forceinline__ uint32_t lds32(unsigned a) {
 }
 
 // Splits the n fp32 values of x into three bf16 terms hi + mid + lo (x == hi + mid + lo up to
-// the rounding of lo, i.e. fp32 precision), written as rows 0..2 of xt [4][n]; row 3 is zero.
-// The tensor-core GEMVs multiply these terms by the bf16 weights: every product is exact and
-// the sums are fp32, so the result equals an fp32 dot product up to summation order.
+// the rounding of lo, i.e. fp32 precision), written as rows 0..2 of xt [4][n + 8]; row 3 is
+// zero. The row pitch n + 8 puts the 8 B-fragment rows a warp reads at one column in distinct
+// banks. The tensor-core GEMVs multiply these terms by the bf16 weights: every product is
+// exact and the sums are fp32, so the result equals an fp32 dot product up to summation order.
 __device__ __forceinline__ void split_terms(const float* x, int n, bf16* xt) {
+  const int pt = n + 8;
   for (int i = threadIdx.x; i < n; i += kCT) {
     const float v = x[i];
     const bf16 h = __float2bfloat16_rn(v);
@@ -385,43 +387,82 @@ __device__ __forceinline__ void split_terms(const float* x, int n, bf16* xt) {
     const bf16 m = __float2bfloat16_rn(r1);
     const bf16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
     xt[i] = h;
-    xt[n + i] = m;
-    xt[2 * n + i] = l;
-    xt[3 * n + i] = __float2bfloat16_rn(0.f);
+    xt[pt + i] = m;
+    xt[2 * pt + i] = l;
+    xt[3 * pt + i] = __float2bfloat16_rn(0.f);
+  }
+}
+
+// Row sums of a 16-row tile's MMA result (columns 0..2 carry the three input terms, column 3
+// is zero): lanes ti = 0 hold rows gi and gi + 8 after the pair reduction.
+__device__ __forceinline__ void tile_rows_out(const float (&d)[4], int ti, int gi, float* part, int row0) {
+  float v0 = d[0] + d[1], v1 = d[2] + d[3];
+  v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+  v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+  if (ti == 0) {
+    part[row0 + gi] = v0;
+    part[row0 + gi + 8] = v1;
   }
 }
 
 // out[i] = W_i . x for a packed section (tiles of this CTA's rows, see Params::pk_q) with the
-// input already split into xt [4][K]. Per slot, warp w multiplies row tile (w / 4) (+4, ...)
-// over the k quarter (w % 4); B column n < 3 carries term n of x, so a row's value is the sum
-// of D's first three columns. The four k-quarter partials are added in a fixed order.
+// input already split into xt [4][K + 8]. Per slot, warp w multiplies row tiles (w / 4),
+// (w / 4) + kCW / 4, ... over the k quarter (w % 4); B column n < 3 carries term n of x, so a
+// row's value is the sum of D's first three columns. The warp's B fragments are loaded once;
+// for K = 256 (4 k-steps per quarter) two row tiles go at a time, their A tiles loaded first
+// and their MMA chains interleaved. The four k-quarter partials are added in a fixed order.
 __device__ __forceinline__ int gemv_mma_sec(Ring rg, int g, Sec s, const bf16* xt, float* out, float* part) {
+  constexpr int kMaxKtn = 8;  // k-steps per quarter held as B fragments (K <= 512)
+  constexpr int kStepRt = kCW / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;
   const int KT = s.kt, K = KT * 16, kq = warp & 3, ktn = KT / 4, kt0 = kq * ktn;
   const int nc = n_chunks(s), rts = s.rpc / KT, PR = (s.rrows + 15) / 16 * 16;
   // this lane's B column: term gi of x for gi < 3, the zero row otherwise
-  const unsigned xb = sa(xt) + 2u * static_cast<unsigned>((gi < 3 ? gi : 3) * K + 2 * ti);
+  const unsigned xb = sa(xt) + 2u * static_cast<unsigned>((gi < 3 ? gi : 3) * (K + 8) + 2 * ti);
+  uint32_t bf[2 * kMaxKtn];
+#pragma unroll
+  for (int j = 0; j < kMaxKtn; ++j) {
+    bf[2 * j] = bf[2 * j + 1] = 0u;
+    if (j < ktn) {
+      const unsigned bk = xb + 32u * static_cast<unsigned>(kt0 + j);
+      bf[2 * j] = lds32(bk);
+      bf[2 * j + 1] = lds32(bk + 16);
+    }
+  }
   for (int ch = 0; ch < nc; ++ch, ++g) {
     const unsigned W = ring_wait(rg, g);
     const int nt = min(s.rpc, s.nrows - ch * s.rpc), nrt = nt / KT;
-    for (int rt = warp >> 2; rt < nrt; rt += kCW / 4) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      const unsigned a0 = W + static_cast<unsigned>((rt * KT + kt0) * kTileBytes + lane * 16);
-#pragma unroll 4
-      for (int j = 0; j < ktn; ++j) {
-        const uint4 a = lds128(a0 + j * kTileBytes);
-        const unsigned bk = xb + 32u * static_cast<unsigned>(kt0 + j);
-        mma_bf16(d, a, lds32(bk), lds32(bk + 16));
+    float* pq = part + kq * PR + ch * rts * 16;
+    if (ktn == 4) {
+      for (int rt = warp >> 2; rt < nrt; rt += 2 * kStepRt) {
+        const int rt2 = rt + kStepRt;
+        const bool two = rt2 < nrt;
+        const unsigned a0 = W + static_cast<unsigned>((rt * KT + kt0) * kTileBytes + lane * 16);
+        const unsigned a1 = W + static_cast<unsigned>(((two ? rt2 : rt) * KT + kt0) * kTileBytes + lane * 16);
+        uint4 a[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          a[j] = lds128(a0 + j * kTileBytes);
+          a[4 + j] = lds128(a1 + j * kTileBytes);
+        }
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mma_bf16(d0, a[j], bf[2 * j], bf[2 * j + 1]);
+          mma_bf16(d1, a[4 + j], bf[2 * j], bf[2 * j + 1]);
+        }
+        tile_rows_out(d0, ti, gi, pq, rt * 16);
+        if (two) tile_rows_out(d1, ti, gi, pq, rt2 * 16);
       }
-      // row sums of columns 0..2 (column 3 is zero): lanes ti = 0, 1 hold them
-      float v0 = d[0] + d[1], v1 = d[2] + d[3];
-      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-      if (ti == 0) {
-        const int row = (ch * rts + rt) * 16 + gi;
-        part[kq * PR + row] = v0;
-        part[kq * PR + row + 8] = v1;
+    } else {
+      for (int rt = warp >> 2; rt < nrt; rt += kStepRt) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned a0 = W + static_cast<unsigned>((rt * KT + kt0) * kTileBytes + lane * 16);
+#pragma unroll
+        for (int j = 0; j < kMaxKtn; ++j)
+          if (j < ktn) mma_bf16(d, lds128(a0 + j * kTileBytes), bf[2 * j], bf[2 * j + 1]);
+        tile_rows_out(d, ti, gi, pq, rt * 16);
       }
     }
     ring_release(rg, g);

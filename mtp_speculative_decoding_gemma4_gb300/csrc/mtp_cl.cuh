@@ -206,7 +206,7 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
   // tensor-core attention: probabilities of a slot of keys as three bf16 terms per head
   if (amma) part = imax(part, (3 * p.nh * (keys_per_slot_mma(dmin * 2) + 8) * 2 + 3) / 4);
   L.part = off;  off += al16(part * 4);
-  L.xt = off;    off += al16(4 * p.H * 2);     // bf16 hi / mid / lo terms of a GEMV input + a zero row
+  L.xt = off;    off += al16(4 * (p.H + 8) * 2);  // bf16 hi / mid / lo terms of a GEMV input + a zero row (pitch H + 8)
   // two alternating buffers of score partials (up to kQkSlices k slices) for one slot of keys;
   // also holds the combine weights, the centroid keys and the candidate lists of the head
   int scf = 2 * kQkSlices * keys_per_slot(p.nkv * dmin * 2) * p.nh;

@@ -309,7 +309,7 @@ def run_mtp(args, rank: int, world: int, dist):
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
     tokens = B * n * world
     head = (3 if shape.use_ordered_embeddings else 1)
-    if args.path in (2, 3, 4):
+    if args.path in (2, 3, 4, 6):
         launches_per_step = 2
     elif args.path == 5:  # per step: staging + tcgen05 GEMM per projection, attention, combine, head
         launches_per_step = 1 + n * (2 + 11 * shape.n_layers + 2 + head) + 1 + 1
@@ -318,7 +318,8 @@ def run_mtp(args, rank: int, world: int, dist):
     kernel_name = {1: "phase kernels", 2: "k_block (persistent draft block, grid barriers)",
                    3: "k_block_ll (latency draft block, resident weights + mailboxes)",
                    4: "k_block_cl (cluster draft block, streamed weights + DSMEM exchanges)",
-                   5: "k_tc_gemm + phase kernels (tcgen05 projections)"}[args.path]
+                   5: "k_tc_gemm + phase kernels (tcgen05 projections)",
+                   6: "k_block_c2 (streamed-tile cluster draft block, tensor-core projections)"}[args.path]
     res = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -433,14 +434,15 @@ def main():
     ap.add_argument("--path", type=int, default=-1,
                     help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
                          "(one sequence), 4: cluster kernel (one sequence), 5: phase kernels with tcgen05 "
-                         "projections; default: 4 for B=1, 5 for B>=32, else 2")
+                         "projections, 6: streamed-tile cluster kernel (one sequence); default: 6 for B=1, 5 "
+                         "for B>=32, else 2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.path < 0:
         bsz = workload(args.config)[1].batch
-        args.path = 4 if bsz == 1 else (5 if bsz >= 32 else 2)
+        args.path = 6 if bsz == 1 else (5 if bsz >= 32 else 2)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

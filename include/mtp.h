@@ -253,8 +253,13 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * a copy of token_embd in token_ordering order and tensor-core tiles of the hidden-wide
  * matrices for it), 5 = one kernel per phase with every projection (and the dense tied
  * head) as a tcgen05 tensor-core GEMM (bf16, max_batch <= 64; mtp_init_weights keeps the
- * tensor maps and a staging buffer of 3 * roundup(max_batch, 32) * max input width bf16).
- * Automatic picks 4 for B = 1 when available, else 3 when available; 5 for B >= 32 when
+ * tensor maps and a staging buffer of 3 * roundup(max_batch, 32) * max input width bf16),
+ * 6 = streamed-tile cluster kernel for one sequence (one 16-CTA cluster; every projection on
+ * tensor cores from weight tiles that mtp_init_weights packs once into one stream per CTA,
+ * about the size of all projection weights; vectors exchanged register-to-peer in
+ * distributed shared memory; bf16 centroid-head shapes within its limits, V = K, 16-byte
+ * aligned hidden and K rows). Automatic picks 6 for B = 1 when available, else 4, else 3;
+ * 5 for B >= 32 when
  * available; else 2 when co-resident, else 1. Results agree within the precision contract.
  * Errors: INVALID_ARG; a forced path the call cannot use makes mtp_draft_block return
  * UNSUPPORTED_SHAPE. */

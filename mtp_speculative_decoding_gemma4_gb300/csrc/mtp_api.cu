@@ -8,6 +8,7 @@
 
 #include "mtp.h"
 #include "mtp_launch.h"
+#include "mtp_c2.cuh"
 #include "mtp_cl.cuh"
 #include "mtp_tc.cuh"
 #include "mtp_ll.cuh"
@@ -37,6 +38,9 @@ struct mtp_handle {
   void* temb_ord;
   void* wpack;
   const __nv_bfloat16 *pk_q[MTP_MAX_LAYERS], *pk_gate[MTP_MAX_LAYERS], *pk_up[MTP_MAX_LAYERS], *pk_cent, *pk_post;
+  // streamed-tile cluster path (one sequence): availability and the packed weight streams
+  int c2_ok;
+  void* c2_stream;
   // tensor-core phase path (batches of 32..64): tensor maps (64-byte aligned host memory) and
   // the staging buffer of the input terms
   mtp::TcPlan* tc;
@@ -445,6 +449,105 @@ bool cl_supported(const mtp_handle* h) {
   return mtp::cl_capacity(smem) >= 1;
 }
 
+// Streamed-tile cluster-path parameters that depend only on the handle.
+mtp::c2::Params c2_template(const mtp_handle* h, int kv_max) {
+  const mtp_config& c = h->cfg;
+  mtp::c2::Params p;
+  memset(&p, 0, sizeof(p));
+  p.bb = c.backbone;
+  p.H = c.hidden;
+  p.nl = c.n_layers;
+  p.nh = c.n_head;
+  p.nkv = c.n_kv_head;
+  p.F = c.ffn;
+  p.V = c.vocab;
+  p.C = c.n_centroids;
+  p.topk = c.top_k;
+  p.vsc = c.use_ordered_embeddings && c.n_centroids > 0 ? c.vocab / c.n_centroids : 0;
+  p.W = c.window;
+  p.d[0] = c.head_dim_swa;
+  p.d[1] = c.head_dim_full;
+  for (int t = 0; t < 2; ++t) {
+    const int d = p.d[t] > 0 ? p.d[t] : 1;
+    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
+    p.dp[t] = mtp::c2_dim_parts(c.n_kv_head > 0 ? c.n_kv_head : 1, d);
+  }
+  p.theta[0] = c.rope_theta_swa;
+  p.theta[1] = c.rope_theta_full;
+  p.eps = c.rms_eps;
+  typedef const __nv_bfloat16* cb;
+  p.wstream = static_cast<cb>(h->c2_stream);
+  p.tgt = static_cast<cb>(h->target_embed);
+  p.temb_ord = static_cast<cb>(h->temb_ord);
+  p.out_norm = h->w.out_norm;
+  p.ord = h->w.token_ordering;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    p.ltype[l] = c.layer_type[l];
+    p.lambda[l] = L.layer_scalar;
+    p.q_norm[l] = L.q_norm;
+    p.attn_norm[l] = L.attn_norm;
+    p.post_attn_norm[l] = L.post_attn_norm;
+    p.ffn_norm[l] = L.ffn_norm;
+    p.post_ffn_norm[l] = L.post_ffn_norm;
+  }
+  for (int t = 0; t < 2; ++t) {
+    p.has_type[t] = has_type(c, t);
+    p.kv_max[t] = kv_max;
+    p.st[t] = static_cast<long long>(c.n_kv_head) * (t ? c.head_dim_full : c.head_dim_swa);
+  }
+  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  return p;
+}
+
+// Whether the streamed-tile cluster path can run this configuration on this device.
+bool c2_supported(const mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings) return false;
+  const mtp::c2::Params p = c2_template(h, c.max_ctx);
+  const int smem = mtp::c2_smem_bytes(p);
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (smem <= 0 || smem > optin) return false;
+  return mtp::c2_capacity(smem) >= 1;
+}
+
+// Packs every projection of the drafter into the per-CTA weight streams of the streamed-tile
+// cluster path (h->c2_stream).
+int build_c2_stream(mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  const mtp::c2::Params p = c2_template(h, c.max_ctx);
+  const void* mats[mtp::c2::kMaxSeq] = {};
+  mats[0] = h->w.pre_proj;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    mats[1 + 6 * l] = L.q;
+    mats[3 + 6 * l] = L.o;
+    mats[4 + 6 * l] = L.gate;
+    mats[5 + 6 * l] = L.up;
+    mats[6 + 6 * l] = L.down;
+  }
+  mats[1 + 6 * c.n_layers] = h->w.centroids;
+  mats[2 + 6 * c.n_layers] = h->w.post_proj;
+  const size_t bytes = static_cast<size_t>(mtp::c2_stream_total(p));
+  cudaError_t e = cudaMalloc(&h->c2_stream, bytes);
+  if (e != cudaSuccess) {
+    h->c2_stream = nullptr;
+    return cuda_fail("allocating the streamed weight tiles", e);
+  }
+  int rc = mtp::c2_pack_all(p, mats, h->c2_stream, 0);
+  e = rc ? cudaErrorUnknown : cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->c2_stream);
+    h->c2_stream = nullptr;
+    return rc ? rc : cuda_fail("packing the streamed weight tiles", e);
+  }
+  return MTP_OK;
+}
+
 // Carves the workspace out of one allocation (sizes for max_batch sequences).
 size_t layout_ws(mtp_handle* h, char* base) {
   const mtp_config& c = h->cfg;
@@ -636,7 +739,9 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
   h->ll_ok = ll_supported(h) ? 1 : 0;
   h->epoch = 64u;
   h->cl_ok = cl_supported(h) ? 1 : 0;
+  h->c2_ok = c2_supported(h) ? 1 : 0;
   h->temb_ord = nullptr;
+  h->c2_stream = nullptr;
   h->ws_bytes = layout_ws(h, nullptr);
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) {
@@ -657,8 +762,8 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     free(h);
     return cuda_fail("clearing the workspace", e);
   }
-  if (h->cl_ok) {
-    // the cluster path reads token_embd rows in token_ordering order (one contiguous block of
+  if (h->cl_ok || h->c2_ok) {
+    // the cluster paths read token_embd rows in token_ordering order (one contiguous block of
     // vocab / n_centroids rows per centroid): a copy made once here
     const size_t bytes = static_cast<size_t>(config->vocab) * config->hidden * 2;
     e = cudaMalloc(&h->temb_ord, bytes);
@@ -673,8 +778,10 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       free(h);
       return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
     }
-    rc = build_packed(h);
+    rc = h->cl_ok ? build_packed(h) : MTP_OK;
+    if (!rc && h->c2_ok) rc = build_c2_stream(h);
     if (rc) {
+      if (h->wpack) cudaFree(h->wpack);
       cudaFree(h->temb_ord);
       cudaFree(h->ws);
       free(h);
@@ -734,6 +841,45 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == MTP_DTYPE_BF16;
   int path = h->path;
+  if (path == 6 || (path == 0 && B == 1 && h->c2_ok)) {
+    if (!h->c2_ok || B != 1) {
+      set_error("the streamed cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->c2_ok);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    const int kvm = has_type(c, 1) ? kv_full->max_ctx : kv_sliding->max_ctx;
+    mtp::c2::Params cp = c2_template(h, kvm);
+    for (int t = 0; t < 2; ++t) {
+      if (!cp.has_type[t]) continue;
+      if (kvs[t]->v && kvs[t]->v != kvs[t]->k) {
+        set_error("the streamed cluster path reads V = K (attention_k_eq_v); pass v = NULL or v = k");
+        return MTP_ERR_UNSUPPORTED_SHAPE;
+      }
+      cp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
+      cp.ctx_len[t] = kvs[t]->ctx_len;
+      cp.st[t] = kvs[t]->stride_t;
+      cp.kv_max[t] = kvs[t]->max_ctx;
+      if ((reinterpret_cast<uintptr_t>(kvs[t]->k) & 15) != 0) {
+        set_error("the streamed cluster path needs 16-byte aligned K rows");
+        return MTP_ERR_UNSUPPORTED_SHAPE;
+      }
+    }
+    cp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
+    cp.tok_in = last_token;
+    cp.pos = pos;
+    cp.out_tokens = out_tokens;
+    cp.out_hidden = out_hidden;
+    cp.n_draft = n_draft;
+    cp.status = h->wsp.status;
+    cp.abort_flag = h->ll_abort;
+    const int smem = mtp::c2_smem_bytes(cp);
+    if (smem <= 0 || (reinterpret_cast<uintptr_t>(hidden) & 15) != 0) {
+      set_error("streamed cluster path: shape, K stride or hidden alignment not supported for this call");
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
+    return mtp::run_c2(cp, smem, st);
+  }
   if (path == 4 || (path == 0 && B == 1 && h->cl_ok)) {
     if (!h->cl_ok || B != 1) {
       set_error("the cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->cl_ok);
@@ -936,8 +1082,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 5) {
-    set_error("need a handle and path in {0, 1, 2, 3, 4, 5}");
+  if (!h || path < 0 || path > 6) {
+    set_error("need a handle and path in {0, 1, 2, 3, 4, 5, 6}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;
@@ -951,6 +1097,7 @@ void mtp_destroy(mtp_handle* h) {
   cudaFree(h->ws);
   if (h->temb_ord) cudaFree(h->temb_ord);
   if (h->wpack) cudaFree(h->wpack);
+  if (h->c2_stream) cudaFree(h->c2_stream);
   if (h->tc_mem) cudaFree(h->tc_mem);
   if (h->tc) free(h->tc);
   free(h);

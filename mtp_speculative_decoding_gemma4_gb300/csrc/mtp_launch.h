@@ -17,6 +17,9 @@ struct Params;
 namespace clk {
 struct Params;
 }
+namespace c2 {
+struct Params;
+}
 
 // Records the calling thread's last error text (printf-style).
 void set_error(const char* fmt, ...);
@@ -47,6 +50,17 @@ int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaS
 // Tensor-core tile packing of a [R][K] bf16 matrix for the cluster kernel (bytes, pack).
 long long packed_tile_bytes(int R, int K);
 int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);
+
+// Streamed-tile cluster draft block (one sequence, one 16-CTA cluster, weights packed into
+// per-CTA tile streams at init): dim parts of its score pass, shared-memory bytes (0: shape
+// not supported), resident clusters for that size, launch; the packed stream's size and the
+// packing of every projection (mats indexed like the step sequence, K entries unused).
+int c2_dim_parts(int nkv, int d);
+int c2_smem_bytes(const c2::Params& p);
+int c2_capacity(int smem);
+int run_c2(const c2::Params& p, int smem, cudaStream_t st);
+long long c2_stream_total(const c2::Params& p);
+int c2_pack_all(const c2::Params& p, const void* const* mats, void* dst, cudaStream_t st);
 
 // Tensor maps of the tensor-core phase path (host memory; see mtp_tc.cuh): every weight
 // matrix, and the staged input terms [3][bp][K] for each input width K.

@@ -15,8 +15,8 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR = 1, 2, 3, 4, 5
-ONE_SEQ = [LATENCY, CLUSTER]  # the two single-sequence paths
+PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR, STREAMED = 1, 2, 3, 4, 5, 6
+ONE_SEQ = [LATENCY, CLUSTER, STREAMED]  # the single-sequence paths
 
 
 def _drafter(index, batch=0, ctx=0, max_batch=0):
@@ -130,9 +130,10 @@ def test_paths_agree_bitwise_on_tokens():
 def test_one_sequence_paths_agree_on_tokens():
     dr, d = _drafter(1)
     a, ha = _run_block(dr, d, 8, LATENCY)
-    b, hb = _run_block(dr, d, 8, CLUSTER)
-    np.testing.assert_array_equal(a, b)
-    assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
+    for path in (CLUSTER, STREAMED):
+        b, hb = _run_block(dr, d, 8, path)
+        np.testing.assert_array_equal(a, b)
+        assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
     dr.close()
 
 

@@ -470,7 +470,6 @@ mtp::c2::Params c2_template(const mtp_handle* h, int kv_max) {
   for (int t = 0; t < 2; ++t) {
     const int d = p.d[t] > 0 ? p.d[t] : 1;
     p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
-    p.dp[t] = mtp::c2_dim_parts(c.n_kv_head > 0 ? c.n_kv_head : 1, d);
   }
   p.theta[0] = c.rope_theta_swa;
   p.theta[1] = c.rope_theta_full;

@@ -231,7 +231,7 @@ __device__ __forceinline__ void ring_release(const Ring& rg, int g) {
 // rows `xp` bytes apart; columns 3..7 are zero) into one accumulator, then writes its row
 // tile's sums (the three term columns added) to part[(w / RT) * RT * 16 + row]. The caller
 // adds the P parts after a barrier (sum_parts). Returns the slot counter after the section.
-__device__ __noinline__ int gemv2(Ring rg, int g, const SecE* se, unsigned xt, int xp, float* part) {
+__device__ __forceinline__ int gemv2(Ring rg, int g, const SecE* se, unsigned xt, int xp, float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   const int RT = se->w.RT, P = se->w.P, KT = se->w.KT, nsl = se->w.nsl;
   const bool act = warp < RT * P;
@@ -285,67 +285,105 @@ __device__ __forceinline__ uint32_t keep_keys(uint32_t v, int key, int n) {
 }
 
 // Attention of the nh query heads over this CTA's keys of one block, on tensor cores: K rows
-// sit in the slots at pitch se->pitch (nkv * d bf16 + 16 bytes); q is given as three bf16
-// terms per head (row 3h + t of qt, pitch (d + 8) elements). Column 4c + t of an MMA carries
-// term t of head c of the KV group (t < 3; the fourth column is zero). Per slot of n <= 32
-// keys:
-//   scores   S[key][col] = K q: tasks (group, 16-key tile, dim part) over the warps, partial
-//            sums per dim part to sp[part][key][head];
-//   softmax  warp h adds the parts, updates the running max / exp-sum of head h and writes
-//            p as three bf16 terms (row 3h + t of pt, pitch kKps + 8);
-//   sums     O^T[dim][col] += K^T P^T: warp tasks (group, 16-dim tile), rescaled by the
-//            running-max correction.
+// sit in the slots at pitch nkv * d bf16 + 16 bytes (kKps rows per slot); q is given as three
+// bf16 terms per head (row 3h + t of qt, pitch (d + 8) elements). Column 4c + t of an MMA
+// carries term t of head c of the KV group (t < 3; the fourth column is zero). The keys go in
+// chunks of up to kSlots slots (16-key tile kt of a chunk is rows (kt % 2) * 16.. of its slot
+// kt / 2); per chunk of n keys:
+//   scores   S[key][col] = K q: tasks (group, key tile, dim part) over the warps, partial sums
+//            per dim part to sp[part][key][head];
+//   softmax  warp h adds the parts, updates the running max / exp-sum of head h over the
+//            chunk and writes p as three bf16 terms (row 3h + t of pt, pitch kSlots kKps + 8);
+//   sums     O^T[dim][col] += K^T P^T: warp tasks (group, 16-dim tile) over every key tile of
+//            the chunk, rescaled once by the running-max correction; a slot is released as
+//            soon as the warp has passed its key tiles.
 // At the end, every unnormalised sum o[h][dim] goes to its owner (CTA (h d + dim) / dpo) at
 // float offset r (2 + dpo) + 2 + (h d + dim) % dpo of the receive buffer xdst, and (m_h, l_h)
 // to float offset r (2 + dpo) of every owner of head h's dims. Returns the slot counter.
-__device__ __noinline__ int att2(Ring rg, int g, const SecE* se, int nh, int nkv, int d, int dpn, float scale,
+// D_, NH_, NKV_ > 0 fix head_dim, heads and KV heads at compile time (0: the runtime values).
+template <int D_, int NH_, int NKV_>
+__device__ __forceinline__ int att3(Ring rg, int g, const SecE* se, int nh_rt, int nkv_rt, int d_rt, float scale,
                                  unsigned qt, float* sp, bf16* pt, float* red, unsigned xdst, unsigned xbar, int dpo,
                                  int r, bool live) {
+  constexpr int CH = kSlots * kKps;  // keys per chunk
+  const int d = D_ > 0 ? D_ : d_rt, nh = NH_ > 0 ? NH_ : nh_rt, nkv = NKV_ > 0 ? NKV_ : nkv_rt;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gi = lane >> 2, ti = lane & 3;
-  const int hpg = nh / nkv, NT = (hpg + 1) / 2, KS = d / 16, MT = d / 16, QP = d + 8, PP = kKps + 8;
-  const int P = se->pitch, nkeys = se->nkeys;
+  const int hpg = nh / nkv, NT = (hpg + 1) / 2, KS = d / 16, MT = d / 16, QP = d + 8;
+  constexpr int PP = CH + 8;
+  const int P = nkv * d * 2 + 16, nkeys = se->nkeys;
   const unsigned pts = sa(pt);
-  float acc[kAttMT][2][4];
-#pragma unroll
-  for (int m = 0; m < kAttMT; ++m)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
-  if (tid < nh) {
-    red[tid] = -INFINITY;
-    red[16 + tid] = 0.f;
-  }
-  // this lane's B row in the head-term layout for n tile nt of group grp (-1: a zero column)
+  // per-lane constants: ldmatrix row offsets (scores: rows + k halves; sums: transposed), the
+  // B rows of the two n tiles of every group
+  const unsigned arow_s = static_cast<unsigned>(((lane & 7) + ((lane >> 3) & 1) * 8) * P + (lane >> 4) * 16);
+  const unsigned arow_w = static_cast<unsigned>(((lane & 7) + (lane >> 4) * 8) * P + ((lane >> 3) & 1) * 16);
   auto brow = [&](int grp, int nt) -> int {
     const int c = nt * 8 + gi, hh = c >> 2, t = c & 3;
     return (t == 3 || hh >= hpg) ? -1 : 3 * (grp * hpg + hh) + t;
   };
+  // weighted-sum tasks of this warp: A offset (group, dim tile) and B offsets per n tile
+  unsigned woff[kAttMT];
+  int wb[kAttMT][2];
+  bool wact[kAttMT];
+  float acc[kAttMT][2][4];
+#pragma unroll
+  for (int m = 0; m < kAttMT; ++m) {
+    const int task = warp + m * kCW;
+    wact[m] = task < nkv * MT;
+    const int grp = wact[m] ? task / MT : 0, mt = wact[m] ? task % MT : 0;
+    woff[m] = arow_w + static_cast<unsigned>(grp * d * 2 + mt * 32);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int rw = nt < NT ? brow(grp, nt) : -1;
+      wb[m][nt] = rw >= 0 ? 2 * (rw * PP + 2 * ti) : -1;
+      acc[m][nt][0] = acc[m][nt][1] = acc[m][nt][2] = acc[m][nt][3] = 0.f;
+    }
+  }
+  if (tid < nh) {
+    red[tid] = -INFINITY;
+    red[16 + tid] = 0.f;
+  }
   const int nslot = (nkeys + kKps - 1) / kKps;
-  for (int c = 0; c < nslot; ++c, ++g) {
-    const unsigned K = ring_wait(rg, g);
-    const int n = min(kKps, nkeys - c * kKps), nkt = (n + 15) / 16;
-    // ---- scores
-    if (warp < nkv * nkt * dpn) {
-      const int dpart = warp % dpn, kt = (warp / dpn) % nkt, grp = warp / (dpn * nkt);
-      const int ks0 = dpart * (KS / dpn), ks1 = ks0 + KS / dpn;
+  for (int c0 = 0; c0 < nslot; c0 += kSlots) {
+    const int ns = min(kSlots, nslot - c0);
+    const int n = min(CH, nkeys - c0 * kKps), nkt = (n + 15) / 16, KT16 = nkt * 16;
+    for (int j = 0; j < ns; ++j) ring_wait(rg, g + j);
+    // slot addresses of the chunk (slot gg of the ring at rg.base + (gg % kSlots) * stride)
+    unsigned sbase[kSlots];
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) sbase[j] = rg.base + static_cast<unsigned>(((g + j) % kSlots) * kSlotStride);
+    // ---- scores: dim parts DP (log2 ldp), the largest power of two with nkv nkt DP <= kCW
+    // dividing d / 16
+    int ldp = 0;
+    while (nkv * nkt * (2 << ldp) <= kCW && KS % (2 << ldp) == 0) ++ldp;
+    const int DP = 1 << ldp;
+    if (warp < nkv * nkt * DP) {
+      const int dpart = warp & (DP - 1), kq = warp >> ldp, kt = kq % nkt, grp = kq / nkt;
+      const int nks = KS >> ldp, ks0 = dpart * nks;
       float sv[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) sv[nt][0] = sv[nt][1] = sv[nt][2] = sv[nt][3] = 0.f;
-      const unsigned arow = K + static_cast<unsigned>((kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * P + grp * d * 2 +
-                                                      (lane >> 4) * 16);
-      int rw[2];
+      unsigned sb = sbase[0];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) rw[nt] = nt < NT ? brow(grp, nt) : -1;
-      for (int ks = ks0; ks < ks1; ++ks) {
-        const uint4 a = ldsm_x4(arow + ks * 32);
+      for (int j = 1; j < kSlots; ++j)
+        if ((kt >> 1) == j) sb = sbase[j];
+      unsigned a_addr = sb + static_cast<unsigned>((kt & 1) * 16 * P + grp * d * 2 + ks0 * 32) + arow_s;
+      unsigned b_addr[2];
+      bool bon[2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int rw = nt < NT ? brow(grp, nt) : -1;
+        bon[nt] = rw >= 0;
+        b_addr[nt] = qt + 2u * static_cast<unsigned>((bon[nt] ? rw : 0) * QP + ks0 * 16 + 2 * ti);
+      }
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint4 a = ldsm_x4(a_addr);
+        a_addr += 32;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           if (nt < NT) {
-            uint32_t b0 = 0u, b1 = 0u;
-            if (rw[nt] >= 0) {
-              const unsigned bq = qt + 2u * static_cast<unsigned>(rw[nt] * QP + ks * 16 + 2 * ti);
-              b0 = lds32(bq);
-              b1 = lds32(bq + 16);
-            }
+            const uint32_t b0 = bon[nt] ? lds32(b_addr[nt]) : 0u;
+            const uint32_t b1 = bon[nt] ? lds32(b_addr[nt] + 16) : 0u;
+            b_addr[nt] += 32;
             mma_bf16(sv[nt], a, b0, b1);
           }
         }
@@ -359,27 +397,42 @@ __device__ __noinline__ int att2(Ring rg, int g, const SecE* se, int nh, int nkv
           const int hh = (nt * 8 + 2 * ti) >> 2;
           if ((ti & 1) == 0 && hh < hpg) {
             const int h = grp * hpg + hh;
-            sp[(dpart * kKps + kt * 16 + gi) * nh + h] = v0;
-            sp[(dpart * kKps + kt * 16 + gi + 8) * nh + h] = v1;
+            float* spp = sp + (dpart * KT16 + kt * 16 + gi) * nh + h;
+            spp[0] = v0;
+            spp[8 * nh] = v1;
           }
         }
       }
     }
     cbar();
-    // ---- running max / exp-sum of head `warp`; p as three bf16 terms
+    // ---- running max / exp-sum of head `warp` over the chunk; p as three bf16 terms
     if (warp < nh) {
-      const int h = warp, j = lane;
-      float v = -INFINITY;
-      if (j < n) {
-        v = 0.f;
-        for (int dpart = 0; dpart < dpn; ++dpart) v += sp[(dpart * kKps + j) * nh + h];
-        v *= scale;
+      const int h = warp;
+      float v[CH / 32];
+      float cm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < CH / 32; ++u) {
+        const int j = lane + 32 * u;
+        v[u] = -INFINITY;
+        if (j < n) {
+          const float* spp = sp + j * nh + h;
+          float s2 = 0.f;
+          for (int dp = 0; dp < DP; ++dp) s2 += spp[dp * KT16 * nh];
+          v[u] = s2 * scale;
+        }
+        cm = fmaxf(cm, v[u]);
       }
       const float mold = red[h];
-      const float mnew = fmaxf(mold, warp_max(v));
-      const float e = j < n ? expf(v - mnew) : 0.f;
-      const float ls = warp_sum(e);
-      if (j < nkt * 16) put3(pt + 3 * h * PP + j, PP, e);
+      const float mnew = fmaxf(mold, warp_max(cm));
+      float ls = 0.f;
+#pragma unroll
+      for (int u = 0; u < CH / 32; ++u) {
+        const int j = lane + 32 * u;
+        const float e = j < n ? expf(v[u] - mnew) : 0.f;
+        ls += e;
+        if (j < KT16) put3(pt + 3 * h * PP + j, PP, e);
+      }
+      ls = warp_sum(ls);
       if (lane == 0) {
         const float corr = expf(mold - mnew);
         red[32 + h] = corr;
@@ -388,52 +441,75 @@ __device__ __noinline__ int att2(Ring rg, int g, const SecE* se, int nh, int nkv
       }
     }
     cbar();
-    // ---- weighted sums of this warp's dim tiles
+    // ---- weighted sums of this warp's dim tiles over the chunk's key tiles
+    {
+      float dg[kAttMT][2][4];
 #pragma unroll
-    for (int m = 0; m < kAttMT; ++m) {
-      const int task = warp + m * kCW;
-      if (task < nkv * MT) {
-        const int grp = task / MT, mt = task % MT;
-        float dg[2][4];
+      for (int m = 0; m < kAttMT; ++m)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) dg[nt][0] = dg[nt][1] = dg[nt][2] = dg[nt][3] = 0.f;
-        int rw[2];
+        for (int nt = 0; nt < 2; ++nt) dg[m][nt][0] = dg[m][nt][1] = dg[m][nt][2] = dg[m][nt][3] = 0.f;
+      for (int kk = 0; kk < nkt; ++kk) {
+        const int j0 = kk * 16;
+        unsigned kb = sbase[0];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) rw[nt] = nt < NT ? brow(grp, nt) : -1;
-        for (int kk = 0; kk < nkt; ++kk) {
-          const int j0 = kk * 16;
-          const unsigned arow = K + static_cast<unsigned>((j0 + (lane & 7) + (lane >> 4) * 8) * P + grp * d * 2 +
-                                                          ((lane >> 3) & 1) * 16);
-          uint4 a = ldsm_x4_t(arow + mt * 32);
-          if (j0 + 16 > n) {  // keys past the slot's rows: zero (their rows hold no K)
-            a.x = keep_keys(a.x, j0 + 2 * ti, n);
-            a.y = keep_keys(a.y, j0 + 2 * ti, n);
-            a.z = keep_keys(a.z, j0 + 8 + 2 * ti, n);
-            a.w = keep_keys(a.w, j0 + 8 + 2 * ti, n);
-          }
+        for (int j = 1; j < kSlots; ++j)
+          if ((kk >> 1) == j) kb = sbase[j];
+        kb += static_cast<unsigned>((kk & 1) * 16 * P);
+        const bool tail = j0 + 16 > n;
+        uint32_t b0[2], b1[2];
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            if (nt < NT) {
-              uint32_t b0 = 0u, b1 = 0u;
-              if (rw[nt] >= 0) {
-                const unsigned bp = pts + 2u * static_cast<unsigned>(rw[nt] * PP + j0 + 2 * ti);
-                b0 = lds32(bp);
-                b1 = lds32(bp + 16);
-              }
-              mma_bf16(dg[nt], a, b0, b1);
-            }
+        for (int nt = 0; nt < 2; ++nt) {
+          b0[nt] = b1[nt] = 0u;
+          if (nt < NT && wb[0][nt] >= 0) {
+            const unsigned bp = pts + static_cast<unsigned>(wb[0][nt] + 2 * j0);
+            b0[nt] = lds32(bp);
+            b1[nt] = lds32(bp + 16);
           }
         }
+#pragma unroll
+        for (int m = 0; m < kAttMT; ++m) {
+          if (wact[m]) {
+            uint4 a = ldsm_x4_t(kb + woff[m]);
+            if (tail) {  // keys past the chunk's rows: zero (their rows hold no K)
+              a.x = keep_keys(a.x, j0 + 2 * ti, n);
+              a.y = keep_keys(a.y, j0 + 2 * ti, n);
+              a.z = keep_keys(a.z, j0 + 8 + 2 * ti, n);
+              a.w = keep_keys(a.w, j0 + 8 + 2 * ti, n);
+            }
+            uint32_t c0 = b0[0], c1 = b1[0], e0 = b0[1], e1 = b1[1];
+            if (m > 0 && (wb[m][0] != wb[0][0] || wb[m][1] != wb[0][1])) {  // another group's heads
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                uint32_t x0 = 0u, x1 = 0u;
+                if (nt < NT && wb[m][nt] >= 0) {
+                  const unsigned bp = pts + static_cast<unsigned>(wb[m][nt] + 2 * j0);
+                  x0 = lds32(bp);
+                  x1 = lds32(bp + 16);
+                }
+                if (nt == 0) { c0 = x0; c1 = x1; } else { e0 = x0; e1 = x1; }
+              }
+            }
+            mma_bf16(dg[m][0], a, c0, c1);
+            if (NT > 1) mma_bf16(dg[m][1], a, e0, e1);
+          }
+        }
+        // this warp is done with slot kk / 2 once it has passed both of its key tiles
+        if ((kk & 1) == 1 || kk == nkt - 1) ring_release(rg, g + (kk >> 1));
+      }
+#pragma unroll
+      for (int m = 0; m < kAttMT; ++m) {
+        const int task = warp + m * kCW;
+        const int grp = wact[m] ? task / MT : 0;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int hh = (nt * 8 + 2 * ti) >> 2;
           const float cr = (nt < NT && hh < hpg) ? red[32 + grp * hpg + hh] : 0.f;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[m][nt][i] = fmaf(acc[m][nt][i], cr, dg[nt][i]);
+          for (int i = 0; i < 4; ++i) acc[m][nt][i] = fmaf(acc[m][nt][i], cr, dg[m][nt][i]);
         }
       }
     }
-    ring_release(rg, g);
+    g += ns;
   }
   // ---- partial sums and (m, l) to the owners of the dims
   if (live) {
@@ -441,7 +517,7 @@ __device__ __noinline__ int att2(Ring rg, int g, const SecE* se, int nh, int nkv
 #pragma unroll
     for (int m = 0; m < kAttMT; ++m) {
       const int task = warp + m * kCW;
-      if (task < nkv * MT) {
+      if (wact[m]) {
         const int grp = task / MT, mt = task % MT;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -827,8 +903,15 @@ __global__ void __launch_bounds__(kT, 1) k_block_c2(const __grid_constant__ Para
         }
         // ---- attention over this CTA's keys; partial sums to the owners of the dims
         arm(xe, kNC * (2 + dpo) * 4);
-        g = att2(rg, g, tab + 2 + 6 * l, p.nh, p.nkv, d, p.dp[lt], p.scale[lt], Us, sp, pt, red, xset(xe), xbar(xe),
-                 dpo, r, live);
+        {
+          const SecE* sk = tab + 2 + 6 * l;
+          if (p.nh == 4 && p.nkv == 1 && d == 512)
+            g = att3<512, 4, 1>(rg, g, sk, 4, 1, 512, p.scale[lt], Us, sp, pt, red, xset(xe), xbar(xe), dpo, r, live);
+          else if (p.nh == 4 && p.nkv == 1 && d == 256)
+            g = att3<256, 4, 1>(rg, g, sk, 4, 1, 256, p.scale[lt], Us, sp, pt, red, xset(xe), xbar(xe), dpo, r, live);
+          else
+            g = att3<0, 0, 0>(rg, g, sk, p.nh, p.nkv, d, p.scale[lt], Us, sp, pt, red, xset(xe), xbar(xe), dpo, r, live);
+        }
         xwait(xe);
         const float* pb = xsf(xe++);
         // ---- combine this CTA's dims (one head): weight of source s is
@@ -991,12 +1074,19 @@ __global__ void __launch_bounds__(kT, 1) k_block_c2(const __grid_constant__ Para
 
 // ------------------------------------------------------------------ packing
 
-// Packs CTA r's section of W [R][K] (bf16, row-major) into its stream: tile (slot s, warp w,
-// j) in the order of WSec, each tile as 32 lanes x 16 bytes in mma.m16n8k16 A-fragment order
-// (lane g = lane / 4, t = lane % 4 holds rows g and g + 8 at columns 2t, 2t + 1 and 2t + 8,
-// 2t + 9); rows past the CTA's share are zero.
-__global__ void k_c2_pack(const bf16* __restrict__ W, int R, int K, int r, uint4* __restrict__ dst) {
+// Packs every CTA's section of W [R][K] (bf16, row-major) into its stream (CTA r =
+// blockIdx.y, at byte offset off.b[r] of dst): tile (slot s, warp w, j < 4) in the order of
+// WSec, each tile as 32 lanes x 16 bytes in mma.m16n8k16 A-fragment order (lane g = lane / 4,
+// t = lane % 4 holds rows g and g + 8 at columns 2t, 2t + 1 and 2t + 8, 2t + 9); rows past the
+// CTA's share are zero.
+struct PackOffsets {
+  long long b[kNC];
+};
+__global__ void k_c2_pack(const bf16* __restrict__ W, int R, int K, const __grid_constant__ PackOffsets off,
+                          char* __restrict__ dst_base) {
+  const int r = blockIdx.y;
   const WSec s = wsec(R, K, r);
+  uint4* dst = reinterpret_cast<uint4*>(dst_base + off.b[r]);
   const int A = s.RT * s.P;
   const long long total = static_cast<long long>(s.RT) * s.KT * 32;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -1044,14 +1134,6 @@ cudaLaunchConfig_t c2_cfg(int smem, cudaStream_t st, cudaLaunchAttribute* at) {
   return cfg;
 }
 }  // namespace
-
-// Dim parts of the score pass for head_dim d: the largest power of two with nkv x 2 key tiles
-// x parts <= kCW compute warps that divides d / 16.
-int c2_dim_parts(int nkv, int d) {
-  int dp = 1;
-  while (nkv * 2 * (2 * dp) <= c2::kCW && (d / 16) % (2 * dp) == 0) dp *= 2;
-  return dp;
-}
 
 int c2_smem_bytes(const c2::Params& p) {
   using namespace c2;
@@ -1121,19 +1203,21 @@ long long c2_stream_total(const c2::Params& p) {
   return b;
 }
 
-// Packs every weight section of every CTA into the stream buffer (layout of stream_bytes).
+// Packs every weight section of every CTA into the stream buffer (layout of stream_bytes):
+// one launch per section, all CTAs at once.
 int c2_pack_all(const c2::Params& p, const void* const* mats, void* dst, cudaStream_t st) {
   using namespace c2;
-  char* out = static_cast<char*>(dst);
-  for (int r = 0; r < kNC; ++r) {
-    for (int i = 0; i < seq_count(p); ++i) {
-      if (seq_is_k(p, i)) continue;
-      int R, K;
-      seq_shape(p, i, R, K);
-      const WSec s = wsec(R, K, r);
-      k_c2_pack<<<64, 256, 0, st>>>(static_cast<const bf16*>(mats[i]), R, K, r, reinterpret_cast<uint4*>(out));
-      out += wsec_bytes(s);
-    }
+  long long base[kNC];
+  base[0] = 0;
+  for (int r = 1; r < kNC; ++r) base[r] = base[r - 1] + stream_bytes(p, r - 1);
+  PackOffsets off;
+  for (int i = 0; i < seq_count(p); ++i) {
+    if (seq_is_k(p, i)) continue;
+    int R, K;
+    seq_shape(p, i, R, K);
+    for (int r = 0; r < kNC; ++r) off.b[r] = base[r];
+    k_c2_pack<<<dim3(32, kNC), 256, 0, st>>>(static_cast<const bf16*>(mats[i]), R, K, off, static_cast<char*>(dst));
+    for (int r = 0; r < kNC; ++r) base[r] += wsec_bytes(wsec(R, K, r));
   }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -20,7 +20,7 @@
 //   PRE   u = [h ; embed(token)] (terms); x0 rows = W_pre u              -> all-gather x0
 //   per block l:
 //     a = attn_norm(x); Q rows                                           -> all-gather q
-//     q_norm + RoPE; attention over this CTA's keys (online softmax over the K slots)
+//     q_norm + RoPE; attention over this CTA's keys (online softmax over chunks of K slots)
 //                                                 -> partial sums to the owner of each dim
 //     owners combine the kNC partials                                    -> all-gather o
 //     O rows                                                             -> all-gather o'
@@ -96,7 +96,6 @@ __host__ __device__ inline long long wsec_bytes(const WSec& s) {
 struct Params {
   int bb, H, nl, nh, nkv, F, V, C, topk, vsc, W;
   int d[2];
-  int dp[2];  // dim parts of the score pass per attention type
   float scale[2], theta[2], eps;
   int ltype[kMaxL];
   float lambda[kMaxL];
@@ -197,9 +196,9 @@ __host__ __device__ inline Layout make_layout(const Params& p) {
   L.x = off;     off += al16(p.H * 4);
   L.y = off;     off += al16(p.H * 4);
   L.part = off;  off += 2 * kCW * 16 * 4;
-  int dpm = imax(p.dp[0], p.dp[1]);
-  L.sp = off;    off += al16(imax(dpm * kKps * p.nh * 4, 2 * (kNC / 2) * p.topk * 8));
-  L.pt = off;    off += al16(3 * p.nh * (kKps + 8) * 2);
+  // score partials: (dim part, key) pairs <= kCW key tiles of 16 keys; the merge's two lists
+  L.sp = off;    off += al16(imax(kCW * 16 * p.nh * 4, 2 * (kNC / 2) * p.topk * 8));
+  L.pt = off;    off += al16(3 * p.nh * (kSlots * kKps + 8) * 2);
   L.red = off;   off += 128 * 4;
   const int h0 = p.has_type[0] ? p.d[0] / 2 : 0, h1 = p.has_type[1] ? p.d[1] / 2 : 0;
   L.cs_off1 = h0;

@@ -52,10 +52,9 @@ long long packed_tile_bytes(int R, int K);
 int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);
 
 // Streamed-tile cluster draft block (one sequence, one 16-CTA cluster, weights packed into
-// per-CTA tile streams at init): dim parts of its score pass, shared-memory bytes (0: shape
+// per-CTA tile streams at init): shared-memory bytes (0: shape
 // not supported), resident clusters for that size, launch; the packed stream's size and the
 // packing of every projection (mats indexed like the step sequence, K entries unused).
-int c2_dim_parts(int nkv, int d);
 int c2_smem_bytes(const c2::Params& p);
 int c2_capacity(int smem);
 int run_c2(const c2::Params& p, int smem, cudaStream_t st);

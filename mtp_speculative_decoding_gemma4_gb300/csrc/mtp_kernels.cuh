@@ -323,7 +323,7 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   auto groups = [&](int) { return s.B; };  // staging runs one sequence per CTA
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
                   long long ld2, unsigned long long* best) -> int {
-    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, p.w.status, p.spin_limit};
+    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit};
     return tc_gemm(&w, &x, a, best != nullptr, st);
   };
   int rc;

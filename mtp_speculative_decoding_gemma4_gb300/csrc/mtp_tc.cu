@@ -109,12 +109,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) char sm_raw[];
   const unsigned raw = sa(sm_raw);
   const unsigned base = (raw + 1023u) & ~1023u;  // the swizzle layout needs 1024-byte alignment
-  const int B = NB * 32, N = 3 * B, SB = stage_bytes(B), KT = a.K / kKStage, ncols = tmem_cols(B);
+  const int B = NB * 32, N = 3 * B, SB = stage_bytes(B), ncols = tmem_cols(B);
+  // this CTA's share of K (split over the S CTAs of a cluster): stages [kt_lo, kt_lo + KT)
+  const int S = DENSE ? 1 : (a.splits > 1 ? a.splits : 1);
+  const int sp = static_cast<int>(blockIdx.x) % S, KTall = a.K / kKStage;
+  const int kt_lo = KTall * sp / S, KT = KTall * (sp + 1) / S - kt_lo;
   const int NG = (KT + kGroup - 1) / kGroup;  // k groups
   const unsigned full0 = base + kStages * SB, empty0 = full0 + 8 * kStages;
   const unsigned gdone0 = empty0 + 8 * kStages, gfree0 = gdone0 + 16;  // per accumulator region
   const unsigned tslot = gfree0 + 16;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tile = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tile = static_cast<int>(blockIdx.x) / S;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -147,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const unsigned st = base + s * SB;
         mbar_expect_tx(full0 + 8 * s, static_cast<unsigned>(SB));
-        tma_load_2d(st, &mapW, kt * kKStage, tile * kM, full0 + 8 * s);
-        tma_load_2d(st + kM * kKStage * 2, &mapX, kt * kKStage, 0, full0 + 8 * s);
+        tma_load_2d(st, &mapW, (kt_lo + kt) * kKStage, tile * kM, full0 + 8 * s);
+        tma_load_2d(st + kM * kKStage * 2, &mapX, (kt_lo + kt) * kKStage, 0, full0 + 8 * s);
         ++issued;
       }
       // no copy may still be in flight when the CTA ends
@@ -207,6 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gfree0 + 8 * region) : "memory");
   }
+  if (!DENSE && S > 1) {
+    // this row's partial sums into this CTA's stage memory (pitch B + 1 floats: conflict-free)
+    float* pbuf = reinterpret_cast<float*>(sm_raw + (base - raw));
+    const int row = 32 * warp + lane;
+#pragma unroll
+    for (int q = 0; q < NB; ++q)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pbuf[row * (B + 1) + 32 * q + j] = acc[q][j];
+  }
+  if (DENSE || S == 1) {
 #pragma unroll
   for (int q = 0; q < NB; ++q) {
     const int b0 = 32 * q;
@@ -239,7 +253,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b0 + lane < a.nvalid) atomicMax(a.best + b0 + lane, k[0]);
     }
   }
+  }
   }  // epilogue warps
+  if (!DENSE && S > 1) {
+    // every CTA of the cluster has its partials in place (the stage memory is idle: every MMA
+    // has completed and every copy has landed); CTA sp adds the S partials of its rows in
+    // order 0..S-1 and stores them; a second barrier keeps the partials alive until then
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (tid < kEpiWarps * 32) {
+      const unsigned pb = base;
+      const int r_lo = kM * sp / S, r_hi = kM * (sp + 1) / S, nrow = r_hi - r_lo;
+      for (int e = tid; e < nrow * a.nvalid; e += kEpiWarps * 32) {
+        const int rr = r_lo + e / a.nvalid, b = e % a.nvalid;
+        const unsigned off = pb + 4u * static_cast<unsigned>(rr * (B + 1) + b);
+        float v = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+          unsigned ra;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(off), "r"(s2));
+          float x;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(ra) : "memory");
+          v += x;
+        }
+        const int r = tile * kM + rr;
+        if (r < a.R) {
+          if (a.out) a.out[static_cast<size_t>(b) * a.ldo + r] = v;
+          if (a.out2) a.out2[static_cast<size_t>(b) * a.ld2 + r] = v;
+        }
+      }
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  }
   fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -307,11 +350,34 @@ int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a,
   const int smem = tc::smem_bytes(a.B);
   auto kern = a.B == 32 ? (dense ? tc::k_tc_gemm<true, 1> : tc::k_tc_gemm<false, 1>)
                         : (dense ? tc::k_tc_gemm<true, 2> : tc::k_tc_gemm<false, 2>);
+  const int tiles = (a.R + tc::kM - 1) / tc::kM, KT = a.K / tc::kKStage;
+  tc::Args aa = a;
+  if (dense) {
+    aa.splits = 1;
+  } else if (aa.splits <= 0) {  // about one wave of CTAs, at least one k stage each, clusters of <= 8
+    int S = 1;
+    while (2 * S <= 8 && 2 * S <= KT && tiles * 2 * S <= 128) S *= 2;
+    aa.splits = S;
+  }
+  if (aa.splits > 8 || aa.splits > KT || (aa.splits > 1 && (a.B + 1) * tc::kM * 4 > tc::kStages * tc::stage_bytes(a.B))) {
+    set_error("tensor-core GEMM: unsupported split %d of K=%d", aa.splits, a.K);
+    return MTP_ERR_UNSUPPORTED_SHAPE;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) {
-    const int grid = (a.R + tc::kM - 1) / tc::kM;
-    kern<<<grid, tc::kThreads, smem, st>>>(*mapW, *mapX, a);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * aa.splits);
+    cfg.blockDim = dim3(tc::kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = aa.splits;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, *mapW, *mapX, aa);
   }
   if (e != cudaSuccess) {
     set_error("tensor-core GEMM launch: %s", cudaGetErrorString(e));

@@ -16,6 +16,11 @@
 //     term columns per sequence and sum the groups in fp32 registers (round to nearest);
 //   * at the end the warps either store Y or, for the dense tied head, keep the largest
 //     (logit, row) key of every sequence (atomicMax).
+// Split K: with splits S > 1 (projections only) the S CTAs of a row tile form a thread-block
+// cluster and take consecutive S-th parts of K; each writes its fp32 partial sums into its
+// own (then idle) stage memory, and after a cluster barrier CTA s adds the S partials of rows
+// [s 128 / S, (s + 1) 128 / S) in a fixed order through distributed shared memory, so the
+// result does not depend on timing.
 #pragma once
 
 #include <cuda.h>
@@ -41,6 +46,7 @@ struct Args {
   float* out2;                   // second copy Y[b * ld2 + r] (may be null)
   long long ld2;
   unsigned long long* best;      // dense head: atomicMax of argmax keys per sequence (or null)
+  int splits;                    // K split over this many CTAs of one cluster (1: no split)
   int* status;
   long long spin_limit;
 };
@@ -60,7 +66,8 @@ __host__ __device__ inline int tmem_cols(int B) {
 // A 2D bf16 tensor map over rows x cols (row pitch `pitch` elements) with a box of
 // box_rows x 64 columns and 128-byte swizzle. Returns MTP_OK or an error code.
 int tc_make_map(CUtensorMap* map, const void* base, long long rows, long long cols, long long pitch, int box_rows);
-// Y = W Xs^T as described above. `dense` selects the argmax epilogue.
+// Y = W Xs^T as described above. `dense` selects the argmax epilogue. a.splits <= 0 picks the
+// split of K automatically (projections); the dense head never splits.
 int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a, bool dense, cudaStream_t st);
 // Whether tcgen05 GEMMs can run on the current device (sm_100 family, driver entry point).
 bool tc_available();

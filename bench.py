@@ -261,6 +261,24 @@ def run_mtp(args, rank: int, world: int, dist):
     draft_ms_mean = sum(draft_ms) / K
     assert dr.status() == 0
 
+    # sampled verification (temperature 1, seeded uniforms) of the same drafts and logits
+    from mtp_speculative_decoding_gemma4_gb300 import verify_sample
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(wl.seed)
+    u_acc = torch.rand((B, n), device="cuda", generator=gen)
+    u_smp = torch.rand((B, n + 1), device="cuda", generator=gen)
+    acc_s = torch.empty(B, dtype=torch.int32, device="cuda")
+    out_s = torch.empty((B, n + 1), dtype=torch.int32, device="cuda")
+    vs_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        vs_ev[i][0].record(stream)
+        verify_sample(logits, out_tok, 1.0, u_acc, u_smp, accept_len=acc_s, out_tokens=out_s, stream=sh)
+        vs_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    vs_ms = sum(e[0].elapsed_time(e[1]) for e in vs_ev) / K
+    vs_rows = int(torch.clamp(acc_s + 1, max=n + 1).sum().item())
+
     # warm-L2 reference figure: back-to-back steps, no flush
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -340,6 +358,10 @@ def run_mtp(args, rank: int, world: int, dist):
         "clocks": clk.summary(),
         "warm_l2": {"ms_per_step": warm_ms, "value": tokens / (warm_ms * 1e-3)},
         "accept_len_mean": float(acc.float().mean().item()),
+        "verify_sample": {"temperature": 1.0, "us": vs_ms * 1e3, "rows_read": vs_rows,
+                          "accept_len_mean": float(acc_s.float().mean().item()),
+                          "achieved_gbs": vs_rows * shape.vocab * 2 / (vs_ms * 1e-3) / 1e9,
+                          "kernel": "k_verify_sample (one CTA per sequence)"},
     }
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, shape, wl, w, inp, base, seconds=args.cpu_seconds)

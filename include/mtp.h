@@ -207,6 +207,32 @@ MTP_API int mtp_set_logit_mask(mtp_handle *h, int32_t mode);
 MTP_API int mtp_verify_greedy(const void *target_logits, const int32_t *draft, int32_t B, int32_t n,
                       int32_t V, int32_t *accept_len, int32_t *out_tokens, void *stream);
 
+/* Sampled verification at temperature T (the pages give the accept-until-disagreement
+ * structure, "Gemma 4 drafter explained", "What is Speculative Decoding?", and note that the
+ * accept rate varies with temperature, "Gemma 4 Multi-Token Prediction (MTP) drafter",
+ * "Status"; they give no stochastic rule). Speculative sampling with the drafter's proposal
+ * a point mass on each drafted token: p_i = softmax(target row i / T); draft i is accepted
+ * while u_accept[b][i] < p_i(draft[b][i]); at the first rejection the emitted token is the
+ * inverse-CDF sample, over increasing ids, of p_i without the drafted token (renormalised)
+ * at u_sample[b][i]; when all n drafts are accepted the extra token is the sample of p_n at
+ * u_sample[b][n]. The emitted tokens are distributed as sampling from the target at T.
+ * T = 0 is mtp_verify_greedy (the uniforms are not read). Decisions are taken in fp32; a
+ * uniform within about 1e-6 (relative) of a decision boundary may fall either way.
+ *   target_logits device [B][n+1][V] bf16
+ *   draft         device [B][n] int32
+ *   temperature   host float, finite, >= 0
+ *   u_accept      device [B][n] fp32 uniforms in [0, 1) (may be NULL when n == 0)
+ *   u_sample      device [B][n+1] fp32 uniforms in [0, 1)
+ *   accept_len    device [B] int32
+ *   out_tokens    device [B][n+1] int32 (-1 padded after the emitted token)
+ * Rows after the first rejection are not read. Asynchronous on `stream`; caller-owned
+ * buffers. Errors: INVALID_ARG (NULL, B < 1, n < 0, V < 1, V % 8 != 0, T < 0 or not
+ * finite), CUDA. */
+MTP_API int mtp_verify_sample(const void *target_logits, const int32_t *draft, int32_t B, int32_t n,
+                              int32_t V, float temperature, const float *u_accept,
+                              const float *u_sample, int32_t *accept_len, int32_t *out_tokens,
+                              void *stream);
+
 /* Size of the static device scratch of mtp_centroid_head_noalloc (1 MiB). */
 #define MTP_NOALLOC_SCRATCH_BYTES (1u << 20)
 

@@ -8,7 +8,7 @@ from .binding import EXPORTS, MtpError, load_library  # noqa: F401
 
 def __getattr__(name):
     # The torch-facing layer is imported lazily so that the C ABI can be loaded without torch.
-    if name in ("Drafter", "verify_greedy", "make_config", "make_kv"):
+    if name in ("Drafter", "verify_greedy", "verify_sample", "make_config", "make_kv"):
         from . import drafter
         return getattr(drafter, name)
     raise AttributeError(name)

@@ -18,7 +18,8 @@ MTP_LAYER_SLIDING, MTP_LAYER_FULL = 0, 1
 
 # Every symbol include/mtp.h declares.
 EXPORTS = ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy", "mtp_get_status",
-           "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc", "mtp_set_logit_mask")
+           "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc", "mtp_set_logit_mask",
+           "mtp_verify_sample")
 MASK_NEG_1E30, MASK_MIN_MINUS_ONE = 0, 1  # enum mtp_logit_mask
 
 
@@ -73,6 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                     vp]
     lib.mtp_centroid_head.argtypes = [vp, vp, i32, vp, vp, vp, vp]
     lib.mtp_verify_greedy.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.mtp_verify_sample.argtypes = [vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp]
     lib.mtp_centroid_head_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.mtp_get_status.argtypes = [vp]
     lib.mtp_set_path.argtypes = [vp, i32]
@@ -82,7 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mtp_last_error.argtypes = []
     lib.mtp_last_error.restype = ctypes.c_char_p
     for name in ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy",
-                 "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc", "mtp_set_logit_mask"):
+                 "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc", "mtp_set_logit_mask",
+                 "mtp_verify_sample"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -123,6 +126,13 @@ def mtp_verify_greedy(target_logits: int, draft: int, B: int, n: int, V: int, ac
                       stream: int = 0) -> None:
     _check(load_library().mtp_verify_greedy(target_logits, draft or None, B, n, V, accept_len, out_tokens,
                                             stream or None), "mtp_verify_greedy")
+
+
+def mtp_verify_sample(target_logits: int, draft: int, B: int, n: int, V: int, temperature: float, u_accept: int,
+                      u_sample: int, accept_len: int, out_tokens: int, stream: int = 0) -> None:
+    _check(load_library().mtp_verify_sample(target_logits, draft or None, B, n, V, float(temperature),
+                                            u_accept or None, u_sample, accept_len, out_tokens, stream or None),
+           "mtp_verify_sample")
 
 
 def mtp_centroid_head_noalloc(y: int, centroids: int, token_ordering: int, token_embd: int, dtype: int, B: int,

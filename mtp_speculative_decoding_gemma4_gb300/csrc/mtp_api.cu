@@ -1058,6 +1058,26 @@ int mtp_verify_greedy(const void* target_logits, const int32_t* draft, int32_t B
   return mtp::run_verify(target_logits, draft, B, n, V, accept_len, out_tokens, static_cast<cudaStream_t>(stream));
 }
 
+int mtp_verify_sample(const void* target_logits, const int32_t* draft, int32_t B, int32_t n, int32_t V,
+                      float temperature, const float* u_accept, const float* u_sample, int32_t* accept_len,
+                      int32_t* out_tokens, void* stream) {
+  mtp::g_err[0] = 0;
+  if (!target_logits || !accept_len || !out_tokens || (n > 0 && (!draft || !u_accept)) || !u_sample) {
+    set_error("target_logits, draft and u_accept (n > 0), u_sample, accept_len and out_tokens must be non-NULL");
+    return MTP_ERR_INVALID_ARG;
+  }
+  if (B < 1 || n < 0 || V < 1 || V % 8 || !aligned16(target_logits) || !(temperature >= 0.f) ||
+      temperature > 3.0e38f) {
+    set_error("need B >= 1, n >= 0, V >= 1 with V %% 8 == 0, 16-byte aligned logits and a finite temperature >= 0 "
+              "(B=%d n=%d V=%d T=%g)", B, n, V, static_cast<double>(temperature));
+    return MTP_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (temperature == 0.f) return mtp::run_verify(target_logits, draft, B, n, V, accept_len, out_tokens, st);
+  return mtp::run_verify_sample(target_logits, draft, B, n, V, temperature, u_accept, u_sample, accept_len, out_tokens,
+                                st);
+}
+
 int mtp_get_status(mtp_handle* h) {
   mtp::g_err[0] = 0;
   if (!h) {

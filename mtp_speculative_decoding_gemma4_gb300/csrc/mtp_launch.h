@@ -75,5 +75,8 @@ int run_phases_tc_bf16(const Params& p, const TcPlan& plan, cudaStream_t st);
 
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st);
+// Sampled verification at temperature > 0 (one CTA per sequence).
+int run_verify_sample(const void* logits, const int* draft, int B, int n, int V, float temperature,
+                      const float* u_accept, const float* u_sample, int* accept_len, int* out_tokens, cudaStream_t st);
 
 }  // namespace mtp

@@ -138,4 +138,155 @@ int run_verify(const void* logits, const int* draft, int B, int n, int V, int* a
   return MTP_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Sampled verification at a temperature T > 0 (speculative sampling with the greedy
+// drafter's proposal a point mass on the drafted token; the pages give the accept-prefix
+// structure and say that accept rates vary with temperature): p_i = softmax(logits_i / T);
+// draft d_i is accepted when u_accept < p_i(d_i); at the first rejection the emitted token is
+// the inverse-CDF sample (increasing ids) of p_i with d_i removed and renormalised, with
+// u_sample; when all drafts are accepted the bonus token is the sample of p_n.
+//
+// One CTA per sequence, rows read in order until the first rejection. Thread t owns the
+// contiguous ids [t C, (t + 1) C) of a row and keeps a running max and exp-sum over them in
+// one pass (16-byte loads, 8 ids at a time); a block reduction gives the row max, the sums
+// rescaled to it are scanned over the threads in id order, which gives the normaliser and
+// every thread's cumulative mass; the thread whose range holds the sample point rescans its
+// ids (L1/L2) to find the sampled id.
+constexpr int kVsThreads = 1024;
+constexpr int kVsWarps = kVsThreads / 32;
+
+__device__ __forceinline__ float block_max_vs(float v, float* sh) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float m = sh[0];
+  for (int w = 1; w < kVsWarps; ++w) m = fmaxf(m, sh[w]);
+  return m;
+}
+// Exclusive prefix over the threads in order; returns it, and the total in *total.
+__device__ __forceinline__ float block_scan_vs(float v, float* sh, float* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  __syncthreads();
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  float before = 0.f, all = 0.f;
+  for (int w = 0; w < kVsWarps; ++w) {
+    if (w < warp) before += sh[w];
+    all += sh[w];
+  }
+  *total = all;
+  return before + inc - v;
+}
+
+__global__ void __launch_bounds__(kVsThreads) k_verify_sample(const __nv_bfloat16* __restrict__ logits,
+                                                              const int* __restrict__ draft, int n, int V, int chunk,
+                                                              float inv_t, const float* __restrict__ u_accept,
+                                                              const float* __restrict__ u_sample,
+                                                              int* __restrict__ accept_len, int* __restrict__ out_tokens) {
+  __shared__ float sh[kVsWarps];
+  __shared__ float pres[kVsThreads];
+  __shared__ int pick;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int lo = min(V, tid * chunk), hi = min(V, lo + chunk);
+  for (int i = tid; i <= n; i += kVsThreads) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = -1;
+  for (int i = 0; i <= n; ++i) {
+    const __nv_bfloat16* row = logits + (static_cast<size_t>(b) * (n + 1) + i) * V;
+    // running max and exp-sum of this thread's ids
+    float m = -INFINITY, s = 0.f;
+    for (int v = lo; v < hi; v += 8) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + v));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+      }
+      float lm = x[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) lm = fmaxf(lm, x[e]);
+      if (lm > m) {
+        s = m == -INFINITY ? 0.f : s * expf((m - lm) * inv_t);
+        m = lm;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += expf((x[e] - m) * inv_t);
+    }
+    const float M = block_max_vs(m, sh);
+    const float sr = s > 0.f ? s * expf((m - M) * inv_t) : 0.f;
+    float Z;
+    float pre = block_scan_vs(sr, sh, &Z);
+    // the accept test of draft d, and the residual mass without it
+    int d = -1;
+    float wd = 0.f;
+    if (i < n) {
+      d = min(max(draft[static_cast<size_t>(b) * n + i], 0), V - 1);
+      wd = expf((__bfloat162float(row[d]) - M) * inv_t);
+      if (u_accept[static_cast<size_t>(b) * n + i] < wd / Z) {
+        if (tid == 0) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = d;
+        continue;  // every thread takes the same decision
+      }
+    }
+    // sample of the residual (rejection) or of p_n (bonus): thread t owns the part
+    // [pre_t, pre_t+1) of the cumulative mass (the last thread with ids owns everything above
+    // its start), so exactly one thread rescans its ids for the point u * Z_eff
+    const float Zeff = Z - wd;
+    const float target = u_sample[static_cast<size_t>(b) * (n + 1) + i] * Zeff;
+    const float pre_e = pre - (d >= 0 && d < lo ? wd : 0.f);
+    __syncthreads();
+    pres[tid] = pre_e;
+    if (tid == 0) pick = -1;
+    __syncthreads();
+    const int tl = (V - 1) / chunk;  // the last thread with ids
+    const float upper = tid < tl ? pres[tid + 1] : INFINITY;
+    if (tid <= tl && pre_e <= target && target < upper) {
+      float acc = pre_e;
+      int t = -1, last = -1;
+      for (int v = lo; v < hi && t < 0; ++v) {
+        const float w = v == d ? 0.f : expf((__bfloat162float(row[v]) - M) * inv_t);
+        if (w > 0.f) last = v;
+        if (w > 0.f && acc + w > target) t = v;
+        acc += w;
+      }
+      pick = t >= 0 ? t : last;  // rounding left the point past the rescanned sum: the last id with mass
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int tok = pick;
+      if (tok < 0) {  // no id of the owner carries mass (underflow): the first id at the row maximum
+        for (int v = 0; v < V; ++v)
+          if (v != d && __bfloat162float(row[v]) == M) {
+            tok = v;
+            break;
+          }
+      }
+      out_tokens[static_cast<size_t>(b) * (n + 1) + i] = tok;
+      accept_len[b] = i;
+    }
+    return;
+  }
+}
+
+int run_verify_sample(const void* logits, const int* draft, int B, int n, int V, float temperature,
+                      const float* u_accept, const float* u_sample, int* accept_len, int* out_tokens, cudaStream_t st) {
+  const int chunk = ((V + kVsThreads - 1) / kVsThreads + 7) / 8 * 8;
+  k_verify_sample<<<B, kVsThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), draft, n, V, chunk,
+                                            1.0f / temperature, u_accept, u_sample, accept_len, out_tokens);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("k_verify_sample launch (%d sequences) failed: %s", B, cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
 }  // namespace mtp

@@ -126,6 +126,22 @@ class Drafter:
             pass
 
 
+def verify_sample(target_logits: torch.Tensor, drafts: torch.Tensor, temperature: float, u_accept: torch.Tensor,
+                  u_sample: torch.Tensor, accept_len=None, out_tokens=None, stream: int = 0):
+    """Sampled verification at a temperature: target_logits bf16 [B][n+1][V], drafts int32
+    [B][n], uniforms fp32 u_accept [B][n] and u_sample [B][n+1] (device tensors)."""
+    Bn, n1, V = target_logits.shape
+    dev = target_logits.device
+    if accept_len is None:
+        accept_len = torch.empty(Bn, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((Bn, n1), dtype=torch.int32, device=dev)
+    B.mtp_verify_sample(_ptr(_need_cuda(target_logits, "target_logits")), _ptr(drafts), Bn, n1 - 1, V, temperature,
+                        _ptr(u_accept), _ptr(_need_cuda(u_sample, "u_sample")), _ptr(accept_len), _ptr(out_tokens),
+                        stream)
+    return accept_len, out_tokens
+
+
 def verify_greedy(target_logits: torch.Tensor, drafts: torch.Tensor, accept_len=None, out_tokens=None,
                   stream: int = 0):
     """Greedy accept-prefix check: target_logits bf16 [B][n+1][V], drafts int32 [B][n]."""

@@ -1,4 +1,5 @@
-"""CPU oracle of the Gemma-4-assistant MTP drafter step, draft block and greedy verify.
+"""CPU oracle of the Gemma-4-assistant MTP drafter step, draft block, greedy verify and
+sampled (temperature) verify.
 
 TEST INFRASTRUCTURE ONLY. Only the test-suite, the package smoke check and the benchmark's
 CPU-baseline leg may import this module. The CUDA library never calls it, and it shares
@@ -34,7 +35,10 @@ Readings where the pages are silent or disagree (each is stated again where it i
   * head i reads KV head i // (n_head / n_kv_head);
   * token_ordering viewed row-major [C][vsc]: centroid c owns ids ordering[c*vsc:(c+1)*vsc];
   * unselected vocabulary entries of the materialised row are -1e30 (fp32), or, in the
-    other variant the pages give, the smallest candidate logit minus one.
+    other variant the pages give, the smallest candidate logit minus one;
+  * sampled verification (the pages only say that accept rates vary with temperature):
+    speculative sampling with the drafter's proposal as a point mass on the drafted token,
+    uniforms passed in by the caller.
 
 Pins: every helper and the centroid head, top-k, attention, verify and the shape counts are
 pinned by the not-gpu tests against closed forms, invariants, brute force and the values
@@ -517,3 +521,66 @@ def accept_rate(n_accept: int, n_drafted: int) -> float:
     """Acceptance rate as the pages report it: accepted drafts over drafted tokens
     ("Gemma 4 Multi-Token Prediction (MTP) drafter", "Runtime implementation")."""
     return n_accept / n_drafted
+
+
+def verify_sample(target_logits: np.ndarray, drafts: np.ndarray, temperature: float, u_accept: np.ndarray,
+                  u_sample: np.ndarray, logits_dtype: str = "bf16"):
+    """Sampled verification of a greedy draft at a temperature.
+
+    The pages give the accept-until-disagreement structure ("Gemma 4 drafter explained",
+    "What is Speculative Decoding?") and note that the accept rate varies with temperature
+    ("Gemma 4 Multi-Token Prediction (MTP) drafter", "Status"); they give no stochastic
+    acceptance rule. This follows speculative sampling (Leviathan, Kalman, Matias 2023;
+    Chen et al. 2023) with the drafter's proposal q = a point mass on the drafted token d_i
+    (the drafter drafts greedily):
+      p_i = softmax(target_logits[i] / T);
+      accept d_i when u_accept[i] < min(1, p_i(d_i) / q(d_i)) = p_i(d_i);
+      at the first rejection emit a sample of the residual max(0, p_i - q) / Z, i.e. p_i with
+      d_i removed and renormalised (inverse CDF over increasing ids: the smallest v whose
+      cumulative residual mass exceeds u_sample[i] * Z);
+      when every draft is accepted emit a sample of p_n with u_sample[n].
+    The emitted tokens are then distributed as sampling from the target at temperature T.
+    T = 0 is greedy verification (verify_greedy).
+
+    target_logits: [B][n+1][V] (bf16 bits or fp32); drafts [B][n]; u_accept [B][n] and
+    u_sample [B][n+1] uniforms in [0, 1). Returns accept_len [B], out_tokens [B][n+1] (-1
+    padded) and, per sequence, the smallest distance (relative to the mass compared against)
+    between a uniform and the boundary that decided the outcome, in fp64.
+    """
+    drafts = np.asarray(drafts, dtype=np.int64)
+    B, n = drafts.shape
+    if temperature == 0.0:
+        acc, out = verify_greedy(target_logits, drafts, logits_dtype)
+        return acc, out, np.full(B, np.inf)
+    if temperature < 0.0:
+        raise ValueError("temperature must be >= 0")
+    acc = np.zeros(B, dtype=np.int64)
+    out = np.full((B, n + 1), -1, dtype=np.int64)
+    margin = np.full(B, np.inf)
+    for b in range(B):
+        i = 0
+        while True:
+            z = decode(target_logits[b, i], logits_dtype).astype(np.float64) / temperature
+            w = np.exp(z - z.max())
+            Z = w.sum()
+            if i < n:
+                d = int(drafts[b, i])
+                pd = w[d] / Z
+                ua = float(u_accept[b, i])
+                margin[b] = min(margin[b], abs(ua - pd))
+                if ua < pd:
+                    out[b, i] = d
+                    i += 1
+                    continue
+                w = w.copy()
+                w[d] = 0.0
+            c = np.cumsum(w)
+            target = float(u_sample[b, i]) * c[-1]
+            t = int(np.searchsorted(c, target, side="right"))
+            t = min(t, len(c) - 1)
+            lo = c[t - 1] if t > 0 else 0.0
+            margin[b] = min(margin[b], min(target - lo, c[t] - target) / c[-1])
+            out[b, i] = t
+            break
+        acc[b] = i
+    return acc, out, margin

@@ -322,6 +322,74 @@ def test_verify_matches_oracle(B, n, V, ties):
     np.testing.assert_array_equal(out.cpu().numpy(), rout)
 
 
+def _sample_case(B, n, V, seed, plant):
+    """Target logits N(0, 1) with a planted value at the draft (probability 0.7) or at another
+    id, drafts, and seeded uniforms."""
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((B, n + 1, V)).astype(np.float32)
+    drafts = rng.integers(0, V, size=(B, n)).astype(np.int32)
+    agree = rng.random((B, n)) < 0.7
+    for b in range(B):
+        for i in range(n):
+            t = drafts[b, i] if agree[b, i] else (drafts[b, i] + 1 + rng.integers(0, V - 1)) % V
+            logits[b, i, t] = plant
+    ua = rng.random((B, n)).astype(np.float32)
+    us = rng.random((B, n + 1)).astype(np.float32)
+    return G.bf16_bits(logits), drafts, ua, us
+
+
+@pytest.mark.parametrize("B,n,V,T,plant", [(64, 8, 262144, 1.0, 16.0), (64, 8, 262144, 0.7, 12.0),
+                                           (5, 4, 4096, 1.0, 4.0), (3, 0, 64, 0.5, 2.0), (7, 1, 8, 2.0, 1.0),
+                                           (4, 3, 131072, 1.5, 20.0)])
+def test_verify_sample_matches_oracle(B, n, V, T, plant):
+    from mtp_speculative_decoding_gemma4_gb300 import verify_sample
+    bits, drafts, ua, us = _sample_case(B, n, V, seed=B * 7 + n * 3 + V % 97, plant=plant)
+    acc, out = verify_sample(to_torch(bits, "bf16"), to_torch(drafts, "i32"), T,
+                             torch.from_numpy(ua).cuda(), torch.from_numpy(us).cuda())
+    torch.cuda.synchronize()
+    acc, out = acc.cpu().numpy(), out.cpu().numpy()
+    racc, rout, margin = O.verify_sample(bits, drafts, T, ua, us)
+    # fp32 decisions may differ from the fp64 oracle only for a uniform within 1e-5 of a
+    # decision boundary (relative to the mass compared against)
+    bad = [b for b in range(B) if acc[b] != racc[b] or not np.array_equal(out[b], rout[b])]
+    assert all(margin[b] < 1e-5 for b in bad), (bad, [margin[b] for b in bad])
+    assert len(bad) <= max(1, B // 32)
+
+
+def test_verify_sample_at_zero_temperature_is_greedy_on_the_device():
+    from mtp_speculative_decoding_gemma4_gb300 import verify_greedy, verify_sample
+    bits, drafts = _verify_case(16, 4, 4096, seed=77, ties=True)
+    t = to_torch(bits, "bf16")
+    d = to_torch(drafts, "i32")
+    u = torch.rand((16, 5), device="cuda")
+    a1, o1 = verify_sample(t, d, 0.0, u[:, :4].contiguous(), u)
+    a2, o2 = verify_greedy(t, d)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(a1.cpu().numpy(), a2.cpu().numpy())
+    np.testing.assert_array_equal(o1.cpu().numpy(), o2.cpu().numpy())
+
+
+def test_verify_sample_first_token_follows_the_target_distribution():
+    # 16384 independent trials of one row: the emitted first token must be distributed as
+    # softmax(row / T) (the draft kept with probability p(d), else a residual sample)
+    from mtp_speculative_decoding_gemma4_gb300 import verify_sample
+    rng = np.random.default_rng(5)
+    B, V, T, d = 16384, 16, 0.9, 3
+    row = rng.standard_normal(V).astype(np.float32)
+    bits = G.bf16_bits(np.broadcast_to(row, (B, 2, V)).copy())
+    p = torch.softmax(torch.tensor(O.decode_bf16(bits[0, 0]).astype(np.float64)) / T, dim=0).numpy()
+    drafts = np.full((B, 1), d, dtype=np.int32)
+    ua = torch.rand((B, 1), device="cuda")
+    us = torch.rand((B, 2), device="cuda")
+    acc, out = verify_sample(to_torch(bits, "bf16"), to_torch(drafts, "i32"), T, ua, us)
+    torch.cuda.synchronize()
+    first = out.cpu().numpy()[:, 0]
+    freq = np.bincount(first, minlength=V) / B
+    sigma = np.sqrt(p * (1 - p) / B)
+    assert np.all(np.abs(freq - p) <= 5 * sigma + 1e-4), (freq, p)
+    assert abs(np.mean(acc.cpu().numpy() == 1) - p[d]) <= 5 * np.sqrt(p[d] * (1 - p[d]) / B)
+
+
 def test_verify_rejects_bad_vocab():
     from mtp_speculative_decoding_gemma4_gb300 import MtpError, verify_greedy
     t = torch.zeros((1, 2, 12), dtype=torch.bfloat16, device="cuda")

@@ -99,3 +99,17 @@ def test_verify_rejects_bad_sizes_before_the_device(lib):
     assert lib.mtp_verify_greedy(fake, fake, 1, 1, 12, fake, fake, None) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_verify_greedy(fake, fake, 0, 1, 16, fake, fake, None) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_verify_greedy(fake, fake, 1, -1, 16, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+
+
+def test_verify_sample_rejects_bad_arguments_before_the_device(lib):
+    fake = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    f = ctypes.c_float
+    assert lib.mtp_verify_sample(None, fake, 1, 1, 16, f(1.0), fake, fake, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, fake, 1, 1, 12, f(1.0), fake, fake, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, fake, 1, 1, 16, f(-0.5), fake, fake, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, fake, 1, 1, 16, f(float("nan")), fake, fake, fake, fake,
+                                 None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, fake, 1, 1, 16, f(float("inf")), fake, fake, fake, fake,
+                                 None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, None, 1, 2, 16, f(1.0), fake, fake, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_verify_sample(fake, fake, 1, 1, 16, f(1.0), fake, None, fake, fake, None) == B.MTP_ERR_INVALID_ARG

@@ -476,3 +476,91 @@ def test_layer_types_read_their_own_k_and_window():
     k_swa = inp.k_swa.copy(); k_swa[b, L - 1] += 5.0          # the sliding layer sees the newest key
     r = _step_y(shape, w, G.StepInputs(inp.hidden, inp.last_token, inp.ctx_len, inp.pos, k_swa, inp.k_full), b)
     assert np.max(np.abs(r.y - ref.y)) > 1e-4
+
+
+# ---------------------------------------------------------------------------------------
+# Sampled verification (speculative sampling with a point-mass proposal on each draft)
+# ---------------------------------------------------------------------------------------
+
+def _bf16_rows(rng, shape, scale=1.0):
+    return G.bf16_bits((scale * rng.standard_normal(shape)).astype(np.float32))
+
+
+def test_verify_sample_at_zero_temperature_is_greedy():
+    rng = np.random.default_rng(11)
+    B, n, V = 6, 4, 64
+    logits = _bf16_rows(rng, (B, n + 1, V))
+    drafts = rng.integers(0, V, size=(B, n))
+    for b in range(0, B, 2):  # some sequences agree with the target for a while
+        drafts[b, :3] = [O.argmax_lowest(O.decode_bf16(logits[b, i]).astype(np.float32)) for i in range(3)]
+    u = rng.random((B, n + 1))
+    acc, out, _ = O.verify_sample(logits, drafts, 0.0, u[:, :n], u)
+    racc, rout = O.verify_greedy(logits, drafts)
+    np.testing.assert_array_equal(acc, racc)
+    np.testing.assert_array_equal(out, rout)
+
+
+def test_verify_sample_tends_to_greedy_as_the_temperature_falls():
+    rng = np.random.default_rng(12)
+    B, n, V = 8, 3, 32
+    vals = np.stack([rng.permutation(V) for _ in range(B * (n + 1))]).reshape(B, n + 1, V).astype(np.float32) * 0.25
+    logits = G.bf16_bits(vals)  # distinct values 0.25 apart: a unique maximum per row
+    drafts = rng.integers(0, V, size=(B, n))
+    drafts[::2, 0] = np.argmax(vals[::2, 0], axis=-1)
+    u = rng.uniform(0.01, 0.99, size=(B, n + 1))
+    acc, out, _ = O.verify_sample(logits, drafts, 1e-3, u[:, :n], u)
+    racc, rout = O.verify_greedy(logits, drafts)
+    np.testing.assert_array_equal(acc, racc)
+    np.testing.assert_array_equal(out, rout)
+
+
+def test_verify_sample_emits_the_target_distribution():
+    # P(first token = v) over (u_accept, u_sample) must equal softmax(logits / T)[v]: the
+    # draft is kept with probability p(d), otherwise v != d comes from p without d
+    # renormalised. Integrated on a midpoint grid of both uniforms (error <= 1 / grid).
+    rng = np.random.default_rng(13)
+    V, T, grid = 6, 0.8, 400
+    logits = _bf16_rows(rng, (1, 2, V))
+    p = torch.softmax(torch.tensor(O.decode_bf16(logits[0, 0]).astype(np.float64)) / T, dim=0).numpy()
+    for d in (int(np.argmax(p)), int(np.argmin(p))):
+        g = (np.arange(grid) + 0.5) / grid
+        ua, us = np.meshgrid(g, g, indexing="ij")
+        M = ua.size
+        lg = np.broadcast_to(logits, (M, 2, V))
+        acc, out, _ = O.verify_sample(lg, np.full((M, 1), d), T, ua.reshape(M, 1), np.repeat(us.reshape(M, 1), 2, 1))
+        freq = np.bincount(out[:, 0], minlength=V) / M
+        np.testing.assert_allclose(freq, p, atol=2.0 / grid)
+        assert abs(np.mean(acc == 1) - p[d]) <= 1.0 / grid  # acceptance probability p(d)
+
+
+def test_verify_sample_bonus_token_follows_the_last_row():
+    rng = np.random.default_rng(14)
+    V, T, grid = 8, 1.3, 2000
+    logits = _bf16_rows(rng, (1, 3, V))
+    vals = O.decode_bf16(logits).astype(np.float32)
+    drafts = np.array([[0, 1]])
+    for i in range(2):  # the drafts carry (almost) all the mass of their rows
+        vals[0, i, :] = -40.0
+        vals[0, i, drafts[0, i]] = 40.0
+    logits = G.bf16_bits(vals)
+    p_last = torch.softmax(torch.tensor(vals[0, 2].astype(np.float64)) / T, dim=0).numpy()
+    us = (np.arange(grid) + 0.5) / grid
+    M = grid
+    lg = np.broadcast_to(logits, (M, 3, V))
+    u_s = np.zeros((M, 3))
+    u_s[:, 2] = us
+    acc, out, _ = O.verify_sample(lg, np.broadcast_to(drafts, (M, 2)), T, np.full((M, 2), 0.5), u_s)
+    assert np.all(acc == 2)
+    np.testing.assert_allclose(np.bincount(out[:, 2], minlength=V) / M, p_last, atol=1.0 / grid)
+
+
+def test_verify_sample_margins_locate_the_decision_boundaries():
+    # a uniform placed exactly on p(d) sits on the accept boundary: margin 0
+    rng = np.random.default_rng(15)
+    V, T = 16, 1.0
+    logits = _bf16_rows(rng, (1, 2, V))
+    p = np.exp(O.decode_bf16(logits[0, 0]).astype(np.float64) / T)
+    p /= p.sum()
+    d = 5
+    _, _, m = O.verify_sample(logits, np.array([[d]]), T, np.array([[p[d]]]), np.array([[0.5, 0.5]]))
+    assert m[0] <= 1e-12

@@ -45,6 +45,16 @@ struct mtp_handle {
   // the staging buffer of the input terms
   mtp::TcPlan* tc;
   void* tc_mem;
+  // multi-launch paths: the draft block of the last argument set as an instantiated CUDA
+  // graph, replayed on an internal stream ordered after / before the caller's stream by
+  // events; a call with different arguments captures again
+  struct {
+    int valid, path;
+    mtp::Params key;
+    cudaGraphExec_t exec;
+    cudaStream_t cs;
+    cudaEvent_t ev_in, ev_out;
+  } gc;
 };
 
 namespace mtp {
@@ -690,6 +700,46 @@ int set_device(const mtp_handle* h) {
 
 }  // namespace
 
+// Runs a multi-launch draft block through the handle's graph cache: replays the instantiated
+// graph when the parameters (every pointer and size the launches take) equal the cached
+// ones, else captures run() on the internal stream and instantiates it. Falls back to
+// direct launches on the caller's stream when graphs are not available.
+template <typename Run>
+int run_graph_cached(mtp_handle* h, int path, const mtp::Params& p, cudaStream_t st, Run run) {
+  auto& G = h->gc;
+  if (!G.cs) return run(st);
+  if (!G.valid || G.path != path || memcmp(&G.key, &p, sizeof(p)) != 0) {
+    if (G.valid) {
+      cudaGraphExecDestroy(G.exec);
+      G.valid = 0;
+    }
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(G.cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail("beginning the draft-block graph capture", e);
+    const int rc = run(G.cs);
+    e = cudaStreamEndCapture(G.cs, &graph);
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      cudaGetLastError();
+      return rc;
+    }
+    if (e != cudaSuccess) return cuda_fail("ending the draft-block graph capture", e);
+    e = cudaGraphInstantiate(&G.exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail("instantiating the draft-block graph", e);
+    memcpy(&G.key, &p, sizeof(p));
+    G.path = path;
+    G.valid = 1;
+  }
+  cudaError_t e = cudaEventRecord(G.ev_in, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(G.cs, G.ev_in, 0);
+  if (e == cudaSuccess) e = cudaGraphLaunch(G.exec, G.cs);
+  if (e == cudaSuccess) e = cudaEventRecord(G.ev_out, G.cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, G.ev_out, 0);
+  if (e != cudaSuccess) return cuda_fail("launching the draft-block graph", e);
+  return MTP_OK;
+}
+
 extern "C" {
 
 const char* mtp_last_error(void) { return mtp::g_err; }
@@ -786,6 +836,16 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       free(h);
       return rc;
     }
+  }
+  // the graph cache's stream and events (graphs are skipped when they cannot be created)
+  if (cudaStreamCreateWithFlags(&h->gc.cs, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->gc.ev_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->gc.ev_out, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->gc.ev_in) cudaEventDestroy(h->gc.ev_in);
+    if (h->gc.cs) cudaStreamDestroy(h->gc.cs);
+    h->gc.cs = nullptr;
+    h->gc.ev_in = h->gc.ev_out = nullptr;
   }
   *out = h;
   return MTP_OK;
@@ -982,7 +1042,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     for (int t = 0; t < 2; ++t)
       p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * h->num_sms,
                                                      h->nsplit_max) : 1;
-    return mtp::run_phases_tc_bf16(p, *h->tc, st);
+    return run_graph_cached(h, 5, p, st, [&](cudaStream_t s2) { return mtp::run_phases_tc_bf16(p, *h->tc, s2); });
   }
   if (path != 1) {
     p.s.ncta_hint = ncta;
@@ -1002,7 +1062,8 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   for (int t = 0; t < 2; ++t)
     p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * h->num_sms,
                                                    h->nsplit_max) : 1;
-  return bf16 ? mtp::run_phases_bf16(p, st) : mtp::run_phases_f32(p, st);
+  return run_graph_cached(h, 1, p, st,
+                          [&](cudaStream_t s2) { return bf16 ? mtp::run_phases_bf16(p, s2) : mtp::run_phases_f32(p, s2); });
 }
 
 int mtp_centroid_head(mtp_handle* h, const float* y, int32_t B, float* out_logits, int32_t* out_token,
@@ -1117,6 +1178,10 @@ void mtp_destroy(mtp_handle* h) {
   if (h->temb_ord) cudaFree(h->temb_ord);
   if (h->wpack) cudaFree(h->wpack);
   if (h->c2_stream) cudaFree(h->c2_stream);
+  if (h->gc.valid) cudaGraphExecDestroy(h->gc.exec);
+  if (h->gc.ev_in) cudaEventDestroy(h->gc.ev_in);
+  if (h->gc.ev_out) cudaEventDestroy(h->gc.ev_out);
+  if (h->gc.cs) cudaStreamDestroy(h->gc.cs);
   if (h->tc_mem) cudaFree(h->tc_mem);
   if (h->tc) free(h->tc);
   free(h);

@@ -480,3 +480,23 @@ def test_draft_verify_loop_accept_length_statistics():
             assert np.array_equal(o[b, :a[b]], dn[b, :a[b]])
             assert o[b, a[b]] >= 0 and np.all(o[b, a[b] + 1:] == -1)
     dr.close()
+
+
+def test_graph_replay_reads_new_contents_and_recaptures_on_new_arguments():
+    # the multi-launch paths replay a captured graph when the arguments repeat: new input
+    # contents behind the same pointers must be read, and a change of n_draft recaptured
+    shape, wl, w, inp = config_data(4)
+    dr, d = _drafter(4)
+    t1, _ = _run_block(dr, d, 2, TENSOR)
+    t2, _ = _run_block(dr, d, 2, TENSOR)          # replay, same inputs
+    np.testing.assert_array_equal(t1, t2)
+    t4, _ = _run_block(dr, d, 4, TENSOR)          # new n_draft: captured again
+    np.testing.assert_array_equal(t4[:, :2], t1)
+    d["last_token"].copy_(torch.roll(d["last_token"], 1))  # new contents, same pointers
+    t5, _ = _run_block(dr, d, 4, TENSOR)
+    dr.close()
+    dr2, _ = _drafter(4)
+    t6, _ = _run_block(dr2, d, 4, TENSOR)         # a fresh handle with the same inputs
+    np.testing.assert_array_equal(t5, t6)
+    assert not np.array_equal(t5, t4)
+    dr2.close()

@@ -456,15 +456,15 @@ def main():
     ap.add_argument("--path", type=int, default=-1,
                     help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
                          "(one sequence), 4: cluster kernel (one sequence), 5: phase kernels with tcgen05 "
-                         "projections, 6: streamed-tile cluster kernel (one sequence); default: 6 for B=1, 5 "
-                         "for B>=32, else 2")
+                         "projections, 6: streamed-tile cluster kernel (one sequence); default: 6 for B=1, "
+                         "else 5")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.path < 0:
         bsz = workload(args.config)[1].batch
-        args.path = 6 if bsz == 1 else (5 if bsz >= 32 else 2)
+        args.path = 6 if bsz == 1 else 5
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

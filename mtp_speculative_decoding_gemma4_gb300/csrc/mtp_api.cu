@@ -1033,7 +1033,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     return mtp::run_ll(lp, smem, st);
   }
   int ncta = h->num_sms;
-  if (path == 5 || (path == 0 && B >= 32 && h->tc)) {
+  if (path == 5 || (path == 0 && B >= 2 && h->tc)) {
     if (!h->tc) {
       set_error("the tensor-core path needs a bf16 drafter with max_batch in [2, %d] on this device", mtp::tc::kMaxB);
       return MTP_ERR_UNSUPPORTED_SHAPE;

@@ -89,6 +89,10 @@ E2B = DrafterShape(
 
 E4B = replace(E2B, name="e4b", backbone=2560)
 
+# E4B with the two shared KV heads one page lists (the benchmark workload follows the other
+# page's "same head structure as E2B", one KV head); a parity-test shape only.
+E4B_KV2 = replace(E4B, name="e4b-kv2", n_kv_head=2)
+
 A4B_DENSE = DrafterShape(
     name="26b-a4b-dense", dtype="bf16", backbone=2816, hidden=1024,
     layer_types=("S", "S", "S", "F"), n_head=8, head_dim_swa=128, head_dim_full=128,

@@ -500,3 +500,23 @@ def test_graph_replay_reads_new_contents_and_recaptures_on_new_arguments():
     np.testing.assert_array_equal(t5, t6)
     assert not np.array_equal(t5, t4)
     dr2.close()
+
+
+@pytest.mark.parametrize("B,path", [(1, 0), (4, TENSOR), (4, PHASES)])
+def test_e4b_with_two_kv_heads_matches_oracle(B, path):
+    # the E4B drafter with two shared KV heads (two query heads per KV head) on the automatic
+    # one-sequence path and on the batched paths
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape = C.E4B_KV2
+    wl = C.Workload(batch=B, ctx=4096, ctx_lo=1024 if B > 1 else None, n_draft=3, seed=2024)
+    w = G.make_weights(shape, wl.seed)
+    inp = G.make_step_inputs(shape, wl, wl.seed)
+    ref = O.draft_block(O.Shape.of(shape), O.decode_weights(w), inp.hidden, inp.last_token, inp.k_swa, inp.k_full,
+                        inp.ctx_len, inp.pos, wl.n_draft)
+    wd, tgt = weights_to_device(w)
+    dr = Drafter(shape, wd, tgt, max_batch=B, max_ctx=wl.ctx)
+    d = inputs_to_device(inp, "bf16")
+    tok, hid = _run_block(dr, d, wl.n_draft, path)
+    cmp = compare_block(tok, hid, ref, "bf16")
+    assert len(cmp.tie_divergences) <= 1
+    dr.close()

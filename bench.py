@@ -361,7 +361,7 @@ def run_mtp(args, rank: int, world: int, dist):
         "verify_sample": {"temperature": 1.0, "us": vs_ms * 1e3, "rows_read": vs_rows,
                           "accept_len_mean": float(acc_s.float().mean().item()),
                           "achieved_gbs": vs_rows * shape.vocab * 2 / (vs_ms * 1e-3) / 1e9,
-                          "kernel": "k_verify_sample (one CTA per sequence)"},
+                          "kernel": "k_verify_sample (one thread-block cluster per sequence)"},
     }
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args, shape, wl, w, inp, base, seconds=args.cpu_seconds)

@@ -146,26 +146,19 @@ int run_verify(const void* logits, const int* draft, int B, int n, int V, int* a
 // the inverse-CDF sample (increasing ids) of p_i with d_i removed and renormalised, with
 // u_sample; when all drafts are accepted the bonus token is the sample of p_n.
 //
-// One CTA per sequence, rows read in order until the first rejection. Thread t owns the
-// contiguous ids [t C, (t + 1) C) of a row and keeps a running max and exp-sum over them in
-// one pass (16-byte loads, 8 ids at a time); a block reduction gives the row max, the sums
-// rescaled to it are scanned over the threads in id order, which gives the normaliser and
-// every thread's cumulative mass; the thread whose range holds the sample point rescans its
-// ids (L1/L2) to find the sampled id.
-constexpr int kVsThreads = 1024;
+// One thread-block cluster per sequence reads the rows in order until the first rejection.
+// CTA c of the cluster owns the contiguous ids [c S, (c + 1) S) of a row and thread t of it
+// the contiguous sub-range [t C, (t + 1) C): each thread keeps a running max and exp-sum
+// over its ids in one pass (16-byte loads), the CTA scans the sums rescaled to its max, and
+// the CTAs exchange (max, sum) through distributed shared memory. Every CTA then forms the
+// row max, the normaliser and the CTAs' cumulative masses in the same order, so all take the
+// same accept decision; the CTA, and in it the thread, whose part of the cumulative mass
+// holds the sample point rescans its ids to find the sampled id.
+constexpr int kVsThreads = 512;
 constexpr int kVsWarps = kVsThreads / 32;
+constexpr int kVsMaxCluster = 16;
 
-__device__ __forceinline__ float block_max_vs(float v, float* sh) {
-  v = warp_max(v);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  float m = sh[0];
-  for (int w = 1; w < kVsWarps; ++w) m = fmaxf(m, sh[w]);
-  return m;
-}
-// Exclusive prefix over the threads in order; returns it, and the total in *total.
+// Exclusive prefix over the CTA's threads in order; returns it, and the total in *total.
 __device__ __forceinline__ float block_scan_vs(float v, float* sh, float* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float inc = v;
@@ -187,22 +180,27 @@ __device__ __forceinline__ float block_scan_vs(float v, float* sh, float* total)
 }
 
 __global__ void __launch_bounds__(kVsThreads) k_verify_sample(const __nv_bfloat16* __restrict__ logits,
-                                                              const int* __restrict__ draft, int n, int V, int chunk,
-                                                              float inv_t, const float* __restrict__ u_accept,
+                                                              const int* __restrict__ draft, int n, int V, int slice,
+                                                              int chunk, float k2, const float* __restrict__ u_accept,
                                                               const float* __restrict__ u_sample,
                                                               int* __restrict__ accept_len, int* __restrict__ out_tokens) {
   __shared__ float sh[kVsWarps];
   __shared__ float pres[kVsThreads];
+  __shared__ float2 ex[2][kVsMaxCluster];  // (max, exp-sum) of every CTA, double-buffered by row
   __shared__ int pick;
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const int lo = min(V, tid * chunk), hi = min(V, lo + chunk);
-  for (int i = tid; i <= n; i += kVsThreads) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = -1;
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = static_cast<int>(cl.num_blocks()), rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / cs, tid = threadIdx.x;
+  const int clo = min(V, rank * slice), chi = min(V, clo + slice);
+  const int lo = min(chi, clo + tid * chunk), hi = min(chi, lo + chunk);
+  if (rank == 0)
+    for (int i = tid; i <= n; i += kVsThreads) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = -1;
+  // weights exp((x - m) / T) as exp2((x - m) * log2(e) / T) = exp2((x - m) * k2)
   for (int i = 0; i <= n; ++i) {
     const __nv_bfloat16* row = logits + (static_cast<size_t>(b) * (n + 1) + i) * V;
-    // running max and exp-sum of this thread's ids
     float m = -INFINITY, s = 0.f;
     for (int v = lo; v < hi; v += 8) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(row + v));
+      const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(row + v));
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
       float x[8];
 #pragma unroll
@@ -215,75 +213,122 @@ __global__ void __launch_bounds__(kVsThreads) k_verify_sample(const __nv_bfloat1
 #pragma unroll
       for (int e = 1; e < 8; ++e) lm = fmaxf(lm, x[e]);
       if (lm > m) {
-        s = m == -INFINITY ? 0.f : s * expf((m - lm) * inv_t);
+        s = m == -INFINITY ? 0.f : s * exp2f((m - lm) * k2);
         m = lm;
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s += expf((x[e] - m) * inv_t);
+      for (int e = 0; e < 8; ++e) s += exp2f((x[e] - m) * k2);
     }
-    const float M = block_max_vs(m, sh);
-    const float sr = s > 0.f ? s * expf((m - M) * inv_t) : 0.f;
-    float Z;
-    float pre = block_scan_vs(sr, sh, &Z);
+    // this CTA: max, and the thread sums rescaled to it, scanned in id order
+    float wm = warp_max(m);
+    __syncthreads();
+    if ((tid & 31) == 0) sh[tid >> 5] = wm;
+    __syncthreads();
+    float Mc = sh[0];
+    for (int w = 1; w < kVsWarps; ++w) Mc = fmaxf(Mc, sh[w]);
+    const float sr = s > 0.f ? s * exp2f((m - Mc) * k2) : 0.f;
+    float Sc;
+    const float pre = block_scan_vs(sr, sh, &Sc);
+    // every CTA's (max, sum) to every CTA
+    if (tid < cs) *cl.map_shared_rank(&ex[i & 1][rank], tid) = make_float2(Mc, Sc);
+    cl.sync();
+    float M = -INFINITY;
+    for (int c = 0; c < cs; ++c) M = fmaxf(M, ex[i & 1][c].x);
+    float Z = 0.f, Pc = 0.f;  // normaliser and this CTA's cumulative mass, in CTA order
+    for (int c = 0; c < cs; ++c) {
+      const float2 e = ex[i & 1][c];
+      const float w = e.y > 0.f ? e.y * exp2f((e.x - M) * k2) : 0.f;
+      if (c < rank) Pc += w;
+      Z += w;
+    }
+    const float fc = Sc > 0.f ? exp2f((Mc - M) * k2) : 0.f;
     // the accept test of draft d, and the residual mass without it
     int d = -1;
     float wd = 0.f;
     if (i < n) {
       d = min(max(draft[static_cast<size_t>(b) * n + i], 0), V - 1);
-      wd = expf((__bfloat162float(row[d]) - M) * inv_t);
+      wd = exp2f((__bfloat162float(row[d]) - M) * k2);
       if (u_accept[static_cast<size_t>(b) * n + i] < wd / Z) {
-        if (tid == 0) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = d;
-        continue;  // every thread takes the same decision
+        if (rank == 0 && tid == 0) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = d;
+        continue;  // every CTA and thread takes the same decision
       }
     }
-    // sample of the residual (rejection) or of p_n (bonus): thread t owns the part
-    // [pre_t, pre_t+1) of the cumulative mass (the last thread with ids owns everything above
-    // its start), so exactly one thread rescans its ids for the point u * Z_eff
-    const float Zeff = Z - wd;
-    const float target = u_sample[static_cast<size_t>(b) * (n + 1) + i] * Zeff;
-    const float pre_e = pre - (d >= 0 && d < lo ? wd : 0.f);
-    __syncthreads();
-    pres[tid] = pre_e;
-    if (tid == 0) pick = -1;
-    __syncthreads();
-    const int tl = (V - 1) / chunk;  // the last thread with ids
-    const float upper = tid < tl ? pres[tid + 1] : INFINITY;
-    if (tid <= tl && pre_e <= target && target < upper) {
-      float acc = pre_e;
-      int t = -1, last = -1;
-      for (int v = lo; v < hi && t < 0; ++v) {
-        const float w = v == d ? 0.f : expf((__bfloat162float(row[v]) - M) * inv_t);
-        if (w > 0.f) last = v;
-        if (w > 0.f && acc + w > target) t = v;
-        acc += w;
+    // sample point of the residual (rejection) or of p_n (bonus); CTA c owns
+    // [P'_c, P'_c+1) of the cumulative mass without d, the last CTA with ids everything above
+    const float target = u_sample[static_cast<size_t>(b) * (n + 1) + i] * (Z - wd);
+    const int cl_last = (V - 1) / slice;
+    float Pn = INFINITY;  // the next CTA's start
+    if (rank < cl_last) {
+      Pn = 0.f;
+      for (int c = 0; c <= rank; ++c) {
+        const float2 e = ex[i & 1][c];
+        Pn += e.y > 0.f ? e.y * exp2f((e.x - M) * k2) : 0.f;
       }
-      pick = t >= 0 ? t : last;  // rounding left the point past the rescanned sum: the last id with mass
+      if (d >= 0 && d < chi) Pn -= wd;
     }
-    __syncthreads();
-    if (tid == 0) {
-      int tok = pick;
-      if (tok < 0) {  // no id of the owner carries mass (underflow): the first id at the row maximum
-        for (int v = 0; v < V; ++v)
-          if (v != d && __bfloat162float(row[v]) == M) {
-            tok = v;
-            break;
-          }
+    const float Pce = Pc - (d >= 0 && d < clo ? wd : 0.f);
+    const bool cta_owns = rank <= cl_last && Pce <= target && target < Pn;
+    if (cta_owns) {
+      const float pe = Pce + pre * fc - (d >= clo && d < lo ? wd : 0.f);
+      pres[tid] = pe;
+      if (tid == 0) pick = -1;
+      __syncthreads();
+      const int tl = (chi - clo - 1) / chunk;  // the CTA's last thread with ids
+      const float upper = tid < tl ? pres[tid + 1] : Pn;
+      if (tid <= tl && pe <= target && target < upper) {
+        float acc = pe;
+        int t = -1, last = -1;
+        for (int v = lo; v < hi && t < 0; ++v) {
+          const float w = v == d ? 0.f : exp2f((__bfloat162float(row[v]) - M) * k2);
+          if (w > 0.f) last = v;
+          if (w > 0.f && acc + w > target) t = v;
+          acc += w;
+        }
+        pick = t >= 0 ? t : last;  // rounding left the point past the rescanned sum: the last id with mass
       }
-      out_tokens[static_cast<size_t>(b) * (n + 1) + i] = tok;
-      accept_len[b] = i;
+      __syncthreads();
+      if (tid == 0) {
+        int tok = pick;
+        if (tok < 0)  // no id of the owner carries mass (underflow): the first id of the slice at its max
+          for (int v = clo; v < chi; ++v)
+            if (v != d && __bfloat162float(row[v]) == Mc) {
+              tok = v;
+              break;
+            }
+        out_tokens[static_cast<size_t>(b) * (n + 1) + i] = tok < 0 ? clo : tok;
+        accept_len[b] = i;
+      }
     }
-    return;
+    break;
   }
+  cl.sync();  // no CTA leaves while a peer may still write its exchange slots
 }
 
 int run_verify_sample(const void* logits, const int* draft, int B, int n, int V, float temperature,
                       const float* u_accept, const float* u_sample, int* accept_len, int* out_tokens, cudaStream_t st) {
-  const int chunk = ((V + kVsThreads - 1) / kVsThreads + 7) / 8 * 8;
-  k_verify_sample<<<B, kVsThreads, 0, st>>>(static_cast<const __nv_bfloat16*>(logits), draft, n, V, chunk,
-                                            1.0f / temperature, u_accept, u_sample, accept_len, out_tokens);
-  const cudaError_t e = cudaGetLastError();
+  int cs = B <= 8 ? 16 : 8;
+  if (cs == 16 && cudaFuncSetAttribute(k_verify_sample, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    cs = 8;
+  }
+  const int slice = ((V + cs * 8 - 1) / (cs * 8)) * 8;
+  const int chunk = ((slice + kVsThreads - 1) / kVsThreads + 7) / 8 * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * cs);
+  cfg.blockDim = dim3(kVsThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cs;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const float k2 = 1.4426950408889634f / temperature;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_verify_sample, static_cast<const __nv_bfloat16*>(logits), draft, n, V,
+                                           slice, chunk, k2, u_accept, u_sample, accept_len, out_tokens);
   if (e != cudaSuccess) {
-    set_error("k_verify_sample launch (%d sequences) failed: %s", B, cudaGetErrorString(e));
+    set_error("k_verify_sample launch (%d clusters of %d) failed: %s", B, cs, cudaGetErrorString(e));
     return MTP_ERR_CUDA;
   }
   return MTP_OK;

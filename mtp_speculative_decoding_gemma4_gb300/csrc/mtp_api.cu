@@ -1039,9 +1039,19 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
       return MTP_ERR_UNSUPPORTED_SHAPE;
     }
     p.s.ncta_hint = 2 * h->num_sms;
-    for (int t = 0; t < 2; ++t)
-      p.s.nsplit[t] = has_type(c, t) ? choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), mtp::kWarps * h->num_sms,
-                                                     h->nsplit_max) : 1;
+    // the tensor-core attention runs one CTA per (sequence, KV head, split): splits for about
+    // two waves of CTAs at the number of them that fit an SM's shared memory
+    for (int t = 0; t < 2; ++t) {
+      if (!has_type(c, t)) {
+        p.s.nsplit[t] = 1;
+        continue;
+      }
+      const int d = t ? c.head_dim_full : c.head_dim_swa;
+      const int sm = mtp::att_tc_smem(d, c.n_kv_head > 0 ? c.n_head / c.n_kv_head : 0);
+      const int per_sm = sm > 0 ? (232448 / sm > 0 ? 232448 / sm : 1) : mtp::kWarps;
+      p.s.nsplit[t] = choose_nsplit(B, c.n_kv_head, attended_keys(c, kvs[t], t), 2 * per_sm * h->num_sms,
+                                    h->nsplit_max);
+    }
     return run_graph_cached(h, 5, p, st, [&](cudaStream_t s2) { return mtp::run_phases_tc_bf16(p, *h->tc, s2); });
   }
   if (path != 1) {

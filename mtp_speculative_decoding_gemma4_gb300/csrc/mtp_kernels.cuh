@@ -339,7 +339,11 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
                      nullptr)))
         return rc;
       if (l > 0) par ^= 1;
-      MTP_LAUNCH_ATT(l);
+      if (att_tc_supported(p, l)) {  // split-KV attention on tensor cores (bf16, V = K)
+        if ((rc = run_att_tc(p, l, st))) return rc;
+      } else {
+        MTP_LAUNCH_ATT(l);
+      }
       MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
       MTP_LAUNCH(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
       if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;

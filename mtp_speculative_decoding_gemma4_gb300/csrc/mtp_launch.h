@@ -70,6 +70,13 @@ struct TcPlan {
   __nv_bfloat16* xs;                         // the staging buffer
   int bp;                                    // sequences of the staged terms (multiple of 32)
 };
+// Split-KV attention of layer l on tensor cores (bf16, V = K, head_dim in {64, 128, 256, 512},
+// at most 4 query heads per KV head): one CTA per (sequence, KV head, split), partials in the
+// layout of the CUDA-core attention phase.
+bool att_tc_supported(const Params& p, int l);
+int att_tc_smem(int D, int hpg);  // shared-memory bytes of one CTA (0: no kernel for the shape)
+int run_att_tc(const Params& p, int l, cudaStream_t st);
+
 // One launch per phase with every GEMV as staging + tcgen05 GEMMs (bf16, B <= bp).
 int run_phases_tc_bf16(const Params& p, const TcPlan& plan, cudaStream_t st);
 

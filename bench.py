@@ -119,6 +119,26 @@ def ncu_traffic(kernel: str, config_index: int):
 
 
 # ---------------------------------------------------------------------------------------
+# replicas: one process per GPU, nothing exchanged on the data path
+# ---------------------------------------------------------------------------------------
+
+def max_over_ranks(values, dist, device="cuda"):
+    """Each timing's maximum over the ranks (the slowest replica bounds the job); the values
+    unchanged without a process group."""
+    if not dist:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the draft tokens of every replica over the slowest step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
+# ---------------------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------------------
 
@@ -314,10 +334,8 @@ def run_mtp(args, rank: int, world: int, dist):
         e2e_s.append(time.perf_counter() - t0)
     e2e_step = sum(e2e_s) / K
 
-    if dist:
-        t = torch.tensor([ms_per_step, e2e_step, draft_ms_mean, warm_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_step, draft_ms_mean, warm_ms = t.tolist()
+    ms_per_step, e2e_step, draft_ms_mean, warm_ms = max_over_ranks([ms_per_step, e2e_step, draft_ms_mean, warm_ms],
+                                                                    dist)
 
     if rank != 0:
         return None
@@ -325,7 +343,7 @@ def run_mtp(args, rank: int, world: int, dist):
     per_launch = alg["total"] * n
     peak, peak_src = measured_peaks()
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
-    tokens = B * n * world
+    tokens = B * n * world  # every replica drafts B * n tokens per step
     head = (3 if shape.use_ordered_embeddings else 1)
     if args.path in (2, 3, 4, 6):
         launches_per_step = 2
@@ -339,7 +357,7 @@ def run_mtp(args, rank: int, world: int, dist):
                    5: "k_tc_gemm + phase kernels (tcgen05 projections)",
                    6: "k_block_c2 (streamed-tile cluster draft block, tensor-core projections)"}[args.path]
     res = {
-        "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_tokens_per_s(B * n, world, ms_per_step), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "us_per_drafter_step": ms_per_step * 1e3 / n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",

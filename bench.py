@@ -42,6 +42,9 @@ HBM_FALLBACK_GBS = 6800.0
 # workload and algorithmic bytes
 # ---------------------------------------------------------------------------------------
 
+SPARSE_HEAD = {"auto": 0, "per-sequence": 1, "cluster-major": 2}  # enum mtp_sparse_head
+
+
 def workload(index: int):
     from mtp_synth import configs as C
     cfg = C.config(index)
@@ -93,10 +96,18 @@ def measured_peaks():
         return HBM_FALLBACK_GBS, "fallback 6.8 TB/s"
 
 
-def kernel_source_hash() -> str:
+# The device code each captured kernel is compiled from (its translation unit and the device
+# headers it includes); other kernels hash the whole csrc directory.
+KERNEL_SOURCES = {"k_block_c2": ("mtp_c2.cu", "mtp_c2.cuh", "mtp_common.cuh"),
+                  "k_block_ll": ("mtp_ll.cu", "mtp_ll.cuh", "mtp_common.cuh")}
+
+
+def kernel_source_hash(kernel: str = "") -> str:
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "mtp_speculative_decoding_gemma4_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(pkg, "*"))):
+    names = KERNEL_SOURCES.get(kernel)
+    paths = ([os.path.join(pkg, n) for n in names] if names else sorted(glob.glob(os.path.join(pkg, "*"))))
+    for p in paths:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
@@ -111,7 +122,7 @@ def ncu_traffic(kernel: str, config_index: int):
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}@config{config_index}"]
-        if e.get("source_hash") != kernel_source_hash():
+        if e.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -227,6 +238,7 @@ def run_mtp(args, rank: int, world: int, dist):
                      for k, v in L.items()} for L in w.layers]
     dr = Drafter(shape, wd, _to_dev(w.target_embed, dt, torch), max_batch=B, max_ctx=wl.ctx)
     dr.set_path(args.path)
+    dr.set_sparse_head(SPARSE_HEAD[args.sparse_head])
     d = dict(hidden=_to_dev(inp.hidden, dt, torch), last_token=_to_dev(inp.last_token, "i32", torch),
              ctx_len=_to_dev(inp.ctx_len, "i32", torch), pos=_to_dev(inp.pos, "i32", torch),
              k_swa=None if inp.k_swa is None else _to_dev(inp.k_swa, dt, torch),
@@ -364,6 +376,7 @@ def run_mtp(args, rank: int, world: int, dist):
         "config": {"workload": f"{shape.name} drafter step: B={B}, ctx {wl.ctx}, draft block {n}, then greedy "
                                f"verify of [{B},{n + 1},{shape.vocab}] bf16 target logits",
                    "batch": B, "ctx": wl.ctx, "n_draft": n, "storage": shape.dtype,
+                   "sparse_head": args.sparse_head,
                    "l2": "flushed before every timed step (256 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": ncu_traffic(kernel_name.split()[0], args.config),
@@ -476,6 +489,9 @@ def main():
                          "(one sequence), 4: cluster kernel (one sequence), 5: phase kernels with tcgen05 "
                          "projections, 6: streamed-tile cluster kernel (one sequence); default: 6 for B=1, "
                          "else 5")
+    ap.add_argument("--sparse-head", choices=sorted(SPARSE_HEAD), default="auto",
+                    help="traversal of the centroid head's candidate rows in the batched paths: per sequence, "
+                         "cluster-major (each selected cluster streamed once per step), or auto (per sequence)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

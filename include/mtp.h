@@ -56,6 +56,14 @@ enum mtp_dtype { MTP_DTYPE_BF16 = 0, MTP_DTYPE_F32 = 1 };
  * either way. */
 enum mtp_logit_mask { MTP_MASK_NEG_1E30 = 0, MTP_MASK_MIN_MINUS_ONE = 1 };
 enum mtp_layer_kind { MTP_LAYER_SLIDING = 0, MTP_LAYER_FULL = 1 };
+/* Traversal of the sparse head (the candidate-row gather and GEMV, steps 3-4 of "Gemma 4
+ * Assistant tensor inventory", "Centroid / ordered embeddings LM head"): per sequence (each
+ * sequence reads the rows of its own top_k clusters), or cluster-major (each distinct
+ * selected cluster is streamed once per step, with bulk copies, for every sequence that
+ * selected it). Both give the same selected sets and the same logits up to fp32 summation
+ * order. AUTO: per sequence (on GB300 the L2 already serves the rows that sequences share,
+ * and the per-sequence gather was the faster of the two at every batch measured). */
+enum mtp_sparse_head { MTP_HEAD_AUTO = 0, MTP_HEAD_PER_SEQUENCE = 1, MTP_HEAD_CLUSTER_MAJOR = 2 };
 
 /* Drafter hyper-parameters.
  * Cited: "Gemma 4 Multi-Token Prediction (MTP) drafter", sections "Conversion" (metadata
@@ -193,6 +201,16 @@ MTP_API int mtp_centroid_head(mtp_handle *h, const float *y, int32_t B, float *o
  * fill. Has no effect on the dense head or on mtp_draft_block (which materialises no row).
  * Errors: INVALID_ARG (NULL handle, unknown mode). */
 MTP_API int mtp_set_logit_mask(mtp_handle *h, int32_t mode);
+
+/* Select the sparse-head traversal (enum mtp_sparse_head) of mtp_draft_block's batched paths
+ * (1 and 5; the persistent path 2 always gathers per sequence) and of mtp_centroid_head on
+ * this handle; default MTP_HEAD_AUTO. Cluster-major reads the token_embd copy in
+ * token_ordering order that init makes for every centroid head, and falls back to the
+ * per-sequence gather where its shared-memory plan does not fit (about max_batch x hidden x 4
+ * bytes of y plus a 4-stage ring of 32 KB must stay under 227 KB). It changes no output beyond
+ * the fp32 summation order of a logit. No effect on the dense head or the single-sequence
+ * paths. Errors: INVALID_ARG (NULL handle, unknown mode). */
+MTP_API int mtp_set_sparse_head(mtp_handle *h, int32_t mode);
 
 /* Greedy accept-prefix verification ("Gemma 4 drafter explained", "What is Speculative
  * Decoding?"): t_i = argmax of target row i (lowest id on ties); accept_len[b] = the

@@ -22,6 +22,7 @@ struct mtp_handle {
   int num_sms;
   int path;
   int mask_mode;  // materialised rows of the centroid head: MTP_MASK_NEG_1E30 / MIN_MINUS_ONE
+  int head_mode;  // sparse head traversal: MTP_HEAD_AUTO / PER_SEQUENCE / CLUSTER_MAJOR
   int dmax;
   int nsplit_max;
   void* ws;
@@ -655,6 +656,7 @@ mtp::Params base_params(const mtp_handle* h, int B) {
   s.C = s.ordered ? c.n_centroids : 0;
   s.topk = s.ordered ? c.top_k : 0;
   s.vsc = s.ordered ? c.vocab / c.n_centroids : 0;
+  s.nsm = h->num_sms;
   s.W = c.window;
   s.d[0] = c.head_dim_swa;
   s.d[1] = c.head_dim_full;
@@ -689,7 +691,13 @@ mtp::Params base_params(const mtp_handle* h, int B) {
     P.lambda = L.layer_scalar;
     P.type = c.layer_type[l];
   }
+  p.temb_ord = h->temb_ord;
   p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  // automatic: per sequence. The rows that several sequences select are then re-read from L2
+  // rather than HBM (the step's DRAM bytes match the cluster-major traversal's), and the
+  // per-sequence gather keeps more loads in flight than the chunked cluster-major stream.
+  s.head_dd = s.ordered && h->head_mode == MTP_HEAD_CLUSTER_MAJOR &&
+              mtp::head_cm_supported(p, c.dtype == MTP_DTYPE_BF16 ? 2 : 4);
   return p;
 }
 
@@ -811,14 +819,15 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     free(h);
     return cuda_fail("clearing the workspace", e);
   }
-  if (h->cl_ok || h->c2_ok) {
-    // the cluster paths read token_embd rows in token_ordering order (one contiguous block of
-    // vocab / n_centroids rows per centroid): a copy made once here
-    const size_t bytes = static_cast<size_t>(config->vocab) * config->hidden * 2;
+  const int row_bytes = config->hidden * (config->dtype == MTP_DTYPE_BF16 ? 2 : 4);
+  if (config->use_ordered_embeddings && row_bytes % 16 == 0) {
+    // the cluster paths and the cluster-major head read token_embd rows in token_ordering
+    // order (one contiguous block of vocab / n_centroids rows per centroid): a copy made once
+    const size_t bytes = static_cast<size_t>(config->vocab) * row_bytes;
     e = cudaMalloc(&h->temb_ord, bytes);
     if (e == cudaSuccess) {
-      rc = mtp::reorder_rows(weights->token_embd, weights->token_ordering, h->temb_ord, config->vocab,
-                             config->hidden, 0);
+      rc = mtp::reorder_rows(weights->token_embd, weights->token_ordering, h->temb_ord, config->vocab, row_bytes,
+                             0);
       e = rc ? cudaErrorUnknown : cudaDeviceSynchronize();
     }
     if (e != cudaSuccess) {
@@ -827,6 +836,9 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       free(h);
       return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
     }
+  }
+  if (!h->temb_ord) h->cl_ok = h->c2_ok = 0;
+  if (h->cl_ok || h->c2_ok) {
     rc = h->cl_ok ? build_packed(h) : MTP_OK;
     if (!rc && h->c2_ok) rc = build_c2_stream(h);
     if (rc) {
@@ -1061,6 +1073,9 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
                                                      h->nsplit_max) : 1;
     const int cap = bf16 ? mtp::persistent_capacity_bf16(p, h->num_sms) : mtp::persistent_capacity_f32(p, h->num_sms);
     if (cap >= ncta) {
+      // the persistent kernel keeps the per-sequence gather: the cluster-major head reads the
+      // top-k phase's lists with bulk copies, which want a kernel boundary after those writes
+      p.s.head_dd = 0;
       return bf16 ? mtp::run_persistent_bf16(p, st) : mtp::run_persistent_f32(p, st);
     }
     if (path == 2) {
@@ -1112,6 +1127,17 @@ int mtp_set_logit_mask(mtp_handle* h, int32_t mode) {
     return MTP_ERR_INVALID_ARG;
   }
   h->mask_mode = mode;
+  return MTP_OK;
+}
+
+int mtp_set_sparse_head(mtp_handle* h, int32_t mode) {
+  mtp::g_err[0] = 0;
+  if (!h || mode < MTP_HEAD_AUTO || mode > MTP_HEAD_CLUSTER_MAJOR) {
+    set_error("need a handle and mode MTP_HEAD_AUTO (0), MTP_HEAD_PER_SEQUENCE (1) or MTP_HEAD_CLUSTER_MAJOR (2), got %d",
+              mode);
+    return MTP_ERR_INVALID_ARG;
+  }
+  h->head_mode = mode;
   return MTP_OK;
 }
 

@@ -1507,23 +1507,22 @@ int cl_capacity(int smem) {
   return n;
 }
 
-// dst[j] = src[ord[j]] for the V rows of H elements: token_embd in token_ordering order, so
-// that the rows of one centroid are one contiguous block.
-__global__ void k_reorder_rows(const __nv_bfloat16* __restrict__ src, const int* __restrict__ ord,
-                               __nv_bfloat16* __restrict__ dst, int V, int H) {
-  const int vec = H / 8;
+// dst[j] = src[ord[j]] for the V rows of row_bytes bytes (a multiple of 16): token_embd in
+// token_ordering order, so that the rows of one centroid are one contiguous block.
+__global__ void k_reorder_rows(const uint4* __restrict__ src, const int* __restrict__ ord, uint4* __restrict__ dst,
+                               int V, int vec) {
   const long long total = static_cast<long long>(V) * vec;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long row = i / vec, c = i % vec;
     const int s = ord[row];
-    reinterpret_cast<uint4*>(dst + row * H)[c] = reinterpret_cast<const uint4*>(src + static_cast<size_t>(s) * H)[c];
+    dst[row * vec + c] = src[static_cast<size_t>(s) * vec + c];
   }
 }
 
-int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaStream_t st) {
-  k_reorder_rows<<<1024, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), ord, static_cast<__nv_bfloat16*>(dst), V,
-                                       H);
+int reorder_rows(const void* src, const int* ord, void* dst, int V, int row_bytes, cudaStream_t st) {
+  k_reorder_rows<<<1024, 256, 0, st>>>(static_cast<const uint4*>(src), ord, static_cast<uint4*>(dst), V,
+                                       row_bytes / 16);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("reordering token_embd: %s", cudaGetErrorString(e));

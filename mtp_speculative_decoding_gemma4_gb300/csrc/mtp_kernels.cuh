@@ -257,6 +257,18 @@ inline int allow_smem(K kernel, int bytes) {
     }                                                                                   \
   } while (0)
 
+// The sparse head over the selected centroids: per sequence, or cluster-major (its own
+// streamed kernel, mtp_head_cm.cu).
+#define MTP_LAUNCH_GATHER()                                                            \
+  do {                                                                                  \
+    if (p.s.head_dd) {                                                                  \
+      const int rc_ = run_head_cm<WT>(p, st);                                           \
+      if (rc_) return rc_;                                                              \
+    } else {                                                                            \
+      MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);                             \
+    }                                                                                   \
+  } while (0)
+
 // Launches the attention kernel of layer l's head dim and group size on `grid` CTAs.
 template <typename WT>
 int launch_att(const Params& p, int l, int grid, cudaStream_t st) {
@@ -302,7 +314,7 @@ int run_phases(const Params& p, cudaStream_t st) {
     MTP_LAUNCH(k_head1<WT>, z.head1, z.smem_head1, p, step, par);
     if (s.ordered) {
       MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
-      MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+      MTP_LAUNCH_GATHER();
     } else {
       MTP_LAUNCH(k_dense<WT>, z.dense, z.smem_dense, p);
     }
@@ -362,7 +374,7 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
     if (s.ordered) {
       if ((rc = gemm(plan.cent, plan.xs_h, s.C, s.H, p.w.cl, s.C, nullptr, 0, nullptr))) return rc;
       MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
-      MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+      MTP_LAUNCH_GATHER();
     } else {
       if ((rc = gemm(plan.temb, plan.xs_h, s.V, s.H, nullptr, 0, nullptr, 0, p.w.best))) return rc;
     }
@@ -419,7 +431,7 @@ int run_head(const Params& p, cudaStream_t st) {
   MTP_LAUNCH(k_head_entry<WT>, z.head_entry, z.smem_head1, p);
   if (s.ordered) {
     MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
-    MTP_LAUNCH(k_gather<WT>, z.gather, z.smem_gather, p);
+    MTP_LAUNCH_GATHER();
     if (p.out_logits && p.mask_mode == MTP_MASK_MIN_MINUS_ONE) {
       MTP_LAUNCH(k_cand_min<WT>, s.B, kWarps * 4, p);
       const long long n = static_cast<long long>(s.B) * s.V;

@@ -34,6 +34,12 @@ int run_persistent_f32(const Params& p, cudaStream_t st);
 int persistent_capacity_f32(const Params& p, int num_sms);
 int run_head_f32(const Params& p, cudaStream_t st);
 
+// Cluster-major sparse head (streams each selected centroid's rows of the token_ordering-order
+// token_embd copy once per step): whether the shape and pointers allow it, and the launch.
+bool head_cm_supported(const Params& p, int elem_bytes);
+template <typename WT>
+int run_head_cm(const Params& p, cudaStream_t st);
+
 // Latency-path draft block (one sequence): shared-memory bytes it needs for these
 // parameters (0: shape not supported), co-resident capacity for that size, launch.
 int ll_smem_bytes(const ll::Params& p);
@@ -46,7 +52,7 @@ int run_ll(const ll::Params& p, int smem, cudaStream_t st);
 int cl_smem_bytes(const clk::Params& p);
 int cl_capacity(int smem);
 int run_cl(const clk::Params& p, int smem, cudaStream_t st);
-int reorder_rows(const void* src, const int* ord, void* dst, int V, int H, cudaStream_t st);
+int reorder_rows(const void* src, const int* ord, void* dst, int V, int row_bytes, cudaStream_t st);
 // Tensor-core tile packing of a [R][K] bf16 matrix for the cluster kernel (bytes, pack).
 long long packed_tile_bytes(int R, int K);
 int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);

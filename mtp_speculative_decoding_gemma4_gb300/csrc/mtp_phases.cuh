@@ -59,6 +59,8 @@ struct ShapeP {
   float theta[2];
   float eps;
   int ncta_hint;  // CTA count the work decomposition is sized for
+  int head_dd;    // sparse head cluster-major (each selected centroid's rows read once per step)
+  int nsm;        // SMs of the device
 };
 
 struct WsP {
@@ -87,6 +89,7 @@ struct Params {
   ShapeP s;
   WsP w;
   const void *pre, *post, *temb, *cent, *tgt;
+  const void* temb_ord;  // token_embd rows in token_ordering order [V][H] (cluster-major head)
   const float* out_norm;
   const int* ord;
   LayerP L[kMaxLayers];

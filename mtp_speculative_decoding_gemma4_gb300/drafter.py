@@ -111,6 +111,11 @@ class Drafter:
         binding.MASK_MIN_MINUS_ONE (smallest selected logit minus one)."""
         B.mtp_set_logit_mask(self.handle, mode)
 
+    def set_sparse_head(self, mode: int) -> None:
+        """Traversal of the centroid head's candidate rows: binding.HEAD_AUTO (default),
+        HEAD_PER_SEQUENCE, or HEAD_CLUSTER_MAJOR (each selected cluster read once per step)."""
+        B.mtp_set_sparse_head(self.handle, mode)
+
     def status(self) -> int:
         return B.mtp_get_status(self.handle)
 

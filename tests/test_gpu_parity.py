@@ -217,6 +217,66 @@ def test_centroid_head_min_minus_one_mask_matches_oracle(index):
     dr.close()
 
 
+@pytest.mark.parametrize("index,B", [(0, 5), (1, 64)])
+def test_cluster_major_head_entry_matches_oracle(index, B):
+    # the head with each selected cluster's rows read once for all sequences that chose it:
+    # same selected sets and tokens as the per-sequence traversal, logits equal up to fp32
+    # summation order, and every row against the oracle. Sequences 0..7 share one hidden
+    # state so that some clusters are listed by many sequences at once.
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
+    shape, wl, w, inp = config_data(index)
+    s, W = decoded(index)
+    rng = np.random.default_rng(25)
+    y = (rng.standard_normal((B, s.hidden)) * 0.8).astype(np.float32)
+    y[1:min(B, 8)] = y[0]
+    dr, _ = _drafter(index, max_batch=B)
+    with pytest.raises(MtpError):
+        dr.set_sparse_head(3)
+    out = {}
+    for mode in (binding.HEAD_PER_SEQUENCE, binding.HEAD_CLUSTER_MAJOR):
+        dr.set_sparse_head(mode)
+        t, lg, c = dr.centroid_head(to_torch(y, "f32"), want_logits=True, want_centroids=True)
+        torch.cuda.synchronize()
+        out[mode] = (t.cpu().numpy(), lg.cpu().numpy(), c.cpu().numpy())
+    tp, lp, cp = out[binding.HEAD_PER_SEQUENCE]
+    tok, logits, cents = out[binding.HEAD_CLUSTER_MAJOR]
+    assert np.array_equal(cp, cents)
+    fill = lp == np.float32(-1e30)
+    assert np.array_equal(fill, logits == np.float32(-1e30))
+    assert np.sum(~fill) == B * s.top_k * s.vsc
+    sel = ~fill
+    assert np.max(np.abs(lp[sel] - logits[sel])) <= 1e-5 * max(1.0, float(np.max(np.abs(lp[sel]))))
+    tol, delta = TOL[shape.dtype], NEAR_TIE[shape.dtype]
+    for b in range(B):
+        ref = O.centroid_head(s, W, y[b].astype(np.float64))
+        if not np.array_equal(cents[b], ref.selected):
+            assert ref.kth_gap < delta, (cents[b], ref.selected, ref.kth_gap)
+            continue
+        assert np.max(np.abs(logits[b][ref.ids].astype(np.float64) - ref.logits)) <= tol
+        if tok[b] != ref.token or tp[b] != tok[b]:
+            assert ref.logit_gap < delta
+    dr.close()
+
+
+@pytest.mark.parametrize("index,batch,path,mode", [(0, 5, PHASES, 2), (1, 3, TENSOR, 2), (2, 0, TENSOR, 2),
+                                                   (4, 0, TENSOR, 2), (4, 0, PHASES, 2), (4, 0, PERSISTENT, 2)])
+def test_sparse_head_traversals_in_the_draft_block(index, batch, path, mode):
+    # the cluster-major traversal (the automatic rule gathers per sequence), two steps at
+    # config 4's 64 sequences; the persistent kernel keeps the per-sequence gather whatever
+    # the mode
+    shape, wl, w, inp = config_data(index, batch)
+    n = 2 if index == 4 else wl.n_draft
+    ref = oracle_block(index, n_draft=n, batch=batch)
+    dr, d = _drafter(index, batch)
+    dr.set_sparse_head(mode)
+    tok, hid = _run_block(dr, d, n, path)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    print(f"config {index} B={tok.shape[0]} path {path} head mode {mode}: {cmp.steps_compared} steps, "
+          f"max hidden err {cmp.max_hidden_err:.3g}, near-tie divergences {cmp.tie_divergences}")
+    assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
 def test_dense_head_entry_matches_oracle():
     shape, wl, w, inp = config_data(3)
     s, W = decoded(3)

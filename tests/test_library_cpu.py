@@ -48,6 +48,8 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.mtp_verify_greedy(None, None, 1, 1, 8, None, None, None) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_set_path(None, 1) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_set_logit_mask(None, B.MASK_MIN_MINUS_ONE) == B.MTP_ERR_INVALID_ARG
+    assert lib.mtp_set_sparse_head(None, B.HEAD_CLUSTER_MAJOR) == B.MTP_ERR_INVALID_ARG
+    assert "MTP_HEAD_CLUSTER_MAJOR" in B.mtp_last_error()
     assert lib.mtp_get_status(None) == B.MTP_ERR_INVALID_ARG
     lib.mtp_destroy(None)
 

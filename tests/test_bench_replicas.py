@@ -54,3 +54,21 @@ def test_reference_arm_prints_on_rank_zero_only():
     class A:
         config, steps, warmup = 0, 1, 0
     assert bench.run_reference(A(), rank=1, world=2) is None
+
+
+def test_traffic_records_name_existing_kernel_sources():
+    # a committed DRAM-traffic figure is reported only while the hash of its kernel's own
+    # sources matches; the listed files must exist, and the hash must not depend on anything else
+    pkg = os.path.join(ROOT, "mtp_speculative_decoding_gemma4_gb300", "csrc")
+    for kernel, names in bench.KERNEL_SOURCES.items():
+        for n in names:
+            assert os.path.isfile(os.path.join(pkg, n)), (kernel, n)
+        assert bench.kernel_source_hash(kernel) == bench.kernel_source_hash(kernel)
+        assert bench.kernel_source_hash(kernel) != bench.kernel_source_hash("")
+    assert bench.ncu_traffic("no_such_kernel", 1) is None
+
+
+def test_sparse_head_switch_maps_to_the_abi_enum():
+    from mtp_speculative_decoding_gemma4_gb300 import binding as B
+    assert bench.SPARSE_HEAD == {"auto": B.HEAD_AUTO, "per-sequence": B.HEAD_PER_SEQUENCE,
+                                 "cluster-major": B.HEAD_CLUSTER_MAJOR}

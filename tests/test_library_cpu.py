@@ -28,6 +28,20 @@ def test_header_declarations_match_binding():
     assert _declared() == sorted(B.EXPORTS)
 
 
+def test_header_enum_values_match_binding():
+    # every enumerator of include/mtp.h against the binding's constant of the same value
+    with open(os.path.join(ROOT, "include", "mtp.h")) as f:
+        text = f.read()
+    enums = {}
+    for body in re.findall(r"enum \w+ \{([^}]*)\}", text):
+        for name, val in re.findall(r"(MTP_\w+)\s*=\s*(\d+)", body):
+            enums[name] = int(val)
+    assert len(enums) >= 15
+    for name, val in enums.items():
+        py = name if hasattr(B, name) else name[len("MTP_"):]
+        assert getattr(B, py) == val, name
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name

@@ -303,8 +303,8 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * about the size of all projection weights; vectors exchanged register-to-peer in
  * distributed shared memory; bf16 centroid-head shapes within its limits, V = K, 16-byte
  * aligned hidden and K rows). Automatic picks 6 for B = 1 when available, else 4, else 3;
- * 5 for B >= 2 when
- * available; else 2 when co-resident, else 1. Results agree within the precision contract.
+ * 5 for B >= 2 when available; else 2 when co-resident, else 1. Results agree within the
+ * precision contract.
  * Errors: INVALID_ARG; a forced path the call cannot use makes mtp_draft_block return
  * UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);

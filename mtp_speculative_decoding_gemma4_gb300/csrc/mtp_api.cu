@@ -42,7 +42,7 @@ struct mtp_handle {
   // streamed-tile cluster path (one sequence): availability and the packed weight streams
   int c2_ok;
   void* c2_stream;
-  // tensor-core phase path (batches of 32..64): tensor maps (64-byte aligned host memory) and
+  // tensor-core phase path (batches of 2..tc::kMaxB): tensor maps (64-byte aligned host memory) and
   // the staging buffer of the input terms
   mtp::TcPlan* tc;
   void* tc_mem;

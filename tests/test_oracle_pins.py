@@ -245,6 +245,37 @@ def test_centroid_head_recovers_planted_token():
     assert head.token in set(order[5 * s.vsc:6 * s.vsc].tolist()) and target in set(head.ids.tolist())
 
 
+def test_near_tie_gaps_are_the_decision_margins():
+    # the gaps that decide whether a GPU/oracle token difference is tolerated: top2_gap is the
+    # largest minus the second largest value (0 for a tie, inf for one value); the head's
+    # kth_gap is the k-th minus the (k+1)-th centroid logit and its logit_gap the top-2 gap of
+    # the candidate logits. Planted on a unit y so every logit is a chosen number.
+    assert O.top2_gap(np.array([3.0, 1.0, 2.0])) == 1.0
+    assert O.top2_gap(np.array([2.0, 2.0, 1.0])) == 0.0
+    assert O.top2_gap(np.array([-1.0, -4.0])) == 3.0
+    assert O.top2_gap(np.array([7.0])) == math.inf
+    s = _tiny_head_shape(V=64, Cn=8, k=3, H=4)
+    order = np.random.default_rng(4).permutation(s.vocab)
+    cent = np.zeros((s.n_centroids, s.hidden))
+    # sorted: 5, 4, 3 | 2.625, 2, ...: the k-th minus (k+1)-th gap is 0.375; the neighbouring
+    # index mistakes would give 0.625 or 1.0
+    cent[:, 0] = [1.0, 5.0, 2.625, 4.0, 0.5, 3.0, -1.0, 2.0]
+    T = np.zeros((s.vocab, s.hidden))
+    members = order.reshape(s.n_centroids, s.vsc)
+    a, b = members[3, 2], members[5, 6]
+    T[a, 0], T[b, 0] = 1.25, 1.0                              # best candidate 1.25, runner-up 1.0
+    T[members[2, 0], 0] = 9.0                                 # in an unselected cluster: ignored
+    W = O.DecodedWeights(None, None, None, T, cent, order, None, "f32")
+    y = np.array([1.0, 0.0, 0.0, 0.0])
+    head = O.centroid_head(s, W, y)
+    assert sorted(head.selected.tolist()) == [1, 3, 5] and head.selected[0] == 1
+    assert head.kth_gap == 0.375
+    assert head.token == a and head.logit_gap == 0.25
+    T[b, 0] = 1.25                                            # an exact tie: gap 0, lowest id
+    head = O.centroid_head(s, W, y)
+    assert head.logit_gap == 0.0 and head.token == min(a, b)
+
+
 def test_vocab_divisible_and_ordering_permutation():
     for cfg in C.CONFIGS:
         s = cfg.shape

@@ -701,6 +701,18 @@ mtp::Params base_params(const mtp_handle* h, int B) {
   return p;
 }
 
+// Frees every device and host allocation of a handle, also of one only partly built (its
+// fields stay NULL until allocated), and the handle itself.
+void release_handle(mtp_handle* h) {
+  if (h->ws) cudaFree(h->ws);
+  if (h->temb_ord) cudaFree(h->temb_ord);
+  if (h->wpack) cudaFree(h->wpack);
+  if (h->c2_stream) cudaFree(h->c2_stream);
+  if (h->tc_mem) cudaFree(h->tc_mem);
+  if (h->tc) free(h->tc);
+  free(h);
+}
+
 int set_device(const mtp_handle* h) {
   cudaError_t e = cudaSetDevice(h->device);
   return e == cudaSuccess ? MTP_OK : cuda_fail("cudaSetDevice", e);
@@ -808,15 +820,13 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
   layout_ws(h, static_cast<char*>(h->ws));
   rc = build_tc(h);
   if (rc) {
-    cudaFree(h->ws);
-    free(h);
+    release_handle(h);
     return rc;
   }
   e = cudaMemset(h->ws, 0, h->ws_bytes);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
-    cudaFree(h->ws);
-    free(h);
+    release_handle(h);
     return cuda_fail("clearing the workspace", e);
   }
   const int row_bytes = config->hidden * (config->dtype == MTP_DTYPE_BF16 ? 2 : 4);
@@ -831,9 +841,7 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       e = rc ? cudaErrorUnknown : cudaDeviceSynchronize();
     }
     if (e != cudaSuccess) {
-      if (h->temb_ord) cudaFree(h->temb_ord);
-      cudaFree(h->ws);
-      free(h);
+      release_handle(h);
       return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
     }
   }
@@ -842,10 +850,7 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     rc = h->cl_ok ? build_packed(h) : MTP_OK;
     if (!rc && h->c2_ok) rc = build_c2_stream(h);
     if (rc) {
-      if (h->wpack) cudaFree(h->wpack);
-      cudaFree(h->temb_ord);
-      cudaFree(h->ws);
-      free(h);
+      release_handle(h);
       return rc;
     }
   }
@@ -1210,17 +1215,11 @@ void mtp_destroy(mtp_handle* h) {
   if (!h) return;
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
-  cudaFree(h->ws);
-  if (h->temb_ord) cudaFree(h->temb_ord);
-  if (h->wpack) cudaFree(h->wpack);
-  if (h->c2_stream) cudaFree(h->c2_stream);
   if (h->gc.valid) cudaGraphExecDestroy(h->gc.exec);
   if (h->gc.ev_in) cudaEventDestroy(h->gc.ev_in);
   if (h->gc.ev_out) cudaEventDestroy(h->gc.ev_out);
   if (h->gc.cs) cudaStreamDestroy(h->gc.cs);
-  if (h->tc_mem) cudaFree(h->tc_mem);
-  if (h->tc) free(h->tc);
-  free(h);
+  release_handle(h);
 }
 
 }  // extern "C"

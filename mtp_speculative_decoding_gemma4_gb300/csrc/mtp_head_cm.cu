@@ -15,8 +15,9 @@
 // lists, for each of its centroids, the sequences that chose it. One CTA per SM; y of the whole
 // batch arrives by one more bulk copy. 8 warps score 8-row batches of a chunk (a lane holds
 // one 16-byte slice of every row; a reduce-scatter over the lanes leaves row (lane >> 2) & 7's
-// logit in lanes 4r..4r+3), and the best (logit, id) key of every listed sequence is reduced in
-// shared memory per centroid before one atomicMax into the step's per-sequence key.
+// logit in lanes 4r..4r+3). The best (logit, id) key of every listed sequence is reduced per
+// centroid (a warp maximum, then one shared atomicMax per warp) before one atomicMax into the
+// step's per-sequence key.
 //
 // Failure handling: a wait on a bulk copy gives up after spin_limit cycles, records
 // MTP_ERR_TIMEOUT in the status word, waits (bounded) for the copies still in flight and

@@ -4,8 +4,7 @@ runs entirely in libmtp.so.
 """
 from __future__ import annotations
 
-import ctypes
-from typing import Optional, Sequence
+from typing import Optional
 
 import torch
 

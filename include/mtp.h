@@ -287,6 +287,16 @@ MTP_API int mtp_centroid_head_noalloc(const float *y, const void *centroids, con
  * a pending CUDA error as MTP_ERR_CUDA. */
 MTP_API int mtp_get_status(mtp_handle *h);
 
+/* Testing only: failure injection on the host side of a device wait. With
+ * skip_arrival_cta >= 0, that CTA of the persistent draft-block kernel (path 2) does not
+ * arrive at the first grid barrier of the next launches; every CTA's bounded wait then
+ * gives up, the call's status word reads MTP_ERR_TIMEOUT (mtp_get_status), the kernel
+ * returns early without a fault, and the handle stays usable. spin_limit_cycles > 0 replaces
+ * the bound of the device waits of the phase and persistent paths (default about 2 s of
+ * clock64 cycles). (-1, 0) restores the defaults. No other path is affected.
+ * Errors: INVALID_ARG (NULL handle, skip_arrival_cta < -1, spin_limit_cycles < 0). */
+MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_limit_cycles);
+
 /* Select the implementation of mtp_draft_block: 0 = automatic, 1 = one kernel per phase,
  * 2 = persistent whole-block kernel with grid barriers, 3 = latency kernel for one sequence
  * (weights and attended K resident in shared memory, CTAs exchanging vectors through

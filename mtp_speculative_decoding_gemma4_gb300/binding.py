@@ -19,7 +19,7 @@ MTP_LAYER_SLIDING, MTP_LAYER_FULL = 0, 1
 # Every symbol include/mtp.h declares.
 EXPORTS = ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy", "mtp_get_status",
            "mtp_set_path", "mtp_destroy", "mtp_last_error", "mtp_centroid_head_noalloc", "mtp_set_logit_mask",
-           "mtp_verify_sample", "mtp_set_sparse_head")
+           "mtp_verify_sample", "mtp_set_sparse_head", "mtp_set_debug")
 MASK_NEG_1E30, MASK_MIN_MINUS_ONE = 0, 1  # enum mtp_logit_mask
 HEAD_AUTO, HEAD_PER_SEQUENCE, HEAD_CLUSTER_MAJOR = 0, 1, 2  # enum mtp_sparse_head
 
@@ -81,13 +81,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mtp_set_path.argtypes = [vp, i32]
     lib.mtp_set_logit_mask.argtypes = [vp, i32]
     lib.mtp_set_sparse_head.argtypes = [vp, i32]
+    lib.mtp_set_debug.argtypes = [vp, i32, ctypes.c_int64]
     lib.mtp_destroy.argtypes = [vp]
     lib.mtp_destroy.restype = None
     lib.mtp_last_error.argtypes = []
     lib.mtp_last_error.restype = ctypes.c_char_p
     for name in ("mtp_init_weights", "mtp_draft_block", "mtp_centroid_head", "mtp_verify_greedy",
                  "mtp_get_status", "mtp_set_path", "mtp_centroid_head_noalloc", "mtp_set_logit_mask",
-                 "mtp_verify_sample", "mtp_set_sparse_head"):
+                 "mtp_verify_sample", "mtp_set_sparse_head", "mtp_set_debug"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -162,6 +163,10 @@ def mtp_set_logit_mask(handle: int, mode: int) -> None:
 
 def mtp_set_sparse_head(handle: int, mode: int) -> None:
     _check(load_library().mtp_set_sparse_head(handle, mode), "mtp_set_sparse_head")
+
+
+def mtp_set_debug(handle: int, skip_arrival_cta: int, spin_limit_cycles: int) -> None:
+    _check(load_library().mtp_set_debug(handle, skip_arrival_cta, spin_limit_cycles), "mtp_set_debug")
 
 
 def mtp_destroy(handle: int) -> None:

@@ -23,6 +23,10 @@ struct mtp_handle {
   int path;
   int mask_mode;  // materialised rows of the centroid head: MTP_MASK_NEG_1E30 / MIN_MINUS_ONE
   int head_mode;  // sparse head traversal: MTP_HEAD_AUTO / PER_SEQUENCE / CLUSTER_MAJOR
+  // testing only (mtp_set_debug): a CTA that skips its first grid-barrier arrival, and a
+  // shorter bound for device waits (0: the defaults)
+  int dbg_skip;
+  long long dbg_spin;
   int dmax;
   int nsplit_max;
   void* ws;
@@ -692,7 +696,8 @@ mtp::Params base_params(const mtp_handle* h, int B) {
     P.type = c.layer_type[l];
   }
   p.temb_ord = h->temb_ord;
-  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  p.spin_limit = h->dbg_spin > 0 ? h->dbg_spin : 4000000000LL;  // ~2 s at 2 GHz
+  p.dbg_skip = h->dbg_skip;
   // automatic: per sequence. The rows that several sequences select are then re-read from L2
   // rather than HBM (the step's DRAM bytes match the cluster-major traversal's), and the
   // per-sequence gather keeps more loads in flight than the chunked cluster-major stream.
@@ -1143,6 +1148,17 @@ int mtp_set_sparse_head(mtp_handle* h, int32_t mode) {
     return MTP_ERR_INVALID_ARG;
   }
   h->head_mode = mode;
+  return MTP_OK;
+}
+
+int mtp_set_debug(mtp_handle* h, int32_t skip_arrival_cta, int64_t spin_limit_cycles) {
+  mtp::g_err[0] = 0;
+  if (!h || skip_arrival_cta < -1 || spin_limit_cycles < 0) {
+    set_error("need a handle, skip_arrival_cta >= -1 and spin_limit_cycles >= 0");
+    return MTP_ERR_INVALID_ARG;
+  }
+  h->dbg_skip = skip_arrival_cta + 1;
+  h->dbg_spin = spin_limit_cycles;
   return MTP_OK;
 }
 

@@ -29,7 +29,7 @@ __device__ inline bool grid_sync(const Params& p, unsigned int& epoch) {
   if (threadIdx.x == 0) {
     const unsigned int target = epoch * gridDim.x;
     __threadfence();
-    atomicAdd(p.w.bar, 1u);
+    if (p.dbg_skip == 0 || epoch != 1u || static_cast<int>(blockIdx.x) != p.dbg_skip - 1) atomicAdd(p.w.bar, 1u);
     const long long t0 = clock64();
     int good = 1;
     while (ld_acquire_u32(p.w.bar) < target) {

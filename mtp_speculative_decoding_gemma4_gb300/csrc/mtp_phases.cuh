@@ -105,6 +105,8 @@ struct Params {
   int* out_centroids;  // head entry: [B][topk] or null
   int mask_mode;       // head entry: unselected logits -1e30 (MTP_MASK_NEG_1E30) or min - 1
   long long spin_limit;  // bounded grid-barrier wait (clock64 cycles)
+  int dbg_skip;          // testing only: CTA dbg_skip - 1 of the persistent kernel does not
+                         // arrive at its first grid barrier, so that barrier times out (0: off)
   // Tensor-core path: when set, a GEMV phase only stages its inputs and writes them as three
   // bf16 terms [3][tc_bp][K_in] (hi, mid, lo of every fp32 input) for the tcgen05 GEMMs.
   __nv_bfloat16* tc_xs;

@@ -115,6 +115,11 @@ class Drafter:
         HEAD_PER_SEQUENCE, or HEAD_CLUSTER_MAJOR (each selected cluster read once per step)."""
         B.mtp_set_sparse_head(self.handle, mode)
 
+    def set_debug(self, skip_arrival_cta: int = -1, spin_limit_cycles: int = 0) -> None:
+        """Testing only: make one CTA of the persistent kernel miss its first grid-barrier
+        arrival (the bounded waits then report MTP_ERR_TIMEOUT) and / or shorten the wait bound."""
+        B.mtp_set_debug(self.handle, skip_arrival_cta, spin_limit_cycles)
+
     def status(self) -> int:
         return B.mtp_get_status(self.handle)
 

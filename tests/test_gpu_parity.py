@@ -2,6 +2,8 @@
 inputs: every benchmark configuration at full size, both implementations of the draft
 block (one launch per phase, and the persistent kernel), the head entry point, greedy
 verification and the edge cases."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -274,6 +276,29 @@ def test_sparse_head_traversals_in_the_draft_block(index, batch, path, mode):
     print(f"config {index} B={tok.shape[0]} path {path} head mode {mode}: {cmp.steps_compared} steps, "
           f"max hidden err {cmp.max_hidden_err:.3g}, near-tie divergences {cmp.tie_divergences}")
     assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
+@pytest.mark.skipif(os.environ.get("MTP_FAULT_TESTS") != "1",
+                    reason="device-timeout injection runs only with MTP_FAULT_TESTS=1")
+def test_a_missing_grid_barrier_arrival_times_out_and_the_handle_recovers():
+    # failure detection without a fault: CTA 0 of the persistent kernel skips its first
+    # grid-barrier arrival, every bounded wait gives up after ~10 ms of cycles, the status
+    # word reads MTP_ERR_TIMEOUT, and the next call on the same handle is correct again
+    from mtp_speculative_decoding_gemma4_gb300 import binding
+    shape, wl, w, inp = config_data(0, 3)
+    ref = oracle_block(0, batch=3)
+    dr, d = _drafter(0, 3)
+    dr.set_path(PERSISTENT)
+    dr.set_debug(skip_arrival_cta=0, spin_limit_cycles=20_000_000)
+    dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], wl.n_draft)
+    torch.cuda.synchronize()
+    assert dr.status() == binding.MTP_ERR_TIMEOUT
+    assert dr.status() == binding.MTP_OK  # reading the word cleared it
+    dr.set_debug()
+    tok, hid = _run_block(dr, d, wl.n_draft, PERSISTENT)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    assert len(cmp.tie_divergences) <= 1
     dr.close()
 
 

@@ -64,6 +64,7 @@ def test_null_arguments_are_rejected_without_a_device(lib):
     assert lib.mtp_set_logit_mask(None, B.MASK_MIN_MINUS_ONE) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_set_sparse_head(None, B.HEAD_CLUSTER_MAJOR) == B.MTP_ERR_INVALID_ARG
     assert "MTP_HEAD_CLUSTER_MAJOR" in B.mtp_last_error()
+    assert lib.mtp_set_debug(None, -1, 0) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_get_status(None) == B.MTP_ERR_INVALID_ARG
     lib.mtp_destroy(None)
 

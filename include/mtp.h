@@ -14,11 +14,13 @@
  *   - Return value: MTP_OK or an MTP_ERR_* code; on error nothing was enqueued and
  *     mtp_last_error() describes the cause (per calling thread).
  *
- * Precision contract (both this library and its CPU oracle): stored tensors are bf16 (or
- * fp32 for fp32 models), activations fp32, every vector entering a projection is rounded
- * to bf16 (bf16 models), the post-projected hidden state fed to the next draft step is
- * rounded to the model dtype, top-k / argmax decide on fp32 values with ties going to
- * the lower centroid index / lower vocabulary id.
+ * Precision contract (both this library and its CPU oracle): stored tensors (weights,
+ * shared K, embedding tables, the caller's hidden state, target logits) are bf16, or fp32
+ * for fp32 models. Activations are fp32 and are never rounded to a narrower type: no
+ * projection input, attention operand or intermediate vector is rounded to bf16, and the
+ * post-projected hidden state carried to the next draft step stays fp32 (unrounded).
+ * Top-k and argmax decide on fp32 values, ties going to the lower centroid index / lower
+ * vocabulary id.
  */
 #ifndef MTP_H_
 #define MTP_H_
@@ -156,8 +158,8 @@ MTP_API int mtp_init_weights(const mtp_config *config, const mtp_weights *weight
 
 /* Run a draft block: n_draft drafter steps for B independent sequences.
  * Step 1 consumes hidden[b] (the target's last hidden state) and last_token[b]; step i+1
- * consumes step i's greedy token and its post-projected hidden state rounded to the
- * model dtype ("Gemma 4 Assistant 使用指南", section 二.3; "Gemma 4 drafter explained",
+ * consumes step i's greedy token and its post-projected hidden state, kept in fp32 without
+ * rounding ("Gemma 4 Assistant 使用指南", section 二.3; "Gemma 4 drafter explained",
  * "Target Activations"). Each step: pre_projection of [hidden ; embed(token)], every block
  * (norm, Q projection, q_norm, RoPE at pos[b], attention over the shared K of the block's
  * type -- sliding blocks attend the last `window` keys, full blocks all ctx_len[b] keys --,
@@ -185,7 +187,7 @@ MTP_API int mtp_draft_block(mtp_handle *h, const void *hidden, const int32_t *la
  * and -- when out_logits != NULL -- the full row filled with -1e30f with the sparse logits
  * scattered at their ids (or the other mask of mtp_set_logit_mask). Dense head
  * (use_ordered_embeddings == 0): all V logits.
- *   y             device [B][H] fp32 (rounded to bf16 inside for bf16 models)
+ *   y             device [B][H] fp32, used as given (never rounded to bf16)
  *   out_logits    device [B][V] fp32 or NULL
  *   out_token     device [B] int32 (argmax, lowest id on ties)
  *   out_centroids device [B][top_k] int32 selected centroids, best first (ties: lower
@@ -261,7 +263,9 @@ MTP_API int mtp_verify_sample(const void *target_logits, const int32_t *draft, i
  * a library convenience. It needs no handle (creating one allocates a workspace): the head's
  * tensors are passed directly, and its scratch lives in a fixed device array of
  * MTP_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the process exits.
- * Results equal mtp_centroid_head's on the same tensors.
+ * Results equal mtp_centroid_head's on the same tensors. token_ordering is not validated
+ * here (mtp_init_weights checks it is a permutation; this entry has no handle): a candidate
+ * whose id lies outside [0, vocab) is skipped, neither read nor written.
  *   y              device [B][hidden] fp32 final-normed hidden states
  *   centroids      device [n_centroids][hidden], dtype (MTP_DTYPE_BF16 or MTP_DTYPE_F32)
  *   token_ordering device [vocab] int32, a permutation viewed [n_centroids][vocab/n_centroids]

@@ -1,5 +1,5 @@
 // Device helpers shared by the libmtp kernels: vector loads of bf16 / fp32 rows,
-// operand rounding, warp and block reductions, and order-preserving (value, id) keys for
+// element conversions, warp and block reductions, and order-preserving (value, id) keys for
 // argmax / top-k with lowest-id tie-breaking.
 #pragma once
 
@@ -18,7 +18,7 @@ template <typename T> struct Elem;
 template <> struct Elem<__nv_bfloat16> {
   static constexpr int kVec = 8;  // elements per 16-byte load
   __device__ static inline float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
-  // Operand rounding of the precision contract: fp32 -> bf16, round to nearest even.
+  // fp32 -> bf16, round to nearest even (storage conversion; activations stay fp32).
   __device__ static inline __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 template <> struct Elem<float> {
@@ -27,8 +27,6 @@ template <> struct Elem<float> {
   __device__ static inline float from_f(float v) { return v; }
 };
 
-// Round an fp32 value the way a projection operand of model dtype T is stored.
-template <typename T> __device__ inline float round_op(float v) { return Elem<T>::to_f(Elem<T>::from_f(v)); }
 
 // 16-byte vector load of kVec elements, converted to fp32.
 __device__ inline void load_vec(const __nv_bfloat16* p, float* out) {

@@ -60,6 +60,7 @@ extern "C" MTP_API int mtp_centroid_head_noalloc(const float* y, const void* cen
                                                  int32_t dtype, int32_t B, int32_t hidden, int32_t n_centroids,
                                                  int32_t top_k, int32_t vocab, float* out_logits,
                                                  int32_t* out_token, int32_t* out_centroids, void* stream) {
+  mtp::set_error("%s", "");
   if (!y || !centroids || !token_ordering || !token_embd || !out_token) {
     mtp::set_error("y, centroids, token_ordering, token_embd and out_token must be non-NULL");
     return MTP_ERR_INVALID_ARG;
@@ -134,6 +135,10 @@ extern "C" MTP_API int mtp_centroid_head_noalloc(const float* y, const void* cen
   p.out_logits = out_logits;
   p.out_tokens = out_token;
   p.out_centroids = out_centroids;
+  // token_ordering is not validated here (a permutation check would need scratch of V
+  // entries): the gather skips any id outside [0, vocab) instead of reading or writing out
+  // of bounds
+  p.check_ids = 1;
   // the argmax keys must start at zero: the head-entry phase clears them before use
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return dtype == MTP_DTYPE_BF16 ? mtp::run_head_bf16(p, st) : mtp::run_head_f32(p, st);

@@ -23,6 +23,8 @@
 //   DENSE  (dense tied head) logits over all rows of token_embd + argmax
 #pragma once
 
+#include <cstddef>
+
 #include "mtp_common.cuh"
 #include "mtp.h"
 
@@ -49,6 +51,7 @@ struct KvP {
   const int* ctx_len;
   long long sb, st;
   int max_ctx;
+  int pad_;  // explicit: Params is compared bytewise by the graph cache
 };
 
 struct ShapeP {
@@ -61,6 +64,7 @@ struct ShapeP {
   int ncta_hint;  // CTA count the work decomposition is sized for
   int head_dd;    // sparse head cluster-major (each selected centroid's rows read once per step)
   int nsm;        // SMs of the device
+  int pad_;       // explicit: Params is compared bytewise by the graph cache
 };
 
 struct WsP {
@@ -100,18 +104,31 @@ struct Params {
   int* out_tokens;     // [B][n_draft] (draft block) or [B] (head entry)
   float* out_hidden;   // [B][n_draft][bb] or null
   int n_draft;
+  int pad0_;
   const float* y_in;   // head entry: [B][H]
   float* out_logits;   // head entry: [B][V] or null
   int* out_centroids;  // head entry: [B][topk] or null
   int mask_mode;       // head entry: unselected logits -1e30 (MTP_MASK_NEG_1E30) or min - 1
+  int check_ids;       // head entry: skip candidate rows whose token_ordering id is outside
+                       // [0, V) (the allocation-free entry, whose ordering is not validated)
   long long spin_limit;  // bounded grid-barrier wait (clock64 cycles)
   int dbg_skip;          // testing only: CTA dbg_skip - 1 of the persistent kernel does not
                          // arrive at its first grid barrier, so that barrier times out (0: off)
+  int pad1_;
   // Tensor-core path: when set, a GEMV phase only stages its inputs and writes them as three
   // bf16 terms [3][tc_bp][K_in] (hi, mid, lo of every fp32 input) for the tcgen05 GEMMs.
   __nv_bfloat16* tc_xs;
   int tc_bp;
+  int pad2_;
 };
+// The graph cache compares whole Params objects with memcmp: no member may be followed by
+// compiler padding, whose bytes a copy need not preserve.
+static_assert(sizeof(KvP) == 3 * sizeof(void*) + 2 * sizeof(long long) + 2 * sizeof(int), "KvP padding");
+static_assert(sizeof(ShapeP) % 8 == 0 && offsetof(Params, w) == sizeof(ShapeP), "ShapeP padding");
+static_assert(offsetof(Params, y_in) == offsetof(Params, n_draft) + 8, "Params padding after n_draft");
+static_assert(offsetof(Params, spin_limit) == offsetof(Params, mask_mode) + 8, "Params padding after mask_mode");
+static_assert(offsetof(Params, tc_xs) == offsetof(Params, dbg_skip) + 8, "Params padding after dbg_skip");
+static_assert(sizeof(Params) == offsetof(Params, tc_bp) + 8, "Params trailing padding");
 
 // ---------------------------------------------------------------- GEMV machinery
 
@@ -1003,7 +1020,11 @@ __device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
       const bool valid = cand < ncand;
       const int cc = valid ? cand : c0;  // rows past the end re-read the first one
       const int cent = p.w.sel[b * p.s.topk + cc / vsc];
-      const int id = p.ord[cent * vsc + cc % vsc];
+      const int id_raw = p.ord[cent * vsc + cc % vsc];
+      // the allocation-free entry does not validate the ordering: an id outside [0, V) is
+      // skipped (row 0 is read in its place and its logit discarded)
+      const bool id_ok = !p.check_ids || static_cast<unsigned>(id_raw) < static_cast<unsigned>(p.s.V);
+      const int id = id_ok ? id_raw : 0;
       float sc[32];
 #pragma unroll
       for (int r = 0; r < 32; ++r) sc[r] = 0.f;
@@ -1024,7 +1045,7 @@ __device__ void phase_gather(const Params& p, int cta, int ncta, char* smem) {
         }
       }
       reduce_scatter<32, 16>(sc, lane);  // lane i: the logit of candidate c0 + i
-      if (valid) {
+      if (valid && id_ok) {
         if (p.out_logits) p.out_logits[static_cast<size_t>(b) * p.s.V + id] = sc[0];
         best = argmax_key(sc[0], id);
       }

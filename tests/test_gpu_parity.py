@@ -2,8 +2,6 @@
 inputs: every benchmark configuration at full size, both implementations of the draft
 block (one launch per phase, and the persistent kernel), the head entry point, greedy
 verification and the edge cases."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -105,6 +103,38 @@ def test_one_sequence_path_short_and_window_edge_contexts(ctx, n_kv, path):
     d = inputs_to_device(inp, "bf16")
     tok, hid = _run_block(dr, d, 4, path)
     compare_block(tok, hid, ref, "bf16")
+    dr.close()
+
+
+def _one_sequence_case(index, ctx_len, storage_ctx, n_draft, seed_offset=0):
+    """B = 1 inputs of configuration `index`'s shape (its seeded weights) at an explicit
+    context length, with K stored for storage_ctx keys (NaN beyond ctx_len)."""
+    shape, wl, w, _ = config_data(index)
+    wl1 = C.Workload(batch=1, ctx=storage_ctx, n_draft=n_draft, seed=wl.seed + seed_offset)
+    inp = G.make_step_inputs(shape, wl1, wl1.seed, ctx_len=np.array([ctx_len], dtype=np.int32))
+    s, W = decoded(index)
+    ref = O.draft_block(s, W, inp.hidden, inp.last_token, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, n_draft)
+    return shape, w, inp, ref
+
+
+@pytest.mark.parametrize("path", [0, STREAMED])
+@pytest.mark.parametrize("index,ctx,storage", [
+    (2, 32768, 32768),   # E4B backbone at the longest context of its workload
+    (2, 20001, 32768),   # E4B, ragged: not a multiple of the 128-key attention chunk
+    (1, 511, 1024),      # E2B, one key short of the sliding window
+    (1, 512, 1024),      # E2B, exactly the window
+    (1, 513, 1024),      # E2B, one key past the window (the sliding layers drop key 0)
+])
+def test_one_sequence_path_long_ragged_and_window_contexts(index, ctx, storage, path):
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape, w, inp, ref = _one_sequence_case(index, ctx, storage, 4)
+    wd, tgt = weights_to_device(w)
+    dr = Drafter(shape, wd, tgt, max_batch=1, max_ctx=storage)
+    d = inputs_to_device(inp, shape.dtype)
+    tok, hid = _run_block(dr, d, 4, path)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    print(f"config {index} ctx {ctx} path {path}: max hidden err {cmp.max_hidden_err:.3g}, "
+          f"near-ties {cmp.tie_divergences}")
     dr.close()
 
 
@@ -279,8 +309,6 @@ def test_sparse_head_traversals_in_the_draft_block(index, batch, path, mode):
     dr.close()
 
 
-@pytest.mark.skipif(os.environ.get("MTP_FAULT_TESTS") != "1",
-                    reason="device-timeout injection runs only with MTP_FAULT_TESTS=1")
 def test_a_missing_grid_barrier_arrival_times_out_and_the_handle_recovers():
     # failure detection without a fault: CTA 0 of the persistent kernel skips its first
     # grid-barrier arrival, every bounded wait gives up after ~10 ms of cycles, the status
@@ -484,48 +512,42 @@ def test_verify_rejects_bad_vocab():
 
 # ------------------------------------------------------------------ draft + verify loop
 
-def _loop(dr, d, shape, wl, rounds, seed, gpu=True):
-    """Draft+verify rounds against the planted synthetic target; returns per-round
-    (drafts, accept_len, out_tokens). The GPU side runs the library; the oracle side the
-    oracle, each from its own drafts."""
+def _planted(base, drafts, agree, alt_raw, V):
+    """The round's target logits: the base logits with each row's +16 maximum planted."""
+    B, n1 = drafts.shape[0], drafts.shape[1] + 1
+    tgt = G.planted_targets(drafts, agree, alt_raw, V)
+    planted = base.copy()
+    planted[np.arange(B)[:, None], np.arange(n1)[None, :], tgt] = G.bf16_bits(np.float32([G.PLANT_VALUE]))[0]
+    return tgt, planted
+
+
+def _loop(dr, d, shape, wl, rounds, seed):
+    """Draft+verify rounds of the library against the planted synthetic target; returns per
+    round (input tokens, drafts, accept_len, out_tokens). Round r > 0 starts from the
+    pregenerated hidden state of round r - 1 and the token emitted after the accepted prefix."""
     B, n, V = wl.batch, wl.n_draft, shape.vocab
     base = G.base_target_logits(B, n + 1, V, seed)
     hist = []
-    if gpu:
-        logits_dev = to_torch(base, "bf16")
-        hidden, tok = d["hidden"], d["last_token"]
-    else:
-        s, W = decoded(4)
-        hidden = config_data(4)[3].hidden
-        tok = config_data(4)[3].last_token
-        inp = config_data(4)[3]
+    logits_dev = to_torch(base, "bf16")
+    hidden, tok = d["hidden"], d["last_token"]
     for r in range(rounds):
         agree, alt_raw = G.round_tables(B, n, V, wl.agree_p, seed, r)
-        if gpu:
-            drafts, _ = dr.draft_block(hidden, tok, d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], n,
-                                       want_hidden=False)
-            dnp = drafts.cpu().numpy()
-            tgt = G.planted_targets(dnp, agree, alt_raw, V)
-            idx = torch.from_numpy(tgt).cuda()
-            bi = torch.arange(B, device="cuda")[:, None]
-            ri = torch.arange(n + 1, device="cuda")[None, :]
-            saved = logits_dev[bi, ri, idx].clone()
-            logits_dev[bi, ri, idx] = G.PLANT_VALUE
-            acc, out = verify_greedy_(logits_dev, drafts)
-            logits_dev[bi, ri, idx] = saved
-            a, o = acc.cpu().numpy(), out.cpu().numpy()
-            hidden = to_torch(G.next_round_hidden(B, shape.backbone, seed, r), "bf16")
-            tok = out[torch.arange(B, device="cuda"), acc.long()].contiguous()
-        else:
-            blk = O.draft_block(s, W, hidden, tok, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, n)
-            dnp = blk.tokens
-            tgt = G.planted_targets(dnp, agree, alt_raw, V)
-            planted = base.copy()
-            planted[np.arange(B)[:, None], np.arange(n + 1)[None, :], tgt] = G.bf16_bits(np.float32([G.PLANT_VALUE]))[0]
-            a, o = O.verify_greedy(planted, dnp)
-            hidden = G.next_round_hidden(B, shape.backbone, seed, r)
-            tok = o[np.arange(B), a].astype(np.int32)
-        hist.append((dnp.copy(), a.copy(), o.copy()))
+        tok_in = tok.cpu().numpy().copy()
+        drafts, _ = dr.draft_block(hidden, tok, d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], n,
+                                   want_hidden=False)
+        dnp = drafts.cpu().numpy()
+        tgt = G.planted_targets(dnp, agree, alt_raw, V)
+        idx = torch.from_numpy(tgt).cuda()
+        bi = torch.arange(B, device="cuda")[:, None]
+        ri = torch.arange(n + 1, device="cuda")[None, :]
+        saved = logits_dev[bi, ri, idx].clone()
+        logits_dev[bi, ri, idx] = G.PLANT_VALUE
+        acc, out = verify_greedy_(logits_dev, drafts)
+        logits_dev[bi, ri, idx] = saved
+        a, o = acc.cpu().numpy(), out.cpu().numpy()
+        hidden = to_torch(G.next_round_hidden(B, shape.backbone, seed, r), "bf16")
+        tok = out[torch.arange(B, device="cuda"), acc.long()].contiguous()
+        hist.append((tok_in, dnp.copy(), a.copy(), o.copy()))
     return hist
 
 
@@ -534,17 +556,38 @@ def verify_greedy_(logits, drafts):
     return verify_greedy(logits, drafts)
 
 
-def test_draft_verify_loop_matches_oracle_for_first_rounds():
+LOOP_ROUNDS_CHECKED = 10
+
+
+@pytest.mark.parametrize("path", [0, PERSISTENT])
+def test_draft_verify_loop_matches_oracle_round_by_round(path):
+    # The loop workload (E2B, B=64, draft block 8) for 10 rounds. Each round the oracle drafts
+    # from the same inputs the library used (teacher forcing: the library's carried token),
+    # so a near-tie divergence in one round does not desynchronise later rounds. Every
+    # drafted token must equal the oracle's unless the oracle's own margin at that step is
+    # below the near-tie bound (per sequence, through compare_block); verification of the
+    # library's drafts against the same planted target is bit-exact.
     shape, wl, w, inp = config_data(4)
+    s, W = decoded(4)
     dr, d = _drafter(4)
-    dr.set_path(PERSISTENT)
-    g = _loop(dr, d, shape, wl, rounds=2, seed=wl.seed)
-    o = _loop(None, None, shape, wl, rounds=2, seed=wl.seed, gpu=False)
-    for r, ((gd, ga, go), (od, oa, oo)) in enumerate(zip(g, o)):
-        same = np.all(gd == od, axis=1)
-        assert same.mean() >= 0.95, f"round {r}: only {same.mean():.2f} of sequences drafted identically"
-        np.testing.assert_array_equal(ga[same], oa[same])
-        np.testing.assert_array_equal(go[same], oo[same])
+    dr.set_path(path)
+    B, n, V = wl.batch, wl.n_draft, shape.vocab
+    g = _loop(dr, d, shape, wl, rounds=LOOP_ROUNDS_CHECKED, seed=wl.seed)
+    base = G.base_target_logits(B, n + 1, V, wl.seed)
+    ties, compared = [], 0
+    for r, (tok_in, gd, ga, go) in enumerate(g):
+        hidden = inp.hidden if r == 0 else G.next_round_hidden(B, shape.backbone, wl.seed, r - 1)
+        ref = O.draft_block(s, W, hidden, tok_in, inp.k_swa, inp.k_full, inp.ctx_len, inp.pos, n)
+        cmp = compare_block(gd, None, ref, shape.dtype)
+        compared += cmp.steps_compared
+        ties += [(r,) + t for t in cmp.tie_divergences]
+        agree, alt_raw = G.round_tables(B, n, V, wl.agree_p, wl.seed, r)
+        _, planted = _planted(base, gd, agree, alt_raw, V)
+        oa, oo = O.verify_greedy(planted, gd)
+        np.testing.assert_array_equal(ga, oa, err_msg=f"accept lengths of round {r}")
+        np.testing.assert_array_equal(go, oo, err_msg=f"emitted tokens of round {r}")
+    print(f"path {path}: {LOOP_ROUNDS_CHECKED} rounds x {B} sequences, {compared} draft steps compared, "
+          f"near-tie divergences (round, sequence, step, oracle margin): {ties}")
     dr.close()
 
 
@@ -555,12 +598,12 @@ def test_draft_verify_loop_accept_length_statistics():
     dr, d = _drafter(4)
     dr.set_path(PERSISTENT)
     g = _loop(dr, d, shape, wl, rounds=wl.rounds, seed=wl.seed)
-    acc = np.concatenate([a for _, a, _ in g]).astype(np.float64)
+    acc = np.concatenate([a for _, _, a, _ in g]).astype(np.float64)
     mean, sd = expected_accept(wl.agree_p, wl.n_draft)
     print(f"mean accept length {acc.mean():.4f} (expected {mean:.4f}) over {acc.size} sequence-rounds")
     assert abs(acc.mean() - mean) < 3 * sd / np.sqrt(acc.size)
     # every output row holds accept_len drafts then the target token, then -1 padding
-    for dn, a, o in g[:50]:
+    for _, dn, a, o in g[:50]:
         for b in range(wl.batch):
             assert np.array_equal(o[b, :a[b]], dn[b, :a[b]])
             assert o[b, a[b]] >= 0 and np.all(o[b, a[b] + 1:] == -1)

@@ -130,3 +130,20 @@ def test_verify_sample_rejects_bad_arguments_before_the_device(lib):
                                  None) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_verify_sample(fake, None, 1, 2, 16, f(1.0), fake, fake, fake, fake, None) == B.MTP_ERR_INVALID_ARG
     assert lib.mtp_verify_sample(fake, fake, 1, 1, 16, f(1.0), fake, None, fake, fake, None) == B.MTP_ERR_INVALID_ARG
+
+
+def test_header_states_the_wide_activation_contract():
+    # the boundary documents what the kernels and the oracle do: activations stay fp32 with
+    # no intermediate rounding, and the carried hidden state is not rounded
+    with open(os.path.join(ROOT, "include", "mtp.h")) as f:
+        text = " ".join(f.read().split())
+    assert "Activations are fp32 and are never rounded to a narrower type" in text
+    assert "stays fp32 (unrounded)" in text
+    for stale in ("is rounded to bf16 (bf16 models)", "rounded to the model dtype", "rounded to bf16 inside"):
+        assert stale not in text, stale
+    # nor does any kernel comment describe rounding activations to bf16
+    csrc = os.path.join(ROOT, "mtp_speculative_decoding_gemma4_gb300", "csrc")
+    for name in os.listdir(csrc):
+        with open(os.path.join(csrc, name)) as f:
+            src = " ".join(f.read().split())
+        assert "rounded to bf16 inside" not in src and "Operand rounding of the precision contract" not in src, name

@@ -99,7 +99,8 @@ def measured_peaks():
 # The device code each captured kernel is compiled from (its translation unit and the device
 # headers it includes); other kernels hash the whole csrc directory.
 KERNEL_SOURCES = {"k_block_c2": ("mtp_c2.cu", "mtp_c2.cuh", "mtp_common.cuh"),
-                  "k_block_ll": ("mtp_ll.cu", "mtp_ll.cuh", "mtp_common.cuh")}
+                  "k_block_ll": ("mtp_ll.cu", "mtp_ll.cuh", "mtp_common.cuh"),
+                  "k_block_gr": ("mtp_grid.cu", "mtp_grid.cuh", "mtp_common.cuh")}
 
 
 def kernel_source_hash(kernel: str = "") -> str:
@@ -215,6 +216,12 @@ def _to_dev(arr, dtype, torch):
     return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
 
 
+def pct(values, q: float) -> float:
+    """The q-quantile (0..1) of the values, nearest rank."""
+    v = sorted(values)
+    return v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
+
+
 def run_mtp(args, rank: int, world: int, dist):
     import numpy as np
     import torch
@@ -265,6 +272,14 @@ def run_mtp(args, rank: int, world: int, dist):
     def verify():
         verify_greedy(logits, out_tok, accept_len=acc, out_tokens=out_v, stream=sh)
 
+    if args.profile_blocks:
+        # exactly this many draft blocks, nothing timed: the program named by the ncu captures
+        for _ in range(args.profile_blocks):
+            draft()
+        torch.cuda.synchronize()
+        assert dr.status() == 0
+        return None
+
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     for _ in range(max(3, args.warmup)):
         draft(); verify()
@@ -291,6 +306,8 @@ def run_mtp(args, rank: int, world: int, dist):
     draft_ms = [e[0].elapsed_time(e[1]) for e in ev]
     ms_per_step = sum(step_ms) / K
     draft_ms_mean = sum(draft_ms) / K
+    spread = {"step_ms_median": statistics.median(step_ms), "step_ms_p90": pct(step_ms, 0.9),
+              "draft_ms_median": statistics.median(draft_ms), "draft_ms_p90": pct(draft_ms, 0.9)}
     assert dr.status() == 0
 
     # sampled verification (temperature 1, seeded uniforms) of the same drafts and logits
@@ -357,7 +374,7 @@ def run_mtp(args, rank: int, world: int, dist):
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
     tokens = B * n * world  # every replica drafts B * n tokens per step
     head = (3 if shape.use_ordered_embeddings else 1)
-    if args.path in (2, 3, 4, 6):
+    if args.path in (2, 3, 4, 6, 7):
         launches_per_step = 2
     elif args.path == 5:  # per step: staging + tcgen05 GEMM per projection, attention, combine, head
         launches_per_step = 1 + n * (2 + 11 * shape.n_layers + 2 + head) + 1 + 1
@@ -367,10 +384,13 @@ def run_mtp(args, rank: int, world: int, dist):
                    3: "k_block_ll (latency draft block, resident weights + mailboxes)",
                    4: "k_block_cl (cluster draft block, streamed weights + DSMEM exchanges)",
                    5: "k_tc_gemm + phase kernels (tcgen05 projections)",
-                   6: "k_block_c2 (streamed-tile cluster draft block, tensor-core projections)"}[args.path]
+                   6: "k_block_c2 (streamed-tile cluster draft block, tensor-core projections)",
+                   7: "k_block_gr (grid draft block: split weights resident in shared memory, cluster + "
+                      "global exchanges)"}[args.path]
     res = {
         "metric": METRIC, "value": job_tokens_per_s(B * n, world, ms_per_step), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "median_ms": spread["step_ms_median"], "p90_ms": spread["step_ms_p90"],
         "us_per_drafter_step": ms_per_step * 1e3 / n, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{shape.name} drafter step: B={B}, ctx {wl.ctx}, draft block {n}, then greedy "
@@ -382,7 +402,8 @@ def run_mtp(args, rank: int, world: int, dist):
                      "traffic": ncu_traffic(kernel_name.split()[0], args.config),
                      "kernel": kernel_name,
                      "alg_bytes_per_launch": per_launch, "alg_bytes_per_step": alg, "peak_source": peak_src,
-                     "kernel_ms": draft_ms_mean},
+                     "kernel_ms": draft_ms_mean, "kernel_ms_median": spread["draft_ms_median"],
+                     "kernel_ms_p90": spread["draft_ms_p90"]},
         "e2e": {"value": tokens / e2e_step, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step * 1e3},
         "gpu_launches": launches_per_step * K,
@@ -404,6 +425,10 @@ def run_mtp(args, rank: int, world: int, dist):
 # ---------------------------------------------------------------------------------------
 
 def blas_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -426,8 +451,7 @@ def oracle_step_runner(shape, wl, w, inp, base):
     return one
 
 
-def cpu_baseline(args, shape, wl, w, inp, base, seconds: float):
-    one = oracle_step_runner(shape, wl, w, inp, base)
+def _time_oracle(one, seconds: float, max_steps: int = 10000):
     one()
     t0 = time.perf_counter()
     steps = 0
@@ -435,11 +459,35 @@ def cpu_baseline(args, shape, wl, w, inp, base, seconds: float):
         one()
         steps += 1
         el = time.perf_counter() - t0
-        if el >= seconds or steps >= 10000:
-            break
-    return {"value": steps * wl.batch * wl.n_draft / el, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{steps} full steps (draft block of {wl.n_draft} + verify) of the same workload, "
-                      f"{el:.1f} s, NumPy fp64"}
+        if el >= seconds or steps >= max_steps:
+            return steps, el
+
+
+def cpu_baseline(args, shape, wl, w, inp, base, seconds: float):
+    """The oracle timed on the host cores (BLAS on every core), and again with one BLAS
+    thread; nproc stated beside both."""
+    one = oracle_step_runner(shape, wl, w, inp, base)
+    steps, el = _time_oracle(one, seconds)
+    res = {"value": steps * wl.batch * wl.n_draft / el, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+           "nproc": os.cpu_count(),
+           "sample": f"{steps} full steps (draft block of {wl.n_draft} + verify) of the same workload, "
+                     f"{el:.1f} s, NumPy fp64"}
+    # the same oracle with one BLAS thread: the reference arm in a child process whose BLAS
+    # libraries start single-threaded (nothing here can change the thread count of a BLAS
+    # that is already loaded)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", WORLD_SIZE="1", RANK="0")
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--config", str(args.config),
+           "--steps", str(max(2, int(args.cpu_seconds / 2))), "--warmup", "1"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")][-1]
+        d = json.loads(line)
+        res["single_thread"] = {"value": d["value"], "unit": UNIT, "cores": 1,
+                                "sample": f"{d['steps']} full steps, one BLAS thread (child process)"}
+    except Exception as e:
+        res["single_thread"] = {"unavailable": f"single-thread oracle run failed: {type(e).__name__}"}
+    return res
 
 
 def run_reference(args, rank: int, world: int):
@@ -487,8 +535,11 @@ def main():
     ap.add_argument("--path", type=int, default=-1,
                     help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
                          "(one sequence), 4: cluster kernel (one sequence), 5: phase kernels with tcgen05 "
-                         "projections, 6: streamed-tile cluster kernel (one sequence); default: 6 for B=1, "
-                         "else 5")
+                         "projections, 6: streamed-tile cluster kernel (one sequence), 7: grid kernel (one "
+                         "sequence); default: 7 for B=1, else 5")
+    ap.add_argument("--profile-blocks", type=int, default=0,
+                    help="run exactly this many draft blocks of the chosen path and exit without timing "
+                         "(the program the ncu captures in profiles/ name)")
     ap.add_argument("--sparse-head", choices=sorted(SPARSE_HEAD), default="auto",
                     help="traversal of the centroid head's candidate rows in the batched paths: per sequence, "
                          "cluster-major (each selected cluster streamed once per step), or auto (per sequence)")
@@ -498,7 +549,7 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.path < 0:
         bsz = workload(args.config)[1].batch
-        args.path = 6 if bsz == 1 else 5
+        args.path = 7 if bsz == 1 else 5
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -297,7 +297,9 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * gives up, the call's status word reads MTP_ERR_TIMEOUT (mtp_get_status), the kernel
  * returns early without a fault, and the handle stays usable. spin_limit_cycles > 0 replaces
  * the bound of the device waits of the phase and persistent paths (default about 2 s of
- * clock64 cycles). (-1, 0) restores the defaults. No other path is affected.
+ * clock64 cycles). On the grid path (7), CTA skip_arrival_cta does not publish its slice of
+ * the first all-reduce of the next launches (with the same timeout outcome), and the bound
+ * applies to its waits too. (-1, 0) restores the defaults. No other path is affected.
  * Errors: INVALID_ARG (NULL handle, skip_arrival_cta < -1, spin_limit_cycles < 0). */
 MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_limit_cycles);
 
@@ -316,7 +318,15 @@ MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_
  * tensor cores from weight tiles that mtp_init_weights packs once into one stream per CTA,
  * about the size of all projection weights; vectors exchanged register-to-peer in
  * distributed shared memory; bf16 centroid-head shapes within its limits, V = K, 16-byte
- * aligned hidden and K rows). Automatic picks 6 for B = 1 when available, else 4, else 3;
+ * aligned hidden and K rows), 7 = grid kernel for one sequence (every co-resident thread-block
+ * cluster of the GPU; each projection split over all CTAs by rows or by input columns, the
+ * split weights and the attended K resident in shared memory for the whole block -- K of long
+ * contexts is read from global memory instead --, vectors exchanged by all-gathers and
+ * all-reduces over distributed shared memory and epoch-tagged global mailboxes; bf16
+ * centroid-head shapes with hidden in {64, 128, 256, 512} whose per-CTA share fits shared
+ * memory, V = K, 16-byte aligned K rows; mtp_init_weights packs the per-CTA weight images,
+ * about the size of all projection weights). Automatic picks 7 for B = 1 when available,
+ * else 6, else 4, else 3;
  * 5 for B >= 2 when available; else 2 when co-resident, else 1. Results agree within the
  * precision contract.
  * Errors: INVALID_ARG; a forced path the call cannot use makes mtp_draft_block return

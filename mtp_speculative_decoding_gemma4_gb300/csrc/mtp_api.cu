@@ -1,5 +1,6 @@
 // C ABI of libmtp (include/mtp.h): argument validation, workspace ownership and dispatch
 // to the drafter-step kernels.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -9,6 +10,7 @@
 #include "mtp.h"
 #include "mtp_launch.h"
 #include "mtp_c2.cuh"
+#include "mtp_grid.cuh"
 #include "mtp_cl.cuh"
 #include "mtp_tc.cuh"
 #include "mtp_ll.cuh"
@@ -46,6 +48,15 @@ struct mtp_handle {
   // streamed-tile cluster path (one sequence): availability and the packed weight streams
   int c2_ok;
   void* c2_stream;
+  // grid path (one sequence): availability, the planned parameters (host), the per-CTA weight
+  // images, the mailboxes and the next epoch
+  int gr_ok;
+  mtp::gr::Params* gr;
+  void* gr_img;
+  unsigned long long* gr_mb;
+  long long gr_mb_words;
+  double* gr_inv;  // RoPE inverse frequencies of both attention types (fp64)
+  unsigned gr_epoch;
   // tensor-core phase path (batches of 2..tc::kMaxB): tensor maps (64-byte aligned host memory) and
   // the staging buffer of the input terms
   mtp::TcPlan* tc;
@@ -562,6 +573,117 @@ int build_c2_stream(mtp_handle* h) {
   return MTP_OK;
 }
 
+// Grid-path parameters that depend only on the handle (shapes, weights), for K of up to
+// kv_max keys.
+mtp::gr::Params gr_template(const mtp_handle* h, int kv_max) {
+  const mtp_config& c = h->cfg;
+  mtp::gr::Params p;
+  memset(&p, 0, sizeof(p));
+  p.bb = c.backbone;
+  p.H = c.hidden;
+  p.nl = c.n_layers;
+  p.nh = c.n_head;
+  p.nkv = c.n_kv_head;
+  p.F = c.ffn;
+  p.V = c.vocab;
+  p.C = c.n_centroids;
+  p.topk = c.top_k;
+  p.vsc = c.use_ordered_embeddings && c.n_centroids > 0 ? c.vocab / c.n_centroids : 0;
+  p.W = c.window;
+  p.d[0] = c.head_dim_swa;
+  p.d[1] = c.head_dim_full;
+  for (int t = 0; t < 2; ++t) {
+    const int d = p.d[t] > 0 ? p.d[t] : 1;
+    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
+  }
+  p.theta[0] = c.rope_theta_swa;
+  p.theta[1] = c.rope_theta_full;
+  p.eps = c.rms_eps;
+  typedef const __nv_bfloat16* cb;
+  p.tgt = static_cast<cb>(h->target_embed);
+  p.temb_ord = static_cast<cb>(h->temb_ord);
+  p.out_norm = h->w.out_norm;
+  p.ord = h->w.token_ordering;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mtp_layer_weights& L = h->w.layer[l];
+    p.ltype[l] = c.layer_type[l];
+    p.lambda[l] = L.layer_scalar;
+    p.q_norm[l] = L.q_norm;
+    p.attn_norm[l] = L.attn_norm;
+    p.post_attn_norm[l] = L.post_attn_norm;
+    p.ffn_norm[l] = L.ffn_norm;
+    p.post_ffn_norm[l] = L.post_ffn_norm;
+  }
+  for (int t = 0; t < 2; ++t) {
+    p.has_type[t] = has_type(c, t) ? 1 : 0;
+    p.kv_max[t] = kv_max;
+    p.st[t] = static_cast<long long>(c.n_kv_head) * (t ? c.head_dim_full : c.head_dim_swa);
+  }
+  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
+  return p;
+}
+
+// Plans the grid path for this handle and, when it fits, packs the per-CTA weight images and
+// allocates the mailboxes (h->gr_ok stays 0 otherwise, and the other paths serve B = 1).
+int build_gr(mtp_handle* h) {
+  const mtp_config& c = h->cfg;
+  h->gr_ok = 0;
+  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings || !h->temb_ord) return MTP_OK;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    return MTP_OK;
+  }
+  mtp::gr::Params* p = static_cast<mtp::gr::Params*>(malloc(sizeof(mtp::gr::Params)));
+  if (!p) return MTP_OK;
+  *p = gr_template(h, c.max_ctx);
+  if (mtp::gr_plan(*p, optin) <= 0) {
+    free(p);
+    return MTP_OK;
+  }
+  h->gr = p;
+  const size_t img = static_cast<size_t>(mtp::gr_image_total(*p));
+  h->gr_mb_words = mtp::gr_mailboxes(*p);
+  cudaError_t e = cudaMalloc(&h->gr_img, img);
+  if (e == cudaSuccess) e = cudaMemset(h->gr_img, 0, img);
+  if (e == cudaSuccess) e = cudaMalloc(&h->gr_mb, static_cast<size_t>(h->gr_mb_words) * 8);
+  if (e == cudaSuccess) e = cudaMemset(h->gr_mb, 0, static_cast<size_t>(h->gr_mb_words) * 8);
+  if (e != cudaSuccess) return cuda_fail("allocating the grid path's weight images and mailboxes", e);
+  const void *q[MTP_MAX_LAYERS], *o[MTP_MAX_LAYERS], *g[MTP_MAX_LAYERS], *u[MTP_MAX_LAYERS], *d[MTP_MAX_LAYERS];
+  for (int l = 0; l < c.n_layers; ++l) {
+    q[l] = h->w.layer[l].q;
+    o[l] = h->w.layer[l].o;
+    g[l] = h->w.layer[l].gate;
+    u[l] = h->w.layer[l].up;
+    d[l] = h->w.layer[l].down;
+  }
+  // RoPE inverse frequencies theta^(-2i/d) of both types, formed once in fp64 (0: no rotation)
+  {
+    const int h0 = c.head_dim_swa / 2, h1 = c.head_dim_full / 2, hm = h0 > h1 ? h0 : h1;
+    std::vector<double> inv(2 * static_cast<size_t>(hm > 0 ? hm : 1), 0.0);
+    const float th[2] = {c.rope_theta_swa, c.rope_theta_full};
+    const int dd[2] = {c.head_dim_swa, c.head_dim_full};
+    for (int t = 0; t < 2; ++t)
+      for (int i = 0; i < dd[t] / 2; ++i)
+        inv[t * hm + i] = th[t] > 0.f ? std::pow(static_cast<double>(th[t]), -2.0 * i / dd[t]) : 0.0;
+    e = cudaMalloc(&h->gr_inv, inv.size() * sizeof(double));
+    if (e == cudaSuccess) e = cudaMemcpy(h->gr_inv, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail("storing the RoPE frequencies", e);
+    p->inv_freq = h->gr_inv;
+  }
+  int rc = mtp::gr_pack(*p, h->w.pre_proj, h->w.post_proj, h->w.centroids, q, o, g, u, d,
+                        static_cast<unsigned char*>(h->gr_img), 0);
+  if (rc) return rc;
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail("packing the grid path's weight images", e);
+  p->img = static_cast<const unsigned char*>(h->gr_img);
+  p->img_bytes = p->L.img_bytes;
+  p->mb = h->gr_mb;
+  h->gr_epoch = 64u;
+  h->gr_ok = 1;
+  return MTP_OK;
+}
+
 // Carves the workspace out of one allocation (sizes for max_batch sequences).
 size_t layout_ws(mtp_handle* h, char* base) {
   const mtp_config& c = h->cfg;
@@ -713,6 +835,10 @@ void release_handle(mtp_handle* h) {
   if (h->temb_ord) cudaFree(h->temb_ord);
   if (h->wpack) cudaFree(h->wpack);
   if (h->c2_stream) cudaFree(h->c2_stream);
+  if (h->gr_img) cudaFree(h->gr_img);
+  if (h->gr_mb) cudaFree(h->gr_mb);
+  if (h->gr_inv) cudaFree(h->gr_inv);
+  if (h->gr) free(h->gr);
   if (h->tc_mem) cudaFree(h->tc_mem);
   if (h->tc) free(h->tc);
   free(h);
@@ -859,6 +985,11 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       return rc;
     }
   }
+  rc = build_gr(h);
+  if (rc) {
+    release_handle(h);
+    return rc;
+  }
   // the graph cache's stream and events (graphs are skipped when they cannot be created)
   if (cudaStreamCreateWithFlags(&h->gc.cs, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->gc.ev_in, cudaEventDisableTiming) != cudaSuccess ||
@@ -922,6 +1053,50 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = c.dtype == MTP_DTYPE_BF16;
   int path = h->path;
+  if (path == 7 || (path == 0 && B == 1 && h->gr_ok)) {
+    if (!h->gr_ok || B != 1) {
+      set_error("the grid path runs one sequence of a supported shape (B=%d, available=%d)", B, h->gr_ok);
+      return MTP_ERR_UNSUPPORTED_SHAPE;
+    }
+    mtp::gr::Params& gp = *h->gr;
+    for (int t = 0; t < 2; ++t) {
+      if (!gp.has_type[t]) continue;
+      if (kvs[t]->v && kvs[t]->v != kvs[t]->k) {
+        set_error("the grid path reads V = K (attention_k_eq_v); pass v = NULL or v = k");
+        return MTP_ERR_UNSUPPORTED_SHAPE;
+      }
+      if ((reinterpret_cast<uintptr_t>(kvs[t]->k) & 15) != 0 || (kvs[t]->stride_t * 2) % 16 != 0) {
+        set_error("the grid path needs 16-byte aligned K rows");
+        return MTP_ERR_UNSUPPORTED_SHAPE;
+      }
+      gp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
+      gp.ctx_len[t] = kvs[t]->ctx_len;
+      gp.st[t] = kvs[t]->stride_t;
+      gp.kv_max[t] = kvs[t]->max_ctx;
+    }
+    gp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
+    gp.tok_in = last_token;
+    gp.pos = pos;
+    gp.out_tokens = out_tokens;
+    gp.out_hidden = out_hidden;
+    gp.n_draft = n_draft;
+    gp.status = h->wsp.status;
+    gp.abort_flag = h->ll_abort;
+    gp.spin_limit = h->dbg_spin > 0 ? h->dbg_spin : 4000000000LL;
+    gp.dbg_skip = h->dbg_skip;
+    const unsigned need = static_cast<unsigned>(n_draft + 1) * mtp::gr::kExPerStep;
+    if (h->gr_epoch > 0xF0000000u - need) {
+      // epochs wrap: clear the mailboxes so that no old word can match a new epoch
+      cudaError_t e = cudaMemsetAsync(h->gr_mb, 0, static_cast<size_t>(h->gr_mb_words) * 8, st);
+      if (e != cudaSuccess) return cuda_fail("clearing the grid path's mailboxes", e);
+      h->gr_epoch = 64u;
+    }
+    gp.epoch_base = h->gr_epoch;
+    h->gr_epoch += need;
+    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
+    return mtp::run_gr(gp, st);
+  }
   if (path == 6 || (path == 0 && B == 1 && h->c2_ok)) {
     if (!h->c2_ok || B != 1) {
       set_error("the streamed cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->c2_ok);
@@ -1219,8 +1394,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 6) {
-    set_error("need a handle and path in {0, 1, 2, 3, 4, 5, 6}");
+  if (!h || path < 0 || path > 7) {
+    set_error("need a handle and path in {0, 1, 2, 3, 4, 5, 6, 7}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;

@@ -1,0 +1,1319 @@
+// Grid draft block for one sequence (B = 1): see mtp_grid.cuh for the data flow.
+//
+// Failure handling: every wait (bulk copies, distributed-shared-memory receives, mailbox
+// polls) is bounded by a clock64 budget. A wait that gives up records MTP_ERR_TIMEOUT in
+// the status word and raises the abort word; a raised abort word makes every other wait of
+// the launch give up at its next check. The CTA then leaves its step loop, waits (bounded)
+// for its own launch-start bulk copies still in flight, and meets its cluster at the final
+// barrier so that no peer writes into an exited CTA. Values taken from exchanged data that
+// address memory (the token, the selected centroids) are range-checked first.
+#include <cmath>
+#include <cstring>
+
+#include "mtp_grid.cuh"
+#include "mtp_launch.h"
+
+namespace mtp {
+namespace gr {
+
+// ------------------------------------------------------------------ primitives
+
+__device__ __forceinline__ unsigned sa(const void* p) { return static_cast<unsigned>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ unsigned mapa(unsigned addr, int rank) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_async_u64(unsigned caddr, unsigned long long v, unsigned cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(caddr), "l"(v),
+               "r"(cbar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
+      "p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_rlx64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_rlx64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_rlx32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ int cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ float bf(bf16 v) { return __bfloat162float(v); }
+
+// ------------------------------------------------------------------ bounded waits
+
+__device__ __forceinline__ void fail(const Params& p) {
+  atomicCAS(p.status, 0, static_cast<int>(MTP_ERR_TIMEOUT));
+  atomicExch(p.abort_flag, 1u);
+}
+// True when the caller must give up: the budget ran out (recorded) or another CTA gave up.
+__device__ __forceinline__ bool expired(const Params& p, long long t0, unsigned n) {
+  if ((n & 63u) != 0u) return false;
+  if (ld_rlx32(p.abort_flag)) return true;
+  if (clock64() - t0 > p.spin_limit) {
+    fail(p);
+    return true;
+  }
+  return false;
+}
+// A waiting thread is suspended until the phase completes or about this many ns pass.
+constexpr unsigned kSuspendNs = 2000;
+__device__ __forceinline__ bool mbar_try_susp(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, "
+      "0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+// Warp 0 waits on the mbarrier phase (acquire at cluster scope: the bytes peers stored with
+// st.async or bulk copies wrote are visible to it); the CTA barrier then orders them before
+// every other thread's reads. The other warps sleep in the barrier instead of polling the
+// shared memory the incoming bytes need. Every thread calls; block-uniform result.
+__device__ __forceinline__ bool mbar_wait(const Params& p, unsigned bar, unsigned parity, bool watch_abort) {
+  int bad = 0;
+  if (threadIdx.x < 32 && !mbar_try_susp(bar, parity)) {
+    const long long t0 = clock64();
+    while (!mbar_try_susp(bar, parity)) {
+      if (watch_abort && ld_rlx32(p.abort_flag)) {
+        bad = 1;
+        break;
+      }
+      if (clock64() - t0 > p.spin_limit) {
+        fail(p);
+        bad = 1;
+        break;
+      }
+    }
+  }
+  return !__syncthreads_or(bad);
+}
+
+__device__ __forceinline__ void put(unsigned long long* mb, long long i, float v, unsigned ep) {
+  st_rlx64(mb + i, (static_cast<unsigned long long>(ep) << 32) | __float_as_uint(v));
+}
+__device__ __forceinline__ void put_u(unsigned long long* mb, long long i, unsigned v, unsigned ep) {
+  st_rlx64(mb + i, (static_cast<unsigned long long>(ep) << 32) | v);
+}
+
+// Mailbox words -> dst[k] (payload bits), k in [0, count). A thread issues the first load of
+// all its words of a pass (up to 16) before waiting on any, then re-polls only the missing
+// ones (bounded). The word index of k comes from a functor; every thread calls; the result
+// is block-uniform.
+constexpr int kGatherBatch = 16;
+template <class Idx>
+__device__ __forceinline__ bool gather_t(const Params& p, const unsigned long long* mb, int count, Idx idx,
+                                         unsigned* dst, unsigned ep) {
+  int bad = 0;
+#pragma unroll 1
+  for (int base = 0; base < count; base += kGatherBatch * kT) {
+    unsigned long long w[kGatherBatch];
+    int ix[kGatherBatch];
+#pragma unroll
+    for (int j = 0; j < kGatherBatch; ++j) {
+      const int k = base + j * kT + static_cast<int>(threadIdx.x);
+      ix[j] = k < count ? static_cast<int>(idx.next()) : -1;
+      w[j] = ix[j] >= 0 ? ld_rlx64(mb + ix[j]) : 0ull;
+    }
+#pragma unroll
+    for (int j = 0; j < kGatherBatch; ++j) {
+      if (ix[j] < 0) continue;
+      if (static_cast<unsigned>(w[j] >> 32) != ep && !bad) {
+        const long long t0 = clock64();
+#pragma unroll 1
+        for (unsigned n = 1;; ++n) {
+          w[j] = ld_rlx64(mb + ix[j]);
+          if (static_cast<unsigned>(w[j] >> 32) == ep) break;
+          if (expired(p, t0, n)) {
+            bad = 1;
+            break;
+          }
+        }
+      }
+      dst[base + j * kT + threadIdx.x] = static_cast<unsigned>(w[j]);
+    }
+  }
+  return !__syncthreads_or(bad);
+}
+// Index functors: next() gives the word index of the thread's next k (k = tid, tid + kT, ...).
+struct IdxLin {
+  long long k;
+  __device__ IdxLin() : k(static_cast<long long>(threadIdx.x) - kT) {}
+  __device__ long long next() { return k += kT; }
+};
+// All-reduce slice: k -> [k >> lg_hs][slice0 + (k & (hs - 1))] with rows of H words.
+struct IdxSlice {
+  int k, lg, msk, H, slice0;
+  __device__ IdxSlice(int lg_hs, int H_, int s0) : k(static_cast<int>(threadIdx.x) - kT), lg(lg_hs),
+                                                   msk((1 << lg_hs) - 1), H(H_), slice0(s0) {}
+  __device__ long long next() {
+    k += kT;
+    return static_cast<long long>(k >> lg) * H + slice0 + (k & msk);
+  }
+};
+// Attention partials of this CTA's dims [q0, q0 + nq) and the (m, l) of the heads they touch,
+// from every attention CTA: k -> (a, j) with j < per; j < nq: dim q0 + j, else (m, l) of head
+// hlo + (j - nq) / 2; word (a nh + h)(d + 2) + e.
+struct IdxPart {
+  int a, j, per, nq, q0, hlo, lg_d, d, nh, da, dj;
+  __device__ IdxPart(int per_, int nq_, int q0_, int hlo_, int lg_d_, int nh_)
+      : per(per_), nq(nq_), q0(q0_), hlo(hlo_), lg_d(lg_d_), d(1 << lg_d_), nh(nh_) {
+    const int t = static_cast<int>(threadIdx.x);
+    a = per > 0 ? t / per : 0;
+    j = per > 0 ? t % per : 0;
+    da = per > 0 ? kT / per : 0;
+    dj = per > 0 ? kT % per : 0;
+    // stepping back once lets next() advance uniformly
+    a -= da;
+    j -= dj;
+    if (j < 0) {
+      j += per;
+      a -= 1;
+    }
+  }
+  __device__ long long next() {
+    a += da;
+    j += dj;
+    if (j >= per) {
+      j -= per;
+      a += 1;
+    }
+    int h, e;
+    if (j < nq) {
+      h = (q0 + j) >> lg_d;
+      e = (q0 + j) & (d - 1);
+    } else {
+      h = hlo + ((j - nq) >> 1);
+      e = d + ((j - nq) & 1);
+    }
+    return (static_cast<long long>(a) * nh + h) * (d + 2) + e;
+  }
+};
+__device__ __forceinline__ bool gather_lin(const Params& p, const unsigned long long* mb, int count, unsigned* dst,
+                                        unsigned ep) {
+  return gather_t(p, mb, count, IdxLin(), dst, ep);
+}
+__device__ __forceinline__ bool gather_slice(const Params& p, const unsigned long long* mb, int count, int slice0,
+                                          unsigned* dst, unsigned ep) {
+  return gather_t(p, mb, count, IdxSlice(p.lg_hs, p.H, slice0), dst, ep);
+}
+__device__ __forceinline__ bool gather_part(const Params& p, const unsigned long long* mb, int count, int per, int nq,
+                                         int q0, int hlo, int lg_d, unsigned* dst, unsigned ep) {
+  return gather_t(p, mb, count, IdxPart(per, nq, q0, hlo, lg_d, p.nh), dst, ep);
+}
+
+// ------------------------------------------------------------------ per-warp vector math
+
+// Lane l holds elements [l * EPL, (l + 1) * EPL) of an H-vector (H = 32 * EPL).
+template <int EPL>
+__device__ __forceinline__ void lds_vec(const float* v, float (&r)[EPL]) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = v[l * EPL + e];
+}
+template <int EPL>
+__device__ __forceinline__ void ldg_vec(const float* v, float (&r)[EPL]) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) r[e] = __ldg(v + l * EPL + e);
+}
+// 1 / sqrt(mean(v^2) + eps) over the warp's H-vector.
+template <int EPL>
+__device__ __forceinline__ float rms_inv(const float (&r)[EPL], float eps) {
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) s = fmaf(r[e], r[e], s);
+  s = warp_sum(s);
+  return rsqrtf(s / static_cast<float>(32 * EPL) + eps);
+}
+__device__ __forceinline__ void bf8(const uint4& u, float* f) {
+  const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h2[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+// Row (bf16, H elements, 16-byte aligned) . vector held by the warp; every lane gets the sum.
+template <int EPL>
+__device__ __forceinline__ float dot_row(const bf16* row, const float (&a)[EPL]) {
+  const int l = threadIdx.x & 31;
+  float s = 0.f;
+  if constexpr (EPL % 8 == 0) {
+#pragma unroll
+    for (int v = 0; v < EPL / 8; ++v) {
+      float f[8];
+      bf8(*reinterpret_cast<const uint4*>(row + l * EPL + 8 * v), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(f[i], a[8 * v + i], s);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s = fmaf(bf(row[l * EPL + e]), a[e], s);
+  }
+  return warp_sum(s);
+}
+
+// ------------------------------------------------------------------ all-reduce
+
+// Sums the H-vector vs[] of every CTA of the grid; returns the shared-memory address of the
+// result (valid until the all-reduce after next). Slot (arn & 1) of the receive buffers and
+// barriers; parity (arn >> 1) & 1. All threads call; *ok is block-uniform.
+__device__ __forceinline__ float* all_reduce(const Params& p, unsigned char* sm, const float* vs, int arn,
+                                          unsigned long long* mbx, unsigned ep, int rank, int g, bool skip_publish,
+                                          bool* ok) {
+  const Layout& L = p.L;
+  const int H = p.H, S = p.S, lg = p.lg_hs, hs = 1 << lg;
+  const int slot = arn & 1;
+  const unsigned par = static_cast<unsigned>(arn >> 1) & 1u;
+  float* rs = reinterpret_cast<float*>(sm + L.rs) + slot * H;  // [source rank][hs]
+  float* ag = reinterpret_cast<float*>(sm + L.ag) + slot * H;  // [H]
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(sm + L.bars);
+  const unsigned rbar = sa(&bars[p.nl + 3 + slot]), abar = sa(&bars[p.nl + 5 + slot]);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_expect_tx(rbar, static_cast<unsigned>(H * 4));
+    mbar_expect_tx(abar, static_cast<unsigned>(H * 4));
+  }
+  __syncthreads();  // vs complete
+  // 1) reduce-scatter in the cluster: dims [q hs, (q + 1) hs) go to rank q
+#pragma unroll 1
+  for (int i2 = tid; i2 < H / 2; i2 += kT) {
+    const int i = 2 * i2, q = i >> lg, e = i & (hs - 1);
+    const unsigned long long v =
+        (static_cast<unsigned long long>(__float_as_uint(vs[i + 1])) << 32) | __float_as_uint(vs[i]);
+    st_async_u64(mapa(sa(rs + rank * hs + e), q), v, mapa(rbar, q));
+  }
+  if (!mbar_wait(p, rbar, par, true)) {
+    *ok = false;
+    return ag;
+  }
+  // 2) this cluster's partial of my slice -> global; every cluster's partial of my slice <- global
+  float* ub = reinterpret_cast<float*>(sm + L.ubuf);
+  if (!skip_publish && tid < hs) {
+    float s = 0.f;
+#pragma unroll 1
+    for (int q = 0; q < S; ++q) s += rs[q * hs + tid];
+    put(mbx, static_cast<long long>(g) * H + rank * hs + tid, s, ep);
+  }
+  if (!gather_slice(p, mbx, p.G * hs, rank * hs, reinterpret_cast<unsigned*>(ub), ep)) {
+    *ok = false;
+    return ag;
+  }
+  // sums over the clusters in a fixed order: P consecutive lanes per dim, then a butterfly
+  {
+    const int lgP = kLgT - lg < 5 ? kLgT - lg : 5;  // log2 of the threads per dim
+    const int P = 1 << lgP;
+    const int e = tid >> lgP, part = tid & (P - 1);
+    float s = 0.f;
+    if (e < hs) {
+#pragma unroll 1
+      for (int gg = part; gg < p.G; gg += P) s += ub[gg * hs + e];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      if (o < P) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (e < hs && part == 0) rs[e] = s;  // the slot's reduce-scatter data is consumed
+  }
+  __syncthreads();
+  // 3) all-gather of the slices in the cluster
+#pragma unroll 1
+  for (int t = tid; t < S * (hs / 2); t += kT) {
+    const int q = t >> (lg - 1), e = 2 * (t & (hs / 2 - 1));
+    const unsigned long long v =
+        (static_cast<unsigned long long>(__float_as_uint(rs[e + 1])) << 32) | __float_as_uint(rs[e]);
+    st_async_u64(mapa(sa(ag + rank * hs + e), q), v, mapa(abar, q));
+  }
+  if (!mbar_wait(p, abar, par, true)) {
+    *ok = false;
+    return ag;
+  }
+  return ag;
+}
+
+// ------------------------------------------------------------------ top-k
+
+// Exclusive prefix sum of v over the CTA's threads in thread order (ws: 48 ints); also the
+// total through *tot.
+__device__ __forceinline__ int block_excl_scan(int v, int* ws, int* tot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += u;
+  }
+  if (lane == 31) ws[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kW ? ws[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    if (lane < kW) ws[32 + lane] = w;
+  }
+  __syncthreads();
+  *tot = ws[32 + kW - 1];
+  const int r = (warp > 0 ? ws[32 + warp - 1] : 0) + x - v;
+  __syncthreads();
+  return r;
+}
+// (value, index) -> key whose maximum is the largest value, lowest index among equal values.
+__device__ __forceinline__ unsigned long long topk_key(const float* cl, int i) {
+  return (static_cast<unsigned long long>(ord_f32(cl[i])) << 32) | (0xffffffffu - static_cast<unsigned>(i));
+}
+
+// Indices of the k largest of cl[0..C) (fp32; equal values: lower index first), written to
+// sel[] in increasing index order. Bound: split the C logits into k groups; the smallest of
+// the k group maxima is at most the k-th largest key, so every selected key lies at or above
+// it. The keys at or above the bound (few: about k to 3k) are compacted in index order and
+// each is ranked against the others. All threads call.
+__device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, const float* cl, int* sel) {
+  const Layout& L = p.L;
+  const int C = p.C, k = p.topk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned long long* gmax = reinterpret_cast<unsigned long long*>(sm + L.gmax);
+  int* ws = reinterpret_cast<int*>(sm + L.red);
+  int* cidx = reinterpret_cast<int*>(sm + L.qs);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm + L.qs + ((L.cand_cap * 4 + 15) & ~15));
+  // group maxima: when the k groups are runs of 2^j whole per-thread chunks, a thread's chunk
+  // maximum and a butterfly over the group's lanes; else one warp per group
+  const int per = cdiv(C, kT), i0 = min(C, tid * per), i1 = min(C, i0 + per);
+  const int tpg = (C / k) / per;  // threads per group
+  const bool tiled = C % k == 0 && (C / k) % per == 0 && tpg >= 1 && tpg <= 32 && (tpg & (tpg - 1)) == 0 &&
+                     tpg * k <= kT;
+  if (tiled) {
+    unsigned long long m = 0ull;
+#pragma unroll 4
+    for (int i = i0; i < i1; ++i) {
+      const unsigned long long key = topk_key(cl, i);
+      m = key > m ? key : m;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      if (o < tpg) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, m, o);
+        m = w > m ? w : m;
+      }
+    if ((tid & (tpg - 1)) == 0 && tid / tpg < k) gmax[tid / tpg] = m;
+  }
+#pragma unroll 1
+  for (int r = tiled ? k : warp; r < k; r += kW) {
+    const int lo = static_cast<int>(static_cast<long long>(C) * r / k), hi = static_cast<int>(static_cast<long long>(C) * (r + 1) / k);
+    unsigned long long m = 0ull;
+#pragma unroll 1
+    for (int i = lo + lane; i < hi; i += 32) {
+      const unsigned long long key = topk_key(cl, i);
+      m = key > m ? key : m;
+    }
+    m = warp_max_u64(m);
+    if (lane == 0) gmax[r] = m;
+  }
+  __syncthreads();
+  // the bound: smallest group maximum (every warp computes it)
+  unsigned long long bnd = ~0ull;
+#pragma unroll 1
+  for (int r = lane; r < k; r += 32) bnd = gmax[r] < bnd ? gmax[r] : bnd;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, bnd, o);
+    bnd = w < bnd ? w : bnd;
+  }
+  // candidates at or above the bound, in index order (contiguous chunks per thread)
+  int n = 0;
+#pragma unroll 1
+  for (int i = i0; i < i1; ++i) n += topk_key(cl, i) >= bnd;
+  int M = 0;
+  int pos = block_excl_scan(n, ws, &M);
+  const bool fits = M <= L.cand_cap;
+  if (fits) {
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i) {
+      const unsigned long long key = topk_key(cl, i);
+      if (key >= bnd) {
+        cidx[pos] = i;
+        ckey[pos] = key;
+        ++pos;
+      }
+    }
+  }
+  __syncthreads();
+  // rank of each candidate among the candidates (or, when they overflow the buffer, among all
+  // keys); selected when fewer than k keys are larger
+  int take = 0, ti = 0;
+  if (fits) {
+    if (tid < M) {
+      const unsigned long long key = ckey[tid];
+      int rk = 0;
+#pragma unroll 8
+      for (int m = 0; m < M; ++m) rk += ckey[m] > key;
+      take = rk < k;
+      ti = cidx[tid];
+    }
+  }
+  int nsel = 0;
+  if (fits) {
+    const int at = block_excl_scan(take, ws, &nsel);
+    if (take && at < k) sel[at] = ti;
+  } else {
+    // slow exact path: every key against every key (only for pathological ties / distributions)
+    int cnt = 0;
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i) {
+      const unsigned long long key = topk_key(cl, i);
+      int rk = 0;
+      if (key >= bnd) {
+#pragma unroll 1
+        for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > key;
+      }
+      cnt += key >= bnd && rk < k;
+    }
+    int at = block_excl_scan(cnt, ws, &nsel);
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i) {
+      const unsigned long long key = topk_key(cl, i);
+      if (key < bnd) continue;
+      int rk = 0;
+#pragma unroll 1
+      for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > key;
+      if (rk < k && at < k) sel[at++] = i;
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ attention of one block
+
+// This CTA's keys of one block: q_norm + RoPE (+ the softmax scale) of every head from the
+// gathered raw q (ub), scores of every (key, head), softmax statistics (max, exp-sum) per
+// head, the probability-weighted key sums (V = K); publishes [c][h][d + 2] (sums, max,
+// exp-sum) to the owners of q's dims. gq0..gq7: the q_norm gains of this thread's first four
+// RoPE pairs (prefetched into registers). All threads call.
+__device__ __forceinline__ void attend(const Params& p, unsigned char* sm, int l, int t, int c, int nk, const bf16* kb,
+                                      long long kst, unsigned long long* ma, unsigned epa, float gq0, float gq1,
+                                      float gq2, float gq3, float gq4, float gq5, float gq6, float gq7) {
+  const Layout& L = p.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nh = p.nh, nkv = p.nkv, lg = p.lg_d[t], d = 1 << lg, grp = nh / nkv, half = d >> 1, ksl = L.ksl;
+  float* ub = reinterpret_cast<float*>(sm + L.ubuf);
+  float* qs = reinterpret_cast<float*>(sm + L.qs);
+  float* sc = reinterpret_cast<float*>(sm + L.sc);
+  float* red = reinterpret_cast<float*>(sm + L.red);
+  const float2* cs = reinterpret_cast<const float2*>(sm + L.cs) + (t ? p.d[0] / 2 : 0);
+  // per-head q_norm factor (one warp per head)
+#pragma unroll 1
+  for (int h = warp; h < nh; h += kW) {
+    float s2 = 0.f;
+#pragma unroll 1
+    for (int e = lane; e < d; e += 32) s2 = fmaf(ub[h * d + e], ub[h * d + e], s2);
+    s2 = warp_sum(s2);
+    if (lane == 0) red[h] = rsqrtf(s2 / static_cast<float>(d) + p.eps);
+  }
+  __syncthreads();
+  {
+    const float* gqn = p.q_norm[l];
+    const float scale = p.scale[t];
+    int k = 0;
+#pragma unroll 1
+    for (int i = tid; i < nh * half; i += kT, ++k) {
+      const int h = i >> (lg - 1), j = i & (half - 1);
+      const float g0 = k == 0 ? gq0 : (k == 1 ? gq2 : (k == 2 ? gq4 : (k == 3 ? gq6 : __ldg(gqn + j))));
+      const float g1 = k == 0 ? gq1 : (k == 1 ? gq3 : (k == 2 ? gq5 : (k == 3 ? gq7 : __ldg(gqn + j + half))));
+      const float rn = red[h];
+      const float a = ub[h * d + j] * rn * g0, b = ub[h * d + j + half] * rn * g1;
+      const float2 cw = cs[j];
+      qs[h * d + j] = (a * cw.x - b * cw.y) * scale;
+      qs[h * d + j + half] = (b * cw.x + a * cw.y) * scale;
+    }
+  }
+  __syncthreads();
+  // scores: one warp per (key, KV head, group of up to 4 of its query heads); every lane a run
+  // of 16-byte vectors of the key
+  const int nvec = d >> 3;
+#pragma unroll 2
+  for (int j = warp; j < nk; j += kW) {
+#pragma unroll 1
+    for (int kh = 0; kh < nkv; ++kh) {
+      const bf16* kr = kb + static_cast<size_t>(j) * kst + kh * d;
+#pragma unroll 1
+      for (int q0 = 0; q0 < grp; q0 += 4) {
+        const float* qh = qs + (kh * grp + q0) * d;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int v = lane; v < nvec; v += 32) {
+          float kf[8];
+          bf8(*reinterpret_cast<const uint4*>(kr + 8 * v), kf);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q0 + q < grp) {
+              const float4* qv = reinterpret_cast<const float4*>(qh + q * d + 8 * v);
+              const float4 a = qv[0], b = qv[1];
+              float u = acc[q];
+              u = fmaf(a.x, kf[0], u);
+              u = fmaf(a.y, kf[1], u);
+              u = fmaf(a.z, kf[2], u);
+              u = fmaf(a.w, kf[3], u);
+              u = fmaf(b.x, kf[4], u);
+              u = fmaf(b.y, kf[5], u);
+              u = fmaf(b.z, kf[6], u);
+              acc[q] = fmaf(b.w, kf[7], u);
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        }
+        if (lane < 4 && q0 + lane < grp) {
+          const float v = lane == 0 ? acc[0] : (lane == 1 ? acc[1] : (lane == 2 ? acc[2] : acc[3]));
+          sc[(kh * grp + q0 + lane) * ksl + j] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // softmax statistics and probabilities (one warp per head)
+#pragma unroll 1
+  for (int h = warp; h < nh; h += kW) {
+    float m = -INFINITY;
+#pragma unroll 1
+    for (int j = lane; j < nk; j += 32) m = fmaxf(m, sc[h * ksl + j]);
+    m = warp_max(m);
+    float lsum = 0.f;
+#pragma unroll 1
+    for (int j = lane; j < nk; j += 32) {
+      const float e = expf(sc[h * ksl + j] - m);
+      sc[h * ksl + j] = e;
+      lsum += e;
+    }
+    lsum = warp_sum(lsum);
+    if (lane == 0) {
+      red[16 + h] = m;
+      red[32 + h] = lsum;
+    }
+  }
+  __syncthreads();
+  // probability-weighted key sums: one thread per two dims of a KV head row and group of up
+  // to 4 of its heads; published straight from registers
+  const int row = nkv * d;
+#pragma unroll 1
+  for (int q0 = 0; q0 < grp; q0 += 4) {
+#pragma unroll 1
+    for (int i2 = tid; i2 < (row >> 1); i2 += kT) {
+      const int i = 2 * i2, kh = i >> lg, e = i & (d - 1);
+      const float* pr = sc + (kh * grp + q0) * ksl;
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      const bf16* kp = kb + i;
+#pragma unroll 4
+      for (int j = 0; j < nk; ++j, kp += kst) {
+        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kp));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float pj = q0 + q < grp ? pr[q * ksl + j] : 0.f;
+          a0[q] = fmaf(pj, kv.x, a0[q]);
+          a1[q] = fmaf(pj, kv.y, a1[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q0 + q < grp) {
+          const long long base = (static_cast<long long>(c) * nh + kh * grp + q0 + q) * (d + 2) + e;
+          put(ma, base, a0[q], epa);
+          put(ma, base + 1, a1[q], epa);
+        }
+    }
+  }
+  if (tid < nh) {
+    put(ma, (static_cast<long long>(c) * nh + tid) * (d + 2) + d, red[16 + tid], epa);
+    put(ma, (static_cast<long long>(c) * nh + tid) * (d + 2) + d + 1, red[32 + tid], epa);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int EPL>
+__global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const Layout& L = p.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, rank = cluster_rank(), g = c / p.S;
+  const int H = p.H, nl = p.nl, nh = p.nh;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(sm + L.bars);
+  float* ub = reinterpret_cast<float*>(sm + L.ubuf);
+  float* hc = reinterpret_cast<float*>(sm + L.hc);
+  float* vs = reinterpret_cast<float*>(sm + L.vs);
+  float* vh = reinterpret_cast<float*>(sm + L.vh);
+  float* ms = reinterpret_cast<float*>(sm + L.ms);
+  float2* cs = reinterpret_cast<float2*>(sm + L.cs);
+  float* red = reinterpret_cast<float*>(sm + L.red);
+  unsigned long long* wkeys = reinterpret_cast<unsigned long long*>(sm + L.keys);
+  int* sel = reinterpret_cast<int*>(sm + L.sel);
+  const int kbar = nl + 2;
+
+  // ---- this CTA's shares (computed once): key ranges per type, q dims per type, FFN rows,
+  // pre / post columns, centroid rows, candidate slots
+  // (scalars per type, selected with t ? : -- no dynamically indexed local arrays, whose
+  // accesses would go to local memory)
+  int klo0 = 0;
+  Range kr0{0, 0}, kr1{0, 0}, qr0{0, 0}, qr1{0, 0};
+  if (p.has_type[0]) {
+    int Lc = p.ctx_len[0][0];
+    Lc = Lc < 0 ? 0 : (Lc > p.kv_max[0] ? p.kv_max[0] : Lc);
+    klo0 = Lc - p.W > 0 ? Lc - p.W : 0;
+    kr0 = c < p.A[0] ? split(Lc - klo0, p.A[0], c) : Range{0, 0};
+    qr0 = split(nh * p.d[0], p.N, c);
+  }
+  if (p.has_type[1]) {
+    int Lc = p.ctx_len[1][0];
+    Lc = Lc < 0 ? 0 : (Lc > p.kv_max[1] ? p.kv_max[1] : Lc);
+    kr1 = c < p.A[1] ? split(Lc, p.A[1], c) : Range{0, 0};
+    qr1 = split(nh * p.d[1], p.N, c);
+  }
+  const Range fr = split(p.F, p.N, c), hr = split(p.bb, p.N, c), cr = split(p.C, p.N, c);
+  const Range candr = split(p.topk * p.vsc, p.N, c);
+  const int nf = fr.hi - fr.lo, nhc = hr.hi - hr.lo, ncr = cr.hi - cr.lo;
+  // bulk copy of this CTA's keys of type t into the shared K region (one mbarrier phase)
+  int kph = 0, kwaited = 0, kcur = -1;
+  auto k_issue = [&](int t) {
+    if (tid == 0) {
+      const Range kt = t ? kr1 : kr0;
+      const int n = kt.hi - kt.lo, row = p.nkv * p.d[t];
+      const bf16* k0 = p.k[t] + static_cast<size_t>((t ? 0 : klo0) + kt.lo) * static_cast<size_t>(p.st[t]);
+      mbar_expect_tx(sa(&bars[kbar]), static_cast<unsigned>(n > 0 ? n * row * 2 : 0));
+      if (n > 0) {
+        if (p.st[t] == row) {
+          bulk_g2s(sa(sm + L.kbuf), k0, static_cast<unsigned>(n * row * 2), sa(&bars[kbar]));
+        } else {
+#pragma unroll 1
+          for (int j = 0; j < n; ++j)
+            bulk_g2s(sa(sm + L.kbuf + j * row * 2), k0 + static_cast<size_t>(j) * p.st[t],
+                     static_cast<unsigned>(row * 2), sa(&bars[kbar]));
+        }
+      }
+    }
+    ++kph;
+    kcur = t;
+  };
+  auto k_resident = [&](int t) { return p.has_type[t] && p.kres[t] && c < p.A[t]; };
+
+  // ---- launch start: barriers, bulk copies of this CTA's weight image and first keys
+  if (tid == 0) {
+#pragma unroll 1
+    for (int i = 0; i < nl + 7; ++i) mbar_init(sa(&bars[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const unsigned char* src = p.img + static_cast<size_t>(c) * static_cast<size_t>(p.img_bytes);
+#pragma unroll 1
+    for (int gi = 0; gi < nl + 2; ++gi) {
+      const unsigned b = static_cast<unsigned>(L.grp_bytes[gi]);
+      mbar_expect_tx(sa(&bars[gi]), b);
+      if (b) bulk_g2s(sa(sm + L.grp_off[gi]), src + L.grp_off[gi], b, sa(&bars[gi]));
+    }
+  }
+  if (k_resident(p.ltype[0])) k_issue(p.ltype[0]);
+  __syncthreads();
+  cluster_sync_all();  // every peer's barriers are initialised before any st.async
+
+  // RoPE (cos, sin) at the block's constant position: angle pos * inv_freq in fp64, reduced
+  // to [-pi, pi] in fp64, then sin / cos of the reduced angle in fp32 (fast forms: absolute
+  // error below 1e-6 on [-pi, pi])
+  {
+    const double pos = static_cast<double>(p.pos[0]);
+    const int h0 = p.d[0] / 2, h1 = p.d[1] / 2, hm = h0 > h1 ? h0 : h1;
+    const double two_pi = 6.283185307179586, inv_two_pi = 0.15915494309189535;
+#pragma unroll 1
+    for (int i = tid; i < h0 + h1; i += kT) {
+      const int t = i < h0 ? 0 : 1, ii = t ? i - h0 : i;
+      const double ang = pos * p.inv_freq[t * hm + ii];
+      const double r = fma(-rint(ang * inv_two_pi), two_pi, ang);
+      const float rf = static_cast<float>(r);
+      cs[i] = make_float2(__cosf(rf), __sinf(rf));
+    }
+  }
+#pragma unroll 1
+  for (int r = tid; r < nhc; r += kT) hc[r] = bf(p.hidden_in[hr.lo + r]);
+  int tok = p.tok_in[0];
+  if (tok < 0 || tok >= p.V) {
+    if (c == 0 && tid == 0) atomicCAS(p.status, 0, static_cast<int>(MTP_ERR_INVALID_ARG));
+    tok = 0;
+  }
+  __syncthreads();
+
+  bool ok = true;
+  unsigned loaded = 0u;  // load groups already waited for
+  auto need_group = [&](int gi) {
+    if (ok && !(loaded >> gi & 1u)) {
+      ok = mbar_wait(p, sa(&bars[gi]), 0u, true);
+      loaded |= 1u << gi;
+    }
+  };
+  // PRE partial over the h columns: W_pre[:, my h cols] h'[my cols]
+  auto pre_h = [&]() {
+    const bf16* pre = reinterpret_cast<const bf16*>(sm + L.pre);
+#pragma unroll 1
+    for (int i = tid; i < H; i += kT) {
+      const bf16* wh = pre + i * L.kcp;
+      float v = 0.f;
+#pragma unroll 1
+      for (int k = 0; k < nhc; ++k) v = fmaf(bf(wh[k]), hc[k], v);
+      vh[i] = v;
+    }
+  };
+  int arn = 0;
+  need_group(0);
+  if (ok) pre_h();
+
+#pragma unroll 1
+  for (int s = 0; s < p.n_draft && ok; ++s) {
+    const unsigned ep0 = p.epoch_base + static_cast<unsigned>(s) * kExPerStep;
+    const long long* xo = p.ex_off[s & 1];
+    // ---------------- PRE: x0 = W_pre [h ; embed(tok)] over my columns, then all-reduce
+#pragma unroll 1
+    for (int r = tid; r < nhc; r += kT) red[r] = bf(p.tgt[static_cast<size_t>(tok) * p.bb + hr.lo + r]);
+    float gA[EPL];
+    ldg_vec<EPL>(p.attn_norm[0], gA);
+    __syncthreads();
+    {
+      const bf16* pre = reinterpret_cast<const bf16*>(sm + L.pre);
+#pragma unroll 1
+      for (int i = tid; i < H; i += kT) {
+        const bf16* we = pre + (H + i) * L.kcp;
+        float v = vh[i];
+#pragma unroll 1
+        for (int k = 0; k < nhc; ++k) v = fmaf(bf(we[k]), red[k], v);
+        vs[i] = v;
+      }
+    }
+    const bool skip = p.dbg_skip == c + 1 && s == 0;
+    float* xr = all_reduce(p, sm, vs, arn++, p.mb + xo[0], ep0, rank, g, skip, &ok);
+    if (!ok) break;
+    float x[EPL];
+    lds_vec<EPL>(xr, x);
+
+#pragma unroll 1
+    for (int l = 0; l < nl && ok; ++l) {
+      need_group(1 + l);
+      if (!ok) break;
+      const int t = p.ltype[l], lg = p.lg_d[t], d = 1 << lg, QD = nh * d;
+      const Range q_r = t ? qr1 : qr0;
+      const int nq = q_r.hi - q_r.lo;
+      // ---------------- Q: a = norm(x); my rows of W_q a
+      {
+        const float r = rms_inv<EPL>(x, p.eps);
+        float a[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) a[e] = x[e] * r * gA[e];
+        const bf16* wq = reinterpret_cast<const bf16*>(sm + L.q[l]);
+        unsigned long long* mq = p.mb + xo[ex_q(l)];
+#pragma unroll 1
+        for (int rr = warp; rr < nq; rr += kW) {
+          const float v = dot_row<EPL>(wq + rr * H, a);
+          if (lane == 0) put(mq, q_r.lo + rr, v, ep0 + ex_q(l));
+        }
+      }
+      // ---------------- ATT (attention CTAs): the partial softmax of my keys
+      unsigned long long* ma = p.mb + xo[ex_att(l)];
+      if (c < p.A[t]) {
+        // q_norm gains of this thread's first RoPE pairs, loaded before the q gather waits
+        float gq0 = 0.f, gq1 = 0.f, gq2 = 0.f, gq3 = 0.f, gq4 = 0.f, gq5 = 0.f, gq6 = 0.f, gq7 = 0.f;
+        {
+          const int half = d / 2, np = nh * half;
+          const float* gqn = p.q_norm[l];
+          if (tid < np) { gq0 = __ldg(gqn + (tid & (half - 1))); gq1 = __ldg(gqn + (tid & (half - 1)) + half); }
+          if (tid + kT < np) { gq2 = __ldg(gqn + ((tid + kT) & (half - 1))); gq3 = __ldg(gqn + ((tid + kT) & (half - 1)) + half); }
+          if (tid + 2 * kT < np) { gq4 = __ldg(gqn + ((tid + 2 * kT) & (half - 1))); gq5 = __ldg(gqn + ((tid + 2 * kT) & (half - 1)) + half); }
+          if (tid + 3 * kT < np) { gq6 = __ldg(gqn + ((tid + 3 * kT) & (half - 1))); gq7 = __ldg(gqn + ((tid + 3 * kT) & (half - 1)) + half); }
+        }
+        if (!gather_lin(p, p.mb + xo[ex_q(l)], QD, reinterpret_cast<unsigned*>(ub), ep0 + ex_q(l))) {
+          ok = false;
+          break;
+        }
+        const bool res = k_resident(t);
+        if (res) {
+          if (kcur != t) k_issue(t);  // not scheduled ahead (cannot happen with the schedule below)
+          if (kwaited < kph) {
+            ok = mbar_wait(p, sa(&bars[kbar]), static_cast<unsigned>(kph - 1) & 1u, true);
+            kwaited = kph;
+            if (!ok) break;
+          }
+        }
+        const Range kt = t ? kr1 : kr0;
+        const bf16* kb = res ? reinterpret_cast<const bf16*>(sm + L.kbuf)
+                             : p.k[t] + static_cast<size_t>((t ? 0 : klo0) + kt.lo) * static_cast<size_t>(p.st[t]);
+        const long long kst = res ? static_cast<long long>(p.nkv) * d : p.st[t];
+        attend(p, sm, l, t, c, kt.hi - kt.lo, kb, kst, ma, ep0 + ex_att(l), gq0, gq1, gq2, gq3, gq4, gq5, gq6, gq7);
+        // the next block of the other type (here or in the next step) finds its keys loaded
+        const bool last = l == nl - 1;
+        const int tn = p.ltype[last ? 0 : l + 1];
+        if (tn != t && k_resident(tn) && !(last && s == p.n_draft - 1)) {
+          __syncthreads();  // every read of the region is done
+          k_issue(tn);
+        }
+      }
+      // ---------------- O: combine the partials of my dims; partial o' = W_o[:, my dims] o
+      {
+        const int hlo = nq > 0 ? q_r.lo >> lg : 0, nht = heads_touched(q_r.lo, q_r.hi, d);
+        const int per = nq + 2 * nht, At = p.A[t];
+        if (!gather_part(p, ma, At * per, per, nq, q_r.lo, hlo, lg, reinterpret_cast<unsigned*>(ub),
+                         ep0 + ex_att(l))) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int w = warp; w < nq; w += kW) {
+          const int hl = ((q_r.lo + w) >> lg) - hlo;
+          float m = -INFINITY;
+#pragma unroll 4
+          for (int a = lane; a < At; a += 32) m = fmaxf(m, ub[a * per + nq + 2 * hl]);
+          m = warp_max(m);
+          float num = 0.f, den = 0.f;
+#pragma unroll 4
+          for (int a = lane; a < At; a += 32) {
+            const float ma_ = ub[a * per + nq + 2 * hl];
+            const float wgt = ma_ == -INFINITY ? 0.f : expf(ma_ - m);
+            num = fmaf(wgt, ub[a * per + w], num);
+            den = fmaf(wgt, ub[a * per + nq + 2 * hl + 1], den);
+          }
+          num = warp_sum(num);
+          den = warp_sum(den);
+          if (lane == 0) red[w] = den > 0.f ? num / den : 0.f;
+        }
+        __syncthreads();
+        const bf16* wo = reinterpret_cast<const bf16*>(sm + L.o[l]);
+#pragma unroll 1
+        for (int i = tid; i < H; i += kT) {
+          float v = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < nq; ++k) v = fmaf(bf(wo[i * L.nqp[l] + k]), red[k], v);
+          vs[i] = v;
+        }
+      }
+      float gPA[EPL], gF[EPL];
+      ldg_vec<EPL>(p.post_attn_norm[l], gPA);
+      ldg_vec<EPL>(p.ffn_norm[l], gF);
+      float* opr = all_reduce(p, sm, vs, arn++, p.mb + xo[ex_o(l)], ep0 + ex_o(l), rank, g, false, &ok);
+      if (!ok) break;
+      // ---------------- MLP: x += norm(o'); f = norm(x); my rows of gelu(W_g f) * W_u f
+      {
+        float o[EPL];
+        lds_vec<EPL>(opr, o);
+        const float ro = rms_inv<EPL>(o, p.eps);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x[e] += o[e] * ro * gPA[e];
+        const float rx = rms_inv<EPL>(x, p.eps);
+        float f[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) f[e] = x[e] * rx * gF[e];
+        const bf16* wg = reinterpret_cast<const bf16*>(sm + L.g[l]);
+        const bf16* wu = reinterpret_cast<const bf16*>(sm + L.u[l]);
+#pragma unroll 1
+        for (int rr = warp; rr < nf; rr += kW) {
+          const float gv = dot_row<EPL>(wg + rr * H, f);
+          const float uv = dot_row<EPL>(wu + rr * H, f);
+          if (lane == 0) ms[rr] = gelu_tanh(gv) * uv;
+        }
+        __syncthreads();
+        const bf16* wd = reinterpret_cast<const bf16*>(sm + L.dn[l]);
+#pragma unroll 1
+        for (int i = tid; i < H; i += kT) {
+          float v = 0.f;
+#pragma unroll 1
+          for (int k = 0; k < nf; ++k) v = fmaf(bf(wd[i * L.nfp + k]), ms[k], v);
+          vs[i] = v;
+        }
+      }
+      float gPF[EPL];
+      ldg_vec<EPL>(p.post_ffn_norm[l], gPF);
+      ldg_vec<EPL>(l + 1 < nl ? p.attn_norm[l + 1] : p.out_norm, gA);
+      float* dnr = all_reduce(p, sm, vs, arn++, p.mb + xo[ex_dn(l)], ep0 + ex_dn(l), rank, g, false, &ok);
+      if (!ok) break;
+      {
+        float dn[EPL];
+        lds_vec<EPL>(dnr, dn);
+        const float rd = rms_inv<EPL>(dn, p.eps);
+        const float lam = p.lambda[l];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x[e] = (x[e] + dn[e] * rd * gPF[e]) * lam;
+      }
+    }
+    if (!ok) break;
+
+    // ---------------- HEAD: y = output_norm(x) (gains in gA); my rows of h' and the centroid logits
+    need_group(nl + 1);
+    if (!ok) break;
+    float y[EPL];
+    {
+      const float r = rms_inv<EPL>(x, p.eps);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) y[e] = x[e] * r * gA[e];
+    }
+    {
+      const bf16* wp = reinterpret_cast<const bf16*>(sm + L.post);
+      const bf16* wc = reinterpret_cast<const bf16*>(sm + L.cent);
+      unsigned long long* mc = p.mb + xo[ex_cent(nl)];
+      const unsigned epc = ep0 + ex_cent(nl);
+#pragma unroll 1
+      for (int rr = warp; rr < ncr + nhc; rr += kW) {
+        if (rr < ncr) {
+          const float v = dot_row<EPL>(wc + rr * H, y);
+          if (lane == 0) put(mc, cr.lo + rr, v, epc);
+        } else {
+          const int q = rr - ncr;
+          const float v = dot_row<EPL>(wp + q * H, y);
+          if (lane == 0) {
+            hc[q] = v;
+            if (p.out_hidden) p.out_hidden[static_cast<size_t>(s) * p.bb + hr.lo + q] = v;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (s + 1 < p.n_draft) pre_h();  // the next step's h part, while the other CTAs catch up
+    // ---------------- TOP-K over the gathered centroid logits, then my candidate rows
+    if (!gather_lin(p, p.mb + xo[ex_cent(nl)], p.C, reinterpret_cast<unsigned*>(ub), ep0 + ex_cent(nl))) {
+      ok = false;
+      break;
+    }
+    topk_select(p, sm, ub, sel);
+    {
+      unsigned long long best = 0ull;
+      const int lgv = p.lg_vsc;
+#pragma unroll 1
+      for (int sl = candr.lo + warp; sl < candr.hi; sl += kW) {
+        int ce = sel[sl >> lgv];
+        ce = ce < 0 ? 0 : (ce >= p.C ? p.C - 1 : ce);
+        const long long rowi = (static_cast<long long>(ce) << lgv) + (sl & ((1 << lgv) - 1));
+        const int id = __ldg(p.ord + rowi);
+        const float v = dot_row<EPL>(p.temb_ord + rowi * H, y);
+        const unsigned long long key = argmax_key(v, id);
+        best = key > best ? key : best;
+      }
+      if (lane == 0) wkeys[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        unsigned long long b = lane < kW ? wkeys[lane] : 0ull;
+        b = warp_max_u64(b);
+        const int id = key_id(b);
+        if (lane == 0) {
+          unsigned long long* mk = p.mb + xo[ex_key(nl)];
+          put_u(mk, 2 * c, static_cast<unsigned>(b >> 32), ep0 + ex_key(nl));
+          put_u(mk, 2 * c + 1, static_cast<unsigned>(b), ep0 + ex_key(nl));
+        }
+        // warm L2 with this candidate's embedding row: the next step's PRE reads it if it wins
+        if (b != 0ull && id >= 0 && id < p.V && s + 1 < p.n_draft) {
+#pragma unroll 1
+          for (int off = lane * 128; off < p.bb * 2; off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.tgt + static_cast<size_t>(id) * p.bb) + off));
+        }
+      }
+    }
+    if (!gather_lin(p, p.mb + xo[ex_key(nl)], 2 * p.N, reinterpret_cast<unsigned*>(ub), ep0 + ex_key(nl))) {
+      ok = false;
+      break;
+    }
+    {
+      const unsigned* uk = reinterpret_cast<const unsigned*>(ub);
+      unsigned long long b = 0ull;
+#pragma unroll 1
+      for (int a = lane; a < p.N; a += 32) {
+        const unsigned long long kk = (static_cast<unsigned long long>(uk[2 * a]) << 32) | uk[2 * a + 1];
+        b = kk > b ? kk : b;
+      }
+      b = warp_max_u64(b);
+      int nt = key_id(b);
+      if (nt < 0 || nt >= p.V) nt = 0;
+      tok = nt;
+      if (c == 0 && tid == 0) p.out_tokens[s] = nt;
+    }
+  }
+  // ---- end: copies still in flight write shared memory; peers may still write into it
+#pragma unroll 1
+  for (int gi = 0; gi < nl + 2; ++gi)
+    if (!(loaded >> gi & 1u)) mbar_wait(p, sa(&bars[gi]), 0u, false);
+  if (kwaited < kph) mbar_wait(p, sa(&bars[kbar]), static_cast<unsigned>(kph - 1) & 1u, false);
+  __syncthreads();
+  cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ weight images
+
+// Copies one projection's share of every CTA into the per-CTA images. Row mode: dst [rows][K]
+// holds rows split(R, N, c) of W [R][K]. Column mode: dst [R][pitch] holds columns
+// col0 + split(Kpart, N, c) of W [R][Ktot]. Shares shorter than the section are zero-padded.
+struct PackJob {
+  const bf16* W;
+  int R, Ktot, col0, Kpart, mode, rows_max, pitch;  // mode 0 rows, 1 columns
+  long long sec_off;
+};
+__global__ void k_gr_pack(PackJob j, int N, long long img_bytes, unsigned char* dst) {
+  const int c = blockIdx.x;
+  bf16* out = reinterpret_cast<bf16*>(dst + static_cast<size_t>(c) * img_bytes + j.sec_off);
+  if (j.mode == 0) {
+    const Range r = split(j.R, N, c);
+    const long long n = static_cast<long long>(j.rows_max) * j.Ktot;
+    #pragma unroll 1
+    for (long long i = threadIdx.x + static_cast<long long>(blockIdx.y) * blockDim.x; i < n;
+         i += static_cast<long long>(blockDim.x) * gridDim.y) {
+      const int rr = static_cast<int>(i / j.Ktot), k = static_cast<int>(i % j.Ktot);
+      out[i] = r.lo + rr < r.hi ? j.W[static_cast<size_t>(r.lo + rr) * j.Ktot + k] : __float2bfloat16(0.f);
+    }
+  } else {
+    const Range r = split(j.Kpart, N, c);
+    const long long n = static_cast<long long>(j.R) * j.pitch;
+    #pragma unroll 1
+    for (long long i = threadIdx.x + static_cast<long long>(blockIdx.y) * blockDim.x; i < n;
+         i += static_cast<long long>(blockDim.x) * gridDim.y) {
+      const int row = static_cast<int>(i / j.pitch), k = static_cast<int>(i % j.pitch);
+      out[i] = r.lo + k < r.hi ? j.W[static_cast<size_t>(row) * j.Ktot + j.col0 + r.lo + k] : __float2bfloat16(0.f);
+    }
+  }
+}
+
+}  // namespace gr
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+template <int EPL>
+bool gr_attr(int smem) {
+  if (cudaFuncSetAttribute(gr::k_block_gr<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(gr::k_block_gr<EPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+template <int EPL>
+int gr_clusters(int S, int smem) {
+  if (!gr_attr<EPL>(smem)) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(S);
+  cfg.blockDim = dim3(gr::kT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<void*>(gr::k_block_gr<EPL>), &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+int clusters_for(int H, int S, int smem) {
+  switch (H) {
+    case 64: return gr_clusters<2>(S, smem);
+    case 128: return gr_clusters<4>(S, smem);
+    case 256: return gr_clusters<8>(S, smem);
+    case 512: return gr_clusters<16>(S, smem);
+    default: return 0;
+  }
+}
+
+// Attention CTAs, resident-key rows and the layout for a grid of N CTAs; false when the
+// shape cannot run on it.
+bool plan_for(gr::Params& p, int N, int S, int G, bool k_full_res, bool k_swa_res, int optin) {
+  p.N = N;
+  p.S = S;
+  p.G = G;
+  for (int t = 0; t < 2; ++t) {
+    if (!p.has_type[t]) {
+      p.A[t] = 0;
+      p.kres[t] = 0;
+      p.kslots[t] = 0;
+      continue;
+    }
+    const int keys = t == 0 ? (p.kv_max[t] < p.W ? p.kv_max[t] : p.W) : p.kv_max[t];
+    int A = gr::cdiv(keys, gr::kKeysPerCta);
+    A = A < 1 ? 1 : (A > N ? N : A);
+    p.A[t] = A;
+    p.kslots[t] = gr::cdiv(keys, A);
+    p.kres[t] = t == 0 ? (k_swa_res ? 1 : 0) : (k_full_res ? 1 : 0);
+  }
+  p.L = gr::make_layout(p);
+  const gr::Layout& L = p.L;
+  if (L.kc > 64 || L.total > optin) return false;
+  #pragma unroll 1
+  for (int l = 0; l < p.nl; ++l)
+    if (L.nq[l] > 64 || L.nf > 64 * 1024) return false;
+  return true;
+}
+
+}  // namespace
+
+// Chooses the cluster size and grid (every co-resident cluster of the largest size whose
+// plan fits, preferring attended keys resident in shared memory), fills the layout; returns
+// the dynamic shared-memory bytes (0: shape not supported by this path).
+int gr_plan(gr::Params& p, int optin) {
+  const int H = p.H;
+  if (H != 64 && H != 128 && H != 256 && H != 512) return 0;
+  if (p.nl < 1 || p.nl > gr::kMaxL || p.nh < 1 || p.nh > gr::kMaxHeads || p.nkv < 1 || p.nh % p.nkv ||
+      p.nh / p.nkv > gr::kMaxGroup)
+    return 0;
+  if (p.topk < 1 || p.topk > gr::kMaxTopK || p.C < p.topk || p.vsc < 1 || static_cast<long long>(p.C) * p.vsc != p.V)
+    return 0;
+  #pragma unroll 1
+  for (int l = 0; l < p.nl; ++l) {
+    const int d = p.d[p.ltype[l]];
+    if (d < 8 || d % 8 || p.nh * d > 8192) return 0;
+  }
+  for (int t = 0; t < 2; ++t)
+    if (p.has_type[t] && ((p.st[t] * 2) % 16 || (p.nkv * p.d[t] * 2) % 16)) return 0;
+  if (p.bb % 8) return 0;
+  // index arithmetic by shifts: head dims, vsc and every slice width are powers of two
+  auto lg2 = [](int v) {
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return (1 << l) == v ? l : -1;
+  };
+  for (int t = 0; t < 2; ++t) {
+    p.lg_d[t] = 0;
+    if (!p.has_type[t]) continue;
+    p.lg_d[t] = lg2(p.d[t]);
+    if (p.lg_d[t] < 3) return 0;
+  }
+  p.lg_vsc = lg2(p.vsc);
+  if (p.lg_vsc < 0) return 0;
+  const bool res_opts[3][2] = {{true, true}, {false, true}, {false, false}};
+  #pragma unroll 1
+  for (const auto& ro : res_opts) {
+    #pragma unroll 1
+    for (int S : {16, 8, 4}) {
+      if (H / S < 2 || (H / S) % 2) continue;
+      gr::Params q = p;
+      q.lg_hs = 0;
+      while ((1 << q.lg_hs) < H / S) ++q.lg_hs;
+      const int G = clusters_for(H, S, optin);
+      if (G < 1) continue;
+      if (!plan_for(q, G * S, S, G, ro[0], ro[1], optin)) continue;
+      // the grid must be co-resident at the planned size
+      const int G2 = clusters_for(H, S, q.L.total);
+      if (G2 < G) continue;
+      p = q;
+      return p.L.total;
+    }
+  }
+  return 0;
+}
+
+long long gr_image_total(const gr::Params& p) { return static_cast<long long>(p.N) * p.L.img_bytes; }
+
+// Packs every CTA's weight image (layout of gr::Layout) from the caller's matrices.
+int gr_pack(const gr::Params& p, const void* pre, const void* post, const void* cent, const void* const* q,
+            const void* const* o, const void* const* gate, const void* const* up, const void* const* down,
+            unsigned char* dst, cudaStream_t st) {
+  using gr::PackJob;
+  typedef const __nv_bfloat16* cb;
+  const gr::Layout& L = p.L;
+  const int H = p.H;
+  auto launch = [&](PackJob j) {
+    gr::k_gr_pack<<<dim3(p.N, 8), 256, 0, st>>>(j, p.N, L.img_bytes, dst);
+  };
+  launch(PackJob{static_cast<cb>(pre), H, 2 * p.bb, 0, p.bb, 1, 0, L.kcp, L.pre});
+  launch(PackJob{static_cast<cb>(pre), H, 2 * p.bb, p.bb, p.bb, 1, 0, L.kcp, L.pre + 2LL * H * L.kcp});
+  launch(PackJob{static_cast<cb>(post), p.bb, H, 0, 0, 0, L.kc, 0, L.post});
+  #pragma unroll 1
+  for (int l = 0; l < p.nl; ++l) {
+    const int QD = p.nh * p.d[p.ltype[l]];
+    launch(PackJob{static_cast<cb>(q[l]), QD, H, 0, 0, 0, L.nq[l], 0, L.q[l]});
+    launch(PackJob{static_cast<cb>(o[l]), H, QD, 0, QD, 1, 0, L.nqp[l], L.o[l]});
+    launch(PackJob{static_cast<cb>(gate[l]), p.F, H, 0, 0, 0, L.nf, 0, L.g[l]});
+    launch(PackJob{static_cast<cb>(up[l]), p.F, H, 0, 0, 0, L.nf, 0, L.u[l]});
+    launch(PackJob{static_cast<cb>(down[l]), H, p.F, 0, p.F, 1, 0, L.nfp, L.dn[l]});
+  }
+  launch(PackJob{static_cast<cb>(cent), p.C, H, 0, 0, 0, L.ncent, 0, L.cent});
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("packing the grid path's weight images: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+// Mailbox offsets of every exchange (both step parities); returns the total words.
+long long gr_mailboxes(gr::Params& p) {
+  long long off = 0;
+  const int n = gr::ex_count(p.nl);
+  for (int par = 0; par < 2; ++par)
+    #pragma unroll 1
+    for (int x = 0; x < gr::kMaxEx; ++x) {
+      p.ex_off[par][x] = off;
+      if (x < n) off += (gr::ex_words(p, x) + 31) & ~31LL;
+    }
+  return off;
+}
+
+int run_gr(const gr::Params& p, cudaStream_t st) {
+  const int smem = p.L.total;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = p.S;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(p.N);
+  cfg.blockDim = dim3(gr::kT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (p.H) {
+    case 64: e = gr_attr<2>(smem) ? cudaLaunchKernelEx(&cfg, gr::k_block_gr<2>, p) : cudaErrorInvalidValue; break;
+    case 128: e = gr_attr<4>(smem) ? cudaLaunchKernelEx(&cfg, gr::k_block_gr<4>, p) : cudaErrorInvalidValue; break;
+    case 256: e = gr_attr<8>(smem) ? cudaLaunchKernelEx(&cfg, gr::k_block_gr<8>, p) : cudaErrorInvalidValue; break;
+    case 512: e = gr_attr<16>(smem) ? cudaLaunchKernelEx(&cfg, gr::k_block_gr<16>, p) : cudaErrorInvalidValue; break;
+    default: break;
+  }
+  if (e != cudaSuccess) {
+    set_error("grid draft-block launch (%d CTAs in clusters of %d, %d B shared memory): %s", p.N, p.S, smem,
+              cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
+}  // namespace mtp

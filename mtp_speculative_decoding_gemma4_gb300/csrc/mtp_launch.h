@@ -20,6 +20,9 @@ struct Params;
 namespace c2 {
 struct Params;
 }
+namespace gr {
+struct Params;
+}
 
 // Records the calling thread's last error text (printf-style).
 void set_error(const char* fmt, ...);
@@ -66,6 +69,18 @@ int c2_capacity(int smem);
 int run_c2(const c2::Params& p, int smem, cudaStream_t st);
 long long c2_stream_total(const c2::Params& p);
 int c2_pack_all(const c2::Params& p, const void* const* mats, void* dst, cudaStream_t st);
+
+// Grid draft block (one sequence, every co-resident cluster, split weights resident in shared
+// memory): the plan (cluster size, grid, layout; returns the shared-memory bytes, 0 when the
+// shape is not supported), the per-CTA weight images, the mailbox offsets (returns the words
+// of both step parities) and the launch.
+int gr_plan(gr::Params& p, int optin);
+long long gr_image_total(const gr::Params& p);
+int gr_pack(const gr::Params& p, const void* pre, const void* post, const void* cent, const void* const* q,
+            const void* const* o, const void* const* gate, const void* const* up, const void* const* down,
+            unsigned char* dst, cudaStream_t st);
+long long gr_mailboxes(gr::Params& p);
+int run_gr(const gr::Params& p, cudaStream_t st);
 
 // Tensor maps of the tensor-core phase path (host memory; see mtp_tc.cuh): every weight
 // matrix, and the staged input terms [3][bp][K] for each input width K.

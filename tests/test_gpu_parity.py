@@ -15,8 +15,8 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR, STREAMED = 1, 2, 3, 4, 5, 6
-ONE_SEQ = [LATENCY, CLUSTER, STREAMED]  # the single-sequence paths
+PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR, STREAMED, GRID = 1, 2, 3, 4, 5, 6, 7
+ONE_SEQ = [LATENCY, CLUSTER, STREAMED, GRID]  # the single-sequence paths
 
 
 def _drafter(index, batch=0, ctx=0, max_batch=0):
@@ -117,7 +117,7 @@ def _one_sequence_case(index, ctx_len, storage_ctx, n_draft, seed_offset=0):
     return shape, w, inp, ref
 
 
-@pytest.mark.parametrize("path", [0, STREAMED])
+@pytest.mark.parametrize("path", [0, STREAMED, GRID])
 @pytest.mark.parametrize("index,ctx,storage", [
     (2, 32768, 32768),   # E4B backbone at the longest context of its workload
     (2, 20001, 32768),   # E4B, ragged: not a multiple of the 128-key attention chunk
@@ -126,12 +126,19 @@ def _one_sequence_case(index, ctx_len, storage_ctx, n_draft, seed_offset=0):
     (1, 513, 1024),      # E2B, one key past the window (the sliding layers drop key 0)
 ])
 def test_one_sequence_path_long_ragged_and_window_contexts(index, ctx, storage, path):
-    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter, MtpError, binding
     shape, w, inp, ref = _one_sequence_case(index, ctx, storage, 4)
     wd, tgt = weights_to_device(w)
     dr = Drafter(shape, wd, tgt, max_batch=1, max_ctx=storage)
     d = inputs_to_device(inp, shape.dtype)
-    tok, hid = _run_block(dr, d, 4, path)
+    try:
+        tok, hid = _run_block(dr, d, 4, path)
+    except MtpError as e:
+        # a forced single-sequence path may refuse a shape outside its plan (the streamed
+        # cluster kernel takes no E4B backbone); the automatic path must always run
+        dr.close()
+        assert path != 0 and e.code == binding.MTP_ERR_UNSUPPORTED_SHAPE, e
+        pytest.skip(f"path {path} does not take this shape: {e}")
     cmp = compare_block(tok, hid, ref, shape.dtype)
     print(f"config {index} ctx {ctx} path {path}: max hidden err {cmp.max_hidden_err:.3g}, "
           f"near-ties {cmp.tie_divergences}")
@@ -325,6 +332,28 @@ def test_a_missing_grid_barrier_arrival_times_out_and_the_handle_recovers():
     assert dr.status() == binding.MTP_OK  # reading the word cleared it
     dr.set_debug()
     tok, hid = _run_block(dr, d, wl.n_draft, PERSISTENT)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    assert len(cmp.tie_divergences) <= 1
+    dr.close()
+
+
+def test_grid_path_timeout_is_reported_and_the_handle_recovers():
+    # failure detection without a fault on the default one-sequence path: CTA 0 of the grid
+    # kernel does not publish its slice of the first all-reduce, every bounded wait gives up
+    # after ~10 ms of cycles, the status word reads MTP_ERR_TIMEOUT, and the next call on the
+    # same handle matches the oracle
+    from mtp_speculative_decoding_gemma4_gb300 import binding
+    shape, wl, w, inp = config_data(1)
+    ref = oracle_block(1)
+    dr, d = _drafter(1)
+    dr.set_path(GRID)
+    dr.set_debug(skip_arrival_cta=0, spin_limit_cycles=20_000_000)
+    dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], wl.n_draft)
+    torch.cuda.synchronize()
+    assert dr.status() == binding.MTP_ERR_TIMEOUT
+    assert dr.status() == binding.MTP_OK
+    dr.set_debug()
+    tok, hid = _run_block(dr, d, wl.n_draft, GRID)
     cmp = compare_block(tok, hid, ref, shape.dtype)
     assert len(cmp.tie_divergences) <= 1
     dr.close()

@@ -99,7 +99,6 @@ def measured_peaks():
 # The device code each captured kernel is compiled from (its translation unit and the device
 # headers it includes); other kernels hash the whole csrc directory.
 KERNEL_SOURCES = {"k_block_c2": ("mtp_c2.cu", "mtp_c2.cuh", "mtp_common.cuh"),
-                  "k_block_ll": ("mtp_ll.cu", "mtp_ll.cuh", "mtp_common.cuh"),
                   "k_block_gr": ("mtp_grid.cu", "mtp_grid.cuh", "mtp_common.cuh")}
 
 
@@ -374,15 +373,13 @@ def run_mtp(args, rank: int, world: int, dist):
     achieved = per_launch / (draft_ms_mean * 1e-3) / 1e9
     tokens = B * n * world  # every replica drafts B * n tokens per step
     head = (3 if shape.use_ordered_embeddings else 1)
-    if args.path in (2, 3, 4, 6, 7):
+    if args.path in (2, 6, 7):
         launches_per_step = 2
     elif args.path == 5:  # per step: staging + tcgen05 GEMM per projection, attention, combine, head
         launches_per_step = 1 + n * (2 + 11 * shape.n_layers + 2 + head) + 1 + 1
     else:
         launches_per_step = 1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1
     kernel_name = {1: "phase kernels", 2: "k_block (persistent draft block, grid barriers)",
-                   3: "k_block_ll (latency draft block, resident weights + mailboxes)",
-                   4: "k_block_cl (cluster draft block, streamed weights + DSMEM exchanges)",
                    5: "k_tc_gemm + phase kernels (tcgen05 projections)",
                    6: "k_block_c2 (streamed-tile cluster draft block, tensor-core projections)",
                    7: "k_block_gr (grid draft block: split weights resident in shared memory, cluster + "
@@ -533,10 +530,9 @@ def main():
     ap.add_argument("--impl", choices=["mtp", "reference"], default="mtp")
     ap.add_argument("--config", type=int, default=1, help="benchmark configuration index (default 1: E2B, B=1)")
     ap.add_argument("--path", type=int, default=-1,
-                    help="1: one launch per phase, 2: persistent kernel with grid barriers, 3: latency kernel "
-                         "(one sequence), 4: cluster kernel (one sequence), 5: phase kernels with tcgen05 "
-                         "projections, 6: streamed-tile cluster kernel (one sequence), 7: grid kernel (one "
-                         "sequence); default: 7 for B=1, else 5")
+                    help="1: one launch per phase, 2: persistent kernel with grid barriers, 5: phase kernels "
+                         "with tcgen05 projections, 6: streamed-tile cluster kernel (one sequence), 7: grid "
+                         "kernel (one sequence); default: 7 for B=1, else 5")
     ap.add_argument("--profile-blocks", type=int, default=0,
                     help="run exactly this many draft blocks of the chosen path and exit without timing "
                          "(the program the ncu captures in profiles/ name)")

@@ -304,33 +304,27 @@ MTP_API int mtp_get_status(mtp_handle *h);
 MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_limit_cycles);
 
 /* Select the implementation of mtp_draft_block: 0 = automatic, 1 = one kernel per phase,
- * 2 = persistent whole-block kernel with grid barriers, 3 = latency kernel for one sequence
- * (weights and attended K resident in shared memory, CTAs exchanging vectors through
- * mailboxes; bf16 centroid-head shapes whose per-SM share fits shared memory, V = K),
- * 4 = cluster kernel for one sequence (one 16-CTA thread-block cluster streams the weights
- * and the attended K through shared memory and exchanges vectors in distributed shared
- * memory; bf16 centroid-head shapes within its buffer limits, V = K; mtp_init_weights keeps
- * a copy of token_embd in token_ordering order and tensor-core tiles of the hidden-wide
- * matrices for it), 5 = one kernel per phase with every projection (and the dense tied
- * head) as a tcgen05 tensor-core GEMM (bf16, max_batch <= 64; mtp_init_weights keeps the
- * tensor maps and a staging buffer of 3 * roundup(max_batch, 32) * max input width bf16),
- * 6 = streamed-tile cluster kernel for one sequence (one 16-CTA cluster; every projection on
- * tensor cores from weight tiles that mtp_init_weights packs once into one stream per CTA,
- * about the size of all projection weights; vectors exchanged register-to-peer in
- * distributed shared memory; bf16 centroid-head shapes within its limits, V = K, 16-byte
- * aligned hidden and K rows), 7 = grid kernel for one sequence (every co-resident thread-block
- * cluster of the GPU; each projection split over all CTAs by rows or by input columns, the
- * split weights and the attended K resident in shared memory for the whole block -- K of long
- * contexts is read from global memory instead --, vectors exchanged by all-gathers and
- * all-reduces over distributed shared memory and epoch-tagged global mailboxes; bf16
- * centroid-head shapes with hidden in {64, 128, 256, 512} whose per-CTA share fits shared
- * memory, V = K, 16-byte aligned K rows; mtp_init_weights packs the per-CTA weight images,
- * about the size of all projection weights). Automatic picks 7 for B = 1 when available,
- * else 6, else 4, else 3;
- * 5 for B >= 2 when available; else 2 when co-resident, else 1. Results agree within the
- * precision contract.
- * Errors: INVALID_ARG; a forced path the call cannot use makes mtp_draft_block return
- * UNSUPPORTED_SHAPE. */
+ * 2 = persistent whole-block kernel with grid barriers, 5 = one kernel per phase with every
+ * projection (and the dense tied head) as a tcgen05 tensor-core GEMM (bf16, max_batch <= 64;
+ * mtp_init_weights keeps the tensor maps and a staging buffer of 3 * roundup(max_batch, 32) *
+ * max input width bf16), 6 = streamed-tile cluster kernel for one sequence (one 16-CTA
+ * cluster; every projection on tensor cores from weight tiles that mtp_init_weights packs
+ * once into one stream per CTA, about the size of all projection weights; vectors exchanged
+ * register-to-peer in distributed shared memory; bf16 centroid-head shapes within its
+ * limits, one KV head, V = K, 16-byte aligned hidden and K rows), 7 = grid kernel for one
+ * sequence (every co-resident thread-block cluster of the GPU; each projection split over
+ * all CTAs by rows or by input columns, the split weights and the attended K resident in
+ * shared memory -- K of long contexts is read from global memory instead --, vectors
+ * exchanged by all-gathers and all-reduces over distributed shared memory and epoch-tagged
+ * global mailboxes; bf16 centroid-head shapes with hidden in {64, 128, 256, 512},
+ * power-of-two head dims and vocab / n_centroids, whose per-CTA share fits shared memory,
+ * V = K, 16-byte aligned K rows; mtp_init_weights packs the per-CTA weight images, about the
+ * size of all projection weights). Paths 3 and 4 (earlier single-sequence kernels) no longer
+ * exist and are rejected. Automatic picks 7 for B = 1 when available, else 6; 5 for B >= 2
+ * when available; else 2 when co-resident, else 1. Results agree within the precision
+ * contract.
+ * Errors: INVALID_ARG (NULL handle, path outside {0, 1, 2, 5, 6, 7}); a forced path the call
+ * cannot use makes mtp_draft_block return UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);
 
 /* Free the workspace and the handle (synchronises). NULL is ignored. */

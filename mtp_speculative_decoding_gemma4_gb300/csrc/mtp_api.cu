@@ -11,9 +11,7 @@
 #include "mtp_launch.h"
 #include "mtp_c2.cuh"
 #include "mtp_grid.cuh"
-#include "mtp_cl.cuh"
 #include "mtp_tc.cuh"
-#include "mtp_ll.cuh"
 #include "mtp_phases.cuh"
 
 struct mtp_handle {
@@ -34,17 +32,11 @@ struct mtp_handle {
   void* ws;
   size_t ws_bytes;
   mtp::WsP wsp;
-  // latency path (one sequence): availability, mailboxes, epoch counter, abort word
-  int ll_ok;
-  unsigned long long* mb[10];
-  unsigned* ll_abort;
-  unsigned epoch;
-  // cluster path (one sequence): availability, token_embd in token_ordering order, and the
-  // hidden-wide matrices re-laid out as tensor-core tiles (one allocation)
-  int cl_ok;
+  // abort word of the single-sequence paths (a bounded wait that gives up raises it)
+  unsigned* abort_word;
+  // token_embd in token_ordering order (the rows of one centroid contiguous): single-sequence
+  // paths and the cluster-major head
   void* temb_ord;
-  void* wpack;
-  const __nv_bfloat16 *pk_q[MTP_MAX_LAYERS], *pk_gate[MTP_MAX_LAYERS], *pk_up[MTP_MAX_LAYERS], *pk_cent, *pk_post;
   // streamed-tile cluster path (one sequence): availability and the packed weight streams
   int c2_ok;
   void* c2_stream;
@@ -210,191 +202,6 @@ int check_ordering(const mtp_config& c, const int32_t* ord) {
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-// Latency-path parameters that depend only on the handle (shapes, weights, CTA count).
-mtp::ll::Params ll_template(const mtp_handle* h, int kv_max) {
-  const mtp_config& c = h->cfg;
-  mtp::ll::Params p;
-  memset(&p, 0, sizeof(p));
-  p.N = h->num_sms;
-  p.bb = c.backbone;
-  p.H = c.hidden;
-  p.nl = c.n_layers;
-  p.nh = c.n_head;
-  p.nkv = c.n_kv_head;
-  p.F = c.ffn;
-  p.V = c.vocab;
-  p.C = c.n_centroids;
-  p.topk = c.top_k;
-  p.vsc = c.use_ordered_embeddings ? c.vocab / c.n_centroids : 0;
-  p.W = c.window;
-  p.d[0] = c.head_dim_swa;
-  p.d[1] = c.head_dim_full;
-  for (int t = 0; t < 2; ++t) {
-    const int d = p.d[t] > 0 ? p.d[t] : 1;
-    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
-  }
-  p.theta[0] = c.rope_theta_swa;
-  p.theta[1] = c.rope_theta_full;
-  p.eps = c.rms_eps;
-  typedef const __nv_bfloat16* cb;
-  p.pre = static_cast<cb>(h->w.pre_proj);
-  p.post = static_cast<cb>(h->w.post_proj);
-  p.temb = static_cast<cb>(h->w.token_embd);
-  p.cent = static_cast<cb>(h->w.centroids);
-  p.tgt = static_cast<cb>(h->target_embed);
-  p.out_norm = h->w.out_norm;
-  p.ord = h->w.token_ordering;
-  for (int l = 0; l < c.n_layers; ++l) {
-    const mtp_layer_weights& L = h->w.layer[l];
-    p.ltype[l] = c.layer_type[l];
-    p.lambda[l] = L.layer_scalar;
-    p.q[l] = static_cast<cb>(L.q);
-    p.o[l] = static_cast<cb>(L.o);
-    p.gate[l] = static_cast<cb>(L.gate);
-    p.up[l] = static_cast<cb>(L.up);
-    p.down[l] = static_cast<cb>(L.down);
-    p.q_norm[l] = L.q_norm;
-    p.attn_norm[l] = L.attn_norm;
-    p.post_attn_norm[l] = L.post_attn_norm;
-    p.ffn_norm[l] = L.ffn_norm;
-    p.post_ffn_norm[l] = L.post_ffn_norm;
-  }
-  for (int t = 0; t < 2; ++t) {
-    p.has_type[t] = has_type(c, t);
-    p.kv_max[t] = kv_max;
-  }
-  p.spin_limit = 4000000000LL;
-  return p;
-}
-
-// Whether the latency path can run this configuration on this device.
-bool ll_supported(const mtp_handle* h) {
-  const mtp_config& c = h->cfg;
-  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings || c.n_head > 8) return false;
-  for (int l = 0; l < c.n_layers; ++l) {
-    const int d = c.layer_type[l] ? c.head_dim_full : c.head_dim_swa;
-    if (d % 8 || c.hidden % 8 || c.backbone % 8 || c.ffn % 8) return false;
-  }
-  const mtp::ll::Params p = ll_template(h, c.max_ctx);
-  const int smem = mtp::ll_smem_bytes(p);
-  int optin = 0;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  if (smem <= 0 || smem > optin) return false;
-  return mtp::ll_capacity(smem, h->num_sms) >= h->num_sms;
-}
-
-// Cluster-path parameters that depend only on the handle.
-mtp::clk::Params cl_template(const mtp_handle* h, int kv_max) {
-  const mtp_config& c = h->cfg;
-  mtp::clk::Params p;
-  memset(&p, 0, sizeof(p));
-  p.bb = c.backbone;
-  p.H = c.hidden;
-  p.nl = c.n_layers;
-  p.nh = c.n_head;
-  p.nkv = c.n_kv_head;
-  p.F = c.ffn;
-  p.V = c.vocab;
-  p.C = c.n_centroids;
-  p.topk = c.top_k;
-  p.vsc = c.use_ordered_embeddings && c.n_centroids > 0 ? c.vocab / c.n_centroids : 0;
-  p.W = c.window;
-  p.d[0] = c.head_dim_swa;
-  p.d[1] = c.head_dim_full;
-  for (int t = 0; t < 2; ++t) {
-    const int d = p.d[t] > 0 ? p.d[t] : 1;
-    p.scale[t] = c.attn_scale > 0.f ? c.attn_scale : 1.0f / sqrtf(static_cast<float>(d));
-  }
-  p.theta[0] = c.rope_theta_swa;
-  p.theta[1] = c.rope_theta_full;
-  p.eps = c.rms_eps;
-  typedef const __nv_bfloat16* cb;
-  p.pre = static_cast<cb>(h->w.pre_proj);
-  p.post = static_cast<cb>(h->w.post_proj);
-  p.cent = static_cast<cb>(h->w.centroids);
-  p.tgt = static_cast<cb>(h->target_embed);
-  p.temb_ord = static_cast<cb>(h->temb_ord);
-  p.mma = h->wpack != nullptr;
-  p.pk_cent = h->pk_cent;
-  p.pk_post = h->pk_post;
-  p.out_norm = h->w.out_norm;
-  p.ord = h->w.token_ordering;
-  for (int l = 0; l < c.n_layers; ++l) {
-    const mtp_layer_weights& L = h->w.layer[l];
-    p.ltype[l] = c.layer_type[l];
-    p.lambda[l] = L.layer_scalar;
-    p.q[l] = static_cast<cb>(L.q);
-    p.o[l] = static_cast<cb>(L.o);
-    p.gate[l] = static_cast<cb>(L.gate);
-    p.up[l] = static_cast<cb>(L.up);
-    p.down[l] = static_cast<cb>(L.down);
-    p.q_norm[l] = L.q_norm;
-    p.attn_norm[l] = L.attn_norm;
-    p.post_attn_norm[l] = L.post_attn_norm;
-    p.ffn_norm[l] = L.ffn_norm;
-    p.post_ffn_norm[l] = L.post_ffn_norm;
-    p.pk_q[l] = h->pk_q[l];
-    p.pk_gate[l] = h->pk_gate[l];
-    p.pk_up[l] = h->pk_up[l];
-  }
-  for (int t = 0; t < 2; ++t) {
-    p.has_type[t] = has_type(c, t);
-    p.kv_max[t] = kv_max;
-  }
-  p.spin_limit = 4000000000LL;  // ~2 s at 2 GHz
-  return p;
-}
-
-// Re-lays out the hidden-wide matrices (Q, gate, up per block; centroids; post_projection)
-// as tensor-core tiles for the cluster path. Returns MTP_OK with h->wpack NULL when the shape
-// does not allow it (the path then uses its CUDA-core GEMVs).
-int build_packed(mtp_handle* h) {
-  const mtp_config& c = h->cfg;
-  h->wpack = nullptr;
-  const int H = c.hidden;
-  if (H % 64 != 0 || H > 512) return MTP_OK;  // the GEMV keeps a k quarter of B fragments (H / 64 <= 8 steps)
-  struct Item {
-    const void* W;
-    int R;
-    const __nv_bfloat16** out;
-  };
-  std::vector<Item> items;
-  for (int l = 0; l < c.n_layers; ++l) {
-    const int d = c.layer_type[l] ? c.head_dim_full : c.head_dim_swa;
-    items.push_back({h->w.layer[l].q, c.n_head * d, &h->pk_q[l]});
-    items.push_back({h->w.layer[l].gate, c.ffn, &h->pk_gate[l]});
-    items.push_back({h->w.layer[l].up, c.ffn, &h->pk_up[l]});
-  }
-  items.push_back({h->w.centroids, c.n_centroids, &h->pk_cent});
-  items.push_back({h->w.post_proj, c.backbone, &h->pk_post});
-  size_t total = 0;
-  for (const Item& it : items) total += static_cast<size_t>(mtp::packed_tile_bytes(it.R, H));
-  void* buf = nullptr;
-  cudaError_t e = cudaMalloc(&buf, total);
-  if (e != cudaSuccess) return cuda_fail("allocating the tensor-core weight tiles", e);
-  size_t off = 0;
-  for (const Item& it : items) {
-    char* dst = static_cast<char*>(buf) + off;
-    const int rc = mtp::pack_tiles(it.W, it.R, H, dst, 0);
-    if (rc) {
-      cudaFree(buf);
-      return rc;
-    }
-    *it.out = reinterpret_cast<const __nv_bfloat16*>(dst);
-    off += static_cast<size_t>(mtp::packed_tile_bytes(it.R, H));
-  }
-  e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) {
-    cudaFree(buf);
-    return cuda_fail("packing the tensor-core weight tiles", e);
-  }
-  h->wpack = buf;
-  return MTP_OK;
-}
-
 // Tensor maps and staging buffer of the tensor-core phase path; leaves h->tc NULL when the
 // configuration or the device does not allow it.
 int build_tc(mtp_handle* h) {
@@ -458,21 +265,6 @@ int build_tc(mtp_handle* h) {
   }
   h->tc = plan;
   return MTP_OK;
-}
-
-// Whether the cluster path can run this configuration on this device.
-bool cl_supported(const mtp_handle* h) {
-  const mtp_config& c = h->cfg;
-  if (c.dtype != MTP_DTYPE_BF16 || !c.use_ordered_embeddings) return false;
-  const mtp::clk::Params p = cl_template(h, c.max_ctx);
-  const int smem = mtp::cl_smem_bytes(p);
-  int optin = 0;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  if (smem <= 0 || smem > optin) return false;
-  return mtp::cl_capacity(smem) >= 1;
 }
 
 // Streamed-tile cluster-path parameters that depend only on the handle.
@@ -716,14 +508,7 @@ size_t layout_ws(mtp_handle* h, char* base) {
   w.cs = static_cast<float2*>(take(8 * B * 2 * (dmax / 2)));
   w.bar = static_cast<unsigned int*>(take(16));
   w.status = static_cast<int*>(take(16));
-  h->ll_abort = static_cast<unsigned*>(take(16));
-  for (int i = 0; i < 10; ++i) h->mb[i] = nullptr;
-  if (h->ll_ok) {
-    mtp::ll::Params lp = ll_template(h, c.max_ctx);
-    const mtp::ll::MailboxSizes m = mtp::ll::mailbox_sizes(lp);
-    const long long n[10] = {m.x0, m.q, m.part, m.o, m.op, m.m, m.dn, m.h, m.cent, m.key};
-    for (int i = 0; i < 10; ++i) h->mb[i] = static_cast<unsigned long long*>(take(8 * static_cast<size_t>(n[i])));
-  }
+  h->abort_word = static_cast<unsigned*>(take(16));
   w.nsplit_max = static_cast<int>(ns);
   w.dmax = static_cast<int>(dmax);
   return off;
@@ -833,7 +618,6 @@ mtp::Params base_params(const mtp_handle* h, int B) {
 void release_handle(mtp_handle* h) {
   if (h->ws) cudaFree(h->ws);
   if (h->temb_ord) cudaFree(h->temb_ord);
-  if (h->wpack) cudaFree(h->wpack);
   if (h->c2_stream) cudaFree(h->c2_stream);
   if (h->gr_img) cudaFree(h->gr_img);
   if (h->gr_mb) cudaFree(h->gr_mb);
@@ -936,9 +720,6 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
   int ns = (config->max_ctx + 31) / 32;
   if (ns > 4 * h->num_sms) ns = 4 * h->num_sms;
   h->nsplit_max = ns < 1 ? 1 : ns;
-  h->ll_ok = ll_supported(h) ? 1 : 0;
-  h->epoch = 64u;
-  h->cl_ok = cl_supported(h) ? 1 : 0;
   h->c2_ok = c2_supported(h) ? 1 : 0;
   h->temb_ord = nullptr;
   h->c2_stream = nullptr;
@@ -976,10 +757,9 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
       return rc ? rc : cuda_fail("building the cluster-ordered token_embd copy", e);
     }
   }
-  if (!h->temb_ord) h->cl_ok = h->c2_ok = 0;
-  if (h->cl_ok || h->c2_ok) {
-    rc = h->cl_ok ? build_packed(h) : MTP_OK;
-    if (!rc && h->c2_ok) rc = build_c2_stream(h);
+  if (!h->temb_ord) h->c2_ok = 0;
+  if (h->c2_ok) {
+    rc = build_c2_stream(h);
     if (rc) {
       release_handle(h);
       return rc;
@@ -1081,7 +861,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     gp.out_hidden = out_hidden;
     gp.n_draft = n_draft;
     gp.status = h->wsp.status;
-    gp.abort_flag = h->ll_abort;
+    gp.abort_flag = h->abort_word;
     gp.spin_limit = h->dbg_spin > 0 ? h->dbg_spin : 4000000000LL;
     gp.dbg_skip = h->dbg_skip;
     const unsigned need = static_cast<unsigned>(n_draft + 1) * mtp::gr::kExPerStep;
@@ -1093,7 +873,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     }
     gp.epoch_base = h->gr_epoch;
     h->gr_epoch += need;
-    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    cudaError_t e = cudaMemsetAsync(h->abort_word, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
     return mtp::run_gr(gp, st);
   }
@@ -1126,110 +906,17 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     cp.out_hidden = out_hidden;
     cp.n_draft = n_draft;
     cp.status = h->wsp.status;
-    cp.abort_flag = h->ll_abort;
+    cp.abort_flag = h->abort_word;
     const int smem = mtp::c2_smem_bytes(cp);
     if (smem <= 0 || (reinterpret_cast<uintptr_t>(hidden) & 15) != 0) {
       set_error("streamed cluster path: shape, K stride or hidden alignment not supported for this call");
       return MTP_ERR_UNSUPPORTED_SHAPE;
     }
-    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
+    cudaError_t e = cudaMemsetAsync(h->abort_word, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
     return mtp::run_c2(cp, smem, st);
   }
-  if (path == 4 || (path == 0 && B == 1 && h->cl_ok)) {
-    if (!h->cl_ok || B != 1) {
-      set_error("the cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->cl_ok);
-      return MTP_ERR_UNSUPPORTED_SHAPE;
-    }
-    const int kvm = has_type(c, 1) ? kv_full->max_ctx : kv_sliding->max_ctx;
-    mtp::clk::Params cp = cl_template(h, kvm);
-    for (int t = 0; t < 2; ++t) {
-      if (!cp.has_type[t]) continue;
-      if (kvs[t]->v) {
-        set_error("the cluster path reads V = K (attention_k_eq_v); pass v = NULL");
-        return MTP_ERR_UNSUPPORTED_SHAPE;
-      }
-      cp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
-      cp.ctx_len[t] = kvs[t]->ctx_len;
-      cp.st[t] = kvs[t]->stride_t;
-      cp.kv_max[t] = kvs[t]->max_ctx;
-    }
-    cp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
-    cp.tok_in = last_token;
-    cp.pos = pos;
-    cp.out_tokens = out_tokens;
-    cp.out_hidden = out_hidden;
-    cp.n_draft = n_draft;
-    cp.status = h->wsp.status;
-    cp.abort_flag = h->ll_abort;
-    const int smem = mtp::cl_smem_bytes(cp);
-    if (smem <= 0) {
-      set_error("cluster path: shape not supported for this call");
-      return MTP_ERR_UNSUPPORTED_SHAPE;
-    }
-    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
-    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
-    return mtp::run_cl(cp, smem, st);
-  }
-  if (path == 3 || (path == 0 && B == 1 && h->ll_ok)) {
-    if (!h->ll_ok || B != 1) {
-      set_error("the latency path runs one sequence of a supported shape (B=%d, available=%d)", B, h->ll_ok);
-      return MTP_ERR_UNSUPPORTED_SHAPE;
-    }
-    const int kvm = has_type(c, 1) ? kv_full->max_ctx : kv_sliding->max_ctx;
-    mtp::ll::Params lp = ll_template(h, kvm);
-    for (int t = 0; t < 2; ++t) {
-      if (!lp.has_type[t]) continue;
-      lp.k[t] = static_cast<const __nv_bfloat16*>(kvs[t]->k);
-      lp.v[t] = static_cast<const __nv_bfloat16*>(kvs[t]->v);
-      lp.ctx_len[t] = kvs[t]->ctx_len;
-      lp.sb[t] = kvs[t]->stride_b;
-      lp.st[t] = kvs[t]->stride_t;
-      lp.kv_max[t] = kvs[t]->max_ctx;
-    }
-    if (lp.v[0] || lp.v[1]) {
-      set_error("the latency path reads V = K (attention_k_eq_v); pass v = NULL");
-      return MTP_ERR_UNSUPPORTED_SHAPE;
-    }
-    lp.hidden_in = static_cast<const __nv_bfloat16*>(hidden);
-    lp.tok_in = last_token;
-    lp.pos = pos;
-    lp.out_tokens = out_tokens;
-    lp.out_hidden = out_hidden;
-    lp.n_draft = n_draft;
-    lp.mb_x0 = h->mb[0];
-    lp.mb_q = h->mb[1];
-    lp.mb_part = h->mb[2];
-    lp.mb_o = h->mb[3];
-    lp.mb_op = h->mb[4];
-    lp.mb_m = h->mb[5];
-    lp.mb_dn = h->mb[6];
-    lp.mb_h = h->mb[7];
-    lp.mb_cent = h->mb[8];
-    lp.mb_key = h->mb[9];
-    lp.status = h->wsp.status;
-    lp.abort_flag = h->ll_abort;
-    const unsigned span = static_cast<unsigned>(n_draft + 1) * mtp::ll::kExPerStep;
-    if (h->epoch > 0xffffffffu - span) {
-      // epochs wrap: clear every mailbox so that no stale word can carry a reused epoch
-      char* lo = reinterpret_cast<char*>(h->mb[0]);
-      char* hi = static_cast<char*>(h->ws) + h->ws_bytes;
-      cudaError_t e = cudaMemsetAsync(lo, 0, static_cast<size_t>(hi - lo), st);
-      if (e != cudaSuccess) return cuda_fail("clearing the mailboxes", e);
-      h->epoch = 64u;
-    }
-    lp.epoch_base = h->epoch;
-    h->epoch += span;
-    const int smem = mtp::ll_smem_bytes(lp);
-    if (smem <= 0) {
-      set_error("latency path: shape not supported for this call");
-      return MTP_ERR_UNSUPPORTED_SHAPE;
-    }
-    cudaError_t e = cudaMemsetAsync(h->ll_abort, 0, sizeof(unsigned), st);
-    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
-    return mtp::run_ll(lp, smem, st);
-  }
-  int ncta = h->num_sms;
+  const int ncta = h->num_sms;
   if (path == 5 || (path == 0 && B >= 2 && h->tc)) {
     if (!h->tc) {
       set_error("the tensor-core path needs a bf16 drafter with max_batch in [2, %d] on this device", mtp::tc::kMaxB);
@@ -1394,8 +1081,8 @@ int mtp_get_status(mtp_handle* h) {
 
 int mtp_set_path(mtp_handle* h, int32_t path) {
   mtp::g_err[0] = 0;
-  if (!h || path < 0 || path > 7) {
-    set_error("need a handle and path in {0, 1, 2, 3, 4, 5, 6, 7}");
+  if (!h || path < 0 || path > 7 || path == 3 || path == 4) {
+    set_error("need a handle and path in {0, 1, 2, 5, 6, 7}");
     return MTP_ERR_INVALID_ARG;
   }
   h->path = path;

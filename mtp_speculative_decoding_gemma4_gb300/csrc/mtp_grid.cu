@@ -1316,4 +1316,31 @@ int run_gr(const gr::Params& p, cudaStream_t st) {
   return MTP_OK;
 }
 
+// ------------------------------------------------------------------ token_embd reordering
+
+namespace {
+// dst[j] = src[ord[j]] for the V rows of vec 16-byte vectors each.
+__global__ void k_reorder_rows(const uint4* __restrict__ src, const int* __restrict__ ord, uint4* __restrict__ dst,
+                               int V, int vec) {
+  const long long total = static_cast<long long>(V) * vec;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / vec, c = i % vec;
+    const int s = ord[row];
+    dst[row * vec + c] = src[static_cast<size_t>(s) * vec + c];
+  }
+}
+}  // namespace
+
+int reorder_rows(const void* src, const int* ord, void* dst, int V, int row_bytes, cudaStream_t st) {
+  k_reorder_rows<<<1024, 256, 0, st>>>(static_cast<const uint4*>(src), ord, static_cast<uint4*>(dst), V,
+                                       row_bytes / 16);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("reordering token_embd: %s", cudaGetErrorString(e));
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
+
 }  // namespace mtp

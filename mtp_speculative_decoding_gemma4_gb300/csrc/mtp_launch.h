@@ -1,5 +1,5 @@
 // Internal interface between the C ABI (mtp_api.cu) and the dtype-specific kernel
-// translation units (mtp_bf16.cu, mtp_f32.cu, mtp_ll.cu, mtp_cl.cu, mtp_verify.cu).
+// translation units (mtp_bf16.cu, mtp_f32.cu, mtp_c2.cu, mtp_grid.cu, mtp_tc.cu, mtp_verify.cu, ...).
 #pragma once
 
 #include <cuda.h>
@@ -11,12 +11,6 @@
 namespace mtp {
 
 struct Params;
-namespace ll {
-struct Params;
-}
-namespace clk {
-struct Params;
-}
 namespace c2 {
 struct Params;
 }
@@ -43,22 +37,9 @@ bool head_cm_supported(const Params& p, int elem_bytes);
 template <typename WT>
 int run_head_cm(const Params& p, cudaStream_t st);
 
-// Latency-path draft block (one sequence): shared-memory bytes it needs for these
-// parameters (0: shape not supported), co-resident capacity for that size, launch.
-int ll_smem_bytes(const ll::Params& p);
-int ll_capacity(int smem, int num_sms);
-int run_ll(const ll::Params& p, int smem, cudaStream_t st);
-
-// Cluster-path draft block (one sequence, one 16-CTA cluster): shared-memory bytes (0: shape
-// not supported), resident clusters for that size, launch; and the init-time copy of
-// token_embd in token_ordering order that the path reads.
-int cl_smem_bytes(const clk::Params& p);
-int cl_capacity(int smem);
-int run_cl(const clk::Params& p, int smem, cudaStream_t st);
+// token_embd rows in token_ordering order (dst[j] = src[ord[j]], rows of row_bytes, a
+// multiple of 16): the rows of one centroid become one contiguous block.
 int reorder_rows(const void* src, const int* ord, void* dst, int V, int row_bytes, cudaStream_t st);
-// Tensor-core tile packing of a [R][K] bf16 matrix for the cluster kernel (bytes, pack).
-long long packed_tile_bytes(int R, int K);
-int pack_tiles(const void* W, int R, int K, void* dst, cudaStream_t st);
 
 // Streamed-tile cluster draft block (one sequence, one 16-CTA cluster, weights packed into
 // per-CTA tile streams at init): shared-memory bytes (0: shape

@@ -15,8 +15,8 @@ from _util import (NEAR_TIE, TOL, compare_block, config_data, decoded, expected_
 
 pytestmark = pytest.mark.gpu
 
-PHASES, PERSISTENT, LATENCY, CLUSTER, TENSOR, STREAMED, GRID = 1, 2, 3, 4, 5, 6, 7
-ONE_SEQ = [LATENCY, CLUSTER, STREAMED, GRID]  # the single-sequence paths
+PHASES, PERSISTENT, TENSOR, STREAMED, GRID = 1, 2, 5, 6, 7
+ONE_SEQ = [STREAMED, GRID]  # the single-sequence paths
 
 
 def _drafter(index, batch=0, ctx=0, max_batch=0):
@@ -168,11 +168,21 @@ def test_paths_agree_bitwise_on_tokens():
 
 def test_one_sequence_paths_agree_on_tokens():
     dr, d = _drafter(1)
-    a, ha = _run_block(dr, d, 8, LATENCY)
-    for path in (CLUSTER, STREAMED):
+    a, ha = _run_block(dr, d, 8, GRID)
+    for path in (STREAMED, PERSISTENT):
         b, hb = _run_block(dr, d, 8, path)
         np.testing.assert_array_equal(a, b)
         assert np.max(np.abs(ha - hb)) <= TOL["bf16"]
+    dr.close()
+
+
+def test_removed_paths_are_rejected():
+    from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding
+    dr, _ = _drafter(0)
+    for path in (3, 4, 8, -1):
+        with pytest.raises(MtpError) as e:
+            dr.set_path(path)
+        assert e.value.code == binding.MTP_ERR_INVALID_ARG
     dr.close()
 
 

@@ -131,9 +131,10 @@ __device__ __forceinline__ void put_u(unsigned long long* mb, long long i, unsig
   st_rlx64(mb + i, (static_cast<unsigned long long>(ep) << 32) | v);
 }
 
-// Mailbox words -> dst[k] (payload bits), k in [0, count). A thread issues the first load of
-// all its words of a pass (up to 16) before waiting on any, then re-polls only the missing
-// ones (bounded). The word index of k comes from a functor; every thread calls; the result
+// Mailbox words -> dst[k] (payload bits), k in [0, count). Per pass a thread takes up to 16
+// of its words: it issues the loads of all of them, then in rounds re-issues the loads of every
+// word still missing before checking any, so a round costs one L2 round trip however many of
+// its words are late. The word index of k comes from a functor; every thread calls; the result
 // is block-uniform.
 constexpr int kGatherBatch = 16;
 template <class Idx>
@@ -144,28 +145,28 @@ __device__ __forceinline__ bool gather_t(const Params& p, const unsigned long lo
   for (int base = 0; base < count; base += kGatherBatch * kT) {
     unsigned long long w[kGatherBatch];
     int ix[kGatherBatch];
+    unsigned miss = 0u;
 #pragma unroll
     for (int j = 0; j < kGatherBatch; ++j) {
       const int k = base + j * kT + static_cast<int>(threadIdx.x);
       ix[j] = k < count ? static_cast<int>(idx.next()) : -1;
       w[j] = ix[j] >= 0 ? ld_rlx64(mb + ix[j]) : 0ull;
+      if (ix[j] >= 0) miss |= 1u << j;
     }
-#pragma unroll
-    for (int j = 0; j < kGatherBatch; ++j) {
-      if (ix[j] < 0) continue;
-      if (static_cast<unsigned>(w[j] >> 32) != ep && !bad) {
-        const long long t0 = clock64();
+    const long long t0 = clock64();
 #pragma unroll 1
-        for (unsigned n = 1;; ++n) {
-          w[j] = ld_rlx64(mb + ix[j]);
-          if (static_cast<unsigned>(w[j] >> 32) == ep) break;
-          if (expired(p, t0, n)) {
-            bad = 1;
-            break;
-          }
+    for (unsigned n = 1; !bad; ++n) {
+#pragma unroll
+      for (int j = 0; j < kGatherBatch; ++j)
+        if ((miss >> j & 1u) && static_cast<unsigned>(w[j] >> 32) == ep) {
+          dst[base + j * kT + threadIdx.x] = static_cast<unsigned>(w[j]);
+          miss &= ~(1u << j);
         }
-      }
-      dst[base + j * kT + threadIdx.x] = static_cast<unsigned>(w[j]);
+      if (!miss) break;
+#pragma unroll
+      for (int j = 0; j < kGatherBatch; ++j)
+        if (miss >> j & 1u) w[j] = ld_rlx64(mb + ix[j]);
+      if (expired(p, t0, n)) bad = 1;
     }
   }
   return !__syncthreads_or(bad);

@@ -218,7 +218,9 @@ MTP_API int mtp_set_sparse_head(mtp_handle *h, int32_t mode);
  * Decoding?"): t_i = argmax of target row i (lowest id on ties); accept_len[b] = the
  * largest m with draft[b][i] == t_i for all i < m; out_tokens[b] = draft[b][0..m) followed
  * by t_m (the target's correction, or its extra token when m == n), then -1 padding.
- * Rows after the first disagreement are not read.
+ * Rows after the first disagreement never change the result. Rows are read in batches of
+ * five (one memory round trip per batch); batches after the one holding the first
+ * disagreement are not read.
  *   target_logits device [B][n+1][V] bf16
  *   draft         device [B][n] int32
  *   accept_len    device [B] int32

@@ -866,15 +866,15 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     gp.dbg_skip = h->dbg_skip;
     const unsigned need = static_cast<unsigned>(n_draft + 1) * mtp::gr::kExPerStep;
     if (h->gr_epoch > 0xF0000000u - need) {
-      // epochs wrap: clear the mailboxes so that no old word can match a new epoch
+      // epochs wrap: clear the mailboxes and the abort word (which holds the epoch base of a
+      // launch that gave up) so that no old word can match a new epoch
       cudaError_t e = cudaMemsetAsync(h->gr_mb, 0, static_cast<size_t>(h->gr_mb_words) * 8, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(h->abort_word, 0, sizeof(unsigned), st);
       if (e != cudaSuccess) return cuda_fail("clearing the grid path's mailboxes", e);
       h->gr_epoch = 64u;
     }
     gp.epoch_base = h->gr_epoch;
     h->gr_epoch += need;
-    cudaError_t e = cudaMemsetAsync(h->abort_word, 0, sizeof(unsigned), st);
-    if (e != cudaSuccess) return cuda_fail("clearing the abort word", e);
     return mtp::run_gr(gp, st);
   }
   if (path == 6 || (path == 0 && B == 1 && h->c2_ok)) {

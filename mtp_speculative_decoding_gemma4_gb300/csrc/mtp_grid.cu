@@ -75,14 +75,17 @@ __device__ __forceinline__ float bf(bf16 v) { return __bfloat162float(v); }
 
 // ------------------------------------------------------------------ bounded waits
 
+// The abort word holds the epoch base of the launch that gave up: a word left by an earlier
+// launch never matches, so no launch has to clear it first.
 __device__ __forceinline__ void fail(const Params& p) {
   atomicCAS(p.status, 0, static_cast<int>(MTP_ERR_TIMEOUT));
-  atomicExch(p.abort_flag, 1u);
+  atomicExch(p.abort_flag, p.epoch_base);
 }
+__device__ __forceinline__ bool aborted(const Params& p) { return ld_rlx32(p.abort_flag) == p.epoch_base; }
 // True when the caller must give up: the budget ran out (recorded) or another CTA gave up.
 __device__ __forceinline__ bool expired(const Params& p, long long t0, unsigned n) {
   if ((n & 63u) != 0u) return false;
-  if (ld_rlx32(p.abort_flag)) return true;
+  if (aborted(p)) return true;
   if (clock64() - t0 > p.spin_limit) {
     fail(p);
     return true;
@@ -110,7 +113,7 @@ __device__ __forceinline__ bool mbar_wait(const Params& p, unsigned bar, unsigne
   if (threadIdx.x < 32 && !mbar_try_susp(bar, parity)) {
     const long long t0 = clock64();
     while (!mbar_try_susp(bar, parity)) {
-      if (watch_abort && ld_rlx32(p.abort_flag)) {
+      if (watch_abort && aborted(p)) {
         bad = 1;
         break;
       }
@@ -407,7 +410,10 @@ __device__ __forceinline__ unsigned long long topk_key(const float* cl, int i) {
 // the k group maxima is at most the k-th largest key, so every selected key lies at or above
 // it. The keys at or above the bound (few: about k to 3k) are compacted in index order and
 // each is ranked against the others. All threads call.
-__device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, const float* cl, int* sel) {
+//
+// Any C and k: one warp per group, ranks by ballots (shapes the tiled form below does not
+// cover, and candidate sets that overflow its buffer).
+__device__ __forceinline__ void topk_generic(const Params& p, unsigned char* sm, const float* cl, int* sel) {
   const Layout& L = p.L;
   const int C = p.C, k = p.topk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -415,19 +421,22 @@ __device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, 
   int* ws = reinterpret_cast<int*>(sm + L.red);
   int* cidx = reinterpret_cast<int*>(sm + L.qs);
   unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm + L.qs + ((L.cand_cap * 4 + 15) & ~15));
+  // this thread's contiguous chunk of keys, kept in registers (up to kChunk)
+  constexpr int kChunk = 8;
+  const int per = cdiv(C, kT), i0 = min(C, tid * per), i1 = min(C, i0 + per);
+  const bool regs = per <= kChunk;
+  unsigned long long key[kChunk];
+#pragma unroll
+  for (int j = 0; j < kChunk; ++j) key[j] = regs && i0 + j < i1 ? topk_key(cl, i0 + j) : 0ull;
   // group maxima: when the k groups are runs of 2^j whole per-thread chunks, a thread's chunk
   // maximum and a butterfly over the group's lanes; else one warp per group
-  const int per = cdiv(C, kT), i0 = min(C, tid * per), i1 = min(C, i0 + per);
   const int tpg = (C / k) / per;  // threads per group
-  const bool tiled = C % k == 0 && (C / k) % per == 0 && tpg >= 1 && tpg <= 32 && (tpg & (tpg - 1)) == 0 &&
+  const bool tiled = regs && C % k == 0 && (C / k) % per == 0 && tpg >= 1 && tpg <= 32 && (tpg & (tpg - 1)) == 0 &&
                      tpg * k <= kT;
   if (tiled) {
     unsigned long long m = 0ull;
-#pragma unroll 4
-    for (int i = i0; i < i1; ++i) {
-      const unsigned long long key = topk_key(cl, i);
-      m = key > m ? key : m;
-    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) m = key[j] > m ? key[j] : m;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
       if (o < tpg) {
@@ -442,8 +451,8 @@ __device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, 
     unsigned long long m = 0ull;
 #pragma unroll 1
     for (int i = lo + lane; i < hi; i += 32) {
-      const unsigned long long key = topk_key(cl, i);
-      m = key > m ? key : m;
+      const unsigned long long kk = topk_key(cl, i);
+      m = kk > m ? kk : m;
     }
     m = warp_max_u64(m);
     if (lane == 0) gmax[r] = m;
@@ -458,66 +467,185 @@ __device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, 
     const unsigned long long w = __shfl_xor_sync(0xffffffffu, bnd, o);
     bnd = w < bnd ? w : bnd;
   }
-  // candidates at or above the bound, in index order (contiguous chunks per thread)
+  // candidates at or above the bound, in index order
   int n = 0;
+  if (regs) {
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) n += key[j] >= bnd && key[j] != 0ull;
+  } else {
 #pragma unroll 1
-  for (int i = i0; i < i1; ++i) n += topk_key(cl, i) >= bnd;
+    for (int i = i0; i < i1; ++i) n += topk_key(cl, i) >= bnd;
+  }
   int M = 0;
   int pos = block_excl_scan(n, ws, &M);
   const bool fits = M <= L.cand_cap;
   if (fits) {
+    if (regs) {
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        if (key[j] >= bnd && key[j] != 0ull) {
+          cidx[pos] = i0 + j;
+          ckey[pos] = key[j];
+          ++pos;
+        }
+    } else {
 #pragma unroll 1
-    for (int i = i0; i < i1; ++i) {
-      const unsigned long long key = topk_key(cl, i);
-      if (key >= bnd) {
-        cidx[pos] = i;
-        ckey[pos] = key;
-        ++pos;
+      for (int i = i0; i < i1; ++i) {
+        const unsigned long long kk = topk_key(cl, i);
+        if (kk >= bnd) {
+          cidx[pos] = i;
+          ckey[pos] = kk;
+          ++pos;
+        }
       }
     }
   }
   __syncthreads();
-  // rank of each candidate among the candidates (or, when they overflow the buffer, among all
-  // keys); selected when fewer than k keys are larger
-  int take = 0, ti = 0;
-  if (fits) {
-    if (tid < M) {
-      const unsigned long long key = ckey[tid];
-      int rk = 0;
-#pragma unroll 8
-      for (int m = 0; m < M; ++m) rk += ckey[m] > key;
-      take = rk < k;
-      ti = cidx[tid];
-    }
-  }
   int nsel = 0;
   if (fits) {
+    // rank of each candidate among the candidates: one warp per candidate, the lanes comparing
+    // 32 candidates at a time (ballot + population count); selected when fewer than k are larger
+    int* flag = reinterpret_cast<int*>(sm + L.gmax);  // the group maxima are no longer needed
+#pragma unroll 1
+    for (int m = warp; m < M; m += kW) {
+      const unsigned long long kk = ckey[m];
+      int rk = 0;
+#pragma unroll 2
+      for (int b = 0; b < M; b += 32) {
+        const bool gt = b + lane < M && ckey[b + lane] > kk;
+        rk += __popc(__ballot_sync(0xffffffffu, gt));
+      }
+      if (lane == 0) flag[m] = rk < k ? 1 : 0;
+    }
+    __syncthreads();
+    // compaction in candidate (= index) order: one candidate per thread
+    const int take = tid < M ? flag[tid] : 0;
     const int at = block_excl_scan(take, ws, &nsel);
-    if (take && at < k) sel[at] = ti;
+    if (take && at < k) sel[at] = cidx[tid];
   } else {
     // slow exact path: every key against every key (only for pathological ties / distributions)
     int cnt = 0;
 #pragma unroll 1
     for (int i = i0; i < i1; ++i) {
-      const unsigned long long key = topk_key(cl, i);
+      const unsigned long long kk = topk_key(cl, i);
       int rk = 0;
-      if (key >= bnd) {
+      if (kk >= bnd) {
 #pragma unroll 1
-        for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > key;
+        for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > kk;
       }
-      cnt += key >= bnd && rk < k;
+      cnt += kk >= bnd && rk < k;
     }
     int at = block_excl_scan(cnt, ws, &nsel);
 #pragma unroll 1
     for (int i = i0; i < i1; ++i) {
-      const unsigned long long key = topk_key(cl, i);
-      if (key < bnd) continue;
+      const unsigned long long kk = topk_key(cl, i);
+      if (kk < bnd) continue;
       int rk = 0;
 #pragma unroll 1
-      for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > key;
+      for (int m = 0; m < C && rk < k; ++m) rk += topk_key(cl, m) > kk;
       if (rk < k && at < k) sel[at++] = i;
     }
   }
+  __syncthreads();
+}
+
+// The tiled form: C = 256 * per (per <= 8 keys in each thread's registers) and k groups of
+// tpg = C / (k * per) consecutive threads (a power of two <= 32). The group maxima and their
+// minimum (the bound) are taken on the 32-bit order of the values: a bound on the value alone
+// still lies at or below the k-th largest key. The candidates (values at or above it) are
+// compacted in index order with their full keys (value, then lower index first), and each is
+// ranked by counting the larger candidate keys, two threads per candidate when at most 128.
+// Three prefix sums by warp totals in shared memory (one barrier each).
+__device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, const float* cl, int* sel) {
+  const Layout& L = p.L;
+  const int k = p.topk, lgper = p.tk_lg_per, lgtpg = p.tk_lg_tpg;
+  if (lgtpg < 0) {
+    topk_generic(p, sm, cl, sel);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per = 1 << lgper, tpg = 1 << lgtpg, i0 = tid << lgper;
+  int* wsb = reinterpret_cast<int*>(sm + L.red);  // [kW] warp minima of the group maxima
+  int* wsc = wsb + kW;                            // [kW] warp candidate counts
+  int* wss = wsb + 2 * kW;                        // [kW] warp selection counts
+  int* cidx = reinterpret_cast<int*>(sm + L.qs);
+  unsigned long long* ckey = reinterpret_cast<unsigned long long*>(sm + L.qs + ((L.cand_cap * 4 + 15) & ~15));
+  int* part = reinterpret_cast<int*>(sm + L.gmax);  // [2][128] partial ranks
+  unsigned v[8];
+  if (per == 8) {
+    const float4 a = reinterpret_cast<const float4*>(cl + i0)[0], b = reinterpret_cast<const float4*>(cl + i0)[1];
+    v[0] = ord_f32(a.x), v[1] = ord_f32(a.y), v[2] = ord_f32(a.z), v[3] = ord_f32(a.w);
+    v[4] = ord_f32(b.x), v[5] = ord_f32(b.y), v[6] = ord_f32(b.z), v[7] = ord_f32(b.w);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = j < per ? ord_f32(cl[i0 + j]) : 0u;
+  }
+  // group maxima (a tree over the thread's keys, then a butterfly over the group's lanes), and
+  // their minimum over the warp's groups
+  unsigned gm = max(max(max(v[0], v[1]), max(v[2], v[3])), max(max(v[4], v[5]), max(v[6], v[7])));
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned w = __shfl_xor_sync(0xffffffffu, gm, o);
+    gm = o < tpg ? max(gm, w) : min(gm, w);
+  }
+  if (lane == 0) wsb[warp] = static_cast<int>(gm);
+  __syncthreads();
+  unsigned bnd = 0xffffffffu;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) bnd = min(bnd, static_cast<unsigned>(wsb[w]));
+  // candidates: values at or above the bound, compacted in index order
+  int n = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) n += j < per && v[j] >= bnd;
+  int x = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += u;
+  }
+  if (lane == 31) wsc[warp] = x;
+  __syncthreads();
+  int M = 0, pos = x - n;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) {
+    const int c = wsc[w];
+    M += c;
+    pos += w < warp ? c : 0;
+  }
+  const int M8 = (M + 7) & ~7;
+  if (M8 > L.cand_cap) {  // block-uniform; only for heavy ties at the bound
+    topk_generic(p, sm, cl, sel);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < per && v[j] >= bnd) {
+      cidx[pos] = i0 + j;
+      ckey[pos] = (static_cast<unsigned long long>(v[j]) << 32) | (0xffffffffu - static_cast<unsigned>(i0 + j));
+      ++pos;
+    }
+  if (tid < M8 - M) ckey[M + tid] = 0ull;  // padding: never larger than a candidate
+  __syncthreads();
+  // ranks: the number of larger candidate keys; candidate m, half h of the candidates
+  const bool two = M8 <= 128;
+  const int m = two ? (tid & 127) : tid, h = two ? (tid >> 7) : 0;
+  const int span = two ? (M8 >> 1) : M8, j0 = h * span;
+  if (m < M) {
+    const unsigned long long mk = ckey[m];
+    int rk = 0;
+#pragma unroll 4
+    for (int j = j0; j < j0 + span; ++j) rk += ckey[j] > mk;
+    part[(h << 7) + m] = rk;
+  }
+  __syncthreads();
+  const bool take = tid < M && (two ? part[tid] + part[128 + tid] : part[tid]) < k;
+  const unsigned bal = __ballot_sync(0xffffffffu, take);
+  if (lane == 0) wss[warp] = __popc(bal);
+  __syncthreads();
+  int at = __popc(bal & ((1u << lane) - 1u));
+#pragma unroll
+  for (int w = 0; w < kW; ++w) at += w < warp ? wss[w] : 0;
+  if (take && at < k) sel[at] = cidx[tid];
   __syncthreads();
 }
 
@@ -566,47 +694,69 @@ __device__ __forceinline__ void attend(const Params& p, unsigned char* sm, int l
     }
   }
   __syncthreads();
-  // scores: one warp per (key, KV head, group of up to 4 of its query heads); every lane a run
-  // of 16-byte vectors of the key
+  // scores: one warp per (pair of keys, KV head, group of up to 4 of its query heads); every
+  // lane a run of 16-byte vectors of the keys; the 8 partial sums (2 keys x 4 heads) are
+  // reduced by a transposed butterfly that leaves each sum in 4 lanes
   const int nvec = d >> 3;
-#pragma unroll 2
-  for (int j = warp; j < nk; j += kW) {
+#pragma unroll 1
+  for (int j0 = 2 * warp; j0 < nk; j0 += 2 * kW) {
+    const bool two = j0 + 1 < nk;
 #pragma unroll 1
     for (int kh = 0; kh < nkv; ++kh) {
-      const bf16* kr = kb + static_cast<size_t>(j) * kst + kh * d;
+      const bf16* kr0 = kb + static_cast<size_t>(j0) * kst + kh * d;
+      const bf16* kr1 = two ? kr0 + kst : kr0;
 #pragma unroll 1
       for (int q0 = 0; q0 < grp; q0 += 4) {
         const float* qh = qs + (kh * grp + q0) * d;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // [key][head]
 #pragma unroll 1
         for (int v = lane; v < nvec; v += 32) {
-          float kf[8];
-          bf8(*reinterpret_cast<const uint4*>(kr + 8 * v), kf);
+          float k0[8], k1[8];
+          bf8(*reinterpret_cast<const uint4*>(kr0 + 8 * v), k0);
+          bf8(*reinterpret_cast<const uint4*>(kr1 + 8 * v), k1);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             if (q0 + q < grp) {
               const float4* qv = reinterpret_cast<const float4*>(qh + q * d + 8 * v);
               const float4 a = qv[0], b = qv[1];
-              float u = acc[q];
-              u = fmaf(a.x, kf[0], u);
-              u = fmaf(a.y, kf[1], u);
-              u = fmaf(a.z, kf[2], u);
-              u = fmaf(a.w, kf[3], u);
-              u = fmaf(b.x, kf[4], u);
-              u = fmaf(b.y, kf[5], u);
-              u = fmaf(b.z, kf[6], u);
-              acc[q] = fmaf(b.w, kf[7], u);
+              const float qq[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+              float u0 = acc[q], u1 = acc[4 + q];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                u0 = fmaf(qq[i], k0[i], u0);
+                u1 = fmaf(qq[i], k1[i], u1);
+              }
+              acc[q] = u0;
+              acc[4 + q] = u1;
             }
           }
         }
+        // butterfly: 8 values over offsets 16, 8, 4 (each halving the values a lane keeps),
+        // then the full sum over offsets 2 and 1; lane l ends with value (l >> 2) & 7
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        for (int i = 0; i < 4; ++i) {
+          const bool up = lane & 16;
+          const float send = up ? acc[i] : acc[i + 4], keep = up ? acc[i + 4] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
-        if (lane < 4 && q0 + lane < grp) {
-          const float v = lane == 0 ? acc[0] : (lane == 1 ? acc[1] : (lane == 2 ? acc[2] : acc[3]));
-          sc[(kh * grp + q0 + lane) * ksl + j] = v;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const bool up = lane & 8;
+          const float send = up ? acc[i] : acc[i + 2], keep = up ? acc[i + 2] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        {
+          const bool up = lane & 4;
+          const float send = up ? acc[0] : acc[1], keep = up ? acc[1] : acc[0];
+          acc[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 2);
+        acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+        // value index: bit 2 from lane bit 4, bit 1 from lane bit 3, bit 0 from lane bit 2
+        if ((lane & 3) == 0) {
+          const int vi = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+          const int key = vi >> 2, q = vi & 3;
+          if (q0 + q < grp && (key == 0 || two)) sc[(kh * grp + q0 + q) * ksl + j0 + key] = acc[0];
         }
       }
     }
@@ -688,6 +838,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
   float* red = reinterpret_cast<float*>(sm + L.red);
   unsigned long long* wkeys = reinterpret_cast<unsigned long long*>(sm + L.keys);
   int* sel = reinterpret_cast<int*>(sm + L.sel);
+  float* qsbuf = reinterpret_cast<float*>(sm + L.qs);  // free outside the attention: combine weights
   const int kbar = nl + 2;
 
   // ---- this CTA's shares (computed once): key ranges per type, q dims per type, FFN rows,
@@ -898,23 +1049,35 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
           ok = false;
           break;
         }
+        // per head touched: the sources' weights exp(m_a - M) and the denominator (one warp per
+        // head); then per dim the weighted sum of the sources' partials (one warp per dim)
+        float* wgt = qsbuf;  // [nht][At] source weights
 #pragma unroll 1
-        for (int w = warp; w < nq; w += kW) {
-          const int hl = ((q_r.lo + w) >> lg) - hlo;
+        for (int hl = warp; hl < nht; hl += kW) {
           float m = -INFINITY;
 #pragma unroll 4
           for (int a = lane; a < At; a += 32) m = fmaxf(m, ub[a * per + nq + 2 * hl]);
           m = warp_max(m);
-          float num = 0.f, den = 0.f;
+          float den = 0.f;
 #pragma unroll 4
           for (int a = lane; a < At; a += 32) {
             const float ma_ = ub[a * per + nq + 2 * hl];
-            const float wgt = ma_ == -INFINITY ? 0.f : expf(ma_ - m);
-            num = fmaf(wgt, ub[a * per + w], num);
-            den = fmaf(wgt, ub[a * per + nq + 2 * hl + 1], den);
+            const float w_ = ma_ == -INFINITY ? 0.f : expf(ma_ - m);
+            wgt[hl * At + a] = w_;
+            den = fmaf(w_, ub[a * per + nq + 2 * hl + 1], den);
           }
-          num = warp_sum(num);
           den = warp_sum(den);
+          if (lane == 0) red[48 + hl] = den;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int w = warp; w < nq; w += kW) {
+          const int hl = ((q_r.lo + w) >> lg) - hlo;
+          float num = 0.f;
+#pragma unroll 4
+          for (int a = lane; a < At; a += 32) num = fmaf(wgt[hl * At + a], ub[a * per + w], num);
+          num = warp_sum(num);
+          const float den = red[48 + hl];
           if (lane == 0) red[w] = den > 0.f ? num / den : 0.f;
         }
         __syncthreads();
@@ -1178,8 +1341,17 @@ bool plan_for(gr::Params& p, int N, int S, int G, bool k_full_res, bool k_swa_re
   const gr::Layout& L = p.L;
   if (L.kc > 64 || L.total > optin) return false;
   #pragma unroll 1
-  for (int l = 0; l < p.nl; ++l)
-    if (L.nq[l] > 64 || L.nf > 64 * 1024) return false;
+  for (int l = 0; l < p.nl; ++l) {
+    const int t = p.ltype[l], d = p.d[t];
+    if (L.nq[l] > 48) return false;  // combine: o values in red[0, 48), denominators in red[48, 64)
+    int ht = 0;
+    for (int c = 0; c < N; ++c) {
+      const gr::Range r = gr::split(p.nh * d, N, c);
+      const int h = gr::heads_touched(r.lo, r.hi, d);
+      ht = h > ht ? h : ht;
+    }
+    if (ht > 16 || ht * p.A[t] > gr::max_qd(p)) return false;  // combine weights live in the q buffer
+  }
   return true;
 }
 
@@ -1218,6 +1390,15 @@ int gr_plan(gr::Params& p, int optin) {
   }
   p.lg_vsc = lg2(p.vsc);
   if (p.lg_vsc < 0) return 0;
+  // top-k tiling: C = 256 * per with per <= 8, and k groups of a power-of-two <= 32 threads
+  p.tk_lg_per = p.tk_lg_tpg = -1;
+  if (p.C % gr::kT == 0 && p.C % p.topk == 0) {
+    const int per = p.C / gr::kT, tpg = (p.C / p.topk) / per;
+    if (per <= 8 && lg2(per) >= 0 && (p.C / p.topk) % per == 0 && tpg <= 32 && lg2(tpg) >= 0) {
+      p.tk_lg_per = lg2(per);
+      p.tk_lg_tpg = lg2(tpg);
+    }
+  }
   const bool res_opts[3][2] = {{true, true}, {false, true}, {false, false}};
   #pragma unroll 1
   for (const auto& ro : res_opts) {

@@ -61,6 +61,7 @@ __host__ __device__ inline Range split(int R, int N, int c) {
 }
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline int max3(int a, int b, int c) { return a > b ? (a > c ? a : c) : (b > c ? b : c); }
 __host__ __device__ inline int even(int v) { return (v + 1) & ~1; }
 
 // Exchange indices within a step: 0 PRE AR; per block l: Q AG, ATT, O AR, DN AR; CENT AG; KEY AG.
@@ -97,9 +98,9 @@ struct Layout {
   int cs;               // RoPE (cos, sin) [d_s / 2 + d_f / 2] float2
   int rs, ag;           // AR receive buffers [2][H] each
   int vh;               // PRE partial over the h columns [H] (computed before the token is known)
-  int red;              // 64 floats
+  int red;              // 64 floats (combine: [0, nq) o values, [48, 64) head denominators)
   int keys;             // [kW] u64 warp keys
-  int gmax;             // [kMaxTopK] u64 group maxima of the top-k bound
+  int gmax;             // top-k: [kMaxTopK] u64 group maxima, then ranks ([2][128] or [cand_cap] int)
   int sel;              // [kMaxTopK] selected centroids
   int bars;             // mbarriers: load groups (nl + 2), K, RS[2], AG[2]
   int total;
@@ -118,6 +119,7 @@ struct Params {
   int kslots[2]; // largest key share of an attention CTA (shared-memory rows / score slots)
   int has_type[2];
   int lg_d[2], lg_hs, lg_vsc;  // log2 of the head dims, of H / S and of vsc (all powers of two)
+  int tk_lg_per, tk_lg_tpg;    // top-k tiling: log2 of keys per thread and of threads per group (-1: untiled)
   // weights: per-CTA images [N][img_bytes] in the shared-memory layout (made at init)
   const unsigned char* img;
   long long img_bytes;
@@ -258,7 +260,7 @@ inline Layout make_layout(const Params& p) {
   L.keys = off;
   off += al16(kW * 8);
   L.gmax = off;
-  off += al16(kMaxTopK * 8);
+  off += al16(max3(kMaxTopK * 8, 2 * 128 * 4, L.cand_cap * 4));  // group maxima, then ranks
   L.sel = off;
   off += al16(kMaxTopK * 4);
   L.bars = off;

@@ -3,12 +3,14 @@
 // the target first disagrees; the target's own token replaces the first rejected draft, or
 // is appended when every draft was accepted).
 //
-// One thread-block cluster per sequence scans the target rows in order. Each CTA of the
-// cluster takes a contiguous slice of the row (16-byte loads, the next row prefetched into
-// registers while the current one is reduced), reduces it to one (value, id) key, and
-// writes that key into every CTA's shared memory (DSMEM). After a cluster barrier each CTA
-// holds all slice keys, takes the row argmax (largest bf16 value, lowest id on ties) and the
-// same accept/stop decision; rows after the first disagreement are never read.
+// One thread-block cluster per sequence scans the target rows in batches of up to
+// kVerifyRowBatch rows. Each CTA of the cluster takes a contiguous slice of every row
+// (16-byte streaming loads, all rows of the batch in flight at once so that one memory round
+// trip serves the batch), reduces each row's slice to one (value, id) key, and writes the keys
+// into every CTA's shared memory (DSMEM). After one cluster barrier per batch each CTA holds
+// all slice keys, takes each row's argmax (largest bf16 value, lowest id on ties) and walks the
+// batch's accept/stop decisions in order. Rows after the first disagreement never change the
+// result; the batches after the one holding it are never read.
 #include <cooperative_groups.h>
 
 #include "mtp_common.cuh"
@@ -20,13 +22,14 @@ namespace mtp {
 
 constexpr int kVerifyThreads = 512;
 constexpr int kVerifyMaxCluster = 16;
-constexpr int kVerifyVecPerThread = 4;  // 16-byte vectors per thread per row (covers 16384 / CTA)
+constexpr int kVerifyVecPerThread = 4;  // 16-byte vectors per thread per row and pass (16384 / CTA)
+constexpr int kVerifyRowBatch = 5;      // rows whose first pass is in flight together
 
-__global__ void __launch_bounds__(kVerifyThreads) k_verify(const __nv_bfloat16* __restrict__ logits,
-                                                          const int* __restrict__ draft, int n, int V, int slice,
-                                                          int* __restrict__ accept_len, int* __restrict__ out_tokens) {
-  __shared__ unsigned long long keys[2][kVerifyMaxCluster];
-  __shared__ unsigned long long wk[kVerifyThreads / 32];
+__global__ void __launch_bounds__(kVerifyThreads, 1) k_verify(const __nv_bfloat16* __restrict__ logits,
+                                                             const int* __restrict__ draft, int n, int V, int slice,
+                                                             int* __restrict__ accept_len, int* __restrict__ out_tokens) {
+  __shared__ unsigned long long keys[2][kVerifyRowBatch][kVerifyMaxCluster];
+  __shared__ unsigned long long wk[kVerifyRowBatch][kVerifyThreads / 32];
   cg::cluster_group cl = cg::this_cluster();
   const int cs = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
@@ -37,11 +40,10 @@ __global__ void __launch_bounds__(kVerifyThreads) k_verify(const __nv_bfloat16* 
   if (rank == 0)
     for (int i = threadIdx.x; i <= n; i += kVerifyThreads) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = -1;
 
-  // registers of the current and the next row: up to kVerifyVecPerThread vectors each;
-  // slices wider than that are walked in further passes
+  // the first pass of every row of a batch sits in registers; slices wider than one pass are
+  // walked in further passes, one row at a time
   const int per_pass = kVerifyThreads * 8 * kVerifyVecPerThread;
   auto row_ptr = [&](int i) { return logits + (static_cast<size_t>(b) * (n + 1) + i) * V; };
-  uint4 cur[kVerifyVecPerThread], nxt[kVerifyVecPerThread];
   auto load_pass = [&](uint4* dst, const __nv_bfloat16* row, int base) {
 #pragma unroll
     for (int v = 0; v < kVerifyVecPerThread; ++v) {
@@ -67,39 +69,56 @@ __global__ void __launch_bounds__(kVerifyThreads) k_verify(const __nv_bfloat16* 
     return best;
   };
 
-  load_pass(cur, row_ptr(0), lo);
-  for (int i = 0; i <= n; ++i) {
-    const __nv_bfloat16* row = row_ptr(i);
-    unsigned long long best = 0ull;
-    // further passes of this row (slices wider than one pass)
-    for (int base = lo + per_pass; base < hi; base += per_pass) {
-      uint4 tmp[kVerifyVecPerThread];
-      load_pass(tmp, row, base);
-      best = reduce_pass(tmp, base, best);
+  int buf = 0;
+#pragma unroll 1
+  for (int i0 = 0; i0 <= n; i0 += kVerifyRowBatch, buf ^= 1) {
+    const int R = min(kVerifyRowBatch, n + 1 - i0);
+    uint4 cur[kVerifyRowBatch][kVerifyVecPerThread];
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r)
+      if (r < R) load_pass(cur[r], row_ptr(i0 + r), lo);
+    unsigned long long best[kVerifyRowBatch];
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) {
+      best[r] = 0ull;
+      if (r < R) {
+        best[r] = reduce_pass(cur[r], lo, 0ull);
+        // further passes of this row (slices wider than one pass)
+#pragma unroll 1
+        for (int base = lo + per_pass; base < hi; base += per_pass) {
+          uint4 tmp[kVerifyVecPerThread];
+          load_pass(tmp, row_ptr(i0 + r), base);
+          best[r] = reduce_pass(tmp, base, best[r]);
+        }
+      }
     }
-    if (i < n) load_pass(nxt, row_ptr(i + 1), lo);  // prefetch the next row's first pass
-    best = reduce_pass(cur, lo, best);
-    best = warp_max_u64(best);
-    if (lane == 0) wk[warp] = best;
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) {
+      const unsigned long long m = warp_max_u64(best[r]);
+      if (lane == 0) wk[r][warp] = m;
+    }
     __syncthreads();
-    if (threadIdx.x < cs) {
+    // thread (row r, peer q) sends this CTA's key of row r to peer q
+    if (threadIdx.x < R * cs) {
+      const int r = threadIdx.x / cs, q = threadIdx.x - r * cs;
       unsigned long long m = 0ull;
-      for (int w = 0; w < kVerifyThreads / 32; ++w) m = wk[w] > m ? wk[w] : m;
-      unsigned long long* dst = cl.map_shared_rank(&keys[i & 1][rank], threadIdx.x);
-      *dst = m;
+      for (int w = 0; w < kVerifyThreads / 32; ++w) m = wk[r][w] > m ? wk[r][w] : m;
+      *cl.map_shared_rank(&keys[buf][r][rank], q) = m;
     }
     cl.sync();
-    unsigned long long m = 0ull;
-    for (int r = 0; r < cs; ++r) m = keys[i & 1][r] > m ? keys[i & 1][r] : m;
-    const int t = key_id(m);
-    const bool accept = i < n && draft[static_cast<size_t>(b) * n + i] == t;
-    if (rank == 0 && threadIdx.x == 0) {
-      out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
-      if (!accept) accept_len[b] = i;
+    bool go = true;
+    for (int r = 0; r < R && go; ++r) {
+      unsigned long long m = 0ull;
+      for (int q = 0; q < cs; ++q) m = keys[buf][r][q] > m ? keys[buf][r][q] : m;
+      const int i = i0 + r, t = key_id(m);
+      const bool accept = i < n && draft[static_cast<size_t>(b) * n + i] == t;
+      if (rank == 0 && threadIdx.x == 0) {
+        out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
+        if (!accept) accept_len[b] = i;
+      }
+      go = accept;
     }
-    if (!accept) break;
-#pragma unroll
-    for (int v = 0; v < kVerifyVecPerThread; ++v) cur[v] = nxt[v];
+    if (!go) break;
   }
   cl.sync();  // no CTA leaves while its shared keys may still be written by another
 }

@@ -463,13 +463,31 @@ def _verify_case(B, n, V, seed, ties=False):
 
 
 @pytest.mark.parametrize("B,n,V,ties", [(64, 8, 262144, False), (3, 0, 64, False), (5, 4, 4096, True),
-                                        (7, 1, 8, False), (2, 8, 131072, True)])
+                                        (7, 1, 8, False), (2, 8, 131072, True), (1, 4, 262144, False),
+                                        (1, 9, 4096, True), (1, 5, 262144, True)])
 def test_verify_matches_oracle(B, n, V, ties):
     from mtp_speculative_decoding_gemma4_gb300 import verify_greedy
     bits, drafts = _verify_case(B, n, V, seed=B * 1000 + n, ties=ties)
     acc, out = verify_greedy(to_torch(bits, "bf16"), to_torch(drafts, "i32"))
     torch.cuda.synchronize()
     racc, rout = O.verify_greedy(bits, drafts)
+    np.testing.assert_array_equal(acc.cpu().numpy(), racc)
+    np.testing.assert_array_equal(out.cpu().numpy(), rout)
+
+
+@pytest.mark.parametrize("B,n", [(1, 4), (1, 12), (6, 6)])
+def test_verify_ignores_rows_after_the_first_disagreement(B, n):
+    """Rows after each sequence's first disagreement are overwritten with NaN (bf16 0x7fc1);
+    they share a read batch with the rows before them, yet the result is the oracle's."""
+    from mtp_speculative_decoding_gemma4_gb300 import verify_greedy
+    V = 8192
+    bits, drafts = _verify_case(B, n, V, seed=77 + B * 13 + n, ties=False)
+    racc, rout = O.verify_greedy(bits, drafts)
+    poisoned = bits.copy()
+    for b in range(B):
+        poisoned[b, int(racc[b]) + 1:, :] = 0x7FC1
+    acc, out = verify_greedy(to_torch(poisoned, "bf16"), to_torch(drafts, "i32"))
+    torch.cuda.synchronize()
     np.testing.assert_array_equal(acc.cpu().numpy(), racc)
     np.testing.assert_array_equal(out.cpu().numpy(), rout)
 

@@ -50,6 +50,13 @@ __device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// A read-only global load kept in program order with the other volatile asm: issued before a
+// wait, consumed after it (the compiler would otherwise sink the load to its first use).
+__device__ __forceinline__ float ldg_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ void st_rlx64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -413,7 +420,7 @@ __device__ __forceinline__ unsigned long long topk_key(const float* cl, int i) {
 //
 // Any C and k: one warp per group, ranks by ballots (shapes the tiled form below does not
 // cover, and candidate sets that overflow its buffer).
-__device__ __forceinline__ void topk_generic(const Params& p, unsigned char* sm, const float* cl, int* sel) {
+__device__ __noinline__ void topk_generic(const Params& p, unsigned char* sm, const float* cl, int* sel) {
   const Layout& L = p.L;
   const int C = p.C, k = p.topk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -654,11 +661,11 @@ __device__ __forceinline__ void topk_select(const Params& p, unsigned char* sm, 
 // This CTA's keys of one block: q_norm + RoPE (+ the softmax scale) of every head from the
 // gathered raw q (ub), scores of every (key, head), softmax statistics (max, exp-sum) per
 // head, the probability-weighted key sums (V = K); publishes [c][h][d + 2] (sums, max,
-// exp-sum) to the owners of q's dims. gq0..gq7: the q_norm gains of this thread's first four
-// RoPE pairs (prefetched into registers). All threads call.
+// exp-sum) to the owners of q's dims. Any head dim (the general form). g[0..7]: the q_norm
+// gains (j, j + d/2) of this thread's first four RoPE pairs, loaded before the q gather waits.
+// All threads call.
 __device__ __forceinline__ void attend(const Params& p, unsigned char* sm, int l, int t, int c, int nk, const bf16* kb,
-                                      long long kst, unsigned long long* ma, unsigned epa, float gq0, float gq1,
-                                      float gq2, float gq3, float gq4, float gq5, float gq6, float gq7) {
+                                      long long kst, unsigned long long* ma, unsigned epa, const float (&g)[16]) {
   const Layout& L = p.L;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nh = p.nh, nkv = p.nkv, lg = p.lg_d[t], d = 1 << lg, grp = nh / nkv, half = d >> 1, ksl = L.ksl;
@@ -684,8 +691,14 @@ __device__ __forceinline__ void attend(const Params& p, unsigned char* sm, int l
 #pragma unroll 1
     for (int i = tid; i < nh * half; i += kT, ++k) {
       const int h = i >> (lg - 1), j = i & (half - 1);
-      const float g0 = k == 0 ? gq0 : (k == 1 ? gq2 : (k == 2 ? gq4 : (k == 3 ? gq6 : __ldg(gqn + j))));
-      const float g1 = k == 0 ? gq1 : (k == 1 ? gq3 : (k == 2 ? gq5 : (k == 3 ? gq7 : __ldg(gqn + j + half))));
+      float g0, g1;
+      if (k < 4) {  // prefetched: the gains of this thread's first four pairs
+        g0 = k == 0 ? g[0] : (k == 1 ? g[2] : (k == 2 ? g[4] : g[6]));
+        g1 = k == 0 ? g[1] : (k == 1 ? g[3] : (k == 2 ? g[5] : g[7]));
+      } else {
+        g0 = __ldg(gqn + j);
+        g1 = __ldg(gqn + j + half);
+      }
       const float rn = red[h];
       const float a = ub[h * d + j] * rn * g0, b = ub[h * d + j + half] * rn * g1;
       const float2 cw = cs[j];
@@ -819,6 +832,202 @@ __device__ __forceinline__ void attend(const Params& p, unsigned char* sm, int l
   }
 }
 
+// The same for head dims d = 32 * DL (256 or 512) and four query heads (V = K):
+//   A: warp h takes head h's q_norm statistic over all d dims.
+//   B: lane i holds the 8-dim runs starting at 8 (i + 32 v), v < DL / 8, of q for every head
+//      (q_norm gain, RoPE with the partner dims d/2 away, softmax scale); warp w takes keys w,
+//      w + 8, ... in passes of KB keys: the lane's partial dot products of the pass's keys
+//      with the four heads are summed over the lanes by a transposed butterfly, and the lanes
+//      that end with a whole (key, head) score store it.
+//   C: warp h: softmax statistics of head h over the keys; probabilities in place.
+//   D: warp w owns dims [w d/8, (w+1) d/8), d/256 consecutive dims per lane: the
+//      probability-weighted key sums of its dims for every head, published with the
+//      statistics as [c][h][d + 2].
+// The (cos, sin) table is lane-major for these dims (consecutive lanes read consecutive
+// entries). g: this lane's q_norm gains of its runs, then (d = 256) of its partner runs,
+// loaded before the q gather waits. All threads call.
+template <int DL>
+__device__ __forceinline__ void attend_g(const Params& p, unsigned char* sm, int t, int c, int nk, const bf16* kb,
+                                         long long kst, unsigned long long* ma, unsigned epa, const float (&g)[16]) {
+  constexpr int d = 32 * DL, half = d / 2, NV = DL / 8, LG = half / 8, NH = 4;
+  constexpr int KB = DL == 8 ? 1 : 4, NVAL = KB * NH, DPL = d / 256, DW = d / kW;
+  const Layout& L = p.L;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nkv = p.nkv;
+  const float* ub = reinterpret_cast<const float*>(sm + L.ubuf);
+  float* sc = reinterpret_cast<float*>(sm + L.sc);    // [key][head] scores, then probabilities
+  float* red = reinterpret_cast<float*>(sm + L.red);  // [h]: q_norm factor; [16 + h] max; [32 + h] exp-sum
+  const float2* cs = reinterpret_cast<const float2*>(sm + L.cs) + (t ? p.d[0] / 2 : 0);
+  // A
+  if (warp < NH) {
+    const float4* qv = reinterpret_cast<const float4*>(ub + warp * d);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < d / 128; ++i) {
+      const float4 a = qv[lane + 32 * i];
+      ss = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w, ss))));
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = rsqrtf(ss / static_cast<float>(d) + p.eps);
+  }
+  __syncthreads();
+  // B: q runs of every head
+  float q[NH][DL];
+  {
+    const float scale = p.scale[t];
+    const int pl = NV == 2 ? lane : (lane & 15);  // pair run of this lane
+    float2 cw[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) cw[e] = cs[e * LG + pl];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float rn = red[h];
+      float x[DL], y[DL];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const float4* a4 = reinterpret_cast<const float4*>(ub + h * d + 8 * (lane + 32 * v));
+        const float4 a = a4[0], b = a4[1];
+        x[8 * v] = a.x, x[8 * v + 1] = a.y, x[8 * v + 2] = a.z, x[8 * v + 3] = a.w;
+        x[8 * v + 4] = b.x, x[8 * v + 5] = b.y, x[8 * v + 6] = b.z, x[8 * v + 7] = b.w;
+      }
+      if (NV == 2) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = x[8 + e], y[8 + e] = x[e];
+#pragma unroll
+        for (int i = 0; i < DL; ++i) x[i] *= rn * g[i], y[i] *= rn * g[(i + 8) & 15];
+      } else {
+        const float4* a4 = reinterpret_cast<const float4*>(ub + h * d + 8 * (lane ^ 16));
+        const float4 a = a4[0], b = a4[1];
+        y[0] = a.x, y[1] = a.y, y[2] = a.z, y[3] = a.w, y[4] = b.x, y[5] = b.y, y[6] = b.z, y[7] = b.w;
+#pragma unroll
+        for (int i = 0; i < DL; ++i) x[i] *= rn * g[i], y[i] *= rn * g[8 + i];
+      }
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const bool lo = NV == 2 ? v == 0 : lane < 16;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xv = x[8 * v + e], yv = y[8 * v + e];
+          q[h][8 * v + e] = (lo ? fmaf(xv, cw[e].x, -yv * cw[e].y) : fmaf(xv, cw[e].x, yv * cw[e].y)) * scale;
+        }
+      }
+    }
+  }
+  // B: scores, KB keys per pass
+#pragma unroll 1
+  for (int j0 = warp; j0 < nk; j0 += KB * kW) {
+    float v[NVAL];
+#pragma unroll
+    for (int i = 0; i < NVAL; ++i) v[i] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KB; ++kk) {
+      const int j = j0 + kk * kW;
+      if (j < nk) {
+#pragma unroll
+        for (int kh = 0; kh < NH; ++kh) {
+          if (kh < nkv) {
+            float kf[DL];
+#pragma unroll
+            for (int u = 0; u < NV; ++u)
+              bf8(*reinterpret_cast<const uint4*>(kb + static_cast<long long>(j) * kst + kh * d + 8 * (lane + 32 * u)),
+                  kf + 8 * u);
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+              if ((h * nkv) / NH == kh) {
+                float a = 0.f;
+#pragma unroll
+                for (int i = 0; i < DL; ++i) a = fmaf(q[h][i], kf[i], a);
+                v[kk * NH + h] = a;
+              }
+          }
+        }
+      }
+    }
+    // transposed butterfly: while a lane keeps several values each offset halves them, the
+    // remaining offsets finish the sums; lane i ends with value i / (32 / NVAL)
+#pragma unroll
+    for (int off = 16, n = NVAL; off >= 1; off >>= 1) {
+      if (n > 1) {
+        const bool up = lane & off;
+#pragma unroll
+        for (int i = 0; i < NVAL / 2; ++i)
+          if (i < n / 2) {
+            const float send = up ? v[i] : v[i + n / 2], keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+          }
+        n >>= 1;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+      }
+    }
+    const int vi = lane / (32 / NVAL), j = j0 + (vi / NH) * kW;
+    if ((lane & (32 / NVAL - 1)) == 0 && j < nk) sc[j * NH + (vi & (NH - 1))] = v[0];
+  }
+  __syncthreads();
+  // C
+  if (warp < NH) {
+    const int h = warp;
+    float m = -INFINITY;
+#pragma unroll 1
+    for (int j = lane; j < nk; j += 32) m = fmaxf(m, sc[j * NH + h]);
+    m = warp_max(m);
+    float l = 0.f;
+#pragma unroll 1
+    for (int j = lane; j < nk; j += 32) {
+      const float e = expf(sc[j * NH + h] - m);
+      sc[j * NH + h] = e;
+      l += e;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      red[16 + h] = m;
+      red[32 + h] = l;
+    }
+  }
+  __syncthreads();
+  // D
+  const int dim0 = warp * DW + lane * DPL;
+  float acc[NH][DPL];
+#pragma unroll
+  for (int h = 0; h < NH; ++h)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
+#pragma unroll 4
+  for (int j = 0; j < nk; ++j) {
+    const float4 pv = *reinterpret_cast<const float4*>(sc + j * NH);
+    const float pj[NH] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+    for (int kh = 0; kh < NH; ++kh) {
+      if (kh < nkv) {
+        float kf[DPL];
+        const bf16* kr = kb + static_cast<long long>(j) * kst + kh * d + dim0;
+        if (DPL == 2) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kr));
+          kf[0] = f.x;
+          kf[DPL - 1] = f.y;
+        } else {
+          kf[0] = bf(kr[0]);
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if ((h * nkv) / NH == kh)
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(pj[h], kf[k], acc[h][k]);
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const long long base = (static_cast<long long>(c) * NH + h) * (d + 2);
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) put(ma, base + dim0 + k, acc[h][k], epa);
+  }
+  if (tid < NH) {
+    put(ma, (static_cast<long long>(c) * NH + tid) * (d + 2) + d, red[16 + tid], epa);
+    put(ma, (static_cast<long long>(c) * NH + tid) * (d + 2) + d + 1, red[32 + tid], epa);
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int EPL>
@@ -863,29 +1072,37 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
   const Range fr = split(p.F, p.N, c), hr = split(p.bb, p.N, c), cr = split(p.C, p.N, c);
   const Range candr = split(p.topk * p.vsc, p.N, c);
   const int nf = fr.hi - fr.lo, nhc = hr.hi - hr.lo, ncr = cr.hi - cr.lo;
-  // bulk copy of this CTA's keys of type t into the shared K region (one mbarrier phase)
+  // bulk copies of this CTA's keys of type t into the shared K region (kbuf + koff[t]); one
+  // mbarrier phase per issue (both resident types together when they stay for the launch)
   int kph = 0, kwaited = 0, kcur = -1;
+  auto k_bytes = [&](int t) {
+    const Range kt = t ? kr1 : kr0;
+    return static_cast<unsigned>((kt.hi - kt.lo) * p.nkv * p.d[t] * 2);
+  };
+  auto k_copy = [&](int t) {  // thread 0
+    const Range kt = t ? kr1 : kr0;
+    const int n = kt.hi - kt.lo, row = p.nkv * p.d[t];
+    const bf16* k0 = p.k[t] + static_cast<size_t>((t ? 0 : klo0) + kt.lo) * static_cast<size_t>(p.st[t]);
+    unsigned char* dst = sm + L.kbuf + L.koff[t];
+    if (n <= 0) return;
+    if (p.st[t] == row) {
+      bulk_g2s(sa(dst), k0, static_cast<unsigned>(n * row * 2), sa(&bars[kbar]));
+    } else {
+#pragma unroll 1
+      for (int j = 0; j < n; ++j)
+        bulk_g2s(sa(dst + j * row * 2), k0 + static_cast<size_t>(j) * p.st[t], static_cast<unsigned>(row * 2),
+                 sa(&bars[kbar]));
+    }
+  };
+  auto k_resident = [&](int t) { return p.has_type[t] && p.kres[t] && c < p.A[t]; };
   auto k_issue = [&](int t) {
     if (tid == 0) {
-      const Range kt = t ? kr1 : kr0;
-      const int n = kt.hi - kt.lo, row = p.nkv * p.d[t];
-      const bf16* k0 = p.k[t] + static_cast<size_t>((t ? 0 : klo0) + kt.lo) * static_cast<size_t>(p.st[t]);
-      mbar_expect_tx(sa(&bars[kbar]), static_cast<unsigned>(n > 0 ? n * row * 2 : 0));
-      if (n > 0) {
-        if (p.st[t] == row) {
-          bulk_g2s(sa(sm + L.kbuf), k0, static_cast<unsigned>(n * row * 2), sa(&bars[kbar]));
-        } else {
-#pragma unroll 1
-          for (int j = 0; j < n; ++j)
-            bulk_g2s(sa(sm + L.kbuf + j * row * 2), k0 + static_cast<size_t>(j) * p.st[t],
-                     static_cast<unsigned>(row * 2), sa(&bars[kbar]));
-        }
-      }
+      mbar_expect_tx(sa(&bars[kbar]), k_bytes(t));
+      k_copy(t);
     }
     ++kph;
     kcur = t;
   };
-  auto k_resident = [&](int t) { return p.has_type[t] && p.kres[t] && c < p.A[t]; };
 
   // ---- launch start: barriers, bulk copies of this CTA's weight image and first keys
   if (tid == 0) {
@@ -900,7 +1117,19 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
       if (b) bulk_g2s(sa(sm + L.grp_off[gi]), src + L.grp_off[gi], b, sa(&bars[gi]));
     }
   }
-  if (k_resident(p.ltype[0])) k_issue(p.ltype[0]);
+  if (p.kboth) {
+    const bool r0 = k_resident(0), r1 = k_resident(1);
+    if (r0 || r1) {
+      if (tid == 0) {
+        mbar_expect_tx(sa(&bars[kbar]), (r0 ? k_bytes(0) : 0u) + (r1 ? k_bytes(1) : 0u));
+        if (r0) k_copy(0);
+        if (r1) k_copy(1);
+      }
+      ++kph;
+    }
+  } else if (k_resident(p.ltype[0])) {
+    k_issue(p.ltype[0]);
+  }
   __syncthreads();
   cluster_sync_all();  // every peer's barriers are initialised before any st.async
 
@@ -917,7 +1146,11 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
       const double ang = pos * p.inv_freq[t * hm + ii];
       const double r = fma(-rint(ang * inv_two_pi), two_pi, ang);
       const float rf = static_cast<float>(r);
-      cs[i] = make_float2(__cosf(rf), __sinf(rf));
+      // the four-head form (head dim 256): pair j at (j % 8) * 16 + j / 8, so that lanes
+      // holding consecutive 8-dim runs read consecutive entries
+      const int ht = t ? h1 : h0;
+      const int at = ht == 128 && p.nh == 4 ? (ii & 7) * (ht >> 3) + (ii >> 3) : ii;
+      cs[(t ? h0 : 0) + at] = make_float2(__cosf(rf), __sinf(rf));
     }
   }
 #pragma unroll 1
@@ -1004,15 +1237,23 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
       // ---------------- ATT (attention CTAs): the partial softmax of my keys
       unsigned long long* ma = p.mb + xo[ex_att(l)];
       if (c < p.A[t]) {
-        // q_norm gains of this thread's first RoPE pairs, loaded before the q gather waits
-        float gq0 = 0.f, gq1 = 0.f, gq2 = 0.f, gq3 = 0.f, gq4 = 0.f, gq5 = 0.f, gq6 = 0.f, gq7 = 0.f;
+        // q_norm gains loaded before the q gather waits: for the four-head form this lane's run
+        // (8 dims at 8 lane) and its RoPE partner run (16 lanes away); for the general form the
+        // pairs (j, j + d/2) of this thread's first four RoPE pairs
+        const bool wide = d == 256 && nh == 4;
+        float gw[16];
         {
-          const int half = d / 2, np = nh * half;
           const float* gqn = p.q_norm[l];
-          if (tid < np) { gq0 = __ldg(gqn + (tid & (half - 1))); gq1 = __ldg(gqn + (tid & (half - 1)) + half); }
-          if (tid + kT < np) { gq2 = __ldg(gqn + ((tid + kT) & (half - 1))); gq3 = __ldg(gqn + ((tid + kT) & (half - 1)) + half); }
-          if (tid + 2 * kT < np) { gq4 = __ldg(gqn + ((tid + 2 * kT) & (half - 1))); gq5 = __ldg(gqn + ((tid + 2 * kT) & (half - 1)) + half); }
-          if (tid + 3 * kT < np) { gq6 = __ldg(gqn + ((tid + 3 * kT) & (half - 1))); gq7 = __ldg(gqn + ((tid + 3 * kT) & (half - 1)) + half); }
+          const int half = d / 2, np = nh * half;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (wide) {
+              gw[i] = ldg_early(gqn + 8 * (i < 8 ? lane : (lane ^ 16)) + (i & 7));
+            } else {
+              const int pi = tid + (i >> 1) * kT;
+              gw[i] = i < 8 && pi < np ? ldg_early(gqn + (pi & (half - 1)) + (i & 1) * half) : 0.f;
+            }
+          }
         }
         if (!gather_lin(p, p.mb + xo[ex_q(l)], QD, reinterpret_cast<unsigned*>(ub), ep0 + ex_q(l))) {
           ok = false;
@@ -1020,7 +1261,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
         }
         const bool res = k_resident(t);
         if (res) {
-          if (kcur != t) k_issue(t);  // not scheduled ahead (cannot happen with the schedule below)
+          if (!p.kboth && kcur != t) k_issue(t);  // not scheduled ahead (cannot happen with the schedule below)
           if (kwaited < kph) {
             ok = mbar_wait(p, sa(&bars[kbar]), static_cast<unsigned>(kph - 1) & 1u, true);
             kwaited = kph;
@@ -1028,14 +1269,17 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
           }
         }
         const Range kt = t ? kr1 : kr0;
-        const bf16* kb = res ? reinterpret_cast<const bf16*>(sm + L.kbuf)
+        const bf16* kb = res ? reinterpret_cast<const bf16*>(sm + L.kbuf + L.koff[t])
                              : p.k[t] + static_cast<size_t>((t ? 0 : klo0) + kt.lo) * static_cast<size_t>(p.st[t]);
         const long long kst = res ? static_cast<long long>(p.nkv) * d : p.st[t];
-        attend(p, sm, l, t, c, kt.hi - kt.lo, kb, kst, ma, ep0 + ex_att(l), gq0, gq1, gq2, gq3, gq4, gq5, gq6, gq7);
+        if (wide)
+          attend_g<8>(p, sm, t, c, kt.hi - kt.lo, kb, kst, ma, ep0 + ex_att(l), gw);
+        else
+          attend(p, sm, l, t, c, kt.hi - kt.lo, kb, kst, ma, ep0 + ex_att(l), gw);
         // the next block of the other type (here or in the next step) finds its keys loaded
         const bool last = l == nl - 1;
         const int tn = p.ltype[last ? 0 : l + 1];
-        if (tn != t && k_resident(tn) && !(last && s == p.n_draft - 1)) {
+        if (!p.kboth && tn != t && k_resident(tn) && !(last && s == p.n_draft - 1)) {
           __syncthreads();  // every read of the region is done
           k_issue(tn);
         }
@@ -1319,10 +1563,11 @@ int clusters_for(int H, int S, int smem) {
 
 // Attention CTAs, resident-key rows and the layout for a grid of N CTAs; false when the
 // shape cannot run on it.
-bool plan_for(gr::Params& p, int N, int S, int G, bool k_full_res, bool k_swa_res, int optin) {
+bool plan_for(gr::Params& p, int N, int S, int G, bool k_full_res, bool k_swa_res, bool k_both, int optin) {
   p.N = N;
   p.S = S;
   p.G = G;
+  p.kboth = k_both ? 1 : 0;
   for (int t = 0; t < 2; ++t) {
     if (!p.has_type[t]) {
       p.A[t] = 0;
@@ -1399,7 +1644,9 @@ int gr_plan(gr::Params& p, int optin) {
       p.tk_lg_tpg = lg2(tpg);
     }
   }
-  const bool res_opts[3][2] = {{true, true}, {false, true}, {false, false}};
+  // attended keys resident in shared memory: both types for the whole launch, else both
+  // taking turns in one region, else the sliding type only, else none
+  const bool res_opts[4][3] = {{true, true, true}, {true, true, false}, {false, true, false}, {false, false, false}};
   #pragma unroll 1
   for (const auto& ro : res_opts) {
     #pragma unroll 1
@@ -1410,7 +1657,7 @@ int gr_plan(gr::Params& p, int optin) {
       while ((1 << q.lg_hs) < H / S) ++q.lg_hs;
       const int G = clusters_for(H, S, optin);
       if (G < 1) continue;
-      if (!plan_for(q, G * S, S, G, ro[0], ro[1], optin)) continue;
+      if (!plan_for(q, G * S, S, G, ro[0], ro[1], ro[2], optin)) continue;
       // the grid must be co-resident at the planned size
       const int G2 = clusters_for(H, S, q.L.total);
       if (G2 < G) continue;

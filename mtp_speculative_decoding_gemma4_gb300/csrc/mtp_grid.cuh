@@ -86,7 +86,9 @@ struct Layout {
   int pre, post, q[kMaxL], o[kMaxL], g[kMaxL], u[kMaxL], dn[kMaxL], cent;
   int grp_off[kMaxL + 2], grp_bytes[kMaxL + 2];
   int img_bytes;
-  int kbuf, kbuf_bytes; // K rows of the resident attention type [kslots][nkv * d] (one type at a time)
+  int kbuf, kbuf_bytes; // K rows of the resident attention types [kslots][nkv * d]: both at once
+                        // (type t at kbuf + koff[t]) or one type at a time (koff 0)
+  int koff[2];
   int ubuf, u_words;    // gather scratch (fp32)
   int qs;               // normed, rotated, scaled q [nh * dmax]; in the head: top-k candidates
   int cand_cap;         // top-k candidates the qs region holds
@@ -117,6 +119,7 @@ struct Params {
   int kres[2];   // 1: the CTA's keys of the type are bulk-copied into the shared K region before the
                  // first block of that type (the region holds one type at a time); 0: read from global
   int kslots[2]; // largest key share of an attention CTA (shared-memory rows / score slots)
+  int kboth;     // 1: the resident types' keys are loaded once, side by side, for the whole launch
   int has_type[2];
   int lg_d[2], lg_hs, lg_vsc;  // log2 of the head dims, of H / S and of vsc (all powers of two)
   int tk_lg_per, tk_lg_tpg;    // top-k tiling: log2 of keys per thread and of threads per group (-1: untiled)
@@ -206,9 +209,17 @@ inline Layout make_layout(const Params& p) {
   L.img_bytes = off;
   L.kbuf = off;
   L.kbuf_bytes = 0;
-  for (int t = 0; t < 2; ++t)
-    if (p.has_type[t] && p.kres[t] && p.kslots[t] * p.nkv * p.d[t] * 2 > L.kbuf_bytes)
-      L.kbuf_bytes = p.kslots[t] * p.nkv * p.d[t] * 2;
+  L.koff[0] = L.koff[1] = 0;
+  for (int t = 0; t < 2; ++t) {
+    if (!p.has_type[t] || !p.kres[t]) continue;
+    const int b = p.kslots[t] * p.nkv * p.d[t] * 2;
+    if (p.kboth) {
+      L.koff[t] = L.kbuf_bytes;
+      L.kbuf_bytes += al16(b);
+    } else if (b > L.kbuf_bytes) {
+      L.kbuf_bytes = b;
+    }
+  }
   off += al16(L.kbuf_bytes);
   // gather scratch: q (max QD), centroid logits (C), attention partials of my dims
   // (A x (nq + 2 x heads touched)), AR slices (G x H / S), argmax keys (2N)

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify(const __nv_bfloat1
                                                              int* __restrict__ accept_len, int* __restrict__ out_tokens) {
   __shared__ unsigned long long keys[2][kVerifyRowBatch][kVerifyMaxCluster];
   __shared__ unsigned long long wk[kVerifyRowBatch][kVerifyThreads / 32];
+  __shared__ int dtok[2][kVerifyRowBatch];
   cg::cluster_group cl = cg::this_cluster();
   const int cs = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
@@ -73,6 +74,9 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify(const __nv_bfloat1
 #pragma unroll 1
   for (int i0 = 0; i0 <= n; i0 += kVerifyRowBatch, buf ^= 1) {
     const int R = min(kVerifyRowBatch, n + 1 - i0);
+    // the batch's drafted tokens, read once ahead of the decisions (made after a barrier below)
+    if (threadIdx.x < R && i0 + static_cast<int>(threadIdx.x) < n)
+      dtok[buf][threadIdx.x] = draft[static_cast<size_t>(b) * n + i0 + threadIdx.x];
     uint4 cur[kVerifyRowBatch][kVerifyVecPerThread];
 #pragma unroll
     for (int r = 0; r < kVerifyRowBatch; ++r)
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify(const __nv_bfloat1
       unsigned long long m = 0ull;
       for (int q = 0; q < cs; ++q) m = keys[buf][r][q] > m ? keys[buf][r][q] : m;
       const int i = i0 + r, t = key_id(m);
-      const bool accept = i < n && draft[static_cast<size_t>(b) * n + i] == t;
+      const bool accept = i < n && dtok[buf][r] == t;
       if (rank == 0 && threadIdx.x == 0) {
         out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
         if (!accept) accept_len[b] = i;

@@ -300,8 +300,11 @@ MTP_API int mtp_get_status(mtp_handle *h);
  * returns early without a fault, and the handle stays usable. spin_limit_cycles > 0 replaces
  * the bound of the device waits of the phase and persistent paths (default about 2 s of
  * clock64 cycles). On the grid path (7), CTA skip_arrival_cta does not publish its slice of
- * the first all-reduce of the next launches (with the same timeout outcome), and the bound
- * applies to its waits too. (-1, 0) restores the defaults. No other path is affected.
+ * the first all-reduce of the next launches; on the streamed cluster path (6), CTA
+ * skip_arrival_cta of the cluster sends none of its rows in the launch's first exchange; on
+ * the tensor-core path (5), CTA skip_arrival_cta of the first projection GEMM issues no copy
+ * for its last k stage. Each has the same timeout outcome, and the bound applies to the
+ * waits of these paths too. (-1, 0) restores the defaults. No other path is affected.
  * Errors: INVALID_ARG (NULL handle, skip_arrival_cta < -1, spin_limit_cycles < 0). */
 MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_limit_cycles);
 

@@ -907,6 +907,8 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     cp.n_draft = n_draft;
     cp.status = h->wsp.status;
     cp.abort_flag = h->abort_word;
+    cp.spin_limit = h->dbg_spin > 0 ? h->dbg_spin : 4000000000LL;
+    cp.dbg_skip = h->dbg_skip;
     const int smem = mtp::c2_smem_bytes(cp);
     if (smem <= 0 || (reinterpret_cast<uintptr_t>(hidden) & 15) != 0) {
       set_error("streamed cluster path: shape, K stride or hidden alignment not supported for this call");

@@ -823,7 +823,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_c2(const __grid_constant__ Para
     // all-gather of the rows of a section (fp32, at the rows' offsets)
     auto gather_rows = [&](const SecE* se, const float* part, int total) -> const float* {
       arm(xe, 4 * total);
-      if (live)
+      if (live && !(xe == 0 && p.dbg_skip == r + 1))
         for (int i = tid; i < se->w.rows; i += kCT)
           bcast_f32(xset(xe) + 4u * static_cast<unsigned>(se->w.lo + i), xbar(xe), sum_parts(part, se, i));
       xwait(xe);

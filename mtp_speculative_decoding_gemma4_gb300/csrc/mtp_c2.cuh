@@ -119,6 +119,7 @@ struct Params {
   int* status;
   unsigned* abort_flag;
   long long spin_limit;
+  int dbg_skip;  // testing: CTA dbg_skip - 1 sends none of its rows in the launch's first exchange
 };
 
 // The projection of step-sequence entry `idx` (R rows x K): 0 PRE | per block l: 1+6l Q,

@@ -334,8 +334,8 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   ps.tc_bp = plan.bp;
   auto groups = [&](int) { return s.B; };  // staging runs one sequence per CTA
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
-                  long long ld2, unsigned long long* best) -> int {
-    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit};
+                  long long ld2, unsigned long long* best, int dbg_cta = -1) -> int {
+    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit, dbg_cta};
     return tc_gemm(&w, &x, a, best != nullptr, st);
   };
   int rc;
@@ -343,7 +343,9 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   int par = 0;
   for (int step = 0; step < p.n_draft; ++step) {
     MTP_LAUNCH(k_pre<WT>, groups(2 * s.bb), z.smem_pre, ps, step, par);
-    if ((rc = gemm(plan.pre, plan.xs_pre, s.H, 2 * s.bb, p.w.x[par], s.H, nullptr, 0, nullptr))) return rc;
+    if ((rc = gemm(plan.pre, plan.xs_pre, s.H, 2 * s.bb, p.w.x[par], s.H, nullptr, 0, nullptr,
+                   step == 0 ? p.dbg_skip - 1 : -1)))
+      return rc;
     for (int l = 0; l < s.nl; ++l) {
       const int t = p.L[l].type, QD = s.nh * s.d[t];
       MTP_LAUNCH(k_q<WT>, groups(s.H), z.smem_q, ps, l, par);

@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = kt % kStages;
         if (kt >= kStages && !wait_bar(empty0 + 8 * s, static_cast<unsigned>((kt / kStages - 1) & 1), a.status, a.spin_limit))
           break;
+        if (kt == KT - 1 && static_cast<int>(blockIdx.x) == a.dbg_cta) break;  // testing: the MMA warp's wait runs out
         const unsigned st = base + s * SB;
         mbar_expect_tx(full0 + 8 * s, static_cast<unsigned>(SB));
         tma_load_2d(st, &mapW, (kt_lo + kt) * kKStage, tile * kM, full0 + 8 * s);

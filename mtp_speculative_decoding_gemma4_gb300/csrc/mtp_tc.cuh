@@ -49,6 +49,7 @@ struct Args {
   int splits;                    // K split over this many CTAs of one cluster (1: no split)
   int* status;
   long long spin_limit;
+  int dbg_cta;  // testing: this CTA's producer issues no copy for its last k stage (-1: none)
 };
 
 __host__ __device__ inline int stage_bytes(int B) { return kM * kKStage * 2 + 3 * B * kKStage * 2; }

@@ -369,6 +369,30 @@ def test_grid_path_timeout_is_reported_and_the_handle_recovers():
     dr.close()
 
 
+@pytest.mark.parametrize("index,batch,path", [(1, 0, STREAMED), (1, 3, TENSOR)])
+def test_cluster_and_tensor_core_timeouts_are_reported_and_the_handle_recovers(index, batch, path):
+    # failure detection without a fault, one test per kernel family: on the streamed cluster
+    # path (k_block_c2) CTA 0 sends none of its rows in the launch's first exchange; on the
+    # tensor-core path the first projection GEMM's CTA 0 (k_tc_gemm) issues no copy for its
+    # last k stage. Either way a bounded wait gives up after ~10 ms of cycles, the status word
+    # reads MTP_ERR_TIMEOUT, and the next call on the same handle matches the oracle.
+    from mtp_speculative_decoding_gemma4_gb300 import binding
+    shape, wl, w, inp = config_data(index, batch)
+    ref = oracle_block(index, batch=batch)
+    dr, d = _drafter(index, batch)
+    dr.set_path(path)
+    dr.set_debug(skip_arrival_cta=0, spin_limit_cycles=20_000_000)
+    dr.draft_block(d["hidden"], d["last_token"], d["k_swa"], d["k_full"], d["ctx_len"], d["pos"], wl.n_draft)
+    torch.cuda.synchronize()
+    assert dr.status() == binding.MTP_ERR_TIMEOUT
+    assert dr.status() == binding.MTP_OK
+    dr.set_debug()
+    tok, hid = _run_block(dr, d, wl.n_draft, path)
+    cmp = compare_block(tok, hid, ref, shape.dtype)
+    assert len(cmp.tie_divergences) <= max(1, cmp.steps_compared // 50)
+    dr.close()
+
+
 def test_dense_head_entry_matches_oracle():
     shape, wl, w, inp = config_data(3)
     s, W = decoded(3)

@@ -272,9 +272,11 @@ def run_mtp(args, rank: int, world: int, dist):
         verify_greedy(logits, out_tok, accept_len=acc, out_tokens=out_v, stream=sh)
 
     if args.profile_blocks:
-        # exactly this many draft blocks, nothing timed: the program named by the ncu captures
+        # exactly this many steps (draft block + verify), nothing timed: the program named by
+        # the ncu captures
         for _ in range(args.profile_blocks):
             draft()
+            verify()
         torch.cuda.synchronize()
         assert dr.status() == 0
         return None
@@ -534,7 +536,7 @@ def main():
                          "with tcgen05 projections, 6: streamed-tile cluster kernel (one sequence), 7: grid "
                          "kernel (one sequence); default: 7 for B=1, else 5")
     ap.add_argument("--profile-blocks", type=int, default=0,
-                    help="run exactly this many draft blocks of the chosen path and exit without timing "
+                    help="run exactly this many steps (draft block + verify) of the chosen path and exit without timing "
                          "(the program the ncu captures in profiles/ name)")
     ap.add_argument("--sparse-head", choices=sorted(SPARSE_HEAD), default="auto",
                     help="traversal of the centroid head's candidate rows in the batched paths: per sequence, "

@@ -218,9 +218,10 @@ MTP_API int mtp_set_sparse_head(mtp_handle *h, int32_t mode);
  * Decoding?"): t_i = argmax of target row i (lowest id on ties); accept_len[b] = the
  * largest m with draft[b][i] == t_i for all i < m; out_tokens[b] = draft[b][0..m) followed
  * by t_m (the target's correction, or its extra token when m == n), then -1 padding.
- * Rows after the first disagreement never change the result. Rows are read in batches of
- * five (one memory round trip per batch); batches after the one holding the first
- * disagreement are not read.
+ * Rows after the first disagreement never change the result. Rows are read in batches of up
+ * to five (copied together into shared memory); batches after the one holding the first
+ * disagreement are not read. accept_len[b] = -1 reports that a bounded device wait on those
+ * copies gave up (not expected on a working GPU); that sequence's undecided rows stay -1.
  *   target_logits device [B][n+1][V] bf16
  *   draft         device [B][n] int32
  *   accept_len    device [B] int32

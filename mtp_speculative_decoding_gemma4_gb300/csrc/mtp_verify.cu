@@ -13,6 +13,10 @@
 // result; the batches after the one holding it are never read.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+#include <climits>
+#include <mutex>
+
 #include "mtp_common.cuh"
 #include "mtp_launch.h"
 
@@ -127,23 +131,240 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify(const __nv_bfloat1
   cl.sync();  // no CTA leaves while its shared keys may still be written by another
 }
 
+// The same with the rows' slices copied into shared memory by the bulk-copy engine (one copy
+// per row and CTA, a transaction barrier per row slot): the copies of a batch are in flight
+// together without holding registers. Each CTA takes its slice's largest value with packed
+// bf16 maxima, then the first position holding it (packed compares), and the cluster keeps
+// the largest value (fp32 comparison, so -0 equals +0), lowest position. Every wait on a copy is bounded; a CTA whose wait gives up marks the
+// sequence (every CTA of the cluster learns it with the keys), which then gets
+// accept_len = -1 and no further rows. Used when at least one row slice fits the
+// shared-memory budget (rb rows per batch).
+constexpr int kVerifySmemMax = 200 * 1024;
+constexpr long long kVerifySpin = 1LL << 32;  // about 2 s of clock64 cycles
+
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ bool vbar_try(unsigned bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000u)
+      : "memory");
+  return ok != 0;
+}
+// false when the phase did not complete within the bound
+__device__ __forceinline__ bool vbar_wait(unsigned bar, unsigned parity) {
+  if (vbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!vbar_try(bar, parity))
+    if (clock64() - t0 > kVerifySpin) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kVerifyThreads, 1) k_verify_bulk(const __nv_bfloat16* __restrict__ logits,
+                                                                  const int* __restrict__ draft, int n, int V,
+                                                                  int slice, int rb, int* __restrict__ accept_len,
+                                                                  int* __restrict__ out_tokens) {
+  extern __shared__ __align__(128) unsigned char vsm[];
+  __shared__ unsigned long long keys[2][kVerifyRowBatch][kVerifyMaxCluster];  // (max bits, first position)
+  __shared__ float wmax[kVerifyRowBatch][kVerifyThreads / 32];
+  __shared__ int wfirst[kVerifyRowBatch][kVerifyThreads / 32];
+  __shared__ int dtok[2][kVerifyRowBatch];
+  __shared__ int bads[2][kVerifyMaxCluster];
+  __shared__ __align__(8) unsigned long long bar[kVerifyRowBatch];
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / cs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lo = rank * slice, hi = min(V, lo + slice), cnt = hi > lo ? hi - lo : 0;
+  const unsigned bytes = static_cast<unsigned>(cnt) * 2u;
+  const unsigned sbase = static_cast<unsigned>(__cvta_generic_to_shared(vsm));
+  auto bar_a = [&](int r) { return static_cast<unsigned>(__cvta_generic_to_shared(&bar[r])); };
+  auto row_ptr = [&](int i) { return logits + (static_cast<size_t>(b) * (n + 1) + i) * V; };
+
+  if (tid == 0) {
+    for (int r = 0; r < rb; ++r)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a(r)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (rank == 0)
+    for (int i = tid; i <= n; i += kVerifyThreads) out_tokens[static_cast<size_t>(b) * (n + 1) + i] = -1;
+  __syncthreads();
+
+  int buf = 0, pend = 0;  // pend: slots of a batch left by a failed wait (drained before the end)
+  unsigned ph = 0u;
+#pragma unroll 1
+  for (int i0 = 0; i0 <= n; i0 += rb, buf ^= 1, ph ^= 1u) {
+    const int R = min(rb, n + 1 - i0);
+    if (tid < R && i0 + tid < n) dtok[buf][tid] = draft[static_cast<size_t>(b) * n + i0 + tid];
+    if (tid == 0) {
+      // the slots' previous contents were read before the last cluster barrier
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int r = 0; r < R; ++r) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a(r)), "r"(bytes) : "memory");
+        if (bytes)
+          asm volatile(
+              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                  sbase + static_cast<unsigned>(r * slice * 2)),
+              "l"(row_ptr(i0 + r) + lo), "r"(bytes), "r"(bar_a(r))
+              : "memory");
+      }
+    }
+    pend = R;
+    int bad = 0;
+    // pass 1: the largest value of each row slice (bf16 pairs, packed max)
+    float cmax[kVerifyRowBatch];
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) {
+      float m = -INFINITY;
+      if (r < R) {
+        if (!vbar_wait(bar_a(r), ph)) bad = 1;
+        const uint4* row = reinterpret_cast<const uint4*>(vsm + r * slice * 2);
+        __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
+#pragma unroll 4
+        for (int v = tid; v < cnt / 8; v += kVerifyThreads) {
+          const uint4 u = row[v];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+          m2 = __hmax2(__hmax2(m2, h[0]), __hmax2(h[1], __hmax2(h[2], h[3])));
+        }
+        const float2 f = __bfloat1622float2(m2);
+        m = warp_max(fmaxf(f.x, f.y));
+      }
+      if (lane == 0) wmax[r][warp] = m;
+    }
+    const int cta_bad = __syncthreads_or(bad);
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) {
+      float m = -INFINITY;
+      for (int w = 0; w < kVerifyThreads / 32; ++w) m = fmaxf(m, wmax[r][w]);
+      cmax[r] = m;
+    }
+    // pass 2: the first position of that value in the slice (equal values: lowest id)
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) {
+      int first = INT_MAX;
+      if (r < R) {
+        const uint4* row = reinterpret_cast<const uint4*>(vsm + r * slice * 2);
+        const __nv_bfloat162 t2 = __float2bfloat162_rn(cmax[r]);
+#pragma unroll 4
+        for (int v = tid; v < cnt / 8 && first == INT_MAX; v += kVerifyThreads) {
+          const uint4 u = row[v];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 3; e >= 0; --e) {  // last to first: the lowest match is kept
+            const __nv_bfloat162 q = __heq2(h[e], t2);
+            const unsigned qb = *reinterpret_cast<const unsigned*>(&q);
+            if (qb) first = lo + 8 * v + 2 * e + ((qb & 0xffffu) ? 0 : 1);
+          }
+        }
+        first = warp_min_i(first);
+      }
+      if (lane == 0) wfirst[r][warp] = first;
+    }
+    __syncthreads();
+    // thread (row r, peer q) sends this CTA's (max, first position) of row r to peer q; thread
+    // R * cs + q its flag
+    if (tid < R * cs) {
+      const int r = tid / cs, q = tid - r * cs;
+      int first = INT_MAX;
+      float cm = -INFINITY;
+      for (int w = 0; w < kVerifyThreads / 32; ++w) {
+        first = min(first, wfirst[r][w]);
+        cm = fmaxf(cm, wmax[r][w]);
+      }
+      const unsigned long long kv =
+          (static_cast<unsigned long long>(__float_as_uint(cm)) << 32) | static_cast<unsigned>(first);
+      *cl.map_shared_rank(&keys[buf][r][rank], q) = kv;
+    } else if (tid < R * cs + cs) {
+      *cl.map_shared_rank(&bads[buf][rank], tid - R * cs) = cta_bad;
+    }
+    cl.sync();
+    bool any_bad = false;
+    for (int q = 0; q < cs; ++q) any_bad = any_bad || bads[buf][q] != 0;
+    if (any_bad) {
+      if (rank == 0 && tid == 0) accept_len[b] = -1;
+      break;
+    }
+    bool go = true;
+    for (int r = 0; r < R && go; ++r) {
+      // the largest value over the slices (compared as fp32: -0 equals +0), lowest position
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      for (int q = 0; q < cs; ++q) {
+        const unsigned long long kv = keys[buf][r][q];
+        const float v = __uint_as_float(static_cast<unsigned>(kv >> 32));
+        const int f = static_cast<int>(static_cast<unsigned>(kv));
+        if (f != INT_MAX && (bi == INT_MAX || v > bv || (v == bv && f < bi))) {
+          bv = v;
+          bi = f;
+        }
+      }
+      const int i = i0 + r, t = bi == INT_MAX ? 0 : bi;
+      const bool accept = i < n && dtok[buf][r] == t;
+      if (rank == 0 && tid == 0) {
+        out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
+        if (!accept) accept_len[b] = i;
+      }
+      go = accept;
+    }
+    pend = 0;
+    if (!go) break;
+  }
+  // a batch left by a failed wait may still have copies in flight: drain them (bounded; the
+  // loop ended by break, so ph is still that batch's parity)
+  if (pend && tid == 0)
+    for (int r = 0; r < pend; ++r) vbar_wait(bar_a(r), ph);
+  cl.sync();  // no CTA leaves while its shared keys may still be written by another
+}
+
+namespace {
+int cuda_fail_v(const char* what, cudaError_t e) {
+  cudaGetLastError();
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  return MTP_ERR_CUDA;
+}
+}  // namespace
+
 int run_verify(const void* logits, const int* draft, int B, int n, int V, int* accept_len, int* out_tokens,
                cudaStream_t st) {
-  // cluster size: 16 CTAs per sequence when the grid is small, else 8 (portable)
-  int cs = B <= 8 ? 16 : 8;
-  int slice = ((V + cs * 8 - 1) / (cs * 8)) * 8;
-  if (cs == 16) {
-    cudaError_t e = cudaFuncSetAttribute(k_verify, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) {
+  // function attributes, set once per device: 16-CTA clusters (when the device takes them)
+  // and the bulk-copy form's shared-memory budget
+  static std::mutex mu;
+  static int attrs_of[64] = {0};  // per device: 0 not set yet; 2: 16-CTA clusters available; 1: not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    dev = 0;
+  }
+  int attrs;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    attrs = attrs_of[dev] - 1;
+    if (attrs < 0) {
+      cudaError_t e = cudaFuncSetAttribute(k_verify, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k_verify_bulk, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attrs = e == cudaSuccess ? 1 : 0;
       cudaGetLastError();
-      cs = 8;
-      slice = ((V + cs * 8 - 1) / (cs * 8)) * 8;
+      e = cudaFuncSetAttribute(k_verify_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, kVerifySmemMax);
+      if (e != cudaSuccess) return cuda_fail_v("k_verify_bulk shared memory attribute", e);
+      attrs_of[dev] = attrs + 1;
     }
   }
+  // cluster size: 16 CTAs per sequence when the grid is small, else 8 (portable)
+  const int cs = B <= 8 && attrs == 1 ? 16 : 8;
+  const int slice = ((V + cs * 8 - 1) / (cs * 8)) * 8;
+  // rows of one CTA slice per batch in the shared-memory budget: the bulk-copy form when at
+  // least one fits
+  const int rb = std::min(kVerifyRowBatch, kVerifySmemMax / (slice * 2));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(B * cs);
   cfg.blockDim = dim3(kVerifyThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = rb >= 1 ? static_cast<size_t>(rb) * slice * 2 : 0;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -152,8 +373,10 @@ int run_verify(const void* logits, const int* draft, int B, int n, int V, int* a
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_verify, static_cast<const __nv_bfloat16*>(logits), draft, n, V, slice,
-                                     accept_len, out_tokens);
+  cudaError_t e = rb >= 1 ? cudaLaunchKernelEx(&cfg, k_verify_bulk, static_cast<const __nv_bfloat16*>(logits), draft, n,
+                                               V, slice, rb, accept_len, out_tokens)
+                          : cudaLaunchKernelEx(&cfg, k_verify, static_cast<const __nv_bfloat16*>(logits), draft, n, V,
+                                               slice, accept_len, out_tokens);
   if (e != cudaSuccess) {
     set_error("k_verify launch (%d clusters of %d) failed: %s", B, cs, cudaGetErrorString(e));
     return MTP_ERR_CUDA;

@@ -518,7 +518,10 @@ def run_reference(args, rank: int, world: int):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{shape.name} drafter step: B={B}, ctx {wl.ctx}, draft block {n}, then greedy "
                                    f"verify of [{B},{n + 1},{shape.vocab}] bf16 target logits",
-                       "batch": B, "ctx": wl.ctx, "n_draft": n, "parallelism": "host"},
+                       "batch": B, "ctx": wl.ctx, "n_draft": n, "storage": shape.dtype,
+                       "sparse_head": args.sparse_head,
+                       "l2": "host run (the GPU arm flushes 256 MiB of L2 before every timed step)",
+                       "parallelism": "host"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                              "sample": f"{args.steps} full steps of the workload, NumPy fp64"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -84,6 +84,7 @@ struct Lay {
 
 template <int D, int HPG>
 __global__ void __launch_bounds__(kT) k_att_tc(const __grid_constant__ Params p, int l) {
+  pdl_enter();
   using LY = Lay<D, HPG>;
   constexpr int P = LY::P, QP = LY::QP, PP = LY::PP;
   constexpr int NT = (HPG + 1) / 2, KS = D / 16, MT = D / 16, half = D / 2;
@@ -333,8 +334,18 @@ int launch(const Params& p, int l, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k_att_tc<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess) {
     const int t = p.L[l].type;
-    k_att_tc<D, HPG><<<p.s.B * p.s.nkv * p.s.nsplit[t], kT, smem, st>>>(p, l);
-    e = cudaGetLastError();
+    // a programmatic dependent launch in the tensor-core path's chain (pdl_enter waits)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.s.B * p.s.nkv * p.s.nsplit[t]);
+    cfg.blockDim = dim3(kT);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k_att_tc<D, HPG>, p, l);
   }
   if (e != cudaSuccess) {
     set_error("tensor-core attention launch: %s", cudaGetErrorString(e));

@@ -61,6 +61,14 @@ __device__ inline void load_vec_stream(const float* p, float* out) {
 
 // ---------------------------------------------------------------- reductions
 
+// Programmatic dependent launch (the tensor-core path's chain of launches): let the next
+// kernel of the chain begin launching now, then wait until the kernels this one depends on
+// have completed and their writes are visible. Both return at once for a launch that did
+// not opt in, so every kernel of the library may call it first.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 __device__ inline float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

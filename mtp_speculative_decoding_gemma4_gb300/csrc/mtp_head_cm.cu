@@ -115,6 +115,7 @@ __host__ __device__ inline Geo geometry(const ShapeP& s, int eb) {
 
 template <typename WT>
 __global__ void __launch_bounds__(kThreads, 1) k_head_cm(Params p, Geo g) {
+  pdl_enter();
   extern __shared__ __align__(128) char smem_raw[];
   constexpr int V = Elem<WT>::kVec;  // elements per 16-byte slice
   const int H = p.s.H, vsc = p.s.vsc, C = p.s.C, B = p.s.B, K = p.s.topk, nsel = B * K;

@@ -50,9 +50,14 @@ __device__ inline bool grid_sync(const Params& p, unsigned int& epoch) {
 
 // ---------------------------------------------------------------- per-phase kernels
 
-#define MTP_KERNEL_PROLOGUE extern __shared__ __align__(16) char smem[];
+#define MTP_KERNEL_PROLOGUE \
+  extern __shared__ __align__(16) char smem[]; \
+  pdl_enter();
 
-template <typename WT> __global__ void __launch_bounds__(kThreads) k_rope(Params p) { phase_rope(p, blockIdx.x, gridDim.x); }
+template <typename WT> __global__ void __launch_bounds__(kThreads) k_rope(Params p) {
+  pdl_enter();
+  phase_rope(p, blockIdx.x, gridDim.x);
+}
 template <typename WT> __global__ void __launch_bounds__(kThreads) k_pre(Params p, int step, int par) {
   MTP_KERNEL_PROLOGUE phase_pre<WT>(p, step, par, blockIdx.x, gridDim.x, smem);
 }
@@ -91,6 +96,7 @@ template <typename WT> __global__ void __launch_bounds__(kThreads) k_dense(Param
   MTP_KERNEL_PROLOGUE phase_dense<WT>(p, blockIdx.x, gridDim.x, smem);
 }
 template <typename WT> __global__ void __launch_bounds__(kThreads) k_fin(Params p, int stride, int col) {
+  pdl_enter();
   phase_fin(p, stride, col, blockIdx.x, gridDim.x);
 }
 
@@ -257,6 +263,32 @@ inline int allow_smem(K kernel, int bytes) {
     }                                                                                   \
   } while (0)
 
+// The same as a programmatic dependent launch (the tensor-core path's chain): the kernel may
+// start launching while its predecessor runs and waits for it in pdl_enter().
+#define MTP_LAUNCH_PDL(kernel, grid, smem_bytes, ...)                                   \
+  do {                                                                                  \
+    if ((grid) > 0) {                                                                   \
+      int rc_ = allow_smem(kernel, smem_bytes);                                         \
+      if (rc_) return rc_;                                                              \
+      cudaLaunchConfig_t cfg_ = {};                                                     \
+      cfg_.gridDim = dim3(grid);                                                        \
+      cfg_.blockDim = dim3(kThreads);                                                   \
+      cfg_.dynamicSmemBytes = static_cast<size_t>(smem_bytes);                          \
+      cfg_.stream = st;                                                                 \
+      cudaLaunchAttribute at_[1];                                                       \
+      at_[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                   \
+      at_[0].val.programmaticStreamSerializationAllowed = 1;                            \
+      cfg_.attrs = at_;                                                                 \
+      cfg_.numAttrs = 1;                                                                \
+      cudaError_t e_ = cudaLaunchKernelEx(&cfg_, kernel, __VA_ARGS__);                  \
+      if (e_ != cudaSuccess) {                                                          \
+        cudaGetLastError();                                                             \
+        set_error("launch of %s failed: %s", #kernel, cudaGetErrorString(e_));          \
+        return MTP_ERR_CUDA;                                                            \
+      }                                                                                 \
+    }                                                                                   \
+  } while (0)
+
 // The sparse head over the selected centroids: per sequence, or cluster-major (its own
 // streamed kernel, mtp_head_cm.cu).
 #define MTP_LAUNCH_GATHER()                                                            \
@@ -336,19 +368,19 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
                   long long ld2, unsigned long long* best, int dbg_cta = -1) -> int {
     tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit, dbg_cta};
-    return tc_gemm(&w, &x, a, best != nullptr, st);
+    return tc_gemm(&w, &x, a, best != nullptr, st, true);
   };
   int rc;
   MTP_LAUNCH(k_rope<WT>, s.B, 0, p);
   int par = 0;
   for (int step = 0; step < p.n_draft; ++step) {
-    MTP_LAUNCH(k_pre<WT>, groups(2 * s.bb), z.smem_pre, ps, step, par);
+    MTP_LAUNCH_PDL(k_pre<WT>, groups(2 * s.bb), z.smem_pre, ps, step, par);
     if ((rc = gemm(plan.pre, plan.xs_pre, s.H, 2 * s.bb, p.w.x[par], s.H, nullptr, 0, nullptr,
                    step == 0 ? p.dbg_skip - 1 : -1)))
       return rc;
     for (int l = 0; l < s.nl; ++l) {
       const int t = p.L[l].type, QD = s.nh * s.d[t];
-      MTP_LAUNCH(k_q<WT>, groups(s.H), z.smem_q, ps, l, par);
+      MTP_LAUNCH_PDL(k_q<WT>, groups(s.H), z.smem_q, ps, l, par);
       if ((rc = gemm(plan.q[l], plan.xs_h, QD, s.H, p.w.qraw, static_cast<long long>(s.nh) * p.w.dmax, nullptr, 0,
                      nullptr)))
         return rc;
@@ -358,30 +390,30 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
       } else {
         MTP_LAUNCH_ATT(l);
       }
-      MTP_LAUNCH(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
-      MTP_LAUNCH(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
+      MTP_LAUNCH_PDL(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
+      MTP_LAUNCH_PDL(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
       if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;
-      MTP_LAUNCH(k_gu<WT>, groups(s.H), z.smem_gu, ps, l, par);
+      MTP_LAUNCH_PDL(k_gu<WT>, groups(s.H), z.smem_gu, ps, l, par);
       if ((rc = gemm(plan.gate[l], plan.xs_h, s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr))) return rc;
       if ((rc = gemm(plan.up[l], plan.xs_h, s.F, s.H, p.w.up, s.F, nullptr, 0, nullptr))) return rc;
       par ^= 1;
-      MTP_LAUNCH(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
+      MTP_LAUNCH_PDL(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
       if ((rc = gemm(plan.down[l], plan.xs_f, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
     }
-    MTP_LAUNCH(k_head1<WT>, groups(s.H), z.smem_head1, ps, step, par);
+    MTP_LAUNCH_PDL(k_head1<WT>, groups(s.H), z.smem_head1, ps, step, par);
     float* hout = p.out_hidden ? p.out_hidden + static_cast<size_t>(step) * s.bb : nullptr;
     if ((rc = gemm(plan.post, plan.xs_h, s.bb, s.H, hout, static_cast<long long>(p.n_draft) * s.bb, p.w.h_cur, s.bb,
                    nullptr)))
       return rc;
     if (s.ordered) {
       if ((rc = gemm(plan.cent, plan.xs_h, s.C, s.H, p.w.cl, s.C, nullptr, 0, nullptr))) return rc;
-      MTP_LAUNCH(k_topk<WT>, z.topk, z.smem_topk, p);
+      MTP_LAUNCH_PDL(k_topk<WT>, z.topk, z.smem_topk, p);
       MTP_LAUNCH_GATHER();
     } else {
       if ((rc = gemm(plan.temb, plan.xs_h, s.V, s.H, nullptr, 0, nullptr, 0, p.w.best))) return rc;
     }
   }
-  MTP_LAUNCH(k_fin<WT>, 1, 0, p, p.n_draft, p.n_draft - 1);
+  MTP_LAUNCH_PDL(k_fin<WT>, 1, 0, p, p.n_draft, p.n_draft - 1);
   return MTP_OK;
 }
 

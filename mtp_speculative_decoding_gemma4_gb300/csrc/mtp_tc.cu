@@ -107,6 +107,10 @@ template <bool DENSE, int NB>  // NB: sequences / 32 (1 or 2)
 __global__ void __launch_bounds__(kThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX, const Args a) {
   extern __shared__ __align__(1024) char sm_raw[];
+  // programmatic dependent launch: the next kernel may start launching; the producer waits
+  // for this kernel's predecessors only before its first read of the staged operand (the
+  // weights do not depend on them), and every other read or write follows from that
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const unsigned raw = sa(sm_raw);
   const unsigned base = (raw + 1023u) & ~1023u;  // the swizzle layout needs 1024-byte alignment
   const int B = NB * 32, N = 3 * B, SB = stage_bytes(B), ncols = tmem_cols(B);
@@ -143,13 +147,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kEpiWarps) {
     if (lane == 0) {
-      // ---- producer: W tile rows and all of Xs, 64 columns per stage
-      int issued = 0;
-      for (int kt = 0; kt < KT; ++kt) {
+      // ---- producer: W tile rows and all of Xs, 64 columns per stage. The first stages' W
+      // tiles are requested before the wait for the kernels that write Xs.
+      // testing: with dbg_cta this CTA issues no copy for its last stage (the MMA warp's wait
+      // on it runs out)
+      const int last = static_cast<int>(blockIdx.x) == a.dbg_cta ? KT - 1 : KT;
+      const int pre = min(last, kStages);
+      for (int kt = 0; kt < pre; ++kt) {
+        mbar_expect_tx(full0 + 8 * kt, static_cast<unsigned>(SB));
+        tma_load_2d(base + kt * SB, &mapW, (kt_lo + kt) * kKStage, tile * kM, full0 + 8 * kt);
+      }
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      for (int kt = 0; kt < pre; ++kt)
+        tma_load_2d(base + kt * SB + kM * kKStage * 2, &mapX, (kt_lo + kt) * kKStage, 0, full0 + 8 * kt);
+      int issued = pre;
+      for (int kt = pre; kt < last; ++kt) {
         const int s = kt % kStages;
-        if (kt >= kStages && !wait_bar(empty0 + 8 * s, static_cast<unsigned>((kt / kStages - 1) & 1), a.status, a.spin_limit))
+        if (!wait_bar(empty0 + 8 * s, static_cast<unsigned>((kt / kStages - 1) & 1), a.status, a.spin_limit))
           break;
-        if (kt == KT - 1 && static_cast<int>(blockIdx.x) == a.dbg_cta) break;  // testing: the MMA warp's wait runs out
         const unsigned st = base + s * SB;
         mbar_expect_tx(full0 + 8 * s, static_cast<unsigned>(SB));
         tma_load_2d(st, &mapW, (kt_lo + kt) * kKStage, tile * kM, full0 + 8 * s);
@@ -342,7 +357,8 @@ int tc_make_map(CUtensorMap* map, const void* base, long long rows, long long co
   return MTP_OK;
 }
 
-int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a, bool dense, cudaStream_t st) {
+int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a, bool dense, cudaStream_t st,
+            bool pdl) {
   if (a.B < 32 || a.B > tc::kMaxB || a.B % 32 || a.nvalid < 1 || a.nvalid > a.B || a.K < tc::kKStage ||
       a.K % tc::kKStage || a.R < 1) {
     set_error("tensor-core GEMM: unsupported R=%d K=%d B=%d", a.R, a.K, a.B);
@@ -371,13 +387,15 @@ int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a,
     cfg.blockDim = dim3(tc::kThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = aa.splits;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // pdl_enter waits
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, *mapW, *mapX, aa);
   }
   if (e != cudaSuccess) {

@@ -69,7 +69,8 @@ __host__ __device__ inline int tmem_cols(int B) {
 int tc_make_map(CUtensorMap* map, const void* base, long long rows, long long cols, long long pitch, int box_rows);
 // Y = W Xs^T as described above. `dense` selects the argmax epilogue. a.splits <= 0 picks the
 // split of K automatically (projections); the dense head never splits.
-int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a, bool dense, cudaStream_t st);
+int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a, bool dense, cudaStream_t st,
+            bool pdl = false);
 // Whether tcgen05 GEMMs can run on the current device (sm_100 family, driver entry point).
 bool tc_available();
 

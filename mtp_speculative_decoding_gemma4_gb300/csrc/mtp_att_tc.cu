@@ -84,7 +84,9 @@ struct Lay {
 
 template <int D, int HPG>
 __global__ void __launch_bounds__(kT) k_att_tc(const __grid_constant__ Params p, int l) {
-  pdl_enter();
+  // programmatic dependent launch: the first K chunk (the target's cache, which the draft
+  // block never writes) is requested before the wait for the kernels that write q
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using LY = Lay<D, HPG>;
   constexpr int P = LY::P, QP = LY::QP, PP = LY::PP;
   constexpr int NT = (HPG + 1) / 2, KS = D / 16, MT = D / 16, half = D / 2;
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kT) k_att_tc(const __grid_constant__ Params p,
     cp_async_commit();
   };
   load(0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // q_norm + RoPE at the constant position of the group's heads -> three bf16 terms per head
   {

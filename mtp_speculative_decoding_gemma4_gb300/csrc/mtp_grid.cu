@@ -1424,15 +1424,57 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
     {
       unsigned long long best = 0ull;
       const int lgv = p.lg_vsc;
-#pragma unroll 1
-      for (int sl = candr.lo + warp; sl < candr.hi; sl += kW) {
+      auto row_of = [&](int sl) -> long long {
         int ce = sel[sl >> lgv];
         ce = ce < 0 ? 0 : (ce >= p.C ? p.C - 1 : ce);
-        const long long rowi = (static_cast<long long>(ce) << lgv) + (sl & ((1 << lgv) - 1));
-        const int id = __ldg(p.ord + rowi);
-        const float v = dot_row<EPL>(p.temb_ord + rowi * H, y);
-        const unsigned long long key = argmax_key(v, id);
-        best = key > best ? key : best;
+        return (static_cast<long long>(ce) << lgv) + (sl & ((1 << lgv) - 1));
+      };
+      if constexpr (EPL % 8 == 0) {
+        // four rows per warp at a time: every row's vectors and id requested before any sum
+        constexpr int NV = EPL / 8, RW = 4;
+#pragma unroll 1
+        for (int s0 = candr.lo + warp; s0 < candr.hi; s0 += RW * kW) {
+          uint4 rv[RW][NV];
+          int ids[RW];
+#pragma unroll
+          for (int r = 0; r < RW; ++r) {
+            const int sl = s0 + r * kW;
+            if (sl < candr.hi) {
+              const long long rowi = row_of(sl);
+              ids[r] = __ldg(p.ord + rowi);
+              const uint4* rp = reinterpret_cast<const uint4*>(p.temb_ord + rowi * H + lane * EPL);
+#pragma unroll
+              for (int v = 0; v < NV; ++v) rv[r][v] = __ldg(rp + v);
+            } else {
+              ids[r] = 0;
+#pragma unroll
+              for (int v = 0; v < NV; ++v) rv[r][v] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < RW; ++r) {
+            float sum = 0.f;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+              float f[8];
+              bf8(rv[r][v], f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) sum = fmaf(f[i], y[8 * v + i], sum);
+            }
+            sum = warp_sum(sum);
+            const unsigned long long key = argmax_key(sum, ids[r]);
+            if (s0 + r * kW < candr.hi) best = key > best ? key : best;
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int sl = candr.lo + warp; sl < candr.hi; sl += kW) {
+          const long long rowi = row_of(sl);
+          const int id = __ldg(p.ord + rowi);
+          const float v = dot_row<EPL>(p.temb_ord + rowi * H, y);
+          const unsigned long long key = argmax_key(v, id);
+          best = key > best ? key : best;
+        }
       }
       if (lane == 0) wkeys[warp] = best;
       __syncthreads();

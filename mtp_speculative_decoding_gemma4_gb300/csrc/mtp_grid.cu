@@ -301,6 +301,22 @@ __device__ __forceinline__ float dot_row(const bf16* row, const float (&a)[EPL])
   return warp_sum(s);
 }
 
+// Sum of w[k] v[k] over k < n: w a bf16 row of even pitch (4-byte aligned), v fp32 in shared
+// memory (8-byte aligned); pairs of k in two accumulation chains.
+__device__ __forceinline__ float dot_col(const bf16* w, const float* v, int n) {
+  float a0 = 0.f, a1 = 0.f;
+  int k = 0;
+#pragma unroll 4
+  for (; k + 1 < n; k += 2) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(w + k));
+    const float2 u = *reinterpret_cast<const float2*>(v + k);
+    a0 = fmaf(f.x, u.x, a0);
+    a1 = fmaf(f.y, u.y, a1);
+  }
+  if (k < n) a0 = fmaf(bf(w[k]), v[k], a0);
+  return a0 + a1;
+}
+
 // ------------------------------------------------------------------ all-reduce
 
 // Sums the H-vector vs[] of every CTA of the grid; returns the shared-memory address of the
@@ -1174,13 +1190,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
   auto pre_h = [&]() {
     const bf16* pre = reinterpret_cast<const bf16*>(sm + L.pre);
 #pragma unroll 1
-    for (int i = tid; i < H; i += kT) {
-      const bf16* wh = pre + i * L.kcp;
-      float v = 0.f;
-#pragma unroll 1
-      for (int k = 0; k < nhc; ++k) v = fmaf(bf(wh[k]), hc[k], v);
-      vh[i] = v;
-    }
+    for (int i = tid; i < H; i += kT) vh[i] = dot_col(pre + i * L.kcp, hc, nhc);
   };
   int arn = 0;
   need_group(0);
@@ -1199,13 +1209,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
     {
       const bf16* pre = reinterpret_cast<const bf16*>(sm + L.pre);
 #pragma unroll 1
-      for (int i = tid; i < H; i += kT) {
-        const bf16* we = pre + (H + i) * L.kcp;
-        float v = vh[i];
-#pragma unroll 1
-        for (int k = 0; k < nhc; ++k) v = fmaf(bf(we[k]), red[k], v);
-        vs[i] = v;
-      }
+      for (int i = tid; i < H; i += kT) vs[i] = vh[i] + dot_col(pre + (H + i) * L.kcp, red, nhc);
     }
     const bool skip = p.dbg_skip == c + 1 && s == 0;
     float* xr = all_reduce(p, sm, vs, arn++, p.mb + xo[0], ep0, rank, g, skip, &ok);
@@ -1229,9 +1233,14 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
         const bf16* wq = reinterpret_cast<const bf16*>(sm + L.q[l]);
         unsigned long long* mq = p.mb + xo[ex_q(l)];
 #pragma unroll 1
-        for (int rr = warp; rr < nq; rr += kW) {
-          const float v = dot_row<EPL>(wq + rr * H, a);
-          if (lane == 0) put(mq, q_r.lo + rr, v, ep0 + ex_q(l));
+        for (int rr = warp; rr < nq; rr += 2 * kW) {  // two rows at a time: reductions overlap
+          const int r2 = rr + kW;
+          const float v1 = dot_row<EPL>(wq + rr * H, a);
+          const float v2 = r2 < nq ? dot_row<EPL>(wq + r2 * H, a) : 0.f;
+          if (lane == 0) {
+            put(mq, q_r.lo + rr, v1, ep0 + ex_q(l));
+            if (r2 < nq) put(mq, q_r.lo + r2, v2, ep0 + ex_q(l));
+          }
         }
       }
       // ---------------- ATT (attention CTAs): the partial softmax of my keys
@@ -1327,12 +1336,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
         __syncthreads();
         const bf16* wo = reinterpret_cast<const bf16*>(sm + L.o[l]);
 #pragma unroll 1
-        for (int i = tid; i < H; i += kT) {
-          float v = 0.f;
-#pragma unroll 1
-          for (int k = 0; k < nq; ++k) v = fmaf(bf(wo[i * L.nqp[l] + k]), red[k], v);
-          vs[i] = v;
-        }
+        for (int i = tid; i < H; i += kT) vs[i] = dot_col(wo + i * L.nqp[l], red, nq);
       }
       float gPA[EPL], gF[EPL];
       ldg_vec<EPL>(p.post_attn_norm[l], gPA);
@@ -1361,12 +1365,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
         __syncthreads();
         const bf16* wd = reinterpret_cast<const bf16*>(sm + L.dn[l]);
 #pragma unroll 1
-        for (int i = tid; i < H; i += kT) {
-          float v = 0.f;
-#pragma unroll 1
-          for (int k = 0; k < nf; ++k) v = fmaf(bf(wd[i * L.nfp + k]), ms[k], v);
-          vs[i] = v;
-        }
+        for (int i = tid; i < H; i += kT) vs[i] = dot_col(wd + i * L.nfp, ms, nf);
       }
       float gPF[EPL];
       ldg_vec<EPL>(p.post_ffn_norm[l], gPF);
@@ -1398,19 +1397,26 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
       const bf16* wc = reinterpret_cast<const bf16*>(sm + L.cent);
       unsigned long long* mc = p.mb + xo[ex_cent(nl)];
       const unsigned epc = ep0 + ex_cent(nl);
-#pragma unroll 1
-      for (int rr = warp; rr < ncr + nhc; rr += kW) {
+      // rows rr (centroid rows first, then post-projection rows), two per warp at a time so
+      // that their reductions overlap
+      auto row_ptr = [&](int rr) { return rr < ncr ? wc + rr * H : wp + (rr - ncr) * H; };
+      auto row_out = [&](int rr, float v) {
+        if (lane != 0) return;
         if (rr < ncr) {
-          const float v = dot_row<EPL>(wc + rr * H, y);
-          if (lane == 0) put(mc, cr.lo + rr, v, epc);
+          put(mc, cr.lo + rr, v, epc);
         } else {
           const int q = rr - ncr;
-          const float v = dot_row<EPL>(wp + q * H, y);
-          if (lane == 0) {
-            hc[q] = v;
-            if (p.out_hidden) p.out_hidden[static_cast<size_t>(s) * p.bb + hr.lo + q] = v;
-          }
+          hc[q] = v;
+          if (p.out_hidden) p.out_hidden[static_cast<size_t>(s) * p.bb + hr.lo + q] = v;
         }
+      };
+#pragma unroll 1
+      for (int rr = warp; rr < ncr + nhc; rr += 2 * kW) {
+        const int r2 = rr + kW;
+        const float v1 = dot_row<EPL>(row_ptr(rr), y);
+        const float v2 = r2 < ncr + nhc ? dot_row<EPL>(row_ptr(r2), y) : 0.f;
+        row_out(rr, v1);
+        if (r2 < ncr + nhc) row_out(r2, v2);
       }
     }
     __syncthreads();

@@ -145,6 +145,36 @@ def test_one_sequence_path_long_ragged_and_window_contexts(index, ctx, storage, 
     dr.close()
 
 
+@pytest.mark.parametrize("path", [0, STREAMED, GRID])
+def test_one_sequence_top_k_with_every_centroid_logit_tied(path):
+    """Zero centroid rows make all 2048 centroid logits equal: the top 32 must be centroids
+    0..31 (equal values, lower index first: "Centroid / ordered embeddings LM head" step 2
+    with the tie rule of the readings). Every candidate key reaches the bound, so the grid
+    kernel's tiled top-k overflows its candidate buffer and takes its general form. Tokens
+    are compared exactly (the oracle's k-th gap is 0, so the near-tie allowance would excuse
+    anything) and the selection is checked on the oracle side."""
+    from dataclasses import replace
+    from mtp_speculative_decoding_gemma4_gb300 import Drafter
+    shape, wl, w, inp = config_data(1)
+    w0 = replace(w, centroids=np.zeros_like(w.centroids))
+    s = O.Shape.of(shape)
+    ref = O.draft_block(s, O.decode_weights(w0), inp.hidden, inp.last_token, inp.k_swa, inp.k_full, inp.ctx_len,
+                        inp.pos, wl.n_draft)
+    assert (ref.selected == np.arange(shape.top_k)).all()
+    wd, tgt = weights_to_device(w0)
+    dr = Drafter(shape, wd, tgt, max_batch=1, max_ctx=wl.ctx)
+    d = inputs_to_device(inp, shape.dtype)
+    tok, hid = _run_block(dr, d, wl.n_draft, path)
+    # the selection is exact; only a token whose own top-2 logit gap is a near tie may differ
+    # (then the later steps are not compared)
+    for i in range(wl.n_draft):
+        assert np.max(np.abs(hid[0, i].astype(np.float64) - ref.hidden_out[0, i])) <= TOL["bf16"]
+        if tok[0, i] != ref.tokens[0, i]:
+            assert ref.logit_gap[0, i] < NEAR_TIE["bf16"], (i, tok[0, i], ref.tokens[0, i])
+            break
+    dr.close()
+
+
 @pytest.mark.parametrize("path", ONE_SEQ)
 def test_one_sequence_paths_reject_batches(path):
     from mtp_speculative_decoding_gemma4_gb300 import MtpError, binding

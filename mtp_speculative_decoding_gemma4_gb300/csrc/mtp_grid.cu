@@ -57,6 +57,21 @@ __device__ __forceinline__ float ldg_early(const float* p) {
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
+__device__ __forceinline__ int ldg_early_i32(const int* p) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ double ldg_early_f64(const double* p) {
+  double v;
+  asm volatile("ld.global.nc.f64 %0, [%1];" : "=d"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ unsigned short ldg_early_u16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.b16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ void st_rlx64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -73,6 +88,8 @@ __device__ __forceinline__ unsigned ld_rlx32(const unsigned* p) {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ int cluster_rank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -1120,7 +1137,19 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
     kcur = t;
   };
 
-  // ---- launch start: barriers, bulk copies of this CTA's weight image and first keys
+  // ---- launch start. The inputs of the prologue are requested first, all at once (each one
+  // is a memory round trip that would otherwise follow the previous one)
+  const int h0 = p.d[0] / 2, h1 = p.d[1] / 2;
+  const int pos_in = ldg_early_i32(p.pos);
+  const int tok_in = ldg_early_i32(p.tok_in);
+  double fq0 = 0.0, fq1 = 0.0;
+  {
+    const int hm = h0 > h1 ? h0 : h1;
+    if (tid < h0 + h1) fq0 = ldg_early_f64(p.inv_freq + (tid < h0 ? tid : hm + tid - h0));
+    if (tid + kT < h0 + h1) fq1 = ldg_early_f64(p.inv_freq + (tid + kT < h0 ? tid + kT : hm + tid + kT - h0));
+  }
+  const unsigned short hv = tid < nhc ? ldg_early_u16(p.hidden_in + hr.lo + tid) : static_cast<unsigned short>(0);
+  // barriers, bulk copies of this CTA's weight image and first keys
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < nl + 7; ++i) mbar_init(sa(&bars[i]), 1);
@@ -1147,19 +1176,22 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
     k_issue(p.ltype[0]);
   }
   __syncthreads();
-  cluster_sync_all();  // every peer's barriers are initialised before any st.async
+  // every peer's barriers must be initialised before any st.async: arrive now, wait just
+  // before the first exchange
+  cluster_arrive();
 
   // RoPE (cos, sin) at the block's constant position: angle pos * inv_freq in fp64, reduced
   // to [-pi, pi] in fp64, then sin / cos of the reduced angle in fp32 (fast forms: absolute
-  // error below 1e-6 on [-pi, pi])
+  // error below 1e-6 on [-pi, pi]); pairs tid and tid + kT (the table has at most 2 kT)
   {
-    const double pos = static_cast<double>(p.pos[0]);
-    const int h0 = p.d[0] / 2, h1 = p.d[1] / 2, hm = h0 > h1 ? h0 : h1;
+    const double pos = static_cast<double>(pos_in);
     const double two_pi = 6.283185307179586, inv_two_pi = 0.15915494309189535;
-#pragma unroll 1
-    for (int i = tid; i < h0 + h1; i += kT) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = tid + k * kT;
+      if (i >= h0 + h1) continue;
       const int t = i < h0 ? 0 : 1, ii = t ? i - h0 : i;
-      const double ang = pos * p.inv_freq[t * hm + ii];
+      const double ang = pos * (k ? fq1 : fq0);
       const double r = fma(-rint(ang * inv_two_pi), two_pi, ang);
       const float rf = static_cast<float>(r);
       // the four-head form (head dim 256): pair j at (j % 8) * 16 + j / 8, so that lanes
@@ -1169,13 +1201,15 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
       cs[(t ? h0 : 0) + at] = make_float2(__cosf(rf), __sinf(rf));
     }
   }
-#pragma unroll 1
-  for (int r = tid; r < nhc; r += kT) hc[r] = bf(p.hidden_in[hr.lo + r]);
-  int tok = p.tok_in[0];
+  if (tid < nhc) hc[tid] = bf(__ushort_as_bfloat16(hv));
+  int tok = tok_in;
   if (tok < 0 || tok >= p.V) {
     if (c == 0 && tid == 0) atomicCAS(p.status, 0, static_cast<int>(MTP_ERR_INVALID_ARG));
     tok = 0;
   }
+  // step 0's embedding row (this CTA's columns) into L2 while the weights arrive
+  if (tid < 2 && nhc > 0)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.tgt + static_cast<size_t>(tok) * p.bb + hr.lo + tid * (nhc - 1)));
   __syncthreads();
 
   bool ok = true;
@@ -1195,6 +1229,7 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
   int arn = 0;
   need_group(0);
   if (ok) pre_h();
+  cluster_wait();
 
 #pragma unroll 1
   for (int s = 0; s < p.n_draft && ok; ++s) {
@@ -1683,6 +1718,7 @@ int gr_plan(gr::Params& p, int optin) {
   }
   p.lg_vsc = lg2(p.vsc);
   if (p.lg_vsc < 0) return 0;
+  if (p.d[0] / 2 + p.d[1] / 2 > 2 * gr::kT) return 0;  // the prologue forms two RoPE pairs per thread
   // top-k tiling: C = 256 * per with per <= 8, and k groups of a power-of-two <= 32 threads
   p.tk_lg_per = p.tk_lg_tpg = -1;
   if (p.C % gr::kT == 0 && p.C % p.topk == 0) {

@@ -314,8 +314,8 @@ MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_
  * projection (and the dense tied head) as a tcgen05 tensor-core GEMM (bf16, max_batch <= 64;
  * mtp_init_weights keeps the tensor maps and a staging buffer of 3 * roundup(max_batch, 32) *
  * max input width bf16), 6 = streamed-tile cluster kernel for one sequence (one 16-CTA
- * cluster; every projection on tensor cores from weight tiles that mtp_init_weights packs
- * once into one stream per CTA, about the size of all projection weights; vectors exchanged
+ * cluster; every projection on tensor cores from weight tiles packed once into one stream
+ * per CTA (see below), about the size of all projection weights; vectors exchanged
  * register-to-peer in distributed shared memory; bf16 centroid-head shapes within its
  * limits, one KV head, V = K, 16-byte aligned hidden and K rows), 7 = grid kernel for one
  * sequence (every co-resident thread-block cluster of the GPU; each projection split over
@@ -329,8 +329,13 @@ MTP_API int mtp_set_debug(mtp_handle *h, int32_t skip_arrival_cta, int64_t spin_
  * exist and are rejected. Automatic picks 7 for B = 1 when available, else 6; 5 for B >= 2
  * when available; else 2 when co-resident, else 1. Results agree within the precision
  * contract.
- * Errors: INVALID_ARG (NULL handle, path outside {0, 1, 2, 5, 6, 7}); a forced path the call
- * cannot use makes mtp_draft_block return UNSUPPORTED_SHAPE. */
+ * The streamed cluster path's weight streams are built (device memory about the size of the
+ * projection weights, packed once; the call synchronises) when path 6 is first selected, or
+ * by mtp_init_weights when the grid path cannot serve the handle and path 6 is the automatic
+ * one-sequence path.
+ * Errors: INVALID_ARG (NULL handle, path outside {0, 1, 2, 5, 6, 7}), CUDA (building the
+ * path-6 streams); a forced path the call cannot use makes mtp_draft_block return
+ * UNSUPPORTED_SHAPE. */
 MTP_API int mtp_set_path(mtp_handle *h, int32_t path);
 
 /* Free the workspace and the handle (synchronises). NULL is ignored. */

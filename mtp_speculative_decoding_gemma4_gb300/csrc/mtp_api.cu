@@ -758,17 +758,19 @@ int mtp_init_weights(const mtp_config* config, const mtp_weights* weights, const
     }
   }
   if (!h->temb_ord) h->c2_ok = 0;
-  if (h->c2_ok) {
+  rc = build_gr(h);
+  if (rc) {
+    release_handle(h);
+    return rc;
+  }
+  // the streamed cluster path's weight streams: now when it is the automatic one-sequence
+  // path (no grid plan), else when mtp_set_path first selects it
+  if (h->c2_ok && !h->gr_ok) {
     rc = build_c2_stream(h);
     if (rc) {
       release_handle(h);
       return rc;
     }
-  }
-  rc = build_gr(h);
-  if (rc) {
-    release_handle(h);
-    return rc;
   }
   // the graph cache's stream and events (graphs are skipped when they cannot be created)
   if (cudaStreamCreateWithFlags(&h->gc.cs, cudaStreamNonBlocking) != cudaSuccess ||
@@ -878,7 +880,7 @@ int mtp_draft_block(mtp_handle* h, const void* hidden, const int32_t* last_token
     return mtp::run_gr(gp, st);
   }
   if (path == 6 || (path == 0 && B == 1 && h->c2_ok)) {
-    if (!h->c2_ok || B != 1) {
+    if (!h->c2_ok || !h->c2_stream || B != 1) {
       set_error("the streamed cluster path runs one sequence of a supported shape (B=%d, available=%d)", B, h->c2_ok);
       return MTP_ERR_UNSUPPORTED_SHAPE;
     }
@@ -1086,6 +1088,11 @@ int mtp_set_path(mtp_handle* h, int32_t path) {
   if (!h || path < 0 || path > 7 || path == 3 || path == 4) {
     set_error("need a handle and path in {0, 1, 2, 5, 6, 7}");
     return MTP_ERR_INVALID_ARG;
+  }
+  if (path == 6 && h->c2_ok && !h->c2_stream) {
+    cudaSetDevice(h->device);
+    const int rc = build_c2_stream(h);  // allocates and packs once; synchronises
+    if (rc) return rc;
   }
   h->path = path;
   return MTP_OK;

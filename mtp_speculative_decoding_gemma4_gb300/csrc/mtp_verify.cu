@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify_bulk(const __nv_bf
   __shared__ int wfirst[kVerifyRowBatch][kVerifyThreads / 32];
   __shared__ int dtok[2][kVerifyRowBatch];
   __shared__ int bads[2][kVerifyMaxCluster];
+  __shared__ float cmx[kVerifyRowBatch];
+  __shared__ int go_s;
   __shared__ __align__(8) unsigned long long bar[kVerifyRowBatch];
   cg::cluster_group cl = cg::this_cluster();
   const int cs = static_cast<int>(cl.num_blocks());
@@ -238,12 +240,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify_bulk(const __nv_bf
       if (lane == 0) wmax[r][warp] = m;
     }
     const int cta_bad = __syncthreads_or(bad);
-#pragma unroll
-    for (int r = 0; r < kVerifyRowBatch; ++r) {
+    if (tid < R) {  // one thread per row: the CTA's maximum
       float m = -INFINITY;
-      for (int w = 0; w < kVerifyThreads / 32; ++w) m = fmaxf(m, wmax[r][w]);
-      cmax[r] = m;
+      for (int w = 0; w < kVerifyThreads / 32; ++w) m = fmaxf(m, wmax[tid][w]);
+      cmx[tid] = m;
     }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kVerifyRowBatch; ++r) cmax[r] = r < R ? cmx[r] : -INFINITY;
     // pass 2: the first position of that value in the slice (equal values: lowest id)
 #pragma unroll
     for (int r = 0; r < kVerifyRowBatch; ++r) {
@@ -284,36 +288,44 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) k_verify_bulk(const __nv_bf
       *cl.map_shared_rank(&bads[buf][rank], tid - R * cs) = cta_bad;
     }
     cl.sync();
-    bool any_bad = false;
-    for (int q = 0; q < cs; ++q) any_bad = any_bad || bads[buf][q] != 0;
-    if (any_bad) {
-      if (rank == 0 && tid == 0) accept_len[b] = -1;
-      break;
-    }
-    bool go = true;
-    for (int r = 0; r < R && go; ++r) {
-      // the largest value over the slices (compared as fp32: -0 equals +0), lowest position
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int q = 0; q < cs; ++q) {
-        const unsigned long long kv = keys[buf][r][q];
-        const float v = __uint_as_float(static_cast<unsigned>(kv >> 32));
-        const int f = static_cast<int>(static_cast<unsigned>(kv));
-        if (f != INT_MAX && (bi == INT_MAX || v > bv || (v == bv && f < bi))) {
-          bv = v;
-          bi = f;
+    // the decisions, taken by warp 0 of every CTA (all take the same), shared with the CTA
+    if (warp == 0) {
+      const bool any_bad = __any_sync(0xffffffffu, lane < cs && bads[buf][lane] != 0);
+      int go = any_bad ? -1 : 1;
+      for (int r = 0; r < R && go == 1; ++r) {
+        // the largest value over the slices (compared as fp32: -0 equals +0), lowest position
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        if (lane < cs) {
+          const unsigned long long kv = keys[buf][r][lane];
+          bv = __uint_as_float(static_cast<unsigned>(kv >> 32));
+          bi = static_cast<int>(static_cast<unsigned>(kv));
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int f2 = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (f2 != INT_MAX && (bi == INT_MAX || v2 > bv || (v2 == bv && f2 < bi))) {
+            bv = v2;
+            bi = f2;
+          }
+        }
+        const int i = i0 + r, t = bi == INT_MAX ? 0 : bi;
+        const bool accept = i < n && dtok[buf][r] == t;
+        if (rank == 0 && lane == 0) {
+          out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
+          if (!accept) accept_len[b] = i;
+        }
+        go = accept ? 1 : 0;
       }
-      const int i = i0 + r, t = bi == INT_MAX ? 0 : bi;
-      const bool accept = i < n && dtok[buf][r] == t;
-      if (rank == 0 && tid == 0) {
-        out_tokens[static_cast<size_t>(b) * (n + 1) + i] = t;
-        if (!accept) accept_len[b] = i;
-      }
-      go = accept;
+      if (any_bad && rank == 0 && lane == 0) accept_len[b] = -1;
+      if (lane == 0) go_s = go;
     }
+    __syncthreads();
+    const int go = go_s;
+    if (go < 0) break;  // a wait gave up: leave with the batch's copies drained below
     pend = 0;
-    if (!go) break;
+    if (go == 0) break;
   }
   // a batch left by a failed wait may still have copies in flight: drain them (bounded; the
   // loop ended by break, so ph is still that batch's parity)

@@ -340,29 +340,42 @@ def run_mtp(args, rank: int, world: int, dist):
 
     # end to end through the public API with host buffers: per step, H2D of the step's
     # inputs from pinned memory, the draft block and verify, D2H of the result, host wait
-    h_hidden = d["hidden"].cpu().pin_memory()
-    h_tok = d["last_token"].cpu().pin_memory()
-    h_pos = d["pos"].cpu().pin_memory()
-    h_ctx = d["ctx_len"].cpu().pin_memory()
-    r_tok = torch.empty((B, n + 1), dtype=torch.int32).pin_memory()
-    r_acc = torch.empty(B, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_tok, h_pos, h_ctx))
-    d2h = r_tok.numel() * 4 + r_acc.numel() * 4
+    # The step's inputs sit back to back (16-byte aligned) in one pinned host buffer and one
+    # device buffer, so each step takes one H2D copy; the draft block reads views of the device
+    # buffer. The results (verified tokens, accept lengths) share one device buffer, read back
+    # by one D2H copy.
+    ins = [d["hidden"], d["last_token"], d["pos"], d["ctx_len"]]
+    offs, total = [], 0
+    for t in ins:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 15) // 16 * 16
+    dev_in = torch.empty(total, dtype=torch.uint8, device="cuda")
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    views = []
+    for t, o in zip(ins, offs):
+        nb = t.numel() * t.element_size()
+        v = dev_in[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        host_in[o:o + nb].copy_(t.cpu().contiguous().view(torch.uint8).reshape(-1))
+        views.append(v)
+    d["hidden"], d["last_token"], d["pos"], d["ctx_len"] = views
+    res = torch.empty(B * (n + 1) + B, dtype=torch.int32, device="cuda")
+    out_v, acc = res[:B * (n + 1)].view(B, n + 1), res[B * (n + 1):]
+    host_res = torch.empty_like(res, device="cpu").pin_memory()
+    h2d = host_in.numel()
+    d2h = host_res.numel() * 4
     e2e_s = []
     for i in range(K):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        d["hidden"].copy_(h_hidden, non_blocking=True)
-        d["last_token"].copy_(h_tok, non_blocking=True)
-        d["pos"].copy_(h_pos, non_blocking=True)
-        d["ctx_len"].copy_(h_ctx, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         draft(); verify()
-        r_tok.copy_(out_v, non_blocking=True)
-        r_acc.copy_(acc, non_blocking=True)
+        host_res.copy_(res, non_blocking=True)
         stream.synchronize()
         e2e_s.append(time.perf_counter() - t0)
     e2e_step = sum(e2e_s) / K
+    assert torch.equal(host_res[:B * (n + 1)].view(B, n + 1), out_v.cpu()), "e2e result read back"
 
     ms_per_step, e2e_step, draft_ms_mean, warm_ms = max_over_ranks([ms_per_step, e2e_step, draft_ms_mean, warm_ms],
                                                                     dist)

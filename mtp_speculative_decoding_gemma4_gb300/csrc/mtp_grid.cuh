@@ -90,17 +90,22 @@ struct Layout {
                         // (type t at kbuf + koff[t]) or one type at a time (koff 0)
   int koff[2];
   int ubuf, u_words;    // gather scratch (fp32)
-  int qs;               // normed, rotated, scaled q [nh * dmax]; in the head: top-k candidates
+  int qs;               // general attention: normed, rotated, scaled q [nh * dmax]; combine:
+                        // per-head source weights; head: top-k candidates
   int cand_cap;         // top-k candidates the qs region holds
-  int sc, ksl;          // scores / probabilities [nh][ksl] (ksl: largest key share)
+  int sc, ksl;          // scores / probabilities: [nh][ksl] (general attention) or [key][nh]
+                        // (four-head form); ksl: largest key share
   int hc;               // h' share [kc] (fp32, carried to the next step)
   int vs;               // partial H-vector of an AR [H] (fp32)
   int xs;               // result of the last AR [H]
   int ms;               // gelu(gate) * up of my rows [nf]
-  int cs;               // RoPE (cos, sin) [d_s / 2 + d_f / 2] float2
+  int cs;               // RoPE (cos, sin) [d_s / 2 + d_f / 2] float2 (lane-major for the
+                        // four-head form's head dim)
   int rs, ag;           // AR receive buffers [2][H] each
   int vh;               // PRE partial over the h columns [H] (computed before the token is known)
-  int red;              // 64 floats (combine: [0, nq) o values, [48, 64) head denominators)
+  int red;              // 64 floats: attention ([h] q_norm factor, [16 + h] max, [32 + h]
+                        // exp-sum), combine ([0, nq) o values, [48, 64) head denominators),
+                        // top-k and prefix-sum warp totals
   int keys;             // [kW] u64 warp keys
   int gmax;             // top-k: [kMaxTopK] u64 group maxima, then ranks ([2][128] or [cand_cap] int)
   int sel;              // [kMaxTopK] selected centroids

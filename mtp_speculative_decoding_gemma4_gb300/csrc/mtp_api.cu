@@ -471,6 +471,7 @@ int build_gr(mtp_handle* h) {
   p->img = static_cast<const unsigned char*>(h->gr_img);
   p->img_bytes = p->L.img_bytes;
   p->mb = h->gr_mb;
+  p->mb_words = h->gr_mb_words;
   h->gr_epoch = 64u;
   h->gr_ok = 1;
   return MTP_OK;

@@ -1149,6 +1149,15 @@ __global__ void __launch_bounds__(kT, 1) k_block_gr(const __grid_constant__ Para
     if (tid + kT < h0 + h1) fq1 = ldg_early_f64(p.inv_freq + (tid + kT < h0 ? tid + kT : hm + tid + kT - h0));
   }
   const unsigned short hv = tid < nhc ? ldg_early_u16(p.hidden_in + hr.lo + tid) : static_cast<unsigned short>(0);
+  // this CTA's share of the mailbox lines into L2: in a cold L2 the first poll of every word
+  // of step 0's exchanges would otherwise wait on DRAM
+  {
+    const long long lines = (p.mb_words * 8 + 127) / 128;
+    const long long l0 = lines * c / p.N, l1 = lines * (c + 1) / p.N;
+    const char* mbc = reinterpret_cast<const char*>(p.mb);
+#pragma unroll 1
+    for (long long ln = l0 + tid; ln < l1; ln += kT) asm volatile("prefetch.global.L2 [%0];" ::"l"(mbc + ln * 128));
+  }
   // barriers, bulk copies of this CTA's weight image and first keys
   if (tid == 0) {
 #pragma unroll 1

@@ -151,6 +151,7 @@ struct Params {
   int n_draft;
   // exchanges
   unsigned long long* mb;
+  long long mb_words;           // mailbox words of the launch (both step parities)
   long long ex_off[2][kMaxEx];  // word offset of each exchange's mailbox region, by step parity
   unsigned epoch_base;
   int* status;

@@ -53,6 +53,7 @@ struct mtp_handle {
   // the staging buffer of the input terms
   mtp::TcPlan* tc;
   void* tc_mem;
+  void* tc_wmem;  // the stacked weight copies of the tensor-core path
   // multi-launch paths: the draft block of the last argument set as an instantiated CUDA
   // graph, replayed on an internal stream ordered after / before the caller's stream by
   // events; a call with different arguments captures again
@@ -208,6 +209,7 @@ int build_tc(mtp_handle* h) {
   const mtp_config& c = h->cfg;
   h->tc = nullptr;
   h->tc_mem = nullptr;
+  h->tc_wmem = nullptr;
   if (c.dtype != MTP_DTYPE_BF16 || c.max_batch < 2 || c.max_batch > mtp::tc::kMaxB || !mtp::tc_available()) return MTP_OK;
   const int bb = c.backbone, H = c.hidden, F = c.ffn;
   int qd[2] = {0, 0};
@@ -257,9 +259,36 @@ int build_tc(mtp_handle* h) {
   xmap(&plan->xs_f, F);
   xmap(&plan->xs_o[0], qd[0]);
   xmap(&plan->xs_o[1], qd[1]);
+  // stacked copies (made once, like the other per-handle weight copies): [gate ; up] per layer
+  // and [post_proj ; centroids], each row block a whole number of 128-row tiles
+  const size_t row = static_cast<size_t>(H) * 2;
+  const int C = c.use_ordered_embeddings ? c.n_centroids : 0;
+  plan->gu_ok = F % mtp::tc::kM == 0;
+  plan->postc_ok = C > 0 && bb % mtp::tc::kM == 0;
+  const size_t gu_bytes = plan->gu_ok ? 2 * static_cast<size_t>(F) * row : 0;
+  const size_t wbytes = gu_bytes * c.n_layers + (plan->postc_ok ? static_cast<size_t>(bb + C) * row : 0);
+  if (!rc && wbytes) {
+    cudaError_t ew = cudaMalloc(&h->tc_wmem, wbytes);
+    char* wb = static_cast<char*>(h->tc_wmem);
+    for (int l = 0; ew == cudaSuccess && plan->gu_ok && l < c.n_layers; ++l) {
+      char* d = wb + l * gu_bytes;
+      ew = cudaMemcpy(d, h->w.layer[l].gate, F * row, cudaMemcpyDeviceToDevice);
+      if (ew == cudaSuccess) ew = cudaMemcpy(d + F * row, h->w.layer[l].up, F * row, cudaMemcpyDeviceToDevice);
+      wmap(&plan->gu[l], d, 2 * F, H);
+    }
+    if (ew == cudaSuccess && plan->postc_ok) {
+      char* d = wb + gu_bytes * c.n_layers;
+      ew = cudaMemcpy(d, h->w.post_proj, bb * row, cudaMemcpyDeviceToDevice);
+      if (ew == cudaSuccess) ew = cudaMemcpy(d + bb * row, h->w.centroids, C * row, cudaMemcpyDeviceToDevice);
+      wmap(&plan->postc, d, bb + C, H);
+    }
+    if (ew != cudaSuccess && !rc) rc = cuda_fail("copying the stacked tensor-core weights", ew);
+  }
   if (rc) {
     cudaFree(h->tc_mem);
     h->tc_mem = nullptr;
+    if (h->tc_wmem) cudaFree(h->tc_wmem);
+    h->tc_wmem = nullptr;
     free(mem);
     return rc;
   }
@@ -625,6 +654,7 @@ void release_handle(mtp_handle* h) {
   if (h->gr_inv) cudaFree(h->gr_inv);
   if (h->gr) free(h->gr);
   if (h->tc_mem) cudaFree(h->tc_mem);
+  if (h->tc_wmem) cudaFree(h->tc_wmem);
   if (h->tc) free(h->tc);
   free(h);
 }

@@ -366,8 +366,9 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   ps.tc_bp = plan.bp;
   auto groups = [&](int) { return s.B; };  // staging runs one sequence per CTA
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
-                  long long ld2, unsigned long long* best, int dbg_cta = -1) -> int {
-    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit, dbg_cta};
+                  long long ld2, unsigned long long* best, int dbg_cta = -1, int R1 = 0, float* out_hi = nullptr,
+                  long long ld_hi = 0) -> int {
+    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit, dbg_cta, R1, out_hi, ld_hi};
     return tc_gemm(&w, &x, a, best != nullptr, st, true);
   };
   int rc;
@@ -394,19 +395,28 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
       MTP_LAUNCH_PDL(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
       if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;
       MTP_LAUNCH_PDL(k_gu<WT>, groups(s.H), z.smem_gu, ps, l, par);
-      if ((rc = gemm(plan.gate[l], plan.xs_h, s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr))) return rc;
-      if ((rc = gemm(plan.up[l], plan.xs_h, s.F, s.H, p.w.up, s.F, nullptr, 0, nullptr))) return rc;
+      if (plan.gu_ok) {  // gate and up as one launch over [gate ; up]
+        if ((rc = gemm(plan.gu[l], plan.xs_h, 2 * s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr, -1, s.F, p.w.up,
+                       s.F)))
+          return rc;
+      } else {
+        if ((rc = gemm(plan.gate[l], plan.xs_h, s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr))) return rc;
+        if ((rc = gemm(plan.up[l], plan.xs_h, s.F, s.H, p.w.up, s.F, nullptr, 0, nullptr))) return rc;
+      }
       par ^= 1;
       MTP_LAUNCH_PDL(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
       if ((rc = gemm(plan.down[l], plan.xs_f, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
     }
     MTP_LAUNCH_PDL(k_head1<WT>, groups(s.H), z.smem_head1, ps, step, par);
     float* hout = p.out_hidden ? p.out_hidden + static_cast<size_t>(step) * s.bb : nullptr;
-    if ((rc = gemm(plan.post, plan.xs_h, s.bb, s.H, hout, static_cast<long long>(p.n_draft) * s.bb, p.w.h_cur, s.bb,
-                   nullptr)))
+    const long long ldh = static_cast<long long>(p.n_draft) * s.bb;
+    const bool postc = s.ordered && plan.postc_ok;  // post_projection and centroids as one launch
+    if ((rc = postc ? gemm(plan.postc, plan.xs_h, s.bb + s.C, s.H, hout, ldh, p.w.h_cur, s.bb, nullptr, -1, s.bb,
+                           p.w.cl, s.C)
+                    : gemm(plan.post, plan.xs_h, s.bb, s.H, hout, ldh, p.w.h_cur, s.bb, nullptr)))
       return rc;
     if (s.ordered) {
-      if ((rc = gemm(plan.cent, plan.xs_h, s.C, s.H, p.w.cl, s.C, nullptr, 0, nullptr))) return rc;
+      if (!postc && (rc = gemm(plan.cent, plan.xs_h, s.C, s.H, p.w.cl, s.C, nullptr, 0, nullptr))) return rc;
       MTP_LAUNCH_PDL(k_topk<WT>, z.topk, z.smem_topk, p);
       MTP_LAUNCH_GATHER();
     } else {

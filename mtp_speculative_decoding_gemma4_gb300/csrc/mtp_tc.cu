@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const unsigned gdone0 = empty0 + 8 * kStages, gfree0 = gdone0 + 16;  // per accumulator region
   const unsigned tslot = gfree0 + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, tile = static_cast<int>(blockIdx.x) / S;
+  const bool hi = a.R1 > 0 && tile * kM >= a.R1;  // this tile's rows belong to the second matrix
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -245,8 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (b0 + j < a.nvalid) {
-            if (a.out) a.out[static_cast<size_t>(b0 + j) * a.ldo + r] = acc[q][j];
-            if (a.out2) a.out2[static_cast<size_t>(b0 + j) * a.ld2 + r] = acc[q][j];
+            if (hi) {
+              a.out_hi[static_cast<size_t>(b0 + j) * a.ld_hi + (r - a.R1)] = acc[q][j];
+            } else {
+              if (a.out) a.out[static_cast<size_t>(b0 + j) * a.ldo + r] = acc[q][j];
+              if (a.out2) a.out2[static_cast<size_t>(b0 + j) * a.ld2 + r] = acc[q][j];
+            }
           }
         }
       }
@@ -292,8 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int r = tile * kM + rr;
         if (r < a.R) {
-          if (a.out) a.out[static_cast<size_t>(b) * a.ldo + r] = v;
-          if (a.out2) a.out2[static_cast<size_t>(b) * a.ld2 + r] = v;
+          if (hi) {
+            a.out_hi[static_cast<size_t>(b) * a.ld_hi + (r - a.R1)] = v;
+          } else {
+            if (a.out) a.out[static_cast<size_t>(b) * a.ldo + r] = v;
+            if (a.out2) a.out2[static_cast<size_t>(b) * a.ld2 + r] = v;
+          }
         }
       }
     }
@@ -362,6 +371,10 @@ int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a,
   if (a.B < 32 || a.B > tc::kMaxB || a.B % 32 || a.nvalid < 1 || a.nvalid > a.B || a.K < tc::kKStage ||
       a.K % tc::kKStage || a.R < 1) {
     set_error("tensor-core GEMM: unsupported R=%d K=%d B=%d", a.R, a.K, a.B);
+    return MTP_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (a.R1 != 0 && (dense || a.R1 < 0 || a.R1 % tc::kM || a.R1 >= a.R || !a.out_hi)) {
+    set_error("tensor-core GEMM: unsupported stacked split R1=%d of R=%d", a.R1, a.R);
     return MTP_ERR_UNSUPPORTED_SHAPE;
   }
   const int smem = tc::smem_bytes(a.B);

@@ -15,7 +15,9 @@
 //     the finished group back (tcgen05.ld, warp w owns rows 32w..32w+31), add its three
 //     term columns per sequence and sum the groups in fp32 registers (round to nearest);
 //   * at the end the warps either store Y or, for the dense tied head, keep the largest
-//     (logit, row) key of every sequence (atomicMax).
+//     (logit, row) key of every sequence (atomicMax). Two projections of the same input
+//     (gate and up; post_projection and the centroids) run as one launch over their stacked
+//     rows, each tile storing into the output of the matrix its rows belong to.
 // Split K: with splits S > 1 (projections only) the S CTAs of a row tile form a thread-block
 // cluster and take consecutive S-th parts of K; each writes its fp32 partial sums into its
 // own (then idle) stage memory, and after a cluster barrier CTA s adds the S partials of rows
@@ -50,6 +52,11 @@ struct Args {
   int* status;
   long long spin_limit;
   int dbg_cta;  // testing: this CTA's producer issues no copy for its last k stage (-1: none)
+  // two stacked matrices in one launch: rows r >= R1 (R1 > 0, a multiple of kM) are stored as
+  // Y[b * ld_hi + (r - R1)] into out_hi instead of out / out2 (0: one matrix)
+  int R1;
+  float* out_hi;
+  long long ld_hi;
 };
 
 __host__ __device__ inline int stage_bytes(int B) { return kM * kKStage * 2 + 3 * B * kKStage * 2; }

@@ -391,7 +391,12 @@ def run_mtp(args, rank: int, world: int, dist):
     if args.path in (2, 6, 7):
         launches_per_step = 2
     elif args.path == 5:  # per step: staging + tcgen05 GEMM per projection, attention, combine, head
-        launches_per_step = 1 + n * (2 + 11 * shape.n_layers + 2 + head) + 1 + 1
+        # per block: Q staging + GEMM, attention, combine (stages O's operand), O GEMM, FFN
+        # staging, and either [gate ; up] with the gated-GELU epilogue + down GEMM or gate, up,
+        # down staging, down; post_projection takes the centroid GEMM along when both tile
+        per_block = 8 if shape.ffn % 64 == 0 else 10
+        stacked_head = shape.use_ordered_embeddings and shape.backbone % 128 == 0
+        launches_per_step = 1 + n * (2 + per_block * shape.n_layers + 2 + head - stacked_head) + 1 + 1
     else:
         launches_per_step = 1 + n * (2 + 6 * shape.n_layers + 2) + 1 + 1
     kernel_name = {1: "phase kernels", 2: "k_block (persistent draft block, grid barriers)",

@@ -259,25 +259,36 @@ int build_tc(mtp_handle* h) {
   xmap(&plan->xs_f, F);
   xmap(&plan->xs_o[0], qd[0]);
   xmap(&plan->xs_o[1], qd[1]);
-  // stacked copies (made once, like the other per-handle weight copies): [gate ; up] per layer
-  // and [post_proj ; centroids], each row block a whole number of 128-row tiles
+  // stacked copies (made once, like the other per-handle weight copies): per layer [gate ; up]
+  // interleaved in 64-row blocks for the gated-GELU epilogue, with its own staging buffer for
+  // the down projection's operand (the gate / up GEMM still reads the shared one); and
+  // [post_proj ; centroids], whose first block is a whole number of 128-row tiles
   const size_t row = static_cast<size_t>(H) * 2;
   const int C = c.use_ordered_embeddings ? c.n_centroids : 0;
-  plan->gu_ok = F % mtp::tc::kM == 0;
+  plan->gu_ok = F % 64 == 0;
   plan->postc_ok = C > 0 && bb % mtp::tc::kM == 0;
   const size_t gu_bytes = plan->gu_ok ? 2 * static_cast<size_t>(F) * row : 0;
-  const size_t wbytes = gu_bytes * c.n_layers + (plan->postc_ok ? static_cast<size_t>(bb + C) * row : 0);
+  const size_t xsf_bytes = plan->gu_ok ? static_cast<size_t>(3) * plan->bp * F * 2 : 0;
+  const size_t pc_bytes = plan->postc_ok ? static_cast<size_t>(bb + C) * row : 0;
+  const size_t wbytes = xsf_bytes + gu_bytes * c.n_layers + pc_bytes;
   if (!rc && wbytes) {
     cudaError_t ew = cudaMalloc(&h->tc_wmem, wbytes);
     char* wb = static_cast<char*>(h->tc_wmem);
+    if (ew == cudaSuccess && plan->gu_ok) {
+      plan->xs_glu = reinterpret_cast<__nv_bfloat16*>(wb);
+      ew = cudaMemset(wb, 0, xsf_bytes);
+      if (ew == cudaSuccess && !rc) rc = mtp::tc_make_map(&plan->xs_f2, wb, 3 * plan->bp, F, F, 3 * plan->bp);
+    }
     for (int l = 0; ew == cudaSuccess && plan->gu_ok && l < c.n_layers; ++l) {
-      char* d = wb + l * gu_bytes;
-      ew = cudaMemcpy(d, h->w.layer[l].gate, F * row, cudaMemcpyDeviceToDevice);
-      if (ew == cudaSuccess) ew = cudaMemcpy(d + F * row, h->w.layer[l].up, F * row, cudaMemcpyDeviceToDevice);
+      char* d = wb + xsf_bytes + l * gu_bytes;
+      const size_t blk = 64 * row;  // 64 rows
+      ew = cudaMemcpy2D(d, 2 * blk, h->w.layer[l].gate, blk, blk, F / 64, cudaMemcpyDeviceToDevice);
+      if (ew == cudaSuccess)
+        ew = cudaMemcpy2D(d + blk, 2 * blk, h->w.layer[l].up, blk, blk, F / 64, cudaMemcpyDeviceToDevice);
       wmap(&plan->gu[l], d, 2 * F, H);
     }
     if (ew == cudaSuccess && plan->postc_ok) {
-      char* d = wb + gu_bytes * c.n_layers;
+      char* d = wb + xsf_bytes + gu_bytes * c.n_layers;
       ew = cudaMemcpy(d, h->w.post_proj, bb * row, cudaMemcpyDeviceToDevice);
       if (ew == cudaSuccess) ew = cudaMemcpy(d + bb * row, h->w.centroids, C * row, cudaMemcpyDeviceToDevice);
       wmap(&plan->postc, d, bb + C, H);

@@ -367,8 +367,9 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
   auto groups = [&](int) { return s.B; };  // staging runs one sequence per CTA
   auto gemm = [&](const CUtensorMap& w, const CUtensorMap& x, int R, int K, float* out, long long ldo, float* out2,
                   long long ld2, unsigned long long* best, int dbg_cta = -1, int R1 = 0, float* out_hi = nullptr,
-                  long long ld_hi = 0) -> int {
-    tc::Args a{R, K, plan.bp, s.B, out, ldo, out2, ld2, best, 0, p.w.status, p.spin_limit, dbg_cta, R1, out_hi, ld_hi};
+                  long long ld_hi = 0, __nv_bfloat16* glu_xs = nullptr) -> int {
+    tc::Args a{R,     K,           plan.bp, s.B,     out,   ldo,    out2,    ld2,     best,
+               0,     p.w.status,  p.spin_limit,     dbg_cta, R1, out_hi, ld_hi, glu_xs, plan.bp, R / 2};
     return tc_gemm(&w, &x, a, best != nullptr, st, true);
   };
   int rc;
@@ -391,21 +392,25 @@ int run_phases_tc(const Params& p, const TcPlan& plan, cudaStream_t st) {
       } else {
         MTP_LAUNCH_ATT(l);
       }
-      MTP_LAUNCH_PDL(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, p, l);
-      MTP_LAUNCH_PDL(k_o<WT>, groups(QD), z.smem_o[t], ps, l);
+      // the combine of the attention splits writes the O projection's staged operand
+      MTP_LAUNCH_PDL(k_cmb<WT>, z.cmb[l], 2 * (kThreads / kCmbDims) * kCmbDims * 4, ps, l);
       if ((rc = gemm(plan.o[l], plan.xs_o[t], s.H, QD, p.w.ao, s.H, nullptr, 0, nullptr))) return rc;
       MTP_LAUNCH_PDL(k_gu<WT>, groups(s.H), z.smem_gu, ps, l, par);
-      if (plan.gu_ok) {  // gate and up as one launch over [gate ; up]
-        if ((rc = gemm(plan.gu[l], plan.xs_h, 2 * s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr, -1, s.F, p.w.up,
-                       s.F)))
+      if (plan.gu_ok) {
+        // gate and up as one launch whose epilogue stages gelu_tanh(gate) * up for the down
+        // projection
+        if ((rc = gemm(plan.gu[l], plan.xs_h, 2 * s.F, s.H, nullptr, 0, nullptr, 0, nullptr, -1, 0, nullptr, 0,
+                       plan.xs_glu)))
           return rc;
+        par ^= 1;
+        if ((rc = gemm(plan.down[l], plan.xs_f2, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
       } else {
         if ((rc = gemm(plan.gate[l], plan.xs_h, s.F, s.H, p.w.gate, s.F, nullptr, 0, nullptr))) return rc;
         if ((rc = gemm(plan.up[l], plan.xs_h, s.F, s.H, p.w.up, s.F, nullptr, 0, nullptr))) return rc;
+        par ^= 1;
+        MTP_LAUNCH_PDL(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
+        if ((rc = gemm(plan.down[l], plan.xs_f, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
       }
-      par ^= 1;
-      MTP_LAUNCH_PDL(k_dn<WT>, groups(s.F), z.smem_dn, ps, l);
-      if ((rc = gemm(plan.down[l], plan.xs_f, s.H, s.F, p.w.dn, s.H, nullptr, 0, nullptr))) return rc;
     }
     MTP_LAUNCH_PDL(k_head1<WT>, groups(s.H), z.smem_head1, ps, step, par);
     float* hout = p.out_hidden ? p.out_hidden + static_cast<size_t>(step) * s.bb : nullptr;

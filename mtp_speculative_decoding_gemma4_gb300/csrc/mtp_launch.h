@@ -70,9 +70,11 @@ struct TcPlan {
   CUtensorMap q[MTP_MAX_LAYERS], o[MTP_MAX_LAYERS], gate[MTP_MAX_LAYERS], up[MTP_MAX_LAYERS], down[MTP_MAX_LAYERS];
   CUtensorMap xs_pre, xs_h, xs_o[2], xs_f;  // K = 2 backbone, hidden, n_head * head_dim (sliding, full), ffn
   // stacked copies of projections that read the same input, one launch each: [gate ; up] of
-  // every layer ([2 ffn][hidden]) and [post_proj ; centroids] ([bb + C][hidden]); 0 in the
-  // flags when a first matrix's rows are not a whole number of tiles
-  CUtensorMap gu[MTP_MAX_LAYERS], postc;
+  // every layer ([2 ffn][hidden], interleaved in 64-row blocks for the gated-GELU epilogue,
+  // which writes the down projection's operand into xs_glu, mapped by xs_f2) and
+  // [post_proj ; centroids] ([bb + C][hidden]); 0 in the flags when the shape does not tile
+  CUtensorMap gu[MTP_MAX_LAYERS], postc, xs_f2;
+  __nv_bfloat16* xs_glu;
   int gu_ok, postc_ok;
   __nv_bfloat16* xs;                         // the staging buffer
   int bp;                                    // sequences of the staged terms (multiple of 32)

@@ -26,6 +26,7 @@
 #include <cstddef>
 
 #include "mtp_common.cuh"
+#include "mtp_stage.cuh"
 #include "mtp.h"
 
 namespace mtp {
@@ -254,15 +255,7 @@ __device__ void gemv_phase(const Params& p, const GemvJob* jobs, int njobs, int 
       __syncthreads();
       for (int i = threadIdx.x; i < nb * K_in; i += kThreads) {
         const int b = i / K_in, k = i % K_in;
-        const float v = in_s[b * K_in + k];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const float r1 = v - __bfloat162float(hi);
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-        const size_t row = static_cast<size_t>(b0 + b) * K_in + k, term = static_cast<size_t>(p.tc_bp) * K_in;
-        p.tc_xs[row] = hi;
-        p.tc_xs[term + row] = mid;
-        p.tc_xs[2 * term + row] = lo;
+        stage_terms(p.tc_xs, p.tc_bp, K_in, b0 + b, k, in_s[b * K_in + k]);
       }
     }
     return;
@@ -742,7 +735,10 @@ __device__ void phase_cmb(const Params& p, int l, int cta, int ncta, char* smem)
         dd += sm[(kGroups + q) * kCmbDims + threadIdx.x];
       }
       const float o = dd > 0.f ? n / dd : 0.f;
-      p.w.o[(static_cast<size_t>(b) * p.s.nh + h) * D + i] = o;
+      if (p.tc_xs)  // tensor-core path: straight into the O projection's staged operand
+        stage_terms(p.tc_xs, p.tc_bp, p.s.nh * D, b, h * D + i, o);
+      else
+        p.w.o[(static_cast<size_t>(b) * p.s.nh + h) * D + i] = o;
     }
     __syncthreads();
   }

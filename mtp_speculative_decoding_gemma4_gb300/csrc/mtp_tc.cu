@@ -6,6 +6,7 @@
 #include "mtp.h"
 #include "mtp_common.cuh"
 #include "mtp_launch.h"
+#include "mtp_stage.cuh"
 #include "mtp_tc.cuh"
 
 namespace mtp {
@@ -237,7 +238,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) pbuf[row * (B + 1) + 32 * q + j] = acc[q][j];
   }
-  if (DENSE || S == 1) {
+  if (!DENSE && S == 1 && a.glu_xs) {
+    // gated GELU: warps 2..3 hold the up rows of the gate rows of warps 0..1; they pass them
+    // through the idle stage memory (every MMA has completed, every copy has landed)
+    float* pbuf = reinterpret_cast<float*>(sm_raw + (base - raw));
+    const int row = 32 * warp + lane;
+    if (warp >= 2) {
+#pragma unroll
+      for (int q = 0; q < NB; ++q)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pbuf[(row - 64) * (B + 1) + 32 * q + j] = acc[q][j];
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+    const int f = 64 * tile + row;
+    if (warp < 2 && f < a.glu_K) {
+#pragma unroll
+      for (int q = 0; q < NB; ++q)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 * q + j < a.nvalid)
+            stage_terms(a.glu_xs, a.glu_bp, a.glu_K, 32 * q + j, f,
+                        gelu_tanh(acc[q][j]) * pbuf[row * (B + 1) + 32 * q + j]);
+    }
+  } else if (DENSE || S == 1) {
 #pragma unroll
   for (int q = 0; q < NB; ++q) {
     const int b0 = 32 * q;
@@ -281,7 +304,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has completed and every copy has landed); CTA sp adds the S partials of its rows in
     // order 0..S-1 and stores them; a second barrier keeps the partials alive until then
     asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    if (tid < kEpiWarps * 32) {
+    if (tid < kEpiWarps * 32 && a.glu_xs) {
+      // gated GELU: CTA sp sums the S partials of its gate rows i and of the up rows i + 64
+      const unsigned pb = base;
+      const int i_lo = 64 * sp / S, i_hi = 64 * (sp + 1) / S, ni = i_hi - i_lo;
+      for (int e = tid; e < ni * a.nvalid; e += kEpiWarps * 32) {
+        const int i = i_lo + e / a.nvalid, b = e % a.nvalid;
+        const unsigned og = pb + 4u * static_cast<unsigned>(i * (B + 1) + b);
+        const unsigned ou = pb + 4u * static_cast<unsigned>((i + 64) * (B + 1) + b);
+        float g = 0.f, u = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+          unsigned rg, ru;
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rg) : "r"(og), "r"(s2));
+          asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ru) : "r"(ou), "r"(s2));
+          float x, y;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(rg) : "memory");
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(y) : "r"(ru) : "memory");
+          g += x;
+          u += y;
+        }
+        const int f = 64 * tile + i;
+        if (f < a.glu_K) stage_terms(a.glu_xs, a.glu_bp, a.glu_K, b, f, gelu_tanh(g) * u);
+      }
+    } else if (tid < kEpiWarps * 32) {
       const unsigned pb = base;
       const int r_lo = kM * sp / S, r_hi = kM * (sp + 1) / S, nrow = r_hi - r_lo;
       for (int e = tid; e < nrow * a.nvalid; e += kEpiWarps * 32) {
@@ -371,6 +416,10 @@ int tc_gemm(const CUtensorMap* mapW, const CUtensorMap* mapX, const tc::Args& a,
   if (a.B < 32 || a.B > tc::kMaxB || a.B % 32 || a.nvalid < 1 || a.nvalid > a.B || a.K < tc::kKStage ||
       a.K % tc::kKStage || a.R < 1) {
     set_error("tensor-core GEMM: unsupported R=%d K=%d B=%d", a.R, a.K, a.B);
+    return MTP_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (a.glu_xs && (dense || a.R1 != 0 || a.R % tc::kM || a.glu_K * 2 != a.R || a.glu_bp < a.nvalid)) {
+    set_error("tensor-core GEMM: unsupported gated-GELU epilogue R=%d glu_K=%d", a.R, a.glu_K);
     return MTP_ERR_UNSUPPORTED_SHAPE;
   }
   if (a.R1 != 0 && (dense || a.R1 < 0 || a.R1 % tc::kM || a.R1 >= a.R || !a.out_hi)) {

@@ -17,7 +17,9 @@
 //   * at the end the warps either store Y or, for the dense tied head, keep the largest
 //     (logit, row) key of every sequence (atomicMax). Two projections of the same input
 //     (gate and up; post_projection and the centroids) run as one launch over their stacked
-//     rows, each tile storing into the output of the matrix its rows belong to.
+//     rows, each tile storing into the output of the matrix its rows belong to; gate and up
+//     interleave their rows so that one tile holds both halves of 64 MLP rows and its
+//     epilogue writes gelu_tanh(gate) * up straight into the down projection's operand.
 // Split K: with splits S > 1 (projections only) the S CTAs of a row tile form a thread-block
 // cluster and take consecutive S-th parts of K; each writes its fp32 partial sums into its
 // own (then idle) stage memory, and after a cluster barrier CTA s adds the S partials of rows
@@ -57,6 +59,12 @@ struct Args {
   int R1;
   float* out_hi;
   long long ld_hi;
+  // gated-GELU epilogue (null: off): W is [gate ; up] interleaved in 64-row blocks (rows
+  // 128t..128t+63 are gate rows 64t..64t+63, the next 64 the same up rows) and, instead of Y,
+  // m = gelu_tanh(gate) * up of every row f < glu_K and sequence b < nvalid is stored as its
+  // three bf16 terms into glu_xs [3][glu_bp][glu_K], the down projection's staged operand
+  __nv_bfloat16* glu_xs;
+  int glu_bp, glu_K;
 };
 
 __host__ __device__ inline int stage_bytes(int B) { return kM * kKStage * 2 + 3 * B * kKStage * 2; }

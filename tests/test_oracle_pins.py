@@ -509,6 +509,60 @@ def test_layer_types_read_their_own_k_and_window():
     assert np.max(np.abs(r.y - ref.y)) > 1e-4
 
 
+def _closed_form_uniform_step(shape, w, inp, b):
+    """The step written out by hand for W_q = 0, W_o = I, W_down = 0: every query is zero, so
+    each block's attention is the plain mean of the keys in its range (V = K), the MLP adds
+    nothing, and the residual stream is a chain of sandwich-norm updates."""
+    f64 = lambda a: np.asarray(a, dtype=np.float64)
+    eps = shape.rms_eps
+    L = int(inp.ctx_len[b]); Wn = shape.window
+    h = f64(inp.hidden[b]); e = f64(w.target_embed[int(inp.last_token[b])])
+    x = f64(w.pre_proj) @ np.concatenate([h, e])
+    for li, t in enumerate(shape.layer_types):
+        lay = w.layers[li]
+        keys = f64(inp.k_full[b] if t == "F" else inp.k_swa[b])[:, 0, :]
+        lo = 0 if t == "F" else max(0, L - Wn)
+        m = keys[lo:L].mean(axis=0)                      # every head reads the one KV head
+        a = np.tile(m, shape.n_head)                     # o, flattened over heads; W_o = I
+        x = float(lay["layer_scalar"]) * (x + f64(lay["post_attn_norm"]) * a / math.sqrt(np.mean(a * a) + eps))
+    y = f64(w.out_norm) * x / math.sqrt(np.mean(x * x) + eps)
+    return y, f64(w.post_proj) @ y
+
+
+@pytest.mark.parametrize("layer_types", [("S", "F"), ("F", "S", "S"), ("S",)])
+def test_zero_query_step_equals_its_closed_form(layer_types):
+    # whole-step composition pin: the concatenation [h ; e], the key range of each block type
+    # (the flipped sliding window, the full context), V = K, the norm placed after W_o and
+    # before the residual add, the layer scalar applied to the updated residual stream, the
+    # output norm and post_projection, against the formula written out above (planting any
+    # one of: a window one key wider, a dropped post-attention norm, the scalar taken before
+    # the add, [e ; h] for [h ; e], or a dropped output-norm gain in the oracle fails it)
+    shape, w, inp = _tiny_model(dtype="f32", layer_types=layer_types)
+    H = shape.hidden
+    assert shape.n_head * shape.head_dim_swa == H and shape.n_head * shape.head_dim_full == H
+    for L in w.layers:
+        L["q"] = np.zeros_like(L["q"])
+        L["o"] = np.eye(H, dtype=np.float32)
+        L["down"] = np.zeros_like(L["down"])
+        L["layer_scalar"] = 0.75
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    for b in range(2):
+        assert int(inp.ctx_len[b]) > shape.window      # the window cuts the sliding range
+        kf = {"S": inp.k_swa[b] if inp.k_swa is not None else None,
+              "F": inp.k_full[b] if inp.k_full is not None else None}
+        r = O.drafter_step(s, W, np.asarray(inp.hidden[b], np.float64), int(inp.last_token[b]), kf, {},
+                           int(inp.ctx_len[b]), int(inp.pos[b]))
+        y, h_out = _closed_form_uniform_step(shape, w, inp, b)
+        np.testing.assert_allclose(r.y, y, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(r.hidden_out, h_out, rtol=1e-11, atol=1e-11)
+    # the inputs make the window matter: one key more in the sliding range moves the result
+    if "S" in layer_types:
+        from dataclasses import replace
+        wider = replace(shape, window=shape.window + 1)
+        y1, _ = _closed_form_uniform_step(wider, w, inp, 0)
+        assert np.max(np.abs(y1 - _closed_form_uniform_step(shape, w, inp, 0)[0])) > 1e-6
+
+
 # ---------------------------------------------------------------------------------------
 # Sampled verification (speculative sampling with a point-mass proposal on each draft)
 # ---------------------------------------------------------------------------------------

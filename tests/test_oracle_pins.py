@@ -563,6 +563,79 @@ def test_zero_query_step_equals_its_closed_form(layer_types):
         assert np.max(np.abs(y1 - _closed_form_uniform_step(shape, w, inp, 0)[0])) > 1e-6
 
 
+@pytest.mark.parametrize("t", ["F", "S"])
+def test_one_planted_key_step_equals_its_closed_form(t):
+    # whole-step pin of the query path: the query of head h is q_norm of its slice of W_q a
+    # (a = attn_norm(x)); at position 0 RoPE is the identity; every key in range is zero
+    # except one, set along head 0's query, so head h's attention output is p_h k* with
+    # p_h = e^s / (e^s + n - 1), s = scale * (q_h . k*) and n the keys in range. Keys
+    # outside the range are large noise, so a wrong range, scale, q_norm or softmax shows.
+    shape, w, inp = _tiny_model(dtype="f32", layer_types=(t,))
+    f64 = lambda a: np.asarray(a, dtype=np.float64)
+    H, nh, d, eps = shape.hidden, shape.n_head, shape.head_dim(t), shape.rms_eps
+    rng = np.random.default_rng(7)
+    lay = w.layers[0]
+    lay["o"] = np.eye(H, dtype=np.float32)
+    lay["down"] = np.zeros_like(lay["down"])
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    b = 0
+    L = int(inp.ctx_len[b])
+    assert L > shape.window
+    lo = 0 if t == "F" else L - shape.window
+    n = L - lo
+    # closed form up to the query
+    h = f64(inp.hidden[b]); e = f64(w.target_embed[int(inp.last_token[b])])
+    x0 = f64(w.pre_proj) @ np.concatenate([h, e])
+    a = f64(lay["attn_norm"]) * x0 / math.sqrt(np.mean(x0 * x0) + eps)
+    qraw = (f64(lay["q"]) @ a).reshape(nh, d)
+    gq = f64(lay["q_norm"])
+    qh = np.stack([gq * qraw[k] / math.sqrt(np.mean(qraw[k] ** 2) + eps) for k in range(nh)])
+    scale = 1.0 / math.sqrt(d)
+    # keys: zero in range except j*, noise outside the range, NaN padding beyond L
+    beta = 3.0 / (scale * np.linalg.norm(qh[0]))
+    kstar = (beta * qh[0] / np.linalg.norm(qh[0])).astype(np.float32)
+    Lmax = (inp.k_full if t == "F" else inp.k_swa).shape[1]
+    K = (50.0 * rng.standard_normal((Lmax, 1, d))).astype(np.float32)
+    K[lo:L] = 0.0
+    jstar = lo + n // 2
+    K[jstar, 0] = kstar
+    K[L:] = np.nan
+    ks = f64(kstar)
+    o = np.concatenate([(lambda sc: math.exp(sc) / (math.exp(sc) + n - 1))(scale * float(qh[k] @ ks)) * ks
+                        for k in range(nh)])
+    x1 = float(lay["layer_scalar"]) * (x0 + f64(lay["post_attn_norm"]) * o / math.sqrt(np.mean(o * o) + eps))
+    y = f64(w.out_norm) * x1 / math.sqrt(np.mean(x1 * x1) + eps)
+    r = O.drafter_step(s, W, h, int(inp.last_token[b]), {t: K}, {}, L, 0)
+    np.testing.assert_allclose(r.o[0].reshape(-1), o, rtol=1e-6, atol=1e-9)   # kstar is fp32-rounded
+    np.testing.assert_allclose(r.y, y, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(r.hidden_out, f64(w.post_proj) @ y, rtol=1e-6, atol=1e-8)
+
+
+def test_mlp_only_step_equals_its_closed_form():
+    # whole-step pin of the MLP path: with W_o = 0 the attention update adds norm(0) = 0, so
+    # one block is x1 = lambda (x0 + g_pf * n(W_down m)), m = gelu_tanh(W_gate f) * (W_up f),
+    # f = g_ffn * n(x0), n(v) = v / sqrt(ms(v) + eps); GELU from torch, not from the oracle
+    shape, w, inp = _tiny_model(dtype="f32", layer_types=("F",))
+    f64 = lambda a: np.asarray(a, dtype=np.float64)
+    eps = shape.rms_eps
+    lay = w.layers[0]
+    lay["o"] = np.zeros_like(lay["o"])
+    n = lambda v: v / math.sqrt(np.mean(v * v) + eps)
+    gelu = lambda v: torch.nn.functional.gelu(torch.from_numpy(v), approximate="tanh").numpy()
+    s = O.Shape.of(shape); W = O.decode_weights(w)
+    for b in range(2):
+        h = f64(inp.hidden[b]); e = f64(w.target_embed[int(inp.last_token[b])])
+        x0 = f64(w.pre_proj) @ np.concatenate([h, e])
+        f = f64(lay["ffn_norm"]) * n(x0)
+        m = gelu(f64(lay["gate"]) @ f) * (f64(lay["up"]) @ f)
+        x1 = float(lay["layer_scalar"]) * (x0 + f64(lay["post_ffn_norm"]) * n(f64(lay["down"]) @ m))
+        y = f64(w.out_norm) * n(x1)
+        r = O.drafter_step(s, W, h, int(inp.last_token[b]), {"F": inp.k_full[b]}, {}, int(inp.ctx_len[b]),
+                           int(inp.pos[b]))
+        np.testing.assert_allclose(r.x_layers[0], x1, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(r.y, y, rtol=1e-10, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------------------
 # Sampled verification (speculative sampling with a point-mass proposal on each draft)
 # ---------------------------------------------------------------------------------------

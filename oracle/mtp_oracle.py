@@ -43,8 +43,8 @@ Readings where the pages are silent or disagree (each is stated again where it i
 Pins: every helper and the centroid head, top-k, attention, verify and the shape counts are
 pinned by the not-gpu tests against closed forms, invariants, brute force and the values
 the pages print. A whole drafter step is pinned through special cases written out by
-hand (zero queries, one planted key at position 0, the MLP path alone, zero blocks); with
-RoPE at a non-zero position and every path active at once it is "parity unpinned" beyond
+hand (zero queries, one planted key at several positions, the MLP path alone, zero
+blocks); with a general query and every path active at once it is "parity unpinned" beyond
 those: the pages publish no logit or token for any input.
 """
 from __future__ import annotations

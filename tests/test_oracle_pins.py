@@ -563,13 +563,22 @@ def test_zero_query_step_equals_its_closed_form(layer_types):
         assert np.max(np.abs(y1 - _closed_form_uniform_step(shape, w, inp, 0)[0])) > 1e-6
 
 
-@pytest.mark.parametrize("t", ["F", "S"])
-def test_one_planted_key_step_equals_its_closed_form(t):
+def _rotate_complex(v, pos, theta):
+    # the rotary reading as complex multiplication: element i and element i + d/2 form
+    # z_i = v_i + j v_{i+d/2}, turned by the angle pos * theta^(-2i/d)
+    half = v.shape[-1] // 2
+    z = (v[:half] + 1j * v[half:]) * np.exp(1j * pos * theta ** (-2.0 * np.arange(half) / v.shape[-1]))
+    return np.concatenate([z.real, z.imag])
+
+
+@pytest.mark.parametrize("t,pos", [("F", 0), ("S", 0), ("F", 4099), ("S", 37)])
+def test_one_planted_key_step_equals_its_closed_form(t, pos):
     # whole-step pin of the query path: the query of head h is q_norm of its slice of W_q a
-    # (a = attn_norm(x)); at position 0 RoPE is the identity; every key in range is zero
-    # except one, set along head 0's query, so head h's attention output is p_h k* with
-    # p_h = e^s / (e^s + n - 1), s = scale * (q_h . k*) and n the keys in range. Keys
-    # outside the range are large noise, so a wrong range, scale, q_norm or softmax shows.
+    # (a = attn_norm(x)), turned by the rotary angles of the block type's theta at `pos`
+    # (at position 0 the identity); every key in range is zero except one, set along head
+    # 0's query, so head h's attention output is p_h k* with p_h = e^s / (e^s + n - 1),
+    # s = scale * (q_h . k*) and n the keys in range. Keys outside the range are large
+    # noise, so a wrong range, scale, q_norm, theta or softmax shows.
     shape, w, inp = _tiny_model(dtype="f32", layer_types=(t,))
     f64 = lambda a: np.asarray(a, dtype=np.float64)
     H, nh, d, eps = shape.hidden, shape.n_head, shape.head_dim(t), shape.rms_eps
@@ -590,6 +599,8 @@ def test_one_planted_key_step_equals_its_closed_form(t):
     qraw = (f64(lay["q"]) @ a).reshape(nh, d)
     gq = f64(lay["q_norm"])
     qh = np.stack([gq * qraw[k] / math.sqrt(np.mean(qraw[k] ** 2) + eps) for k in range(nh)])
+    theta = shape.rope_theta_full if t == "F" else shape.rope_theta_swa
+    qh = np.stack([_rotate_complex(qh[k], pos, theta) for k in range(nh)])
     scale = 1.0 / math.sqrt(d)
     # keys: zero in range except j*, noise outside the range, NaN padding beyond L
     beta = 3.0 / (scale * np.linalg.norm(qh[0]))
@@ -605,7 +616,7 @@ def test_one_planted_key_step_equals_its_closed_form(t):
                         for k in range(nh)])
     x1 = float(lay["layer_scalar"]) * (x0 + f64(lay["post_attn_norm"]) * o / math.sqrt(np.mean(o * o) + eps))
     y = f64(w.out_norm) * x1 / math.sqrt(np.mean(x1 * x1) + eps)
-    r = O.drafter_step(s, W, h, int(inp.last_token[b]), {t: K}, {}, L, 0)
+    r = O.drafter_step(s, W, h, int(inp.last_token[b]), {t: K}, {}, L, pos)
     np.testing.assert_allclose(r.o[0].reshape(-1), o, rtol=1e-6, atol=1e-9)   # kstar is fp32-rounded
     np.testing.assert_allclose(r.y, y, rtol=1e-6, atol=1e-9)
     np.testing.assert_allclose(r.hidden_out, f64(w.post_proj) @ y, rtol=1e-6, atol=1e-8)

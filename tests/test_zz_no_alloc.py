@@ -4,7 +4,7 @@ runtime that owns all device memory): it must give the same tokens, selected cen
 logits as mtp_centroid_head on the same tensors, call after call, although its scratch
 lives in one static device array shared by all calls.
 
-Collected last on purpose: the other GPU tests have run by the time it runs.
+Collected after the main GPU suite on purpose: those tests have run by the time it runs.
 """
 import numpy as np
 import pytest

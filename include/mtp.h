@@ -146,6 +146,10 @@ typedef struct mtp_handle mtp_handle;
 
 /* Validate the configuration and the weights, check token_ordering, allocate the
  * workspace for max_batch sequences, and return a handle.
+ * The weight tensors must stay valid and unchanged while the handle lives: some paths read
+ * them directly, others read device copies made here (token_embd in token_ordering order;
+ * per-CTA weight images of the one-sequence grid path; for max_batch >= 2 in bf16, the
+ * stacked [gate ; up] and [post_proj ; centroids] pairs of the tensor-core path).
  * config/weights: host structs (copied). target_embed: device [V][bb] model dtype, the
  * target's input embedding table that embed(last_token) reads ("Gemma 4 drafter
  * explained", "Target Activations": the input table is shared with the target).

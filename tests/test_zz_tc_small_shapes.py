@@ -25,7 +25,8 @@ TENSOR = 5
 def test_tensor_core_path_at_hidden_64_matches_oracle(B):
     import torch
     from mtp_speculative_decoding_gemma4_gb300 import Drafter
-    shape = replace(C.TINY_F32, dtype="bf16", layer_types=("S", "F", "S"), window=8)
+    # the small bf16 shape of the one-sequence edge-context tests, here with a batch
+    shape = replace(C.TINY_F32, dtype="bf16", layer_types=("S", "F", "S"), window=8, n_head=4, n_kv_head=1)
     wl = C.Workload(batch=B, ctx=64, ctx_lo=9, n_draft=4, seed=77)
     w = G.make_weights(shape, wl.seed)
     inp = G.make_step_inputs(shape, wl, wl.seed)
